@@ -1,0 +1,108 @@
+/*
+ * synth.c -- seeded, counter-based synthetic input generator (host side).
+ *
+ * This module holds none of the method's arithmetic: it only draws the
+ * gradients and optimizer states that both the CPU oracle and the CUDA path
+ * are fed with.  The device-side twin (synth_dev.cu) implements the same
+ * definition, so a large workload can be generated in device memory while the
+ * host regenerates any sampled element bit-for-bit.
+ *
+ * Definition (every step is an exact integer operation or a single IEEE
+ * binary64 operation, so both sides agree bit-for-bit):
+ *   mix(z)      = SplitMix64 output function (Steele, Lea & Flood 2014):
+ *                 z ^= z>>30; z *= 0xBF58476D1CE4E5B9;
+ *                 z ^= z>>27; z *= 0x94D049BB133111EB; z ^= z>>31
+ *   key         = mix(seed * GAMMA + mix(stream + 0x632BE59BD9B4E019))
+ *   draw(i, j)  = mix(key + (8*i + j + 1) * GAMMA),  GAMMA = 0x9E3779B97F4A7C15
+ *   uniforms    : draws j = 0..5 give twelve 32-bit halves k, u = (k + 1/2) 2^-32
+ *   z           = (u_0 + ... + u_11) - 6      (Irwin-Hall(12): mean 0, var 1)
+ *   outlier     : draw j = 6, top 53 bits * 2^-53 < p  -> x *= outlier_scale
+ *   x           = mu + sigma * z   (two roundings, never fused), |x| if asked
+ *   fp32 value  = x rounded to nearest binary32; bf16 value = that binary32
+ *                 rounded to nearest-even bf16.
+ * The twelve uniforms are multiples of 2^-33, so their sum and z are exact in
+ * binary64.
+ *
+ * Build: cc -O2 -ffp-contract=off -fPIC -shared synth.c
+ */
+#include <stdint.h>
+#include <string.h>
+
+#define SYN_GAMMA 0x9E3779B97F4A7C15ull
+
+static uint64_t syn_mix(uint64_t z) {
+    z ^= z >> 30;
+    z *= 0xBF58476D1CE4E5B9ull;
+    z ^= z >> 27;
+    z *= 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    return z;
+}
+
+uint64_t syn_key(uint64_t seed, uint64_t stream) {
+    return syn_mix(seed * SYN_GAMMA + syn_mix(stream + 0x632BE59BD9B4E019ull));
+}
+
+static uint64_t syn_draw(uint64_t key, uint64_t i, uint64_t j) {
+    return syn_mix(key + (8u * i + j + 1u) * SYN_GAMMA);
+}
+
+typedef struct {
+    double mu, sigma, outlier_p, outlier_scale;
+    int absval;
+} syn_dist;
+
+static double syn_value(uint64_t key, uint64_t i, const syn_dist *d) {
+    double acc = 0.0; /* literal left-to-right order: no -ffast-math */
+    for (uint64_t j = 0; j < 6; ++j) {
+        uint64_t w = syn_draw(key, i, j);
+        double hi = ((double)(w >> 32) + 0.5) * 0x1p-32;
+        double lo = ((double)(w & 0xFFFFFFFFull) + 0.5) * 0x1p-32;
+        acc = acc + hi;
+        acc = acc + lo;
+    }
+    double z = acc - 6.0;
+    double prod = d->sigma * z;
+    double x = d->mu + prod;
+    if (d->outlier_p > 0.0) {
+        uint64_t w = syn_draw(key, i, 6);
+        double u = (double)(w >> 11) * 0x1p-53;
+        if (u < d->outlier_p) x = x * d->outlier_scale;
+    }
+    if (d->absval && x < 0.0) x = -x;
+    return x;
+}
+
+static uint16_t syn_bf16_rne(float f) {
+    uint32_t b;
+    memcpy(&b, &f, 4);
+    uint32_t up = b >> 16, lowbits = b & 0xFFFFu;
+    if (lowbits > 0x8000u || (lowbits == 0x8000u && (up & 1u))) up += 1u;
+    return (uint16_t)up;
+}
+
+/* out[k] = value of element start+k, k < count.  kind 0: bf16, 1: fp32. */
+void syn_fill(void *out, int kind, int64_t start, int64_t count, uint64_t seed,
+              uint64_t stream, double mu, double sigma, double outlier_p,
+              double outlier_scale, int absval) {
+    syn_dist d = {mu, sigma, outlier_p, outlier_scale, absval};
+    uint64_t key = syn_key(seed, stream);
+    for (int64_t k = 0; k < count; ++k) {
+        float f = (float)syn_value(key, (uint64_t)(start + k), &d);
+        if (kind == 0) ((uint16_t *)out)[k] = syn_bf16_rne(f);
+        else ((float *)out)[k] = f;
+    }
+}
+
+/* out[k] = value of element idx[k]. */
+void syn_gather(void *out, int kind, const int64_t *idx, int64_t count,
+                uint64_t seed, uint64_t stream, double mu, double sigma,
+                double outlier_p, double outlier_scale, int absval) {
+    syn_dist d = {mu, sigma, outlier_p, outlier_scale, absval};
+    uint64_t key = syn_key(seed, stream);
+    for (int64_t k = 0; k < count; ++k) {
+        float f = (float)syn_value(key, (uint64_t)idx[k], &d);
+        if (kind == 0) ((uint16_t *)out)[k] = syn_bf16_rne(f);
+        else ((float *)out)[k] = f;
+    }
+}
