@@ -1,0 +1,405 @@
+#!/usr/bin/env python
+"""Benchmark of the fused ZeRO reduce + mixed-precision Adam step on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic
+input: the N replica gradients of this rank's shard are averaged in fixed
+order, Adam updates the fp32 master/m/v, and the bf16 working copy is
+written -- one call of the C ABI.
+
+Default workload: the GPT-2-small-sized flat buffer (124M parameters, N = 4
+replicas, rank 0's 31M-parameter shard, 25M-element buckets).  Inputs are
+resident in HBM before the timed region; each step touches 1.05 GB, more
+than the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs its own
+rank's shard on its own GPU, with no collective on the data path (weak
+scaling); the timed region is bracketed by a barrier and a device
+synchronise on every rank, and the slowest rank's time is used.
+
+--impl reference times the CPU oracle (the plain fp64 restatement of the
+method that the tests check the CUDA path against) on the host cores, on
+bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "G params/s updated and achieved HBM GB/s vs ~8 TB/s roofline, at N replicas"
+UNIT = "G params/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ("numerics.cuh", "kernels.cuh", "dpopt.cu")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="gpt2s",
+                    help="tiny | gpt2s | 1p3b | 70b_shard (parity configs; gpt2s is the default)")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work budget of the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "zero_mixed_precision_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_from_profiles(workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"reduce_adam_{workload}_traffic.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_sha256") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.tmp = tempfile.NamedTemporaryFile(prefix="clocks_", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.proc.wait()
+        self.tmp.close()
+        rows = []
+        with open(self.tmp.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) != 7:
+                    continue
+                try:
+                    rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+                except ValueError:
+                    continue
+        os.unlink(self.tmp.name)
+        rows = rows[2:] if len(rows) > 4 else rows  # drop nvidia-smi's start-up samples
+        if not rows:
+            return None
+        reasons = sorted({self.NAMES[i] for _, _, flags in rows for i, fl in enumerate(flags)
+                          if fl.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def oracle_rate(wl, host_grads, budget_s: float, threads: int, max_elems: int | None = None):
+    """Time the oracle on host cores over a bounded sample of the workload's shard.
+    host_grads: N numpy arrays (the shard slices).  Returns (params/s, elems, calls)."""
+    import numpy as np
+    import oracle
+    S = host_grads[0].size
+    chunk = min(S, max_elems or S)
+    master = np.zeros(chunk, np.float32)
+    m = np.zeros(chunk, np.float32)
+    v = np.zeros(chunk, np.float32)
+    sl = [np.ascontiguousarray(g[:chunk]) for g in host_grads]
+    done, calls, t = 0, 0, 0
+    t0 = time.perf_counter()
+    while True:
+        t += 1
+        oracle.reduce_adam_range(sl, 0, chunk, master, m, v, lr=wl.lr, beta1=wl.beta1,
+                                 beta2=wl.beta2, eps=wl.eps, step=t, nthreads=threads)
+        done += chunk
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return done / el, chunk, calls
+
+
+def host_grads_for(wl, max_elems: int):
+    """The rank's shard slices of step 1's gradients, generated on the host."""
+    import synth
+    from synth import STREAM_GRAD, stream_id
+    n = min(wl.shard_elems, max_elems)
+    return [synth.host_fill(wl.grad_kind, wl.shard_base, n, wl.seed, stream_id(STREAM_GRAD, r, 1),
+                            wl.grad_dist(r)) for r in range(wl.n_replicas)]
+
+
+def config_of(wl):
+    return {"workload": f"{wl.name}: {wl.numel:,} params per replica buffer, N={wl.n_replicas} "
+                        f"replicas, rank {wl.shard_rank} shard of {wl.shard_elems:,} params, "
+                        f"{wl.bucket_elems:,}-element buckets, "
+                        f"{'bf16' if wl.grad_kind == 0 else 'fp32'} gradients",
+            "n_replicas": wl.n_replicas, "numel": wl.numel, "shard_params": wl.shard_elems,
+            "bucket_elems": wl.bucket_elems,
+            "bytes_per_param": wl.bytes_per_param(),
+            "l2": f"inputs larger than L2: {wl.shard_elems * wl.bytes_per_param() / 1e9:.3f} GB "
+                  "touched per step vs a 129 MB L2 (no flush)",
+            "parallelism": "one shard per GPU, no data-path collective"}
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    threads = len(os.sched_getaffinity(0))
+    grads = host_grads_for(wl, 4_000_000)
+    # size one step's sample so that warmup + steps take about a minute
+    rate, _, _ = oracle_rate(wl, grads, 0.5, threads, max_elems=1_000_000)
+    per_step = int(max(1, min(len(grads[0]), rate * 60.0 / max(1, args.steps + args.warmup))))
+    import numpy as np
+    import oracle
+    sl = [np.ascontiguousarray(g[:per_step]) for g in grads]
+    master = np.zeros(per_step, np.float32)
+    m = np.zeros(per_step, np.float32)
+    v = np.zeros(per_step, np.float32)
+    hp = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, nthreads=threads)
+    for t in range(1, args.warmup + 1):
+        oracle.reduce_adam_range(sl, 0, per_step, master, m, v, step=t, **hp)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        oracle.reduce_adam_range(sl, 0, per_step, master, m, v, step=args.warmup + 1 + k, **hp)
+    el = time.perf_counter() - t0
+    value = per_step * args.steps / el / 1e9
+    sample = (f"{per_step:,} of the {wl.shard_elems:,} shard params per step "
+              f"(N={wl.n_replicas} bf16 replicas), {args.steps} steps after {args.warmup} warm-up")
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded counter-based generator)", "config": config_of(wl),
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import zero_mixed_precision_gb300 as dp
+    from synth.device import DeviceWorkload
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    # each rank updates its own shard of the same model (weak scaling)
+    from dataclasses import replace
+    wl = replace(wl, shard_rank=(wl.shard_rank + rank) % wl.n_replicas)
+    S, n = wl.shard_elems, wl.n_replicas
+    bpp = wl.bytes_per_param()
+
+    dev = DeviceWorkload(wl, device)
+    dev.fill_states()
+    dev.fill_grads(1)
+    stream = torch.cuda.current_stream(device)
+    hp = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps)
+
+    def step(t):
+        dp.reduce_adam(dev.grads, wl.shard_rank, wl.bucket_elems, dev.master, dev.m, dev.v,
+                       dev.out, step=t, stream=stream, **hp)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        uuid = str(local)
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    for t in range(1, args.warmup + 1):
+        step(t)
+    torch.cuda.synchronize(device)
+    dp.stream_status(stream)
+    time.sleep(0.3)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(device)
+    launches0 = dp.dpopt_launch_count()
+    t_start.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        step(args.warmup + 1 + k)
+        ev[k][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(device)
+    barrier()
+    launches = dp.dpopt_launch_count() - launches0
+    clocks = sampler.stop()
+    dp.stream_status(stream)
+    elapsed_ms = t_start.elapsed_time(t_end)
+    kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    ms_per_step = elapsed_ms / K
+    value = world * S * K / (elapsed_ms / 1e3) / 1e9
+
+    # end to end through the public API: host gradients in, bf16 parameters out
+    hs = [torch.empty(S, dtype=dev.grads[0].dtype, pin_memory=True) for _ in range(n)]
+    for h, g in zip(hs, dev.shard_slices()):
+        h.copy_(g)
+    ds = [torch.empty(S, dtype=dev.grads[0].dtype, device=device) for _ in range(n)]
+    hout = torch.empty(S, dtype=torch.bfloat16, pin_memory=True)
+    Ke = max(1, min(args.e2e_steps, K))
+    barrier()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(Ke):
+        for h, d in zip(hs, ds):
+            d.copy_(h, non_blocking=True)
+        dp.reduce_adam_bucket(ds, 0, dev.master, dev.m, dev.v, dev.out,
+                              step=args.warmup + K + 1 + k, stream=stream, **hp)
+        hout.copy_(dev.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    esize = dev.grads[0].element_size()
+    e2e = {"value": world * S * Ke / (e2e_ms / 1e3) / 1e9, "unit": UNIT,
+           "h2d_bytes_per_step": n * S * esize, "d2h_bytes_per_step": S * 2,
+           "path": "pinned host gradients -> cudaMemcpyAsync -> dpopt_reduce_adam_bucket -> "
+                   "bf16 parameters back to pinned host, one stream"}
+    dp.stream_status(stream)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+
+    peak, peak_kind = load_peaks()
+    achieved = S * bpp / (kernel_ms / 1e3) / 1e9
+    traffic = traffic_from_profiles(wl.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded counter-based generator, generated in HBM)",
+        "config": config_of(wl),
+        "hbm_gbs": world * S * bpp / (ms_per_step / 1e3) / 1e9 / world,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth",
+                     "frac_of_nominal_8tbs": achieved / 8000.0,
+                     "traffic": traffic,
+                     "algorithmic_bytes_per_launch": S * bpp,
+                     "kernel_ms": kernel_ms},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        threads = len(os.sched_getaffinity(0))
+        grads = [h.view(torch.int16).numpy().view("uint16") if h.dtype == torch.bfloat16
+                 else h.numpy() for h in hs]
+        rate, chunk, calls = oracle_rate(wl, grads, args.cpu_seconds, threads,
+                                         max_elems=4_000_000)
+        line["cpu_baseline"] = {
+            "value": rate / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{chunk:,} of the {S:,} shard params (N={n}), {calls} Adam steps, "
+                      f"{args.cpu_seconds:.0f} s of CPU work on {threads} threads"}
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    import synth
+    if args.workload not in synth.WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}")
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        line = run_reference(args, wl)
+    else:
+        line = run_ours(args, wl)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

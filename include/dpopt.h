@@ -1,0 +1,195 @@
+/*
+ * dpopt.h -- C ABI of the fused ZeRO gradient reduce + mixed-precision Adam
+ * step for one GB300 (sm_103a).
+ *
+ * What one call computes, for every element i of one rank's shard:
+ *
+ *   g_i      = ( sum_{r=0..N-1} grad_r[i] ) / N      replica order fixed, ascending
+ *   m_i     <- beta1 * m_i + (1 - beta1) * g_i
+ *   v_i     <- beta2 * v_i + (1 - beta2) * g_i^2
+ *   master_i <- master_i - lr * (m_i / (1 - beta1^t)) / (sqrt(v_i / (1 - beta2^t)) + eps)
+ *   out_i    = bf16(master_i)                        round to nearest, ties to even
+ *
+ * Sources: the synchronised gradient is the sum of the replicas' local
+ * gradients times 1/#Nodes, and the summation order is a choice that changes
+ * floating-point results ("Data Parallelism 数据并行（二）", section "数据并行
+ * 训练 (DP)"); ZeRO-3's reduce-scatter sums the gradients over all ranks and
+ * each rank keeps and updates only its own 1/N shard ("Почему training 70B
+ * модели требует optimizer sharding (ZeRO-3)?", sections 3 and 5); the
+ * states are an fp32 master copy plus fp32 first and second moments beside a
+ * 16-bit working copy, 16 bytes per parameter ("Глава 4.4 --
+ * Распределённое обучение", section 2; the DP page's appendix "DNN 训练的
+ * 内存需求").  The Adam equations are not printed on those pages; the
+ * textbook bias-corrected form (Kingma & Ba 2015) is used, t = step, 1-based.
+ *
+ * Numerics: the replica sum is accumulated in fp32 with an error-free
+ * transformation (TwoSum) and rounded once, so g equals the correctly rounded
+ * average in all but vanishingly rare cases; m, v and the master update are
+ * formed with compensated fp32 arithmetic, so stored values are within
+ * 2.4e-7 relative (about 2 ulp) of an fp64 evaluation.  Every element is
+ * owned by one thread and the order is fixed: results are bitwise identical
+ * from run to run, and do not depend on bucket_elems or on how a shard is cut
+ * into buckets.
+ *
+ * Conventions for every entry point:
+ *  - Memory: the caller owns all memory.  Gradient, state and output pointers
+ *    are DEVICE pointers of the current CUDA device; the pointer tables
+ *    themselves (grads, grad_slices, slice_table) and offsets/lens are HOST
+ *    arrays, read during the call only.  The library allocates no memory.
+ *  - Layout: flat, contiguous, element-indexed.  bf16 values are IEEE
+ *    binary32's upper 16 bits (stored as 2-byte words), fp32 are binary32.
+ *  - In place: master, m, v are read and overwritten; param_bf16_out is only
+ *    written.  Gradients are only read.  Gradient buffers must not overlap any
+ *    state or output range, and the state/output ranges must not overlap one
+ *    another (checked: DPOPT_ERR_INVALID_ARG).
+ *  - Alignment: any element-aligned pointer is accepted; ranges whose pointers
+ *    are all 16-byte aligned take the vectorised path, others a scalar path.
+ *  - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) and the call returns without waiting.  Errors in
+ *    the arguments are reported synchronously; dpopt_stream_status() waits
+ *    for the stream and reports anything the kernels flagged on the device.
+ *  - Errors: every function returns a dpopt_status; nothing is thrown across
+ *    the ABI.  On an error no work has been enqueued, except DPOPT_ERR_CUDA
+ *    from a launch, after which earlier launches of the same call may have run.
+ *  - Threads: all entry points may be called from several host threads; the
+ *    only shared state is a per-device status word and cached device
+ *    attributes.
+ */
+#ifndef DPOPT_H
+#define DPOPT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st *dpopt_stream_t;
+
+typedef enum {
+    DPOPT_OK = 0,
+    DPOPT_ERR_INVALID_ARG = 1, /* a null/overlapping pointer, a size or hyper-parameter out of range */
+    DPOPT_ERR_UNSUPPORTED = 2, /* valid but beyond this build's limits (n_replicas > DPOPT_MAX_REPLICAS) */
+    DPOPT_ERR_CUDA = 3,        /* a CUDA call failed; dpopt_last_error() has its message */
+    DPOPT_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up (reported by dpopt_stream_status) */
+} dpopt_status;
+
+typedef enum {
+    DPOPT_GRAD_BF16 = 0, /* 2-byte bf16 gradients */
+    DPOPT_GRAD_F32 = 1   /* 4-byte fp32 gradients */
+} dpopt_grad_dtype;
+
+#define DPOPT_MAX_REPLICAS 64
+
+/* Full-buffer entry.  Reduce-scatter semantics with all N contributions
+ * resident in this GPU's memory ("Почему training 70B ...", section 5: sum the
+ * gradients over all GPUs, keep only your own shard; then update only that
+ * shard).
+ *
+ *  grads          HOST array of n_replicas DEVICE pointers; grads[r] is replica
+ *                 r's flattened bf16 gradient buffer of `numel` elements.
+ *  n_replicas     N, 1 <= N <= DPOPT_MAX_REPLICAS.
+ *  numel          elements per replica buffer, a multiple of N (>= 0).
+ *  shard_rank     r in [0, N): this rank updates [r*S, (r+1)*S), S = numel / N.
+ *  bucket_elems   fusion-bucket size (>= 1): the shard is cut into buckets of this
+ *                 many elements from its start, the last one ragged (DeepSpeed's
+ *                 reduce_bucket_size over contiguous gradients in the config of
+ *                 "Почему training 70B ...", section 8).  With every
+ *                 contribution resident the buckets are only units of work:
+ *                 the result does not depend on this value.
+ *  master_f32, m_f32, v_f32
+ *                 DEVICE pointers to the S-element fp32 shard states, updated in place.
+ *  param_bf16_out DEVICE pointer to S bf16 elements, written: bf16(master) after the step.
+ *  lr, beta1, beta2, eps
+ *                 Adam hyper-parameters: finite, 0 <= beta < 1, eps >= 0.
+ *  step           t >= 1, the 1-based index of this step (bias correction).
+ *  stream         CUDA stream to enqueue on.
+ * Returns DPOPT_OK or an error status (see the conventions above). */
+int dpopt_reduce_adam(const void *const *grads, int n_replicas, int64_t numel, int shard_rank,
+                      int64_t bucket_elems, float *master_f32, float *m_f32, float *v_f32,
+                      void *param_bf16_out, float lr, float beta1, float beta2, float eps,
+                      int64_t step, dpopt_stream_t stream);
+
+/* dpopt_reduce_adam with the gradient type given (grad_dtype is a
+ * dpopt_grad_dtype); everything else as above. */
+int dpopt_reduce_adam_ex(const void *const *grads, int grad_dtype, int n_replicas, int64_t numel,
+                         int shard_rank, int64_t bucket_elems, float *master_f32, float *m_f32,
+                         float *v_f32, void *param_bf16_out, float lr, float beta1, float beta2,
+                         float eps, int64_t step, dpopt_stream_t stream);
+
+/* Bucket iterator over one shard.  count_out receives ceil(shard_elems /
+ * bucket_elems) (0 for an empty shard); bucket idx covers [offset, offset+len)
+ * of the shard, offset = idx*bucket_elems, len = bucket_elems except for a
+ * ragged last bucket.  Host-only; no device work.
+ * Errors: DPOPT_ERR_INVALID_ARG for shard_elems < 0, bucket_elems < 1, a null
+ * output pointer, or idx outside [0, count). */
+int dpopt_bucket_count(int64_t shard_elems, int64_t bucket_elems, int64_t *count_out);
+int dpopt_bucket_range(int64_t shard_elems, int64_t bucket_elems, int64_t idx, int64_t *offset_out,
+                       int64_t *len_out);
+
+/* One bucket, with the gradients already cut to this rank's bucket (what a
+ * reduce-scatter hands each rank).
+ *  grad_slices    HOST array of n_replicas DEVICE pointers, each to `len`
+ *                 gradient elements of type grad_dtype (replica r's slice).
+ *  shard_offset   first shard element of the bucket (>= 0).
+ *  len            elements in the bucket (>= 0; 0 is a no-op).
+ *  master_f32, m_f32, v_f32, param_bf16_out
+ *                 DEVICE pointers to the START of the shard's arrays; elements
+ *                 [shard_offset, shard_offset+len) are updated / written.
+ * Other arguments as for dpopt_reduce_adam. */
+int dpopt_reduce_adam_bucket(const void *const *grad_slices, int grad_dtype, int n_replicas,
+                             int64_t shard_offset, int64_t len, float *master_f32, float *m_f32,
+                             float *v_f32, void *param_bf16_out, float lr, float beta1,
+                             float beta2, float eps, int64_t step, dpopt_stream_t stream);
+
+/* Many buckets per call (as few kernel launches as the pointer tables allow).
+ *  slice_table    HOST array of n_buckets * n_replicas DEVICE pointers, bucket
+ *                 major: slice_table[b * n_replicas + r] is replica r's slice of
+ *                 bucket b (lens[b] elements of grad_dtype).
+ *  offsets, lens  HOST arrays of n_buckets: bucket b updates shard elements
+ *                 [offsets[b], offsets[b] + lens[b]).  Buckets must not overlap.
+ * Other arguments as for dpopt_reduce_adam_bucket. */
+int dpopt_reduce_adam_buckets(const void *const *slice_table, int grad_dtype, int n_replicas,
+                              const int64_t *offsets, const int64_t *lens, int64_t n_buckets,
+                              float *master_f32, float *m_f32, float *v_f32, void *param_bf16_out,
+                              float lr, float beta1, float beta2, float eps, int64_t step,
+                              dpopt_stream_t stream);
+
+/* Wait for `stream`, then return and clear the current device's status word:
+ * DPOPT_OK, or DPOPT_ERR_TIMEOUT if a bounded device-side wait gave up since the
+ * last call, or DPOPT_ERR_CUDA if the wait itself failed. */
+int dpopt_stream_status(dpopt_stream_t stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *dpopt_status_string(int status);
+
+/* Message of the last DPOPT_ERR_CUDA / DPOPT_ERR_INVALID_ARG raised on the
+ * calling host thread ("" if none).  Valid until the thread's next call. */
+const char *dpopt_last_error(void);
+
+/* Model-state bytes one data-parallel device holds for psi parameters.
+ *  variant 0: mixed-precision Adam, 16 bytes/parameter: 2 (16-bit params) + 2
+ *             (16-bit grads) + 12 (fp32 master, m, v) ("Глава 4.4", section 2).
+ *  variant 1: the ZeRO-3 answer's conservative 70B figure as printed, 2 + 2 + 4
+ *             bytes/parameter (140 + 140 + 280 GB = 560 GB, its section 2).
+ *  zero_stage 0 keeps all; 1 shards the optimizer states over n_dp devices;
+ *  2 also the gradients; 3 also the parameters ("Глава 4.4", section 6:
+ *  16*Psi/N_dp at the most aggressive stage).
+ * Errors: DPOPT_ERR_INVALID_ARG for psi < 0, n_dp < 1, an unknown variant or
+ * stage, or a null bytes_out.  Host-only. */
+int dpopt_state_bytes(int64_t psi, int variant, int n_dp, int zero_stage, double *bytes_out);
+
+/* Kernel launches this library has made from the calling host thread since
+ * the thread started (a running count; the caller takes differences). */
+int64_t dpopt_launch_count(void);
+
+/* Library version, "major.minor.patch". */
+const char *dpopt_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DPOPT_H */

@@ -16,12 +16,13 @@
  *   draw(i, j)  = mix(key + (8*i + j + 1) * GAMMA),  GAMMA = 0x9E3779B97F4A7C15
  *   uniforms    : draws j = 0..5 give twelve 32-bit halves k, u = (k + 1/2) 2^-32
  *   z           = (u_0 + ... + u_11) - 6      (Irwin-Hall(12): mean 0, var 1)
+ *               = (k_0 + ... + k_11 + 6 - 6*2^32) * 2^-32, formed in 64-bit
+ *                 integers and converted once (|.| < 2^36: exact in binary64)
  *   outlier     : draw j = 6, top 53 bits * 2^-53 < p  -> x *= outlier_scale
  *   x           = mu + sigma * z   (two roundings, never fused), |x| if asked
  *   fp32 value  = x rounded to nearest binary32; bf16 value = that binary32
  *                 rounded to nearest-even bf16.
- * The twelve uniforms are multiples of 2^-33, so their sum and z are exact in
- * binary64.
+ * z is therefore exact; only mu + sigma*z rounds.
  *
  * Build: cc -O2 -ffp-contract=off -fPIC -shared synth.c
  */
@@ -53,15 +54,13 @@ typedef struct {
 } syn_dist;
 
 static double syn_value(uint64_t key, uint64_t i, const syn_dist *d) {
-    double acc = 0.0; /* literal left-to-right order: no -ffast-math */
+    int64_t ksum = 0;
     for (uint64_t j = 0; j < 6; ++j) {
         uint64_t w = syn_draw(key, i, j);
-        double hi = ((double)(w >> 32) + 0.5) * 0x1p-32;
-        double lo = ((double)(w & 0xFFFFFFFFull) + 0.5) * 0x1p-32;
-        acc = acc + hi;
-        acc = acc + lo;
+        ksum += (int64_t)(w >> 32);
+        ksum += (int64_t)(w & 0xFFFFFFFFull);
     }
-    double z = acc - 6.0;
+    double z = (double)(ksum + 6 - 6 * (int64_t)0x100000000ll) * 0x1p-32;
     double prod = d->sigma * z;
     double x = d->mu + prod;
     if (d->outlier_p > 0.0) {

@@ -30,20 +30,18 @@ struct Dist {
 };
 
 __device__ inline double value_at(uint64_t key, uint64_t i, const Dist& d) {
-  double acc = 0.0;
+  int64_t ksum = 0;
 #pragma unroll
   for (uint64_t j = 0; j < 6; ++j) {
     uint64_t w = mix64(key + (8u * i + j + 1u) * kGamma);
-    double hi = __dmul_rn(__dadd_rn((double)(w >> 32), 0.5), 0x1p-32);
-    double lo = __dmul_rn(__dadd_rn((double)(w & 0xFFFFFFFFull), 0.5), 0x1p-32);
-    acc = __dadd_rn(acc, hi);
-    acc = __dadd_rn(acc, lo);
+    ksum += (int64_t)(w >> 32);
+    ksum += (int64_t)(w & 0xFFFFFFFFull);
   }
-  double z = __dsub_rn(acc, 6.0);
+  double z = __dmul_rn(__ll2double_rn(ksum + 6 - 6 * (int64_t)0x100000000ll), 0x1p-32);
   double x = __dadd_rn(d.mu, __dmul_rn(d.sigma, z));
   if (d.outlier_p > 0.0) {
     uint64_t w = mix64(key + (8u * i + 6u + 1u) * kGamma);
-    double u = __dmul_rn((double)(w >> 11), 0x1p-53);
+    double u = __dmul_rn(__ull2double_rn(w >> 11), 0x1p-53);
     if (u < d.outlier_p) x = __dmul_rn(x, d.outlier_scale);
   }
   if (d.absval && x < 0.0) x = -x;

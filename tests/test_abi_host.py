@@ -1,0 +1,146 @@
+"""The C ABI on the host (no GPU): the library loads, exports every function
+the header declares, and rejects bad arguments before touching the device."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import oracle
+from tests.test_oracle_pins import _golden_rows
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dpopt.h")
+
+
+@pytest.fixture(scope="module")
+def dp():
+    import __graft_entry__
+    __graft_entry__.build_module().build()
+    import zero_mixed_precision_gb300 as mod
+    return mod
+
+
+def _declared():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dpopt_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(dp):
+    names = _declared()
+    assert len(names) >= 10
+    lib = ctypes.CDLL(dp.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(dp.EXPORTED) == names
+
+
+@pytest.mark.parametrize("lang", ["c", "c++"])
+def test_header_compiles_standalone(lang, tmp_path):
+    src = tmp_path / ("t.c" if lang == "c" else "t.cpp")
+    src.write_text('#include "dpopt.h"\nint main(void){return dpopt_status_string(0) == 0;}\n')
+    cc = "gcc" if lang == "c" else "g++"
+    subprocess.run([cc, "-Wall", "-Werror", "-I", os.path.dirname(HEADER), "-fsyntax-only",
+                    str(src)], check=True)
+
+
+def test_status_strings(dp):
+    for code, name in ((0, "DPOPT_OK"), (1, "DPOPT_ERR_INVALID_ARG"), (2, "DPOPT_ERR_UNSUPPORTED"),
+                       (3, "DPOPT_ERR_CUDA"), (4, "DPOPT_ERR_TIMEOUT"), (99, "DPOPT_UNKNOWN_STATUS")):
+        assert dp.dpopt_status_string(code) == name
+
+
+@pytest.mark.parametrize("row", [r for r in _golden_rows() if r[4] == "total"],
+                         ids=lambda r: r[7][:40])
+def test_state_bytes_matches_printed_figures(dp, row):
+    psi, variant, n_dp, stage, _comp, expected, rel, _cite = row
+    rc, got = dp.dpopt_state_bytes(int(psi), variant, n_dp, stage)
+    assert rc == 0
+    if rel == "eq":
+        assert got == pytest.approx(expected, rel=1e-12)
+    else:
+        assert got > expected
+
+
+@pytest.mark.parametrize("variant", [0, 1])
+@pytest.mark.parametrize("stage", [0, 1, 2, 3])
+@pytest.mark.parametrize("n_dp", [1, 8, 64])
+def test_state_bytes_agrees_with_the_oracle_accounting(dp, variant, stage, n_dp):
+    rc, got = dp.dpopt_state_bytes(70_000_000_000, variant, n_dp, stage)
+    assert rc == 0 and got == pytest.approx(oracle.state_bytes(70e9, variant, n_dp, stage), rel=1e-12)
+
+
+def test_state_bytes_rejects_bad_arguments(dp):
+    for args in ((-1, 0, 1, 0), (1, 2, 1, 0), (1, 0, 0, 0), (1, 0, 1, 4)):
+        assert dp.dpopt_state_bytes(*args)[0] == dp.DPOPT_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("shard,bucket", [(0, 5), (1, 1), (10, 3), (31_000_000, 25_000_000),
+                                          (162_500_000, 50_000_000), (1_093_750_000, 4_000_000),
+                                          (7, 100)])
+def test_bucket_iterator_agrees_with_the_oracle_ranges(dp, shard, bucket):
+    want = oracle.bucket_ranges(shard, bucket)
+    rc, cnt = dp.dpopt_bucket_count(shard, bucket)
+    assert rc == 0 and cnt == len(want)
+    for i, (off, ln) in enumerate(want):
+        assert dp.dpopt_bucket_range(shard, bucket, i) == (0, off, ln)
+    assert dp.dpopt_bucket_range(shard, bucket, cnt)[0] == dp.DPOPT_ERR_INVALID_ARG
+    assert dp.dpopt_bucket_range(shard, bucket, -1)[0] == dp.DPOPT_ERR_INVALID_ARG
+
+
+def test_bucket_iterator_rejects_bad_arguments(dp):
+    assert dp.dpopt_bucket_count(-1, 5)[0] == dp.DPOPT_ERR_INVALID_ARG
+    assert dp.dpopt_bucket_count(5, 0)[0] == dp.DPOPT_ERR_INVALID_ARG
+
+
+# Fake, never-dereferenced device addresses: validation fails before any launch.
+G = [0x10_0000_0000 + r * 0x1_0000_0000 for r in range(64)]
+MASTER, M, V, OUT = 0x90_0000_0000, 0xA0_0000_0000, 0xB0_0000_0000, 0xC0_0000_0000
+HP = (1e-3, 0.9, 0.999, 1e-8)
+
+
+def _full(dp, **over):
+    a = dict(grads=G[:4], n=4, numel=4096, rank=0, bucket=1024, master=MASTER, m=M, v=V, out=OUT,
+             lr=HP[0], b1=HP[1], b2=HP[2], eps=HP[3], step=1, dtype=0)
+    a.update(over)
+    return dp.dpopt_reduce_adam_ex(a["grads"], a["dtype"], a["n"], a["numel"], a["rank"],
+                                   a["bucket"], a["master"], a["m"], a["v"], a["out"], a["lr"],
+                                   a["b1"], a["b2"], a["eps"], a["step"], 0)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(n=0), 1), (dict(n=65, grads=G[:64] + [G[0]]), 2), (dict(numel=4095), 1),
+    (dict(numel=-4), 1), (dict(rank=4), 1), (dict(rank=-1), 1), (dict(bucket=0), 1),
+    (dict(step=0), 1), (dict(step=-3), 1), (dict(lr=float("nan")), 1), (dict(lr=float("inf")), 1),
+    (dict(b1=1.0), 1), (dict(b1=-0.1), 1), (dict(b2=1.0), 1), (dict(b2=float("nan")), 1),
+    (dict(eps=-1e-8), 1), (dict(eps=float("inf")), 1), (dict(master=0), 1), (dict(out=0), 1),
+    (dict(grads=[G[0], 0, G[2], G[3]]), 1), (dict(dtype=7), 1), (dict(master=MASTER + 2), 1),
+    (dict(out=OUT + 1), 1), (dict(grads=[G[0] + 1, G[1], G[2], G[3]]), 1),
+    (dict(m=MASTER + 8), 1),                      # m overlaps master
+    (dict(out=G[0] + 2), 1),                      # output inside gradient buffer 0's shard
+    (dict(master=G[1] + 1000), 1),                # state inside a gradient shard
+])
+def test_full_buffer_entry_rejects_bad_arguments(dp, over, code):
+    assert _full(dp, **over) == code
+    assert dp.dpopt_last_error() != ""
+
+
+def test_null_grads_table_is_rejected(dp):
+    assert dp.dpopt_reduce_adam(None, 2, 8, 0, 4, MASTER, M, V, OUT, *HP, 1, 0) == 1
+
+
+def test_bucket_entries_reject_bad_arguments(dp):
+    args = (MASTER, M, V, OUT, *HP, 1, 0)
+    assert dp.dpopt_reduce_adam_bucket(G[:2], 0, 2, -1, 10, *args) == 1
+    assert dp.dpopt_reduce_adam_bucket(G[:2], 0, 2, 0, -5, *args) == 1
+    assert dp.dpopt_reduce_adam_bucket(G[:2], 3, 2, 0, 10, *args) == 1
+    # overlapping buckets
+    assert dp.dpopt_reduce_adam_buckets(G[:4], 0, 2, [0, 5], [10, 10], *args) == 1
+    # a slice that overlaps the master range
+    assert dp.dpopt_reduce_adam_buckets([G[0], MASTER + 16], 0, 2, [0], [100], *args) == 1
+    # n_replicas beyond the limit
+    assert dp.dpopt_reduce_adam_buckets(G[:64] * 2, 0, 65, [0], [10], *args) == 2

@@ -1,0 +1,13 @@
+"""Fused ZeRO gradient reduce + mixed-precision Adam for one GB300 (sm_103a).
+
+The compute path is libdpopt.so (hand-written CUDA, C ABI in include/dpopt.h);
+this package is its ctypes binding.  Importing it without the built library
+fails loudly; there is no CPU or PyTorch fallback.
+"""
+from .binding import *  # noqa: F401,F403
+from .binding import (  # noqa: F401
+    DpoptError, EXPORTED, LIB_PATH, reduce_adam, reduce_adam_bucket, reduce_adam_buckets,
+    stream_status,
+)
+
+__version__ = "0.1.0"

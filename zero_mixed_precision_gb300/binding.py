@@ -1,0 +1,227 @@
+"""Thin ctypes binding of libdpopt.so (include/dpopt.h).
+
+Argument marshalling only: every step of the reduce + Adam path runs in the
+CUDA kernels of the library.  The ``dpopt_*`` functions take the C ABI's
+arguments (device pointers as ints, a stream handle as an int); the
+lower-case wrappers below take torch tensors and pass their data pointers.
+If the library is missing this module raises at import: there is no
+fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+from . import _build
+
+DPOPT_OK = 0
+DPOPT_ERR_INVALID_ARG = 1
+DPOPT_ERR_UNSUPPORTED = 2
+DPOPT_ERR_CUDA = 3
+DPOPT_ERR_TIMEOUT = 4
+DPOPT_GRAD_BF16 = 0
+DPOPT_GRAD_F32 = 1
+DPOPT_MAX_REPLICAS = 64
+
+LIB_PATH = _build.LIB_PATH
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build the CUDA library first "
+        "(python -c 'import __graft_entry__ as g; g.build()')")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_PP = ctypes.POINTER(ctypes.c_void_p)
+_PI64 = ctypes.POINTER(ctypes.c_int64)
+
+_SIGS = {
+    "dpopt_reduce_adam": ([_PP, _I, _I64, _I, _I64, _P, _P, _P, _P, _F, _F, _F, _F, _I64, _P], _I),
+    "dpopt_reduce_adam_ex": ([_PP, _I, _I, _I64, _I, _I64, _P, _P, _P, _P, _F, _F, _F, _F, _I64,
+                              _P], _I),
+    "dpopt_bucket_count": ([_I64, _I64, _PI64], _I),
+    "dpopt_bucket_range": ([_I64, _I64, _I64, _PI64, _PI64], _I),
+    "dpopt_reduce_adam_bucket": ([_PP, _I, _I, _I64, _I64, _P, _P, _P, _P, _F, _F, _F, _F, _I64,
+                                  _P], _I),
+    "dpopt_reduce_adam_buckets": ([_PP, _I, _I, _PI64, _PI64, _I64, _P, _P, _P, _P, _F, _F, _F, _F,
+                                   _I64, _P], _I),
+    "dpopt_stream_status": ([_P], _I),
+    "dpopt_status_string": ([_I], ctypes.c_char_p),
+    "dpopt_last_error": ([], ctypes.c_char_p),
+    "dpopt_state_bytes": ([_I64, _I, _I, _I, ctypes.POINTER(ctypes.c_double)], _I),
+    "dpopt_version": ([], ctypes.c_char_p),
+    "dpopt_launch_count": ([], _I64),
+}
+
+for _name, (_args, _res) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _res
+
+EXPORTED = tuple(_SIGS)
+
+
+class DpoptError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = _lib.dpopt_last_error().decode(errors="replace")
+        name = _lib.dpopt_status_string(status).decode()
+        super().__init__(f"{where}: {name}" + (f" ({msg})" if msg else ""))
+        self.status = status
+
+
+def _ptr_array(ptrs: Sequence[int]):
+    return (ctypes.c_void_p * len(ptrs))(*ptrs)
+
+
+# ---------------------------------------------------------------------------
+# C ABI, same names
+# ---------------------------------------------------------------------------
+
+def dpopt_reduce_adam(grads: Sequence[int], n_replicas: int, numel: int, shard_rank: int,
+                      bucket_elems: int, master: int, m: int, v: int, param_bf16_out: int,
+                      lr: float, beta1: float, beta2: float, eps: float, step: int,
+                      stream: int = 0) -> int:
+    return _lib.dpopt_reduce_adam(_ptr_array(grads) if grads is not None else None, n_replicas,
+                                  numel, shard_rank, bucket_elems, master, m, v, param_bf16_out,
+                                  lr, beta1, beta2, eps, step, stream)
+
+
+def dpopt_reduce_adam_ex(grads: Sequence[int], grad_dtype: int, n_replicas: int, numel: int,
+                         shard_rank: int, bucket_elems: int, master: int, m: int, v: int,
+                         param_bf16_out: int, lr: float, beta1: float, beta2: float, eps: float,
+                         step: int, stream: int = 0) -> int:
+    return _lib.dpopt_reduce_adam_ex(_ptr_array(grads) if grads is not None else None, grad_dtype,
+                                     n_replicas, numel, shard_rank, bucket_elems, master, m, v,
+                                     param_bf16_out, lr, beta1, beta2, eps, step, stream)
+
+
+def dpopt_bucket_count(shard_elems: int, bucket_elems: int) -> tuple[int, int]:
+    out = ctypes.c_int64(0)
+    rc = _lib.dpopt_bucket_count(shard_elems, bucket_elems, ctypes.byref(out))
+    return rc, out.value
+
+
+def dpopt_bucket_range(shard_elems: int, bucket_elems: int, idx: int) -> tuple[int, int, int]:
+    off, ln = ctypes.c_int64(0), ctypes.c_int64(0)
+    rc = _lib.dpopt_bucket_range(shard_elems, bucket_elems, idx, ctypes.byref(off),
+                                 ctypes.byref(ln))
+    return rc, off.value, ln.value
+
+
+def dpopt_reduce_adam_bucket(grad_slices: Sequence[int], grad_dtype: int, n_replicas: int,
+                             shard_offset: int, length: int, master: int, m: int, v: int,
+                             param_bf16_out: int, lr: float, beta1: float, beta2: float,
+                             eps: float, step: int, stream: int = 0) -> int:
+    return _lib.dpopt_reduce_adam_bucket(
+        _ptr_array(grad_slices) if grad_slices is not None else None, grad_dtype, n_replicas,
+        shard_offset, length, master, m, v, param_bf16_out, lr, beta1, beta2, eps, step, stream)
+
+
+def dpopt_reduce_adam_buckets(slice_table: Sequence[int], grad_dtype: int, n_replicas: int,
+                              offsets: Sequence[int], lens: Sequence[int], master: int, m: int,
+                              v: int, param_bf16_out: int, lr: float, beta1: float, beta2: float,
+                              eps: float, step: int, stream: int = 0) -> int:
+    nb = len(offsets)
+    offs = (ctypes.c_int64 * nb)(*offsets)
+    lns = (ctypes.c_int64 * nb)(*lens)
+    return _lib.dpopt_reduce_adam_buckets(_ptr_array(slice_table), grad_dtype, n_replicas, offs,
+                                          lns, nb, master, m, v, param_bf16_out, lr, beta1, beta2,
+                                          eps, step, stream)
+
+
+def dpopt_stream_status(stream: int = 0) -> int:
+    return _lib.dpopt_stream_status(stream)
+
+
+def dpopt_status_string(status: int) -> str:
+    return _lib.dpopt_status_string(status).decode()
+
+
+def dpopt_last_error() -> str:
+    return _lib.dpopt_last_error().decode(errors="replace")
+
+
+def dpopt_state_bytes(psi: int, variant: int, n_dp: int, zero_stage: int) -> tuple[int, float]:
+    out = ctypes.c_double(0.0)
+    rc = _lib.dpopt_state_bytes(int(psi), variant, n_dp, zero_stage, ctypes.byref(out))
+    return rc, out.value
+
+
+def dpopt_version() -> str:
+    return _lib.dpopt_version().decode()
+
+
+def dpopt_launch_count() -> int:
+    return int(_lib.dpopt_launch_count())
+
+
+# ---------------------------------------------------------------------------
+# torch-tensor wrappers (marshalling only)
+# ---------------------------------------------------------------------------
+
+def _check(rc: int, where: str) -> None:
+    if rc != DPOPT_OK:
+        raise DpoptError(rc, where)
+
+
+def _grad_dtype(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return DPOPT_GRAD_BF16
+    if t.dtype == torch.float32:
+        return DPOPT_GRAD_F32
+    raise TypeError(f"gradients must be bfloat16 or float32, got {t.dtype}")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+def reduce_adam(grads, shard_rank: int, bucket_elems: int, master, m, v, param_bf16_out, *,
+                lr: float, beta1: float, beta2: float, eps: float, step: int, stream=None) -> None:
+    """Full-buffer step: grads are N flattened replica tensors (bf16 or fp32,
+    numel elements each); master/m/v (fp32) and param_bf16_out (bf16) hold
+    this rank's S = numel/N shard."""
+    dt = _grad_dtype(grads[0])
+    rc = dpopt_reduce_adam_ex([g.data_ptr() for g in grads], dt, len(grads), grads[0].numel(),
+                              shard_rank, bucket_elems, master.data_ptr(), m.data_ptr(),
+                              v.data_ptr(), param_bf16_out.data_ptr(), lr, beta1, beta2, eps, step,
+                              _stream_handle(stream))
+    _check(rc, "dpopt_reduce_adam_ex")
+
+
+def reduce_adam_bucket(grad_slices, shard_offset: int, master, m, v, param_bf16_out, *, lr: float,
+                       beta1: float, beta2: float, eps: float, step: int, stream=None) -> None:
+    """One bucket: grad_slices are N tensors of the bucket's length."""
+    dt = _grad_dtype(grad_slices[0])
+    rc = dpopt_reduce_adam_bucket([g.data_ptr() for g in grad_slices], dt, len(grad_slices),
+                                  shard_offset, grad_slices[0].numel(), master.data_ptr(),
+                                  m.data_ptr(), v.data_ptr(), param_bf16_out.data_ptr(), lr, beta1,
+                                  beta2, eps, step, _stream_handle(stream))
+    _check(rc, "dpopt_reduce_adam_bucket")
+
+
+def reduce_adam_buckets(bucket_slices, offsets, master, m, v, param_bf16_out, *, lr: float,
+                        beta1: float, beta2: float, eps: float, step: int, stream=None) -> None:
+    """Many buckets: bucket_slices[b] is a list of N tensors for bucket b,
+    which updates shard elements [offsets[b], offsets[b] + len)."""
+    n = len(bucket_slices[0])
+    dt = _grad_dtype(bucket_slices[0][0])
+    table = [t.data_ptr() for row in bucket_slices for t in row]
+    lens = [row[0].numel() for row in bucket_slices]
+    rc = dpopt_reduce_adam_buckets(table, dt, n, list(offsets), lens, master.data_ptr(),
+                                   m.data_ptr(), v.data_ptr(), param_bf16_out.data_ptr(), lr,
+                                   beta1, beta2, eps, step, _stream_handle(stream))
+    _check(rc, "dpopt_reduce_adam_buckets")
+
+
+def stream_status(stream=None) -> None:
+    _check(dpopt_stream_status(_stream_handle(stream)), "dpopt_stream_status")

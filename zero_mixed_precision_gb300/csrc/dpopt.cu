@@ -1,0 +1,446 @@
+// dpopt.cu -- the C ABI (include/dpopt.h): argument checks, the step's
+// scalars, segment tables and kernel launches.  No memory is allocated here.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "dpopt.h"
+#include "kernels.cuh"
+
+namespace dpopt {
+namespace {
+
+constexpr int kSmallSegs = 1;
+constexpr int kSmallPtrs = DPOPT_MAX_REPLICAS;
+constexpr int kBigSegs = 128;
+constexpr int kBigPtrs = 2048;
+constexpr int kMaxDevices = 64;
+
+using SmallParams = LaunchParams<kSmallSegs, kSmallPtrs>;
+using BigParams = LaunchParams<kBigSegs, kBigPtrs>;
+static_assert(sizeof(BigParams) <= 32000, "kernel parameters must fit the 32 KB limit");
+
+// Sticky per-device status word for bounded device-side waits.
+__device__ unsigned int g_status;
+
+thread_local char g_last_error[512];
+thread_local int64_t g_launches = 0;
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(DPOPT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool is_finite(float x) { return std::isfinite(x); }
+
+// Scalars of step t, in fp64 on the host, split into fp32 pairs.
+Hyper make_hyper(float lr, float beta1, float beta2, float eps, int64_t step, int n) {
+  Hyper h{};
+  const double b1 = beta1, b2 = beta2;
+  auto split = [](double x, float& hi, float& lo) {
+    hi = (float)x;
+    lo = (float)(x - (double)hi);
+  };
+  h.beta1 = beta1;
+  h.beta2 = beta2;
+  split(1.0 - b1, h.c1_hi, h.c1_lo);
+  split(1.0 - b2, h.c2_hi, h.c2_lo);
+  const double bc1 = 1.0 - std::pow(b1, (double)step);
+  const double bc2 = 1.0 - std::pow(b2, (double)step);
+  split((double)lr / bc1, h.a_hi, h.a_lo);
+  split(1.0 / std::sqrt(bc2), h.b_hi, h.b_lo);
+  h.eps = eps;
+  h.n_f = (float)n;
+  h.inv_n = ((n & (n - 1)) == 0) ? (float)(1.0 / n) : 0.f;
+  return h;
+}
+
+int check_hyper(float lr, float beta1, float beta2, float eps, int64_t step) {
+  if (!is_finite(lr)) return fail(DPOPT_ERR_INVALID_ARG, "lr must be finite");
+  if (!is_finite(beta1) || beta1 < 0.f || beta1 >= 1.f)
+    return fail(DPOPT_ERR_INVALID_ARG, "beta1 must lie in [0, 1)");
+  if (!is_finite(beta2) || beta2 < 0.f || beta2 >= 1.f)
+    return fail(DPOPT_ERR_INVALID_ARG, "beta2 must lie in [0, 1)");
+  if (!is_finite(eps) || eps < 0.f) return fail(DPOPT_ERR_INVALID_ARG, "eps must be finite, >= 0");
+  if (step < 1) return fail(DPOPT_ERR_INVALID_ARG, "step must be >= 1");
+  return DPOPT_OK;
+}
+
+int check_replicas(int n_replicas, int grad_dtype) {
+  if (n_replicas < 1) return fail(DPOPT_ERR_INVALID_ARG, "n_replicas must be >= 1");
+  if (n_replicas > DPOPT_MAX_REPLICAS)
+    return fail(DPOPT_ERR_UNSUPPORTED, "n_replicas %d exceeds %d", n_replicas, DPOPT_MAX_REPLICAS);
+  if (grad_dtype != DPOPT_GRAD_BF16 && grad_dtype != DPOPT_GRAD_F32)
+    return fail(DPOPT_ERR_INVALID_ARG, "unknown grad_dtype %d", grad_dtype);
+  return DPOPT_OK;
+}
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+
+bool overlaps(const Range& a, const Range& b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// The four state/output ranges of elements [off, off+len) of the shard arrays.
+int check_states(float* master, float* m, float* v, void* out, int64_t lo_elem, int64_t hi_elem,
+                 Range st[4]) {
+  if (!master || !m || !v || !out)
+    return fail(DPOPT_ERR_INVALID_ARG, "master, m, v and param_bf16_out must be non-null");
+  if (((uintptr_t)master | (uintptr_t)m | (uintptr_t)v) & 3u)
+    return fail(DPOPT_ERR_INVALID_ARG, "fp32 state pointers must be 4-byte aligned");
+  if ((uintptr_t)out & 1u) return fail(DPOPT_ERR_INVALID_ARG, "bf16 output must be 2-byte aligned");
+  st[0] = {(uintptr_t)(master + lo_elem), (uintptr_t)(master + hi_elem)};
+  st[1] = {(uintptr_t)(m + lo_elem), (uintptr_t)(m + hi_elem)};
+  st[2] = {(uintptr_t)(v + lo_elem), (uintptr_t)(v + hi_elem)};
+  st[3] = {(uintptr_t)((uint16_t*)out + lo_elem), (uintptr_t)((uint16_t*)out + hi_elem)};
+  for (int i = 0; i < 4; ++i)
+    for (int j = i + 1; j < 4; ++j)
+      if (overlaps(st[i], st[j]))
+        return fail(DPOPT_ERR_INVALID_ARG, "state/output arrays overlap");
+  return DPOPT_OK;
+}
+
+int check_grad(const void* p, int64_t len, size_t esize, const Range st[4]) {
+  if (!p) return fail(DPOPT_ERR_INVALID_ARG, "null gradient pointer");
+  if ((uintptr_t)p % esize) return fail(DPOPT_ERR_INVALID_ARG, "misaligned gradient pointer");
+  Range g{(uintptr_t)p, (uintptr_t)p + (uintptr_t)len * esize};
+  for (int i = 0; i < 4; ++i)
+    if (overlaps(g, st[i]))
+      return fail(DPOPT_ERR_INVALID_ARG, "a gradient buffer overlaps a state or output array");
+  return DPOPT_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+struct DeviceCache {
+  std::atomic<int> sms[kMaxDevices];
+};
+DeviceCache g_dev;
+
+int sm_count(int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DPOPT_ERR_UNSUPPORTED, "device index too large");
+  int s = g_dev.sms[dev].load(std::memory_order_relaxed);
+  if (s == 0) {
+    e = cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    g_dev.sms[dev].store(s, std::memory_order_relaxed);
+  }
+  *out = s;
+  return DPOPT_OK;
+}
+
+// One segment as the kernel sees it.
+struct SegDesc {
+  const void* const* ptrs;  // n_replicas gradient pointers at the segment start
+  int64_t state_off;
+  int64_t len;
+};
+
+template <int NR, int GK, int MS, int MP>
+int launch_one(const LaunchParams<MS, MP>& p, cudaStream_t stream) {
+  auto kern = reduce_adam_ldg_kernel<NR, GK, MS, MP>;
+  int sms = 0;
+  int rc = sm_count(&sms);
+  if (rc) return rc;
+  static std::atomic<int> per_sm{0};
+  int bps = per_sm.load(std::memory_order_relaxed);
+  if (bps == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, kThreads, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (bps < 1) bps = 1;
+    per_sm.store(bps, std::memory_order_relaxed);
+  }
+  int64_t want = (p.total_groups + kThreads - 1) / kThreads;
+  int64_t cap = (int64_t)sms * bps;
+  unsigned grid = (unsigned)std::max<int64_t>(1, std::min(want, cap));
+  kern<<<grid, kThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  ++g_launches;
+  return DPOPT_OK;
+}
+
+template <int MS, int MP>
+int dispatch(const LaunchParams<MS, MP>& p, int grad_dtype, cudaStream_t stream) {
+  const int n = p.n_rep;
+  if (grad_dtype == DPOPT_GRAD_BF16) {
+    if constexpr (MS == kSmallSegs) {
+      switch (n) {
+        case 1: return launch_one<1, 0>(p, stream);
+        case 2: return launch_one<2, 0>(p, stream);
+        case 4: return launch_one<4, 0>(p, stream);
+        case 8: return launch_one<8, 0>(p, stream);
+        default: break;
+      }
+    }
+    return launch_one<0, 0>(p, stream);
+  }
+  if constexpr (MS == kSmallSegs) {
+    switch (n) {
+      case 1: return launch_one<1, 1>(p, stream);
+      case 2: return launch_one<2, 1>(p, stream);
+      case 4: return launch_one<4, 1>(p, stream);
+      case 8: return launch_one<8, 1>(p, stream);
+      default: break;
+    }
+  }
+  return launch_one<0, 1>(p, stream);
+}
+
+// Fill and launch one LaunchParams from segments [s0, s1).
+template <int MS, int MP>
+int run_segments(LaunchParams<MS, MP>& p, const SegDesc* segs, int s0, int s1, int n,
+                 size_t esize, cudaStream_t stream, int grad_dtype) {
+  int64_t groups = 0;
+  int nseg = 0;
+  for (int s = s0; s < s1; ++s) {
+    const SegDesc& d = segs[s];
+    if (d.len == 0) continue;
+    Seg& sg = p.seg[nseg];
+    sg.first_group = groups;
+    sg.state_off = d.state_off;
+    sg.len = d.len;
+    sg.ptr_base = nseg * n;
+    bool vec = aligned16(p.master + d.state_off) && aligned16(p.m + d.state_off) &&
+               aligned16(p.v + d.state_off) && aligned16(p.out + d.state_off);
+    for (int r = 0; r < n; ++r) {
+      p.gptr[nseg * n + r] = d.ptrs[r];
+      vec = vec && aligned16(d.ptrs[r]);
+    }
+    (void)esize;
+    sg.vec = vec ? 1 : 0;
+    groups += (d.len + kGroup - 1) / kGroup;
+    ++nseg;
+  }
+  if (nseg == 0) return DPOPT_OK;
+  p.seg[nseg].first_group = groups;
+  p.seg[nseg].len = 0;
+  p.nseg = nseg;
+  p.total_groups = groups;
+  return dispatch(p, grad_dtype, stream);
+}
+
+int run(const SegDesc* segs, int nsegs, int grad_dtype, int n, float* master, float* m, float* v,
+        void* out, const Hyper& h, cudaStream_t stream) {
+  const size_t esize = grad_dtype == DPOPT_GRAD_BF16 ? 2 : 4;
+  if (nsegs == 1) {
+    SmallParams p{};
+    p.h = h;
+    p.master = master; p.m = m; p.v = v; p.out = (uint16_t*)out;
+    p.n_rep = n;
+    return run_segments(p, segs, 0, 1, n, esize, stream, grad_dtype);
+  }
+  const int per_launch = std::min(kBigSegs, kBigPtrs / n);
+  static thread_local BigParams p;  // 20 KB: kept off the stack
+  for (int s0 = 0; s0 < nsegs; s0 += per_launch) {
+    std::memset(&p, 0, sizeof p);
+    p.h = h;
+    p.master = master; p.m = m; p.v = v; p.out = (uint16_t*)out;
+    p.n_rep = n;
+    int rc = run_segments(p, segs, s0, std::min(nsegs, s0 + per_launch), n, esize, stream,
+                          grad_dtype);
+    if (rc) return rc;
+  }
+  return DPOPT_OK;
+}
+
+}  // namespace
+}  // namespace dpopt
+
+using namespace dpopt;
+
+extern "C" {
+
+int dpopt_reduce_adam_ex(const void* const* grads, int grad_dtype, int n_replicas, int64_t numel,
+                         int shard_rank, int64_t bucket_elems, float* master_f32, float* m_f32,
+                         float* v_f32, void* param_bf16_out, float lr, float beta1, float beta2,
+                         float eps, int64_t step, dpopt_stream_t stream) {
+  int rc = check_replicas(n_replicas, grad_dtype);
+  if (rc) return rc;
+  if (!grads) return fail(DPOPT_ERR_INVALID_ARG, "grads must be non-null");
+  if (numel < 0 || numel % n_replicas != 0)
+    return fail(DPOPT_ERR_INVALID_ARG, "numel must be >= 0 and a multiple of n_replicas");
+  if (shard_rank < 0 || shard_rank >= n_replicas)
+    return fail(DPOPT_ERR_INVALID_ARG, "shard_rank must lie in [0, n_replicas)");
+  if (bucket_elems < 1) return fail(DPOPT_ERR_INVALID_ARG, "bucket_elems must be >= 1");
+  rc = check_hyper(lr, beta1, beta2, eps, step);
+  if (rc) return rc;
+  const int64_t S = numel / n_replicas;
+  const int64_t base = (int64_t)shard_rank * S;
+  const size_t esize = grad_dtype == DPOPT_GRAD_BF16 ? 2 : 4;
+  if (S == 0) return DPOPT_OK;
+  Range st[4];
+  rc = check_states(master_f32, m_f32, v_f32, param_bf16_out, 0, S, st);
+  if (rc) return rc;
+  const void* ptrs[DPOPT_MAX_REPLICAS];
+  for (int r = 0; r < n_replicas; ++r) {
+    if (!grads[r]) return fail(DPOPT_ERR_INVALID_ARG, "null gradient pointer");
+    ptrs[r] = (const char*)grads[r] + (size_t)base * esize;
+    rc = check_grad(ptrs[r], S, esize, st);
+    if (rc) return rc;
+  }
+  // Every contribution is resident and the buckets tile the shard contiguously,
+  // so the whole shard is one segment: bucket_elems changes neither the
+  // addresses nor the result, only what the bucket iterator reports.
+  SegDesc seg{ptrs, 0, S};
+  Hyper h = make_hyper(lr, beta1, beta2, eps, step, n_replicas);
+  return run(&seg, 1, grad_dtype, n_replicas, master_f32, m_f32, v_f32, param_bf16_out, h,
+             (cudaStream_t)stream);
+}
+
+int dpopt_reduce_adam(const void* const* grads, int n_replicas, int64_t numel, int shard_rank,
+                      int64_t bucket_elems, float* master_f32, float* m_f32, float* v_f32,
+                      void* param_bf16_out, float lr, float beta1, float beta2, float eps,
+                      int64_t step, dpopt_stream_t stream) {
+  return dpopt_reduce_adam_ex(grads, DPOPT_GRAD_BF16, n_replicas, numel, shard_rank, bucket_elems,
+                              master_f32, m_f32, v_f32, param_bf16_out, lr, beta1, beta2, eps,
+                              step, stream);
+}
+
+int dpopt_bucket_count(int64_t shard_elems, int64_t bucket_elems, int64_t* count_out) {
+  if (!count_out || shard_elems < 0 || bucket_elems < 1)
+    return fail(DPOPT_ERR_INVALID_ARG, "bucket_count: invalid argument");
+  *count_out = shard_elems / bucket_elems + (shard_elems % bucket_elems ? 1 : 0);
+  return DPOPT_OK;
+}
+
+int dpopt_bucket_range(int64_t shard_elems, int64_t bucket_elems, int64_t idx,
+                       int64_t* offset_out, int64_t* len_out) {
+  int64_t count = 0;
+  int rc = dpopt_bucket_count(shard_elems, bucket_elems, &count);
+  if (rc) return rc;
+  if (!offset_out || !len_out || idx < 0 || idx >= count)
+    return fail(DPOPT_ERR_INVALID_ARG, "bucket_range: invalid argument");
+  const int64_t off = idx * bucket_elems;
+  *offset_out = off;
+  *len_out = std::min(bucket_elems, shard_elems - off);
+  return DPOPT_OK;
+}
+
+int dpopt_reduce_adam_buckets(const void* const* slice_table, int grad_dtype, int n_replicas,
+                              const int64_t* offsets, const int64_t* lens, int64_t n_buckets,
+                              float* master_f32, float* m_f32, float* v_f32, void* param_bf16_out,
+                              float lr, float beta1, float beta2, float eps, int64_t step,
+                              dpopt_stream_t stream) {
+  int rc = check_replicas(n_replicas, grad_dtype);
+  if (rc) return rc;
+  if (n_buckets < 0) return fail(DPOPT_ERR_INVALID_ARG, "n_buckets must be >= 0");
+  rc = check_hyper(lr, beta1, beta2, eps, step);
+  if (rc) return rc;
+  if (n_buckets == 0) return DPOPT_OK;
+  if (!slice_table || !offsets || !lens)
+    return fail(DPOPT_ERR_INVALID_ARG, "slice_table, offsets and lens must be non-null");
+  if (n_buckets > (int64_t)1 << 30) return fail(DPOPT_ERR_UNSUPPORTED, "too many buckets");
+  const size_t esize = grad_dtype == DPOPT_GRAD_BF16 ? 2 : 4;
+  int64_t lo = INT64_MAX, hi = 0;
+  std::vector<std::pair<int64_t, int64_t>> spans;
+  spans.reserve((size_t)n_buckets);
+  for (int64_t b = 0; b < n_buckets; ++b) {
+    if (offsets[b] < 0 || lens[b] < 0 || offsets[b] > INT64_MAX - lens[b])
+      return fail(DPOPT_ERR_INVALID_ARG, "bucket %lld: bad offset/len", (long long)b);
+    if (lens[b] == 0) continue;
+    lo = std::min(lo, offsets[b]);
+    hi = std::max(hi, offsets[b] + lens[b]);
+    spans.emplace_back(offsets[b], offsets[b] + lens[b]);
+  }
+  if (spans.empty()) return DPOPT_OK;
+  std::sort(spans.begin(), spans.end());
+  for (size_t i = 1; i < spans.size(); ++i)
+    if (spans[i].first < spans[i - 1].second)
+      return fail(DPOPT_ERR_INVALID_ARG, "buckets overlap");
+  Range st[4];
+  rc = check_states(master_f32, m_f32, v_f32, param_bf16_out, lo, hi, st);
+  if (rc) return rc;
+  std::vector<SegDesc> segs;
+  segs.reserve((size_t)n_buckets);
+  for (int64_t b = 0; b < n_buckets; ++b) {
+    if (lens[b] == 0) continue;
+    const void* const* row = slice_table + b * n_replicas;
+    for (int r = 0; r < n_replicas; ++r) {
+      rc = check_grad(row[r], lens[b], esize, st);
+      if (rc) return rc;
+    }
+    segs.push_back(SegDesc{row, offsets[b], lens[b]});
+  }
+  Hyper h = make_hyper(lr, beta1, beta2, eps, step, n_replicas);
+  return run(segs.data(), (int)segs.size(), grad_dtype, n_replicas, master_f32, m_f32, v_f32,
+             param_bf16_out, h, (cudaStream_t)stream);
+}
+
+int dpopt_reduce_adam_bucket(const void* const* grad_slices, int grad_dtype, int n_replicas,
+                             int64_t shard_offset, int64_t len, float* master_f32, float* m_f32,
+                             float* v_f32, void* param_bf16_out, float lr, float beta1,
+                             float beta2, float eps, int64_t step, dpopt_stream_t stream) {
+  int rc = check_replicas(n_replicas, grad_dtype);
+  if (rc) return rc;
+  if (!grad_slices) return fail(DPOPT_ERR_INVALID_ARG, "grad_slices must be non-null");
+  if (shard_offset < 0 || len < 0)
+    return fail(DPOPT_ERR_INVALID_ARG, "shard_offset and len must be >= 0");
+  return dpopt_reduce_adam_buckets(grad_slices, grad_dtype, n_replicas, &shard_offset, &len, 1,
+                                   master_f32, m_f32, v_f32, param_bf16_out, lr, beta1, beta2, eps,
+                                   step, stream);
+}
+
+int dpopt_stream_status(dpopt_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int st = 0;
+  e = cudaMemcpyFromSymbol(&st, g_status, sizeof st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol");
+  if (st != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_status, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
+    return DPOPT_ERR_TIMEOUT;
+  }
+  return DPOPT_OK;
+}
+
+const char* dpopt_status_string(int status) {
+  switch (status) {
+    case DPOPT_OK: return "DPOPT_OK";
+    case DPOPT_ERR_INVALID_ARG: return "DPOPT_ERR_INVALID_ARG";
+    case DPOPT_ERR_UNSUPPORTED: return "DPOPT_ERR_UNSUPPORTED";
+    case DPOPT_ERR_CUDA: return "DPOPT_ERR_CUDA";
+    case DPOPT_ERR_TIMEOUT: return "DPOPT_ERR_TIMEOUT";
+    default: return "DPOPT_UNKNOWN_STATUS";
+  }
+}
+
+const char* dpopt_last_error(void) { return g_last_error; }
+
+int dpopt_state_bytes(int64_t psi, int variant, int n_dp, int zero_stage, double* bytes_out) {
+  if (!bytes_out || psi < 0 || n_dp < 1 || zero_stage < 0 || zero_stage > 3 ||
+      (variant != 0 && variant != 1))
+    return fail(DPOPT_ERR_INVALID_ARG, "state_bytes: invalid argument");
+  const double p = 2.0, g = 2.0, o = variant == 0 ? 12.0 : 4.0;
+  const double n = (double)n_dp, x = (double)psi;
+  const double bp = x * p / (zero_stage >= 3 ? n : 1.0);
+  const double bg = x * g / (zero_stage >= 2 ? n : 1.0);
+  const double bo = x * o / (zero_stage >= 1 ? n : 1.0);
+  *bytes_out = bp + bg + bo;
+  return DPOPT_OK;
+}
+
+int64_t dpopt_launch_count(void) { return g_launches; }
+
+const char* dpopt_version(void) { return "0.1.0"; }
+
+}  // extern "C"

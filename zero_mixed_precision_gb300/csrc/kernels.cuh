@@ -1,0 +1,250 @@
+// kernels.cuh -- the fused reduce + Adam kernel, direct-load form.
+//
+// One launch walks a list of segments (a whole shard, one bucket, or a batch
+// of buckets).  Each segment has its own N replica pointers and a range of the
+// shard's state arrays.  The launch is persistent: gridDim.x is a multiple of
+// the SM count and every thread strides over 8-element groups, so a warp
+// reads 512 contiguous bytes of every bf16 replica and 1 KB of every fp32
+// state array per iteration.  Each element belongs to exactly one thread and
+// the replica order is fixed, so the result is bitwise reproducible.
+//
+// Memory traffic per element is the algorithmic minimum: N gradient reads,
+// master/m/v read once and written once, the bf16 copy written once (no
+// intermediate ever leaves registers).  Gradients are read once, so their
+// loads carry an L2 evict-first policy and skip L1.
+#pragma once
+
+#include "numerics.cuh"
+
+namespace dpopt {
+
+constexpr int kGroup = 8;      // elements per thread per iteration
+constexpr int kThreads = 256;  // threads per CTA
+
+struct Seg {
+  int64_t first_group;  // groups of all earlier segments (prefix sum)
+  int64_t state_off;    // first shard element this segment updates
+  int64_t len;          // elements
+  int32_t ptr_base;     // index of replica 0's pointer in LaunchParams::gptr
+  int32_t vec;          // 1: every pointer of the segment is 16-byte aligned
+};
+
+template <int MAXSEG, int MAXPTR>
+struct LaunchParams {
+  Hyper h;
+  float* master;
+  float* m;
+  float* v;
+  uint16_t* out;
+  int64_t total_groups;
+  int32_t n_rep;
+  int32_t nseg;
+  Seg seg[MAXSEG + 1];  // seg[nseg].first_group == total_groups
+  const void* gptr[MAXPTR];
+};
+
+// ---------------------------------------------------------------------------
+// memory access helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 16 bytes of a gradient buffer: read once, L1 bypassed, L2 evict-first.
+__device__ __forceinline__ uint4 ld_grad16(const void* p, uint64_t pol) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p), "l"(pol));
+  return r;
+}
+
+// 16 bytes of a state array (read here, written back by the same thread).
+__device__ __forceinline__ float4 ld_state16(const float* p) {
+  float4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+      : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+      : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_stream16(float* p, float a, float b, float c, float d) {
+  asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_stream16u(void* p, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.global.cs.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// 8 gradient values of one replica as fp32.  GK 0: bf16 (one 16-byte load),
+// GK 1: fp32 (two 16-byte loads).
+template <int GK>
+struct GradLoad;
+
+template <>
+struct GradLoad<0> {
+  uint4 w;
+  __device__ __forceinline__ void load(const void* base, int64_t e0, uint64_t pol) {
+    w = ld_grad16(static_cast<const uint16_t*>(base) + e0, pol);
+  }
+  __device__ __forceinline__ void zero() { w = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ float get(int k) const {
+    uint32_t x = (k < 2) ? w.x : (k < 4) ? w.y : (k < 6) ? w.z : w.w;
+    return (k & 1) ? bf16_hi(x) : bf16_lo(x);
+  }
+};
+
+template <>
+struct GradLoad<1> {
+  uint4 a, b;
+  __device__ __forceinline__ void load(const void* base, int64_t e0, uint64_t pol) {
+    const float* p = static_cast<const float*>(base) + e0;
+    a = ld_grad16(p, pol);
+    b = ld_grad16(p + 4, pol);
+  }
+  __device__ __forceinline__ void zero() { a = b = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ float get(int k) const {
+    const uint4& q = (k < 4) ? a : b;
+    int j = k & 3;
+    return __uint_as_float(j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w);
+  }
+};
+
+template <int GK>
+__device__ __forceinline__ float ld_grad1(const void* base, int64_t e) {
+  if (GK == 0) {
+    uint16_t h = static_cast<const uint16_t*>(base)[e];
+    return __uint_as_float(((uint32_t)h) << 16);
+  } else {
+    return static_cast<const float*>(base)[e];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// one 8-element group, vector path
+// ---------------------------------------------------------------------------
+
+template <int NR, int GK, class LP>
+__device__ __forceinline__ void group_vec(const LP& p, const Seg& sg, int64_t e0, uint64_t pol) {
+  const int64_t so = sg.state_off + e0;
+  float th[kGroup], mm[kGroup], vv[kGroup];
+  {
+    float4 a = ld_state16(p.master + so), b = ld_state16(p.master + so + 4);
+    th[0] = a.x; th[1] = a.y; th[2] = a.z; th[3] = a.w;
+    th[4] = b.x; th[5] = b.y; th[6] = b.z; th[7] = b.w;
+    a = ld_state16(p.m + so); b = ld_state16(p.m + so + 4);
+    mm[0] = a.x; mm[1] = a.y; mm[2] = a.z; mm[3] = a.w;
+    mm[4] = b.x; mm[5] = b.y; mm[6] = b.z; mm[7] = b.w;
+    a = ld_state16(p.v + so); b = ld_state16(p.v + so + 4);
+    vv[0] = a.x; vv[1] = a.y; vv[2] = a.z; vv[3] = a.w;
+    vv[4] = b.x; vv[5] = b.y; vv[6] = b.z; vv[7] = b.w;
+  }
+  const void* const* gp = p.gptr + sg.ptr_base;
+  CompSum acc[kGroup];
+  if constexpr (NR > 0) {
+    GradLoad<GK> gl[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) gl[r].load(gp[r], e0, pol);
+#pragma unroll
+    for (int k = 0; k < kGroup; ++k) acc[k].init(gl[0].get(k));
+#pragma unroll
+    for (int r = 1; r < NR; ++r) {
+#pragma unroll
+      for (int k = 0; k < kGroup; ++k) acc[k].add(gl[r].get(k));
+    }
+  } else {
+    // runtime replica count: chunks of 8 replicas, loads of a chunk in flight together
+    constexpr int C = 8;
+    const int n = p.n_rep;
+    for (int r0 = 0; r0 < n; r0 += C) {
+      GradLoad<GK> gl[C];
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        if (r0 + j < n) gl[j].load(gp[r0 + j], e0, pol);
+        else gl[j].zero();
+      }
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        if (r0 + j < n) {
+          if (r0 + j == 0) {
+#pragma unroll
+            for (int k = 0; k < kGroup; ++k) acc[k].init(gl[j].get(k));
+          } else {
+#pragma unroll
+            for (int k = 0; k < kGroup; ++k) acc[k].add(gl[j].get(k));
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kGroup; ++k) {
+    float g = acc[k].average(p.h);
+    adam_element(g, th[k], mm[k], vv[k], p.h);
+  }
+  st_stream16(p.master + so, th[0], th[1], th[2], th[3]);
+  st_stream16(p.master + so + 4, th[4], th[5], th[6], th[7]);
+  st_stream16(p.m + so, mm[0], mm[1], mm[2], mm[3]);
+  st_stream16(p.m + so + 4, mm[4], mm[5], mm[6], mm[7]);
+  st_stream16(p.v + so, vv[0], vv[1], vv[2], vv[3]);
+  st_stream16(p.v + so + 4, vv[4], vv[5], vv[6], vv[7]);
+  st_stream16u(p.out + so, to_bf16x2(th[0], th[1]), to_bf16x2(th[2], th[3]),
+               to_bf16x2(th[4], th[5]), to_bf16x2(th[6], th[7]));
+}
+
+// ---------------------------------------------------------------------------
+// a partial or unaligned group, one element at a time
+// ---------------------------------------------------------------------------
+
+template <int GK, class LP>
+__device__ __noinline__ void group_scalar(const LP& p, const Seg& sg, int64_t e0, int count) {
+  const void* const* gp = p.gptr + sg.ptr_base;
+  const int n = p.n_rep;
+  for (int k = 0; k < count; ++k) {
+    const int64_t e = e0 + k;
+    const int64_t so = sg.state_off + e;
+    CompSum acc;
+    acc.init(ld_grad1<GK>(gp[0], e));
+    for (int r = 1; r < n; ++r) acc.add(ld_grad1<GK>(gp[r], e));
+    float th = p.master[so], mm = p.m[so], vv = p.v[so];
+    adam_element(acc.average(p.h), th, mm, vv, p.h);
+    p.master[so] = th;
+    p.m[so] = mm;
+    p.v[so] = vv;
+    p.out[so] = to_bf16(th);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+
+template <int NR, int GK, int MAXSEG, int MAXPTR>
+__global__ void __launch_bounds__(kThreads)
+    reduce_adam_ldg_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p) {
+  const uint64_t pol = evict_first_policy();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int si = 0;
+  for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < p.total_groups;
+       gi += stride) {
+    while (gi >= p.seg[si + 1].first_group) ++si;
+    const Seg& sg = p.seg[si];
+    const int64_t e0 = (gi - sg.first_group) * kGroup;
+    const int64_t rem = sg.len - e0;
+    if (sg.vec && rem >= kGroup) {
+      group_vec<NR, GK>(p, sg, e0, pol);
+    } else {
+      group_scalar<GK>(p, sg, e0, (int)(rem < kGroup ? rem : kGroup));
+    }
+  }
+}
+
+}  // namespace dpopt
