@@ -152,7 +152,10 @@ static void adam_one(double g, float *theta, float *m, float *v, uint16_t *out,
     double v_hat = (double)v32 / h->bc2;
     double delta = h->lr * m_hat / (sqrt(v_hat) + h->eps);
     double th = (double)(*theta);
-    double th_new = th - delta - h->lr * h->weight_decay * th;
+    double th_new = th - delta;
+    if (h->weight_decay != 0.0) { /* plain Adam has no decay term at all */
+        th_new -= h->lr * h->weight_decay * th;
+    }
     float th32 = (float)th_new;
     *m = m32;
     *v = v32;
