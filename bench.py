@@ -62,6 +62,29 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def rank_workload(wl, rank: int):
+    """The workload as rank `rank` runs it: the next rank's shard of the same
+    model (ranks are ZeRO ranks; weak scaling, no data-path collective)."""
+    from dataclasses import replace
+    return replace(wl, shard_rank=(wl.shard_rank + rank) % wl.n_replicas)
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The slowest rank's value (the only cross-rank exchange of the bench)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(world: int, shard_params: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job G params/s: every rank updates shard_params per step."""
+    return world * shard_params * steps / (elapsed_ms / 1e3) / 1e9
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -255,9 +278,7 @@ def run_ours(args, wl):
     device = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=device)
-    # each rank updates its own shard of the same model (weak scaling)
-    from dataclasses import replace
-    wl = replace(wl, shard_rank=(wl.shard_rank + rank) % wl.n_replicas)
+    wl = rank_workload(wl, rank)
     S, n = wl.shard_elems, wl.n_replicas
     bpp = wl.bytes_per_param()
 
@@ -306,14 +327,10 @@ def run_ours(args, wl):
     launches = dp.dpopt_launch_count() - launches0
     clocks = sampler.stop()
     dp.stream_status(stream)
-    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, device)
     kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / K
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=device, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
     ms_per_step = elapsed_ms / K
-    value = world * S * K / (elapsed_ms / 1e3) / 1e9
+    value = throughput(world, S, K, elapsed_ms)
 
     # end to end through the public API: host gradients in, bf16 parameters out
     hs = [torch.empty(S, dtype=dev.grads[0].dtype, pin_memory=True) for _ in range(n)]
@@ -335,13 +352,9 @@ def run_ours(args, wl):
     e1.record(stream)
     torch.cuda.synchronize(device)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=device, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
     esize = dev.grads[0].element_size()
-    e2e = {"value": world * S * Ke / (e2e_ms / 1e3) / 1e9, "unit": UNIT,
+    e2e = {"value": throughput(world, S, Ke, e2e_ms), "unit": UNIT,
            "h2d_bytes_per_step": n * S * esize, "d2h_bytes_per_step": S * 2,
            "path": "pinned host gradients -> cudaMemcpyAsync -> dpopt_reduce_adam_bucket -> "
                    "bf16 parameters back to pinned host, one stream"}

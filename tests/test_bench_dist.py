@@ -1,0 +1,71 @@
+"""Host logic of the multi-rank benchmark, on CPU with gloo, world size 2:
+each rank takes its own shard, only the timing is exchanged (max over ranks),
+and only rank 0 prints."""
+from __future__ import annotations
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    wl = bench.rank_workload(synth.WORKLOADS["gpt2s"], rank)
+    slowest = bench.max_over_ranks(10.0 + 5.0 * rank, world)
+    q.put((rank, wl.shard_rank, wl.shard_base, slowest))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_ranks_take_distinct_shards_and_agree_on_the_slowest_time():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    (r0, s0, b0, t0), (r1, s1, b1, t1) = res
+    assert (s0, s1) == (0, 1) and b1 == 31_000_000 and b0 == 0
+    assert t0 == t1 == 15.0
+
+
+def test_throughput_is_the_whole_job_aggregate():
+    import bench
+    assert bench.throughput(2, 31_000_000, 100, 1000.0) == pytest.approx(6.2)
+    assert bench.throughput(1, 31_000_000, 100, 1000.0) == pytest.approx(3.1)
+
+
+def test_reference_arm_under_torchrun_prints_once_from_rank0():
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl",
+           "reference", "--gpus", "2", "--steps", "3", "--warmup", "1"]
+    out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["unit"] == "G params/s"
+    assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["cpu_baseline"]["kind"] == "oracle"
