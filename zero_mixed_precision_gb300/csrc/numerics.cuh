@@ -12,10 +12,17 @@
 //   one Newton correction of an approximate square root and quotient whose
 //           residual is formed exactly with an FMA (Markstein 1990; Karp &
 //           Markstein 1997).
-// All operations use the explicitly rounded intrinsics so that the compiler
-// neither contracts a multiply-add nor reorders anything.  When an input or a
-// result is not finite, the element falls back to the plain IEEE fp32
-// formula, which propagates Inf and NaN the way the fp64 evaluation does.
+// When an input or a result is not finite, the element falls back to the
+// plain IEEE fp32 formula, which propagates Inf and NaN the way the fp64
+// evaluation does.
+//
+// Every routine is a template over the lane type V: `float` (one element) or
+// `float2` (two elements, evaluated with the packed f32x2 instructions of
+// sm_100+).  Both instantiations perform the same sequence of correctly
+// rounded IEEE operations on every element, so an element gets bit-identical
+// results whichever path (vector body, scalar tail, unaligned range) handles
+// it.  Only explicitly rounded intrinsics are used: nothing is contracted or
+// reordered by the compiler.
 #pragma once
 
 #include <cstdint>
@@ -37,12 +44,35 @@ struct Hyper {
   float pad_;
 };
 
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = __fadd_rn(a, b);
-  float bp = __fsub_rn(s, a);
-  float ap = __fsub_rn(s, bp);
-  e = __fadd_rn(__fsub_rn(a, ap), __fsub_rn(b, bp));
-}
+// ---------------------------------------------------------------------------
+// lane-generic IEEE operations (round to nearest even)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float vadd(float a, float b) { return __fadd_rn(a, b); }
+__device__ __forceinline__ float vmul(float a, float b) { return __fmul_rn(a, b); }
+__device__ __forceinline__ float vfma(float a, float b, float c) { return __fmaf_rn(a, b, c); }
+__device__ __forceinline__ float vneg(float a) { return -a; }
+
+__device__ __forceinline__ float2 vadd(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 vmul(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 vfma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 vneg(float2 a) { return make_float2(-a.x, -a.y); }
+
+template <class V> __device__ __forceinline__ V splat(float s);
+template <> __device__ __forceinline__ float splat<float>(float s) { return s; }
+template <> __device__ __forceinline__ float2 splat<float2>(float s) { return make_float2(s, s); }
+
+template <class V> struct Lanes;
+template <> struct Lanes<float> {
+  static constexpr int n = 1;
+  __device__ static __forceinline__ float& at(float& v, int) { return v; }
+  __device__ static __forceinline__ float get(const float& v, int) { return v; }
+};
+template <> struct Lanes<float2> {
+  static constexpr int n = 2;
+  __device__ static __forceinline__ float& at(float2& v, int i) { return i ? v.y : v.x; }
+  __device__ static __forceinline__ float get(const float2& v, int i) { return i ? v.y : v.x; }
+};
 
 __device__ __forceinline__ bool finite(float x) { return fabsf(x) <= 3.402823466e38f; }
 
@@ -58,23 +88,42 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
+template <class V>
+__device__ __forceinline__ void two_sum(V a, V b, V& s, V& e) {
+  s = vadd(a, b);
+  V bp = vadd(s, vneg(a));
+  V ap = vadd(s, vneg(bp));
+  e = vadd(vadd(a, vneg(ap)), vadd(b, vneg(bp)));
+}
+
 // ---------------------------------------------------------------------------
 // Reduce: running compensated sum over the replicas in ascending order.
 // ---------------------------------------------------------------------------
 
+template <class V>
 struct CompSum {
-  float s, c;  // s + c carries the partial sum with ~48 significant bits
-  __device__ __forceinline__ void init(float x0) { s = x0; c = 0.f; }
-  __device__ __forceinline__ void add(float x) {
-    float t, e;
+  V s, c;  // s + c carries the partial sum with ~48 significant bits
+  __device__ __forceinline__ void init(V x0) {
+    s = x0;
+    c = splat<V>(0.f);
+  }
+  __device__ __forceinline__ void add(V x) {
+    V t, e;
     two_sum(s, x, t, e);
     s = t;
-    c = __fadd_rn(c, e);
+    c = vadd(c, e);
   }
   // fl32(sum) then / N.  A non-finite running sum is returned as it is.
-  __device__ __forceinline__ float average(const Hyper& h) const {
-    float tot = finite(s) ? __fadd_rn(s, c) : s;
-    return h.inv_n != 0.f ? __fmul_rn(tot, h.inv_n) : __fdiv_rn(tot, h.n_f);
+  __device__ __forceinline__ V average(const Hyper& h) const {
+    V tot = vadd(s, c);
+#pragma unroll
+    for (int i = 0; i < Lanes<V>::n; ++i)
+      if (!finite(Lanes<V>::get(s, i))) Lanes<V>::at(tot, i) = Lanes<V>::get(s, i);
+    if (h.inv_n != 0.f) return vmul(tot, splat<V>(h.inv_n));
+#pragma unroll
+    for (int i = 0; i < Lanes<V>::n; ++i)
+      Lanes<V>::at(tot, i) = __fdiv_rn(Lanes<V>::get(tot, i), h.n_f);
+    return tot;
   }
 };
 
@@ -83,84 +132,108 @@ struct CompSum {
 // ---------------------------------------------------------------------------
 
 // m' = beta1*m + (1-beta1)*g
-__device__ __forceinline__ float moment1(float m, float g, const Hyper& h) {
-  float p1 = __fmul_rn(h.beta1, m);
-  float e1 = __fmaf_rn(h.beta1, m, -p1);
-  float p2 = __fmul_rn(h.c1_hi, g);
-  float e2 = __fmaf_rn(h.c1_lo, g, __fmaf_rn(h.c1_hi, g, -p2));
-  float s, e3;
+template <class V>
+__device__ __forceinline__ V moment1(V m, V g, const Hyper& h) {
+  const V b1 = splat<V>(h.beta1), c1h = splat<V>(h.c1_hi), c1l = splat<V>(h.c1_lo);
+  V p1 = vmul(b1, m);
+  V e1 = vfma(b1, m, vneg(p1));
+  V p2 = vmul(c1h, g);
+  V e2 = vfma(c1l, g, vfma(c1h, g, vneg(p2)));
+  V s, e3;
   two_sum(p1, p2, s, e3);
-  float r = __fadd_rn(s, __fadd_rn(__fadd_rn(e1, e2), e3));
-  if (!finite(r)) r = __fmaf_rn(h.beta1, m, __fmul_rn(h.c1_hi, g));
+  V r = vadd(s, vadd(vadd(e1, e2), e3));
+#pragma unroll
+  for (int i = 0; i < Lanes<V>::n; ++i)
+    if (!finite(Lanes<V>::get(r, i)))
+      Lanes<V>::at(r, i) = __fmaf_rn(h.beta1, Lanes<V>::get(m, i), Lanes<V>::get(p2, i));
   return r;
 }
 
 // v' = beta2*v + (1-beta2)*g*g, formed as ((1-beta2)*g)*g so that the square
 // overflows only where the rounded result itself would.
-__device__ __forceinline__ float moment2(float v, float g, const Hyper& h) {
-  float P = __fmul_rn(h.c2_hi, g);
-  float Pe = __fmaf_rn(h.c2_lo, g, __fmaf_rn(h.c2_hi, g, -P));
-  float p2 = __fmul_rn(P, g);
-  float e2 = __fmaf_rn(Pe, g, __fmaf_rn(P, g, -p2));
-  float p1 = __fmul_rn(h.beta2, v);
-  float e1 = __fmaf_rn(h.beta2, v, -p1);
-  float s, e3;
+template <class V>
+__device__ __forceinline__ V moment2(V v, V g, const Hyper& h) {
+  const V b2 = splat<V>(h.beta2), c2h = splat<V>(h.c2_hi), c2l = splat<V>(h.c2_lo);
+  V P = vmul(c2h, g);
+  V Pe = vfma(c2l, g, vfma(c2h, g, vneg(P)));
+  V p2 = vmul(P, g);
+  V e2 = vfma(Pe, g, vfma(P, g, vneg(p2)));
+  V p1 = vmul(b2, v);
+  V e1 = vfma(b2, v, vneg(p1));
+  V s, e3;
   two_sum(p1, p2, s, e3);
-  float r = __fadd_rn(s, __fadd_rn(__fadd_rn(e1, e2), e3));
-  if (!finite(r)) r = __fmaf_rn(h.beta2, v, p2);
+  V r = vadd(s, vadd(vadd(e1, e2), e3));
+#pragma unroll
+  for (int i = 0; i < Lanes<V>::n; ++i)
+    if (!finite(Lanes<V>::get(r, i)))
+      Lanes<V>::at(r, i) = __fmaf_rn(h.beta2, Lanes<V>::get(v, i), Lanes<V>::get(p2, i));
   return r;
 }
 
 // theta' = theta - lr * (m'/bc1) / (sqrt(v'/bc2) + eps), the plain fp32 form,
 // used for non-finite inputs or results.
 __device__ __noinline__ float master_update_plain(float theta, float m_new, float v_new,
-                                                  Hyper h) {
-  float d = __fadd_rn(__fmul_rn(__fsqrt_rn(v_new), h.b_hi), h.eps);
-  float delta = __fdiv_rn(__fmul_rn(h.a_hi, m_new), d);
+                                                  float a_hi, float b_hi, float eps) {
+  float d = __fadd_rn(__fmul_rn(__fsqrt_rn(v_new), b_hi), eps);
+  float delta = __fdiv_rn(__fmul_rn(a_hi, m_new), d);
   return __fsub_rn(theta, delta);
 }
 
 // theta' = theta - a*m' / (b*sqrt(v') + eps) with a = lr/bc1, b = 1/sqrt(bc2),
 // the quotient carried as q + q_lo and the subtraction rounded once.
-__device__ __forceinline__ float master_update(float theta, float m_new, float v_new,
-                                               const Hyper& h) {
-  float s, s_lo;
-  if (v_new >= 0x1p-100f && v_new <= 3.402823466e38f) {
-    float y = rsqrt_approx(v_new);
-    s = __fmul_rn(v_new, y);
-    float r = __fmaf_rn(-s, s, v_new);
-    s_lo = __fmul_rn(r, __fmul_rn(0.5f, y));
-  } else {
-    s = __fsqrt_rn(v_new);
-    s_lo = 0.f;
+template <class V>
+__device__ __forceinline__ V master_update(V theta, V m_new, V v_new, const Hyper& h) {
+  constexpr int L = Lanes<V>::n;
+  // sqrt(v') as s + s_lo: approximate reciprocal square root, one correction
+  V y;
+#pragma unroll
+  for (int i = 0; i < L; ++i) Lanes<V>::at(y, i) = rsqrt_approx(Lanes<V>::get(v_new, i));
+  V s = vmul(v_new, y);
+  V rr = vfma(vneg(s), s, v_new);
+  V s_lo = vmul(rr, vmul(splat<V>(0.5f), y));
+#pragma unroll
+  for (int i = 0; i < L; ++i) {
+    const float vi = Lanes<V>::get(v_new, i);
+    if (!(vi >= 0x1p-100f && vi <= 3.402823466e38f)) {  // zero, tiny, Inf, NaN
+      Lanes<V>::at(s, i) = __fsqrt_rn(vi);
+      Lanes<V>::at(s_lo, i) = 0.f;
+    }
   }
   // D = b*sqrt(v') + eps as D + D_lo
-  float p = __fmul_rn(s, h.b_hi);
-  float pe = __fmaf_rn(s, h.b_hi, -p);
-  float lo = __fmaf_rn(s, h.b_lo, __fmaf_rn(s_lo, h.b_hi, pe));
-  float D, de;
-  two_sum(p, h.eps, D, de);
-  float D_lo = __fadd_rn(lo, de);
+  const V bh = splat<V>(h.b_hi), bl = splat<V>(h.b_lo);
+  V p = vmul(s, bh);
+  V pe = vfma(s, bh, vneg(p));
+  V lo = vfma(s, bl, vfma(s_lo, bh, pe));
+  V D, de;
+  two_sum(p, splat<V>(h.eps), D, de);
+  V D_lo = vadd(lo, de);
   // numerator a*m' as n + n_lo
-  float n = __fmul_rn(h.a_hi, m_new);
-  float n_lo = __fmaf_rn(h.a_lo, m_new, __fmaf_rn(h.a_hi, m_new, -n));
-  // quotient q + q_lo = (n + n_lo) / (D + D_lo)
-  float rD = rcp_approx(D);
-  float q = __fmul_rn(n, rD);
-  float r = __fmaf_rn(-q, D, n);
-  r = __fmaf_rn(-q, D_lo, __fadd_rn(r, n_lo));
-  float q_lo = __fmul_rn(r, rD);
+  const V ah = splat<V>(h.a_hi), al = splat<V>(h.a_lo);
+  V n = vmul(ah, m_new);
+  V n_lo = vfma(al, m_new, vfma(ah, m_new, vneg(n)));
+  // quotient q + q_lo = (n + n_lo) / (D + D_lo): approximate reciprocal, one correction
+  V rD;
+#pragma unroll
+  for (int i = 0; i < L; ++i) Lanes<V>::at(rD, i) = rcp_approx(Lanes<V>::get(D, i));
+  V q = vmul(n, rD);
+  V r = vfma(vneg(q), D, n);
+  r = vfma(vneg(q), D_lo, vadd(r, n_lo));
+  V q_lo = vmul(r, rD);
   // theta - (q + q_lo), rounded once
-  float t, te;
-  two_sum(theta, -q, t, te);
-  float th = __fadd_rn(t, __fsub_rn(te, q_lo));
-  if (!finite(th) || !finite(q_lo)) th = master_update_plain(theta, m_new, v_new, h);
+  V t, te;
+  two_sum(theta, vneg(q), t, te);
+  V th = vadd(t, vadd(te, vneg(q_lo)));
+#pragma unroll
+  for (int i = 0; i < L; ++i)
+    if (!finite(Lanes<V>::get(th, i)) || !finite(Lanes<V>::get(q_lo, i)))
+      Lanes<V>::at(th, i) = master_update_plain(Lanes<V>::get(theta, i), Lanes<V>::get(m_new, i),
+                                                Lanes<V>::get(v_new, i), h.a_hi, h.b_hi, h.eps);
   return th;
 }
 
-// One element of the step after the reduce: updates theta, m, v in place.
-__device__ __forceinline__ void adam_element(float g, float& theta, float& m, float& v,
-                                             const Hyper& h) {
+// One step after the reduce: updates theta, m, v in place.
+template <class V>
+__device__ __forceinline__ void adam_update(V g, V& theta, V& m, V& v, const Hyper& h) {
   m = moment1(m, g, h);
   v = moment2(v, g, h);
   theta = master_update(theta, m, v, h);
@@ -180,7 +253,11 @@ __device__ __forceinline__ uint32_t to_bf16x2(float lo, float hi) {
   return w;
 }
 
+// bf16 -> fp32 is exact: the 16 bits become the top half of a binary32.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+  return make_float2(bf16_lo(w), bf16_hi(w));
+}
 
 }  // namespace dpopt
