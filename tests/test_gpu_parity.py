@@ -201,9 +201,12 @@ def test_wide_exponent_gradients_every_element():
 # entry points, buckets, shards: bitwise invariances
 # ---------------------------------------------------------------------------
 
-def test_bucket_entries_match_full_buffer_bitwise():
+@pytest.mark.parametrize("n", [4, 13, 16])
+def test_bucket_entries_match_full_buffer_bitwise(n):
+    """Bucket sizes move elements between the vector body (scalar or packed
+    lanes) and the scalar tail path; every split must give the same bits."""
     _need_gpu()
-    wl = _small_workload(4, 50_021, rank=2)
+    wl = _small_workload(n, 50_021, rank=2)
     ref = _run_small_full(wl, entry="full")
     for entry, bucket in (("full", 1), ("full", 4096), ("bucket", 7), ("bucket", 4096),
                           ("buckets", 3), ("buckets", 1000), ("buckets", 50_021)):

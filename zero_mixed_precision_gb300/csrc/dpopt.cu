@@ -153,9 +153,9 @@ struct SegDesc {
   int64_t len;
 };
 
-template <int NR, int GK, int MS, int MP>
+template <int NR, int GK, int PACK, int MS, int MP>
 int launch_one(const LaunchParams<MS, MP>& p, cudaStream_t stream) {
-  auto kern = reduce_adam_ldg_kernel<NR, GK, MS, MP>;
+  auto kern = reduce_adam_ldg_kernel<NR, GK, PACK, MS, MP>;
   int sms = 0;
   int rc = sm_count(&sms);
   if (rc) return rc;
@@ -177,31 +177,29 @@ int launch_one(const LaunchParams<MS, MP>& p, cudaStream_t stream) {
   return DPOPT_OK;
 }
 
-template <int MS, int MP>
-int dispatch(const LaunchParams<MS, MP>& p, int grad_dtype, cudaStream_t stream) {
+// Kernel choice by measurement on GB300: the scalar-lane body for N <= 8
+// (optimizer arithmetic dominates), the packed f32x2 body above (the replica
+// sum dominates); N in {1, 2, 4, 8} get a fully unrolled replica loop.
+template <int GK, int MS, int MP>
+int dispatch_gk(const LaunchParams<MS, MP>& p, cudaStream_t stream) {
   const int n = p.n_rep;
-  if (grad_dtype == DPOPT_GRAD_BF16) {
-    if constexpr (MS == kSmallSegs) {
-      switch (n) {
-        case 1: return launch_one<1, 0>(p, stream);
-        case 2: return launch_one<2, 0>(p, stream);
-        case 4: return launch_one<4, 0>(p, stream);
-        case 8: return launch_one<8, 0>(p, stream);
-        default: break;
-      }
-    }
-    return launch_one<0, 0>(p, stream);
-  }
   if constexpr (MS == kSmallSegs) {
     switch (n) {
-      case 1: return launch_one<1, 1>(p, stream);
-      case 2: return launch_one<2, 1>(p, stream);
-      case 4: return launch_one<4, 1>(p, stream);
-      case 8: return launch_one<8, 1>(p, stream);
+      case 1: return launch_one<1, GK, 0>(p, stream);
+      case 2: return launch_one<2, GK, 0>(p, stream);
+      case 4: return launch_one<4, GK, 0>(p, stream);
+      case 8: return launch_one<8, GK, 0>(p, stream);
       default: break;
     }
   }
-  return launch_one<0, 1>(p, stream);
+  if (n <= 8) return launch_one<0, GK, 0>(p, stream);
+  return launch_one<0, GK, 1>(p, stream);
+}
+
+template <int MS, int MP>
+int dispatch(const LaunchParams<MS, MP>& p, int grad_dtype, cudaStream_t stream) {
+  if (grad_dtype == DPOPT_GRAD_BF16) return dispatch_gk<0>(p, stream);
+  return dispatch_gk<1>(p, stream);
 }
 
 // Fill and launch one LaunchParams from segments [s0, s1).

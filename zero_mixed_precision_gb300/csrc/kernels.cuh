@@ -96,6 +96,10 @@ struct GradLoad<0> {
     w = ld_grad16(static_cast<const uint16_t*>(base) + e0, pol);
   }
   __device__ __forceinline__ void zero() { w = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ float get(int k) const {
+    uint32_t x = (k < 2) ? w.x : (k < 4) ? w.y : (k < 6) ? w.z : w.w;
+    return (k & 1) ? bf16_hi(x) : bf16_lo(x);
+  }
   // elements 2j and 2j+1
   __device__ __forceinline__ float2 pair(int j) const {
     return bf16x2_to_float2(j == 0 ? w.x : j == 1 ? w.y : j == 2 ? w.z : w.w);
@@ -111,6 +115,11 @@ struct GradLoad<1> {
     b = ld_grad16(p + 4, pol);
   }
   __device__ __forceinline__ void zero() { a = b = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ float get(int k) const {
+    const uint4& q = (k < 4) ? a : b;
+    int j = k & 3;
+    return __uint_as_float(j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w);
+  }
   __device__ __forceinline__ float2 pair(int j) const {
     const uint4& q = (j < 2) ? a : b;
     return (j & 1) ? make_float2(__uint_as_float(q.z), __uint_as_float(q.w))
@@ -132,8 +141,82 @@ __device__ __forceinline__ float ld_grad1(const void* base, int64_t e) {
 // one 8-element group, vector path
 // ---------------------------------------------------------------------------
 
+// Scalar-lane form: 8 elements per thread, one element per operation.  Fewer
+// register pairings; faster when the optimizer arithmetic dominates (small N).
 template <int NR, int GK, class LP>
-__device__ __forceinline__ void group_vec(const LP& p, const Seg& sg, int64_t e0, uint64_t pol) {
+__device__ __forceinline__ void group_vec_x1(const LP& p, const Seg& sg, int64_t e0,
+                                             uint64_t pol) {
+  const int64_t so = sg.state_off + e0;
+  float th[kGroup], mm[kGroup], vv[kGroup];
+  {
+    float4 a = ld_state16(p.master + so), b = ld_state16(p.master + so + 4);
+    th[0] = a.x; th[1] = a.y; th[2] = a.z; th[3] = a.w;
+    th[4] = b.x; th[5] = b.y; th[6] = b.z; th[7] = b.w;
+    a = ld_state16(p.m + so); b = ld_state16(p.m + so + 4);
+    mm[0] = a.x; mm[1] = a.y; mm[2] = a.z; mm[3] = a.w;
+    mm[4] = b.x; mm[5] = b.y; mm[6] = b.z; mm[7] = b.w;
+    a = ld_state16(p.v + so); b = ld_state16(p.v + so + 4);
+    vv[0] = a.x; vv[1] = a.y; vv[2] = a.z; vv[3] = a.w;
+    vv[4] = b.x; vv[5] = b.y; vv[6] = b.z; vv[7] = b.w;
+  }
+  const void* const* gp = p.gptr + sg.ptr_base;
+  CompSum<float> acc[kGroup];
+  if constexpr (NR > 0) {
+    GradLoad<GK> gl[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) gl[r].load(gp[r], e0, pol);
+#pragma unroll
+    for (int k = 0; k < kGroup; ++k) acc[k].init(gl[0].get(k));
+#pragma unroll
+    for (int r = 1; r < NR; ++r) {
+#pragma unroll
+      for (int k = 0; k < kGroup; ++k) acc[k].add(gl[r].get(k));
+    }
+  } else {
+    // runtime replica count: chunks of 8 replicas, loads of a chunk in flight together
+    constexpr int C = 8;
+    const int n = p.n_rep;
+    for (int r0 = 0; r0 < n; r0 += C) {
+      GradLoad<GK> gl[C];
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        if (r0 + j < n) gl[j].load(gp[r0 + j], e0, pol);
+        else gl[j].zero();
+      }
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        if (r0 + j < n) {
+          if (r0 + j == 0) {
+#pragma unroll
+            for (int k = 0; k < kGroup; ++k) acc[k].init(gl[j].get(k));
+          } else {
+#pragma unroll
+            for (int k = 0; k < kGroup; ++k) acc[k].add(gl[j].get(k));
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kGroup; ++k) {
+    float g = acc[k].average(p.h);
+    adam_update(g, th[k], mm[k], vv[k], p.h);
+  }
+  st_stream16(p.master + so, th[0], th[1], th[2], th[3]);
+  st_stream16(p.master + so + 4, th[4], th[5], th[6], th[7]);
+  st_stream16(p.m + so, mm[0], mm[1], mm[2], mm[3]);
+  st_stream16(p.m + so + 4, mm[4], mm[5], mm[6], mm[7]);
+  st_stream16(p.v + so, vv[0], vv[1], vv[2], vv[3]);
+  st_stream16(p.v + so + 4, vv[4], vv[5], vv[6], vv[7]);
+  st_stream16u(p.out + so, to_bf16x2(th[0], th[1]), to_bf16x2(th[2], th[3]),
+               to_bf16x2(th[4], th[5]), to_bf16x2(th[6], th[7]));
+}
+
+// Packed form: 4 element pairs per thread, every operation on f32x2 lanes.
+// Pays off when the replica sum dominates (large N).
+template <int NR, int GK, class LP>
+__device__ __forceinline__ void group_vec_x2(const LP& p, const Seg& sg, int64_t e0,
+                                             uint64_t pol) {
   constexpr int P = kGroup / 2;  // element pairs per group
   const int64_t so = sg.state_off + e0;
   float2 th[P], mm[P], vv[P];
@@ -250,13 +333,15 @@ __device__ __noinline__ void group_scalar(const LP& p, const Seg& sg, int64_t e0
 // the kernel
 // ---------------------------------------------------------------------------
 
-// Resident CTAs per SM the register budget is sized for: 4 x 256 threads for
-// the unrolled replica counts (<= 64 registers), 2 for the generic one.
-template <int NR>
-constexpr int min_ctas() { return NR > 0 ? 4 : 2; }
+// Resident CTAs per SM the packed form's register budget is sized for: 4 x 256
+// threads (<= 64 registers) with an unrolled replica count, 2 for a runtime one.
+template <int NR, int PACK>
+constexpr int min_ctas() { return NR > 0 ? 4 : (PACK ? 2 : 1); }
 
-template <int NR, int GK, int MAXSEG, int MAXPTR>
-__global__ void __launch_bounds__(kThreads, min_ctas<NR>())
+// PACK selects the lane form of the vector body (0: scalar, 1: f32x2); the
+// two forms give identical bits, so the choice is made by speed alone.
+template <int NR, int GK, int PACK, int MAXSEG, int MAXPTR>
+__global__ void __launch_bounds__(kThreads, min_ctas<NR, PACK>())
     reduce_adam_ldg_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p) {
   const uint64_t pol = evict_first_policy();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -268,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas<NR>())
     const int64_t e0 = (gi - sg.first_group) * kGroup;
     const int64_t rem = sg.len - e0;
     if (sg.vec && rem >= kGroup) {
-      group_vec<NR, GK>(p, sg, e0, pol);
+      if constexpr (PACK) group_vec_x2<NR, GK>(p, sg, e0, pol);
+      else group_vec_x1<NR, GK>(p, sg, e0, pol);
     } else {
       group_scalar<GK>(p, sg, e0, (int)(rem < kGroup ? rem : kGroup));
     }

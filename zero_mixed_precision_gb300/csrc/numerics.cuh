@@ -231,6 +231,42 @@ __device__ __forceinline__ V master_update(V theta, V m_new, V v_new, const Hype
   return th;
 }
 
+// The single-lane form of master_update, written with a branch instead of
+// lane selects (fewer live registers); the same operations on every element.
+template <>
+__device__ __forceinline__ float master_update<float>(float theta, float m_new, float v_new,
+                                                      const Hyper& h) {
+  float s, s_lo;
+  if (v_new >= 0x1p-100f && v_new <= 3.402823466e38f) {
+    float y = rsqrt_approx(v_new);
+    s = __fmul_rn(v_new, y);
+    float rr = __fmaf_rn(-s, s, v_new);
+    s_lo = __fmul_rn(rr, __fmul_rn(0.5f, y));
+  } else {
+    s = __fsqrt_rn(v_new);
+    s_lo = 0.f;
+  }
+  float p = __fmul_rn(s, h.b_hi);
+  float pe = __fmaf_rn(s, h.b_hi, -p);
+  float lo = __fmaf_rn(s, h.b_lo, __fmaf_rn(s_lo, h.b_hi, pe));
+  float D, de;
+  two_sum(p, h.eps, D, de);
+  float D_lo = __fadd_rn(lo, de);
+  float n = __fmul_rn(h.a_hi, m_new);
+  float n_lo = __fmaf_rn(h.a_lo, m_new, __fmaf_rn(h.a_hi, m_new, -n));
+  float rD = rcp_approx(D);
+  float q = __fmul_rn(n, rD);
+  float r = __fmaf_rn(-q, D, n);
+  r = __fmaf_rn(-q, D_lo, __fadd_rn(r, n_lo));
+  float q_lo = __fmul_rn(r, rD);
+  float t, te;
+  two_sum(theta, -q, t, te);
+  float th = __fadd_rn(t, __fadd_rn(te, -q_lo));
+  if (!finite(th) || !finite(q_lo))
+    th = master_update_plain(theta, m_new, v_new, h.a_hi, h.b_hi, h.eps);
+  return th;
+}
+
 // One step after the reduce: updates theta, m, v in place.
 template <class V>
 __device__ __forceinline__ void adam_update(V g, V& theta, V& m, V& v, const Hyper& h) {
