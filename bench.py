@@ -54,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=("auto", "direct", "bulk"), default="auto",
+                    help="kernel policy of the library (both give identical results)")
     return ap.parse_args(argv)
 
 
@@ -212,7 +214,7 @@ def host_grads_for(wl, max_elems: int):
                             wl.grad_dist(r)) for r in range(wl.n_replicas)]
 
 
-def config_of(wl):
+def config_of(wl, kernel=None):
     return {"workload": f"{wl.name}: {wl.numel:,} params per replica buffer, N={wl.n_replicas} "
                         f"replicas, rank {wl.shard_rank} shard of {wl.shard_elems:,} params, "
                         f"{wl.bucket_elems:,}-element buckets, "
@@ -222,7 +224,8 @@ def config_of(wl):
             "bytes_per_param": wl.bytes_per_param(),
             "l2": f"inputs larger than L2: {wl.shard_elems * wl.bytes_per_param() / 1e9:.3f} GB "
                   "touched per step vs a 129 MB L2 (no flush)",
-            "parallelism": "one shard per GPU, no data-path collective"}
+            "parallelism": "one shard per GPU, no data-path collective",
+            **({"kernel_policy": kernel} if kernel else {})}
 
 
 # ---------------------------------------------------------------------------
@@ -279,6 +282,8 @@ def run_ours(args, wl):
     if world > 1:
         dist.init_process_group("nccl", device_id=device)
     wl = rank_workload(wl, rank)
+    dp.dpopt_set_kernel_policy({"auto": dp.DPOPT_KERNEL_AUTO, "direct": dp.DPOPT_KERNEL_DIRECT,
+                                "bulk": dp.DPOPT_KERNEL_BULK}[args.kernel])
     S, n = wl.shard_elems, wl.n_replicas
     bpp = wl.bytes_per_param()
 
@@ -394,7 +399,7 @@ def _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded counter-based generator, generated in HBM)",
-        "config": config_of(wl),
+        "config": config_of(wl, args.kernel),
         "hbm_gbs": S * bpp / (ms_per_step / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth",

@@ -181,6 +181,24 @@ const char *dpopt_last_error(void);
  * stage, or a null bytes_out.  Host-only. */
 int dpopt_state_bytes(int64_t psi, int variant, int n_dp, int zero_stage, double *bytes_out);
 
+/* Which kernel carries the step (process-wide; default DPOPT_KERNEL_AUTO).
+ *  DPOPT_KERNEL_AUTO    the faster of the two for the replica count, by measurement
+ *  DPOPT_KERNEL_DIRECT  direct 16-byte loads from global memory into registers
+ *  DPOPT_KERNEL_BULK    bulk copies (TMA) into a shared-memory ring, where it applies
+ *                       (every pointer 16-byte aligned, n_replicas <= 16); other calls
+ *                       still take the direct-load kernel
+ * Both kernels give bitwise identical results.  Errors: DPOPT_ERR_INVALID_ARG for an
+ * unknown value. */
+typedef enum { DPOPT_KERNEL_AUTO = 0, DPOPT_KERNEL_DIRECT = 1, DPOPT_KERNEL_BULK = 2 } dpopt_kernel_policy;
+int dpopt_set_kernel_policy(int policy);
+int dpopt_get_kernel_policy(void);
+
+/* Diagnostic: enqueue a kernel whose one bounded wait can never be satisfied, so
+ * that it gives up after limit_cycles GPU clock cycles (1 .. 2e9) and sets the
+ * device status word; dpopt_stream_status() then returns DPOPT_ERR_TIMEOUT.  Lets
+ * a caller check that time-outs are reported and that the context stays usable. */
+int dpopt_selftest_wait_timeout(int64_t limit_cycles, dpopt_stream_t stream);
+
 /* Kernel launches this library has made from the calling host thread since
  * the thread started (a running count; the caller takes differences). */
 int64_t dpopt_launch_count(void);

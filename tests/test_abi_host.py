@@ -129,6 +129,19 @@ def test_full_buffer_entry_rejects_bad_arguments(dp, over, code):
     assert dp.dpopt_last_error() != ""
 
 
+def test_kernel_policy_round_trip_and_rejects_unknown(dp):
+    assert dp.dpopt_get_kernel_policy() == dp.DPOPT_KERNEL_AUTO
+    for pol in (dp.DPOPT_KERNEL_DIRECT, dp.DPOPT_KERNEL_BULK, dp.DPOPT_KERNEL_AUTO):
+        assert dp.dpopt_set_kernel_policy(pol) == 0 and dp.dpopt_get_kernel_policy() == pol
+    assert dp.dpopt_set_kernel_policy(7) == dp.DPOPT_ERR_INVALID_ARG
+    assert dp.dpopt_get_kernel_policy() == dp.DPOPT_KERNEL_AUTO
+
+
+def test_selftest_rejects_out_of_range_limits(dp):
+    assert dp.dpopt_selftest_wait_timeout(0, 0) == dp.DPOPT_ERR_INVALID_ARG
+    assert dp.dpopt_selftest_wait_timeout(3_000_000_000, 0) == dp.DPOPT_ERR_INVALID_ARG
+
+
 def test_null_grads_table_is_rejected(dp):
     assert dp.dpopt_reduce_adam(None, 2, 8, 0, 4, MASTER, M, V, OUT, *HP, 1, 0) == 1
 

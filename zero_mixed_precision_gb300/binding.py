@@ -23,6 +23,9 @@ DPOPT_ERR_TIMEOUT = 4
 DPOPT_GRAD_BF16 = 0
 DPOPT_GRAD_F32 = 1
 DPOPT_MAX_REPLICAS = 64
+DPOPT_KERNEL_AUTO = 0
+DPOPT_KERNEL_DIRECT = 1
+DPOPT_KERNEL_BULK = 2
 
 LIB_PATH = _build.LIB_PATH
 
@@ -56,6 +59,9 @@ _SIGS = {
     "dpopt_state_bytes": ([_I64, _I, _I, _I, ctypes.POINTER(ctypes.c_double)], _I),
     "dpopt_version": ([], ctypes.c_char_p),
     "dpopt_launch_count": ([], _I64),
+    "dpopt_set_kernel_policy": ([_I], _I),
+    "dpopt_get_kernel_policy": ([], _I),
+    "dpopt_selftest_wait_timeout": ([_I64, _P], _I),
 }
 
 for _name, (_args, _res) in _SIGS.items():
@@ -160,6 +166,18 @@ def dpopt_launch_count() -> int:
     return int(_lib.dpopt_launch_count())
 
 
+def dpopt_set_kernel_policy(policy: int) -> int:
+    return _lib.dpopt_set_kernel_policy(policy)
+
+
+def dpopt_get_kernel_policy() -> int:
+    return _lib.dpopt_get_kernel_policy()
+
+
+def dpopt_selftest_wait_timeout(limit_cycles: int, stream: int = 0) -> int:
+    return _lib.dpopt_selftest_wait_timeout(limit_cycles, stream)
+
+
 # ---------------------------------------------------------------------------
 # torch-tensor wrappers (marshalling only)
 # ---------------------------------------------------------------------------
@@ -225,3 +243,19 @@ def reduce_adam_buckets(bucket_slices, offsets, master, m, v, param_bf16_out, *,
 
 def stream_status(stream=None) -> None:
     _check(dpopt_stream_status(_stream_handle(stream)), "dpopt_stream_status")
+
+
+class kernel_policy:
+    """Context manager: run the enclosed calls with a given kernel policy."""
+
+    def __init__(self, policy: int):
+        self.policy = policy
+
+    def __enter__(self):
+        self.saved = dpopt_get_kernel_policy()
+        _check(dpopt_set_kernel_policy(self.policy), "dpopt_set_kernel_policy")
+        return self
+
+    def __exit__(self, *exc):
+        dpopt_set_kernel_policy(self.saved)
+        return False

@@ -13,6 +13,7 @@
 
 #include "dpopt.h"
 #include "kernels.cuh"
+#include "tma.cuh"
 
 namespace dpopt {
 namespace {
@@ -25,10 +26,20 @@ constexpr int kMaxDevices = 64;
 
 using SmallParams = LaunchParams<kSmallSegs, kSmallPtrs>;
 using BigParams = LaunchParams<kBigSegs, kBigPtrs>;
+using SmallTma = TmaParams<kSmallSegs, kSmallPtrs>;
+using BigTma = TmaParams<kBigSegs, kBigPtrs>;
 static_assert(sizeof(BigParams) <= 32000, "kernel parameters must fit the 32 KB limit");
+static_assert(sizeof(BigTma) <= 32000, "kernel parameters must fit the 32 KB limit");
 
-// Sticky per-device status word for bounded device-side waits.
-__device__ unsigned int g_status;
+// Bulk-copy kernel: shared memory budget for the stage ring of one CTA, the
+// largest replica count it serves, and how long one bounded wait may spin.
+constexpr uint32_t kTmaSmemBudget = 200 * 1024;
+constexpr int kTmaMaxReplicas = 16;
+constexpr long long kWaitLimitCycles = 2000000000LL;  // about one second
+// Under DPOPT_KERNEL_AUTO the bulk-copy kernel serves N up to this (measured).
+constexpr int kTmaAutoMaxReplicas = 8;
+
+std::atomic<int> g_policy{DPOPT_KERNEL_AUTO};
 
 thread_local char g_last_error[512];
 thread_local int64_t g_launches = 0;
@@ -205,7 +216,7 @@ int dispatch(const LaunchParams<MS, MP>& p, int grad_dtype, cudaStream_t stream)
 // Fill and launch one LaunchParams from segments [s0, s1).
 template <int MS, int MP>
 int run_segments(LaunchParams<MS, MP>& p, const SegDesc* segs, int s0, int s1, int n,
-                 size_t esize, cudaStream_t stream, int grad_dtype) {
+                 cudaStream_t stream, int grad_dtype) {
   int64_t groups = 0;
   int nseg = 0;
   for (int s = s0; s < s1; ++s) {
@@ -222,7 +233,6 @@ int run_segments(LaunchParams<MS, MP>& p, const SegDesc* segs, int s0, int s1, i
       p.gptr[nseg * n + r] = d.ptrs[r];
       vec = vec && aligned16(d.ptrs[r]);
     }
-    (void)esize;
     sg.vec = vec ? 1 : 0;
     groups += (d.len + kGroup - 1) / kGroup;
     ++nseg;
@@ -235,25 +245,146 @@ int run_segments(LaunchParams<MS, MP>& p, const SegDesc* segs, int s0, int s1, i
   return dispatch(p, grad_dtype, stream);
 }
 
+// ---------------------------------------------------------------------------
+// bulk-copy kernel launch
+// ---------------------------------------------------------------------------
+
+template <int NR, int GK, int PACK, int MS, int MP>
+int launch_tma(const TmaParams<MS, MP>& p, cudaStream_t stream) {
+  auto kern = reduce_adam_tma_kernel<NR, GK, PACK, MS, MP>;
+  const size_t dyn = (size_t)p.stages * p.stage_bytes;
+  static std::atomic<size_t> configured{0};
+  if (configured.load(std::memory_order_relaxed) < dyn) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(kTmaSmemBudget + 1024));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    configured.store(kTmaSmemBudget + 1024, std::memory_order_relaxed);
+  }
+  int sms = 0;
+  int rc = sm_count(&sms);
+  if (rc) return rc;
+  int bps = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, kTmaThreads, dyn);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  if (bps < 1) return fail(DPOPT_ERR_UNSUPPORTED, "bulk-copy kernel does not fit an SM");
+  const int64_t want = std::max<int64_t>(p.total_tiles, (int64_t)p.nseg);
+  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * bps));
+  kern<<<grid, kTmaThreads, dyn, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  ++g_launches;
+  return DPOPT_OK;
+}
+
+template <int GK, int MS, int MP>
+int dispatch_tma_gk(const TmaParams<MS, MP>& p, cudaStream_t stream) {
+  switch (p.n_rep) {
+    case 1: return launch_tma<1, GK, 0>(p, stream);
+    case 2: return launch_tma<2, GK, 0>(p, stream);
+    case 4: return launch_tma<4, GK, 0>(p, stream);
+    case 8: return launch_tma<8, GK, 0>(p, stream);
+    default: break;
+  }
+  if (p.n_rep <= 8) return launch_tma<0, GK, 0>(p, stream);
+  return launch_tma<0, GK, 1>(p, stream);
+}
+
+// Whether segments [s0, s1) can go through the bulk-copy kernel: every
+// pointer 16-byte aligned and the replica count within its shared memory.
+bool tma_eligible(const SegDesc* segs, int s0, int s1, int n, int grad_dtype, float* master,
+                  float* m, float* v, void* out) {
+  if (n > kTmaMaxReplicas) return false;
+  const uint32_t gsize = grad_dtype == DPOPT_GRAD_BF16 ? 2u : 4u;
+  if (2u * (uint32_t)kTmaTile * ((uint32_t)n * gsize + 12u) > kTmaSmemBudget) return false;
+  for (int s = s0; s < s1; ++s) {
+    const SegDesc& d = segs[s];
+    if (d.len == 0) continue;
+    if (!aligned16(master + d.state_off) || !aligned16(m + d.state_off) ||
+        !aligned16(v + d.state_off) || !aligned16((uint16_t*)out + d.state_off))
+      return false;
+    for (int r = 0; r < n; ++r)
+      if (!aligned16(d.ptrs[r])) return false;
+  }
+  return true;
+}
+
+template <int MS, int MP>
+int run_segments_tma(TmaParams<MS, MP>& p, const SegDesc* segs, int s0, int s1, int n,
+                     cudaStream_t stream, int grad_dtype) {
+  const uint32_t gsize = grad_dtype == DPOPT_GRAD_BF16 ? 2u : 4u;
+  int64_t tiles = 0;
+  int nseg = 0;
+  for (int s = s0; s < s1; ++s) {
+    const SegDesc& d = segs[s];
+    if (d.len == 0) continue;
+    TmaSeg& sg = p.seg[nseg];
+    sg.first_tile = tiles;
+    sg.state_off = d.state_off;
+    sg.len = d.len;
+    sg.body = d.len & ~(int64_t)(kGroup - 1);
+    sg.ptr_base = nseg * n;
+    for (int r = 0; r < n; ++r) p.gptr[nseg * n + r] = d.ptrs[r];
+    tiles += (sg.body + kTmaTile - 1) / kTmaTile;
+    ++nseg;
+  }
+  if (nseg == 0) return DPOPT_OK;
+  p.seg[nseg].first_tile = tiles;
+  p.nseg = nseg;
+  p.total_tiles = tiles;
+  p.stage_bytes = (uint32_t)kTmaTile * ((uint32_t)n * gsize + 12u);
+  p.stages = (int)std::min<uint32_t>(kTmaMaxStages, kTmaSmemBudget / p.stage_bytes);
+  p.wait_limit = kWaitLimitCycles;
+  if (p.stages < 2) return fail(DPOPT_ERR_UNSUPPORTED, "replica rows do not fit two stages");
+  if (grad_dtype == DPOPT_GRAD_BF16) return dispatch_tma_gk<0>(p, stream);
+  return dispatch_tma_gk<1>(p, stream);
+}
+
+// Kernel choice: the bulk-copy kernel where it applies and the policy allows,
+// else the direct-load kernel.
+bool use_tma(const SegDesc* segs, int s0, int s1, int n, int grad_dtype, float* master,
+             float* m, float* v, void* out) {
+  const int pol = g_policy.load(std::memory_order_relaxed);
+  if (pol == DPOPT_KERNEL_DIRECT) return false;
+  if (!tma_eligible(segs, s0, s1, n, grad_dtype, master, m, v, out)) return false;
+  if (pol == DPOPT_KERNEL_BULK) return true;
+  return n <= kTmaAutoMaxReplicas;
+}
+
 int run(const SegDesc* segs, int nsegs, int grad_dtype, int n, float* master, float* m, float* v,
         void* out, const Hyper& h, cudaStream_t stream) {
-  const size_t esize = grad_dtype == DPOPT_GRAD_BF16 ? 2 : 4;
   if (nsegs == 1) {
+    if (use_tma(segs, 0, 1, n, grad_dtype, master, m, v, out)) {
+      SmallTma p{};
+      p.h = h;
+      p.master = master; p.m = m; p.v = v; p.out = (uint16_t*)out;
+      p.n_rep = n;
+      return run_segments_tma(p, segs, 0, 1, n, stream, grad_dtype);
+    }
     SmallParams p{};
     p.h = h;
     p.master = master; p.m = m; p.v = v; p.out = (uint16_t*)out;
     p.n_rep = n;
-    return run_segments(p, segs, 0, 1, n, esize, stream, grad_dtype);
+    return run_segments(p, segs, 0, 1, n, stream, grad_dtype);
   }
   const int per_launch = std::min(kBigSegs, kBigPtrs / n);
-  static thread_local BigParams p;  // 20 KB: kept off the stack
   for (int s0 = 0; s0 < nsegs; s0 += per_launch) {
-    std::memset(&p, 0, sizeof p);
-    p.h = h;
-    p.master = master; p.m = m; p.v = v; p.out = (uint16_t*)out;
-    p.n_rep = n;
-    int rc = run_segments(p, segs, s0, std::min(nsegs, s0 + per_launch), n, esize, stream,
-                          grad_dtype);
+    const int s1 = std::min(nsegs, s0 + per_launch);
+    int rc;
+    if (use_tma(segs, s0, s1, n, grad_dtype, master, m, v, out)) {
+      static thread_local BigTma p;  // 20 KB: kept off the stack
+      std::memset(&p, 0, sizeof p);
+      p.h = h;
+      p.master = master; p.m = m; p.v = v; p.out = (uint16_t*)out;
+      p.n_rep = n;
+      rc = run_segments_tma(p, segs, s0, s1, n, stream, grad_dtype);
+    } else {
+      static thread_local BigParams p;
+      std::memset(&p, 0, sizeof p);
+      p.h = h;
+      p.master = master; p.m = m; p.v = v; p.out = (uint16_t*)out;
+      p.n_rep = n;
+      rc = run_segments(p, segs, s0, s1, n, stream, grad_dtype);
+    }
     if (rc) return rc;
   }
   return DPOPT_OK;
@@ -438,6 +569,26 @@ int dpopt_state_bytes(int64_t psi, int variant, int n_dp, int zero_stage, double
 }
 
 int64_t dpopt_launch_count(void) { return g_launches; }
+
+int dpopt_set_kernel_policy(int policy) {
+  if (policy != DPOPT_KERNEL_AUTO && policy != DPOPT_KERNEL_DIRECT && policy != DPOPT_KERNEL_BULK)
+    return fail(DPOPT_ERR_INVALID_ARG, "unknown kernel policy %d", policy);
+  g_policy.store(policy, std::memory_order_relaxed);
+  return DPOPT_OK;
+}
+
+int dpopt_get_kernel_policy(void) { return g_policy.load(std::memory_order_relaxed); }
+
+int dpopt_selftest_wait_timeout(int64_t limit_cycles, dpopt_stream_t stream) {
+  if (limit_cycles < 1 || limit_cycles > kWaitLimitCycles)
+    return fail(DPOPT_ERR_INVALID_ARG, "limit_cycles must lie in [1, %lld]",
+                (long long)kWaitLimitCycles);
+  selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((long long)limit_cycles);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  ++g_launches;
+  return DPOPT_OK;
+}
 
 const char* dpopt_version(void) { return "0.1.0"; }
 

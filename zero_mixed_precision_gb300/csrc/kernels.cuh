@@ -21,6 +21,10 @@ namespace dpopt {
 constexpr int kGroup = 8;      // elements per thread per iteration
 constexpr int kThreads = 256;  // threads per CTA
 
+// Sticky per-device status word: bit 0 is set when a bounded device-side wait
+// gave up.  Read and cleared by dpopt_stream_status().
+__device__ unsigned int g_status;
+
 struct Seg {
   int64_t first_group;  // groups of all earlier segments (prefix sum)
   int64_t state_off;    // first shard element this segment updates
@@ -89,12 +93,21 @@ __device__ __forceinline__ void st_stream16u(void* p, uint32_t a, uint32_t b, ui
 template <int GK>
 struct GradLoad;
 
+__device__ __forceinline__ uint4 ld_shared16(uint32_t saddr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(saddr));
+  return r;
+}
+
 template <>
 struct GradLoad<0> {
   uint4 w;
   __device__ __forceinline__ void load(const void* base, int64_t e0, uint64_t pol) {
     w = ld_grad16(static_cast<const uint16_t*>(base) + e0, pol);
   }
+  __device__ __forceinline__ void load_shared(uint32_t saddr) { w = ld_shared16(saddr); }
   __device__ __forceinline__ void zero() { w = make_uint4(0u, 0u, 0u, 0u); }
   __device__ __forceinline__ float get(int k) const {
     uint32_t x = (k < 2) ? w.x : (k < 4) ? w.y : (k < 6) ? w.z : w.w;
@@ -113,6 +126,10 @@ struct GradLoad<1> {
     const float* p = static_cast<const float*>(base) + e0;
     a = ld_grad16(p, pol);
     b = ld_grad16(p + 4, pol);
+  }
+  __device__ __forceinline__ void load_shared(uint32_t saddr) {
+    a = ld_shared16(saddr);
+    b = ld_shared16(saddr + 16);
   }
   __device__ __forceinline__ void zero() { a = b = make_uint4(0u, 0u, 0u, 0u); }
   __device__ __forceinline__ float get(int k) const {
@@ -138,33 +155,72 @@ __device__ __forceinline__ float ld_grad1(const void* base, int64_t e) {
 }
 
 // ---------------------------------------------------------------------------
+// where one 8-element group's inputs come from, where its outputs go
+// ---------------------------------------------------------------------------
+
+// Inputs read straight from global memory (the direct-load kernel).
+template <int GK>
+struct GlobalSource {
+  const void* const* gp;  // the segment's replica pointers
+  int64_t e0;             // group's first element within the segment
+  const float* st[3];     // master, m, v at the group's first element
+  uint64_t pol;
+  __device__ __forceinline__ void grad(GradLoad<GK>& g, int r) const { g.load(gp[r], e0, pol); }
+  __device__ __forceinline__ float4 state(int a, int half) const {
+    return ld_state16(st[a] + 4 * half);
+  }
+};
+
+// Inputs staged in shared memory by bulk copies (the bulk-copy kernel).
+template <int GK>
+struct SharedSource {
+  uint32_t g0;       // shared address of replica 0's 8 values for this thread
+  uint32_t rstride;  // bytes between consecutive replicas' rows
+  uint32_t st[3];    // shared addresses of master, m, v for this thread
+  __device__ __forceinline__ void grad(GradLoad<GK>& g, int r) const {
+    g.load_shared(g0 + (uint32_t)r * rstride);
+  }
+  __device__ __forceinline__ float4 state(int a, int half) const {
+    uint4 u = ld_shared16(st[a] + 16u * half);
+    return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                       __uint_as_float(u.w));
+  }
+};
+
+// Outputs, at the group's first element.
+struct GroupOut {
+  float* master;
+  float* m;
+  float* v;
+  uint16_t* out;
+};
+
+// ---------------------------------------------------------------------------
 // one 8-element group, vector path
 // ---------------------------------------------------------------------------
 
 // Scalar-lane form: 8 elements per thread, one element per operation.  Fewer
 // register pairings; faster when the optimizer arithmetic dominates (small N).
-template <int NR, int GK, class LP>
-__device__ __forceinline__ void group_vec_x1(const LP& p, const Seg& sg, int64_t e0,
-                                             uint64_t pol) {
-  const int64_t so = sg.state_off + e0;
+template <int NR, int GK, class Src>
+__device__ __forceinline__ void group_vec_x1(const Src& src, int n, const Hyper& h,
+                                             const GroupOut& o) {
   float th[kGroup], mm[kGroup], vv[kGroup];
   {
-    float4 a = ld_state16(p.master + so), b = ld_state16(p.master + so + 4);
+    float4 a = src.state(0, 0), b = src.state(0, 1);
     th[0] = a.x; th[1] = a.y; th[2] = a.z; th[3] = a.w;
     th[4] = b.x; th[5] = b.y; th[6] = b.z; th[7] = b.w;
-    a = ld_state16(p.m + so); b = ld_state16(p.m + so + 4);
+    a = src.state(1, 0); b = src.state(1, 1);
     mm[0] = a.x; mm[1] = a.y; mm[2] = a.z; mm[3] = a.w;
     mm[4] = b.x; mm[5] = b.y; mm[6] = b.z; mm[7] = b.w;
-    a = ld_state16(p.v + so); b = ld_state16(p.v + so + 4);
+    a = src.state(2, 0); b = src.state(2, 1);
     vv[0] = a.x; vv[1] = a.y; vv[2] = a.z; vv[3] = a.w;
     vv[4] = b.x; vv[5] = b.y; vv[6] = b.z; vv[7] = b.w;
   }
-  const void* const* gp = p.gptr + sg.ptr_base;
   CompSum<float> acc[kGroup];
   if constexpr (NR > 0) {
     GradLoad<GK> gl[NR];
 #pragma unroll
-    for (int r = 0; r < NR; ++r) gl[r].load(gp[r], e0, pol);
+    for (int r = 0; r < NR; ++r) src.grad(gl[r], r);
 #pragma unroll
     for (int k = 0; k < kGroup; ++k) acc[k].init(gl[0].get(k));
 #pragma unroll
@@ -175,12 +231,11 @@ __device__ __forceinline__ void group_vec_x1(const LP& p, const Seg& sg, int64_t
   } else {
     // runtime replica count: chunks of 8 replicas, loads of a chunk in flight together
     constexpr int C = 8;
-    const int n = p.n_rep;
     for (int r0 = 0; r0 < n; r0 += C) {
       GradLoad<GK> gl[C];
 #pragma unroll
       for (int j = 0; j < C; ++j) {
-        if (r0 + j < n) gl[j].load(gp[r0 + j], e0, pol);
+        if (r0 + j < n) src.grad(gl[j], r0 + j);
         else gl[j].zero();
       }
 #pragma unroll
@@ -199,44 +254,42 @@ __device__ __forceinline__ void group_vec_x1(const LP& p, const Seg& sg, int64_t
   }
 #pragma unroll
   for (int k = 0; k < kGroup; ++k) {
-    float g = acc[k].average(p.h);
-    adam_update(g, th[k], mm[k], vv[k], p.h);
+    float g = acc[k].average(h);
+    adam_update(g, th[k], mm[k], vv[k], h);
   }
-  st_stream16(p.master + so, th[0], th[1], th[2], th[3]);
-  st_stream16(p.master + so + 4, th[4], th[5], th[6], th[7]);
-  st_stream16(p.m + so, mm[0], mm[1], mm[2], mm[3]);
-  st_stream16(p.m + so + 4, mm[4], mm[5], mm[6], mm[7]);
-  st_stream16(p.v + so, vv[0], vv[1], vv[2], vv[3]);
-  st_stream16(p.v + so + 4, vv[4], vv[5], vv[6], vv[7]);
-  st_stream16u(p.out + so, to_bf16x2(th[0], th[1]), to_bf16x2(th[2], th[3]),
+  st_stream16(o.master, th[0], th[1], th[2], th[3]);
+  st_stream16(o.master + 4, th[4], th[5], th[6], th[7]);
+  st_stream16(o.m, mm[0], mm[1], mm[2], mm[3]);
+  st_stream16(o.m + 4, mm[4], mm[5], mm[6], mm[7]);
+  st_stream16(o.v, vv[0], vv[1], vv[2], vv[3]);
+  st_stream16(o.v + 4, vv[4], vv[5], vv[6], vv[7]);
+  st_stream16u(o.out, to_bf16x2(th[0], th[1]), to_bf16x2(th[2], th[3]),
                to_bf16x2(th[4], th[5]), to_bf16x2(th[6], th[7]));
 }
 
 // Packed form: 4 element pairs per thread, every operation on f32x2 lanes.
 // Pays off when the replica sum dominates (large N).
-template <int NR, int GK, class LP>
-__device__ __forceinline__ void group_vec_x2(const LP& p, const Seg& sg, int64_t e0,
-                                             uint64_t pol) {
+template <int NR, int GK, class Src>
+__device__ __forceinline__ void group_vec_x2(const Src& src, int n, const Hyper& h,
+                                             const GroupOut& o) {
   constexpr int P = kGroup / 2;  // element pairs per group
-  const int64_t so = sg.state_off + e0;
   float2 th[P], mm[P], vv[P];
   {
-    float4 a = ld_state16(p.master + so), b = ld_state16(p.master + so + 4);
+    float4 a = src.state(0, 0), b = src.state(0, 1);
     th[0] = make_float2(a.x, a.y); th[1] = make_float2(a.z, a.w);
     th[2] = make_float2(b.x, b.y); th[3] = make_float2(b.z, b.w);
-    a = ld_state16(p.m + so); b = ld_state16(p.m + so + 4);
+    a = src.state(1, 0); b = src.state(1, 1);
     mm[0] = make_float2(a.x, a.y); mm[1] = make_float2(a.z, a.w);
     mm[2] = make_float2(b.x, b.y); mm[3] = make_float2(b.z, b.w);
-    a = ld_state16(p.v + so); b = ld_state16(p.v + so + 4);
+    a = src.state(2, 0); b = src.state(2, 1);
     vv[0] = make_float2(a.x, a.y); vv[1] = make_float2(a.z, a.w);
     vv[2] = make_float2(b.x, b.y); vv[3] = make_float2(b.z, b.w);
   }
-  const void* const* gp = p.gptr + sg.ptr_base;
   CompSum<float2> acc[P];
   if constexpr (NR > 0) {
     GradLoad<GK> gl[NR];
 #pragma unroll
-    for (int r = 0; r < NR; ++r) gl[r].load(gp[r], e0, pol);
+    for (int r = 0; r < NR; ++r) src.grad(gl[r], r);
 #pragma unroll
     for (int j = 0; j < P; ++j) acc[j].init(gl[0].pair(j));
 #pragma unroll
@@ -247,12 +300,11 @@ __device__ __forceinline__ void group_vec_x2(const LP& p, const Seg& sg, int64_t
   } else {
     // runtime replica count: chunks of 8 replicas, loads of a chunk in flight together
     constexpr int C = 8;
-    const int n = p.n_rep;
     {
       GradLoad<GK> gl[C];
 #pragma unroll
       for (int j = 0; j < C; ++j) {
-        if (j < n) gl[j].load(gp[j], e0, pol);
+        if (j < n) src.grad(gl[j], j);
         else gl[j].zero();
       }
 #pragma unroll
@@ -269,7 +321,7 @@ __device__ __forceinline__ void group_vec_x2(const LP& p, const Seg& sg, int64_t
       GradLoad<GK> gl[C];
       if (r0 + C <= n) {
 #pragma unroll
-        for (int j = 0; j < C; ++j) gl[j].load(gp[r0 + j], e0, pol);
+        for (int j = 0; j < C; ++j) src.grad(gl[j], r0 + j);
 #pragma unroll
         for (int j = 0; j < C; ++j) {
 #pragma unroll
@@ -278,7 +330,7 @@ __device__ __forceinline__ void group_vec_x2(const LP& p, const Seg& sg, int64_t
       } else {
 #pragma unroll
         for (int j = 0; j < C; ++j) {
-          if (r0 + j < n) gl[j].load(gp[r0 + j], e0, pol);
+          if (r0 + j < n) src.grad(gl[j], r0 + j);
           else gl[j].zero();
         }
 #pragma unroll
@@ -293,16 +345,16 @@ __device__ __forceinline__ void group_vec_x2(const LP& p, const Seg& sg, int64_t
   }
 #pragma unroll
   for (int j = 0; j < P; ++j) {
-    float2 g = acc[j].average(p.h);
-    adam_update(g, th[j], mm[j], vv[j], p.h);
+    float2 g = acc[j].average(h);
+    adam_update(g, th[j], mm[j], vv[j], h);
   }
-  st_stream16(p.master + so, th[0].x, th[0].y, th[1].x, th[1].y);
-  st_stream16(p.master + so + 4, th[2].x, th[2].y, th[3].x, th[3].y);
-  st_stream16(p.m + so, mm[0].x, mm[0].y, mm[1].x, mm[1].y);
-  st_stream16(p.m + so + 4, mm[2].x, mm[2].y, mm[3].x, mm[3].y);
-  st_stream16(p.v + so, vv[0].x, vv[0].y, vv[1].x, vv[1].y);
-  st_stream16(p.v + so + 4, vv[2].x, vv[2].y, vv[3].x, vv[3].y);
-  st_stream16u(p.out + so, to_bf16x2(th[0].x, th[0].y), to_bf16x2(th[1].x, th[1].y),
+  st_stream16(o.master, th[0].x, th[0].y, th[1].x, th[1].y);
+  st_stream16(o.master + 4, th[2].x, th[2].y, th[3].x, th[3].y);
+  st_stream16(o.m, mm[0].x, mm[0].y, mm[1].x, mm[1].y);
+  st_stream16(o.m + 4, mm[2].x, mm[2].y, mm[3].x, mm[3].y);
+  st_stream16(o.v, vv[0].x, vv[0].y, vv[1].x, vv[1].y);
+  st_stream16(o.v + 4, vv[2].x, vv[2].y, vv[3].x, vv[3].y);
+  st_stream16u(o.out, to_bf16x2(th[0].x, th[0].y), to_bf16x2(th[1].x, th[1].y),
                to_bf16x2(th[2].x, th[2].y), to_bf16x2(th[3].x, th[3].y));
 }
 
@@ -310,8 +362,8 @@ __device__ __forceinline__ void group_vec_x2(const LP& p, const Seg& sg, int64_t
 // a partial or unaligned group, one element at a time
 // ---------------------------------------------------------------------------
 
-template <int GK, class LP>
-__device__ __noinline__ void group_scalar(const LP& p, const Seg& sg, int64_t e0, int count) {
+template <int GK, class LP, class SegT>
+__device__ __noinline__ void group_scalar(const LP& p, const SegT& sg, int64_t e0, int count) {
   const void* const* gp = p.gptr + sg.ptr_base;
   const int n = p.n_rep;
   for (int k = 0; k < count; ++k) {
@@ -353,8 +405,12 @@ __global__ void __launch_bounds__(kThreads, min_ctas<NR, PACK>())
     const int64_t e0 = (gi - sg.first_group) * kGroup;
     const int64_t rem = sg.len - e0;
     if (sg.vec && rem >= kGroup) {
-      if constexpr (PACK) group_vec_x2<NR, GK>(p, sg, e0, pol);
-      else group_vec_x1<NR, GK>(p, sg, e0, pol);
+      const int64_t so = sg.state_off + e0;
+      const GlobalSource<GK> src{p.gptr + sg.ptr_base, e0, {p.master + so, p.m + so, p.v + so},
+                                 pol};
+      const GroupOut o{p.master + so, p.m + so, p.v + so, p.out + so};
+      if constexpr (PACK) group_vec_x2<NR, GK>(src, p.n_rep, p.h, o);
+      else group_vec_x1<NR, GK>(src, p.n_rep, p.h, o);
     } else {
       group_scalar<GK>(p, sg, e0, (int)(rem < kGroup ? rem : kGroup));
     }
