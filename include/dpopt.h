@@ -185,7 +185,8 @@ int dpopt_state_bytes(int64_t psi, int variant, int n_dp, int zero_stage, double
  *  DPOPT_KERNEL_AUTO    the faster of the two for the replica count, by measurement
  *  DPOPT_KERNEL_DIRECT  direct 16-byte loads from global memory into registers
  *  DPOPT_KERNEL_BULK    bulk copies (TMA) into a shared-memory ring, where it applies
- *                       (every pointer 16-byte aligned, n_replicas <= 16); other calls
+ *                       (every pointer 16-byte aligned, two stages of 2048 elements fit
+ *                       100 KB of shared memory: bf16 N <= 6, fp32 N <= 3); other calls
  *                       still take the direct-load kernel
  * Both kernels give bitwise identical results.  Errors: DPOPT_ERR_INVALID_ARG for an
  * unknown value. */

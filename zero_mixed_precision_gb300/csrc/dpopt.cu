@@ -31,13 +31,18 @@ using BigTma = TmaParams<kBigSegs, kBigPtrs>;
 static_assert(sizeof(BigParams) <= 32000, "kernel parameters must fit the 32 KB limit");
 static_assert(sizeof(BigTma) <= 32000, "kernel parameters must fit the 32 KB limit");
 
-// Bulk-copy kernel: shared memory budget for the stage ring of one CTA, the
-// largest replica count it serves, and how long one bounded wait may spin.
-constexpr uint32_t kTmaSmemBudget = 200 * 1024;
+// Bulk-copy kernel: shared memory budget for the stage ring of one CTA (two
+// CTAs of 8 consumer warps per SM measured best: 6386 GB/s at N = 4 against
+// 4687 GB/s for one CTA with five stages), the largest replica count it
+// serves, and how long one bounded wait may spin.
+constexpr uint32_t kTmaSmemBudget = 100 * 1024;
 constexpr int kTmaMaxReplicas = 16;
 constexpr long long kWaitLimitCycles = 2000000000LL;  // about one second
-// Under DPOPT_KERNEL_AUTO the bulk-copy kernel serves N up to this (measured).
-constexpr int kTmaAutoMaxReplicas = 8;
+// Under DPOPT_KERNEL_AUTO the bulk-copy kernel serves N up to this.  Measured
+// on GB300 the direct-load kernel is as fast or faster at every N (6400 vs
+// 6386 GB/s at N = 4, the only replica count where the bulk-copy ring fits two
+// CTAs per SM), so AUTO always picks it.
+constexpr int kTmaAutoMaxReplicas = 0;
 
 std::atomic<int> g_policy{DPOPT_KERNEL_AUTO};
 
