@@ -157,6 +157,73 @@ int dpopt_reduce_adam_buckets(const void *const *slice_table, int grad_dtype, in
                               float lr, float beta1, float beta2, float eps, int64_t step,
                               dpopt_stream_t stream);
 
+/* ------------------------------------------------------------------------- */
+/* AdamW and global-norm gradient clipping                                    */
+/* ------------------------------------------------------------------------- */
+
+/* Options beyond plain Adam.  A zero-initialised struct means plain Adam.
+ * The optimizer of the DeepSpeed example in "Почему training 70B модели требует
+ * optimizer sharding (ZeRO-3)?" (section 8) is AdamW with weight_decay 0.01 and
+ * gradient_clipping 1.0; the pages give no formulas, so these follow AdamW
+ * (Loshchilov & Hutter 2019) and the usual global-norm clipping:
+ *   g      <- fl32(g * c),  c = grad_unscale * min(1, max_grad_norm / (||g||_2 + 1e-6))
+ *            (c in fp64, rounded once to fp32; ||g||_2 = sqrt(*grad_sqnorm))
+ *   master <- (1 - lr*weight_decay) * master - lr * m_hat / (sqrt(v_hat) + eps)       */
+typedef struct {
+    float weight_decay;        /* decoupled weight decay, >= 0 (0: none) */
+    float max_grad_norm;       /* > 0: clip to this global L2 norm (0: no clipping) */
+    const double *grad_sqnorm; /* DEVICE pointer, read when max_grad_norm > 0: the squared
+                                  global L2 norm of the unscaled averaged gradient, summed over
+                                  every rank's shard (dpopt_grad_sqnorm per shard, then one
+                                  scalar all-reduce across ranks) */
+    float grad_unscale;        /* multiply the averaged gradient by this first (1/loss scale,
+                                  a power of two keeps it exact); 0 means 1 */
+} dpopt_step_options;
+
+/* dpopt_reduce_adam_ex with options (opts may be NULL: plain Adam).  Always
+ * takes the direct-load kernel.  Errors as for dpopt_reduce_adam_ex, plus
+ * DPOPT_ERR_INVALID_ARG for a negative or non-finite option, or clipping
+ * without an 8-byte aligned grad_sqnorm. */
+int dpopt_reduce_adamw(const void *const *grads, int grad_dtype, int n_replicas, int64_t numel,
+                       int shard_rank, int64_t bucket_elems, float *master_f32, float *m_f32,
+                       float *v_f32, void *param_bf16_out, float lr, float beta1, float beta2,
+                       float eps, int64_t step, const dpopt_step_options *opts,
+                       dpopt_stream_t stream);
+
+/* dpopt_reduce_adam_buckets with options. */
+int dpopt_reduce_adamw_buckets(const void *const *slice_table, int grad_dtype, int n_replicas,
+                               const int64_t *offsets, const int64_t *lens, int64_t n_buckets,
+                               float *master_f32, float *m_f32, float *v_f32,
+                               void *param_bf16_out, float lr, float beta1, float beta2,
+                               float eps, int64_t step, const dpopt_step_options *opts,
+                               dpopt_stream_t stream);
+
+/* Squared L2 norm of this shard's averaged gradient (the clipping pre-pass):
+ *   *sqnorm_out = sum_i (g_i * grad_unscale)^2      (fp64, DEVICE pointer)
+ * with g_i the same fixed-order average the step computes.  Partial sums over
+ * fixed 65536-element chunks go to `scratch` (a DEVICE buffer the caller owns,
+ * at least dpopt_grad_sqnorm_scratch_bytes() bytes, 8-byte aligned) and are
+ * added in chunk order, so the result is bitwise reproducible and does not
+ * depend on the GPU's SM count.  Arguments as for dpopt_reduce_adam_ex;
+ * grad_unscale 0 means 1.  Errors: DPOPT_ERR_INVALID_ARG for the usual
+ * argument errors, a null/misaligned sqnorm_out or scratch, too small a
+ * scratch, or gradients overlapping either. */
+int dpopt_grad_sqnorm(const void *const *grads, int grad_dtype, int n_replicas, int64_t numel,
+                      int shard_rank, float grad_unscale, double *sqnorm_out, void *scratch,
+                      int64_t scratch_bytes, dpopt_stream_t stream);
+
+/* The same over a batch of bucket slices (arguments as for
+ * dpopt_reduce_adam_buckets). */
+int dpopt_grad_sqnorm_buckets(const void *const *slice_table, int grad_dtype, int n_replicas,
+                              const int64_t *offsets, const int64_t *lens, int64_t n_buckets,
+                              float grad_unscale, double *sqnorm_out, void *scratch,
+                              int64_t scratch_bytes, dpopt_stream_t stream);
+
+/* Scratch bytes dpopt_grad_sqnorm{,_buckets} need for `elems` gradient elements
+ * per replica cut into n_buckets buckets (use n_buckets = 1 for the full-buffer
+ * form): 8 * (ceil(elems / 65536) + n_buckets).  Host-only. */
+int dpopt_grad_sqnorm_scratch_bytes(int64_t elems, int64_t n_buckets, int64_t *bytes_out);
+
 /* Wait for `stream`, then return and clear the current device's status word:
  * DPOPT_OK, or DPOPT_ERR_TIMEOUT if a bounded device-side wait gave up since the
  * last call, or DPOPT_ERR_CUDA if the wait itself failed. */

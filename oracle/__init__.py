@@ -72,6 +72,12 @@ def lib() -> ctypes.CDLL:
         L.orc_f32_to_bf16_array.restype = None
         L.orc_threads_available.argtypes = []
         L.orc_threads_available.restype = I
+        L.orc_grad_sqnorm.argtypes = [P, I, I, I64, I64, F]
+        L.orc_grad_sqnorm.restype = ctypes.c_double
+        L.orc_grad_scale.argtypes = [ctypes.c_double, F, F]
+        L.orc_grad_scale.restype = F
+        L.orc_reduce_adamw_range.argtypes = [P, I, I, I64, I64, P, P, P, P, F, F, F, F, F, F, I64]
+        L.orc_reduce_adamw_range.restype = I
         _lib = L
     return _lib
 
@@ -179,6 +185,37 @@ def reduce_adam_shard(grads: Sequence[np.ndarray], numel: int, shard_rank: int, 
     return reduce_adam_range(grads, shard_rank * s, s, master, m, v, lr=lr, beta1=beta1,
                              beta2=beta2, eps=eps, step=step, weight_decay=weight_decay,
                              nthreads=nthreads)
+
+
+def grad_sqnorm(grads: Sequence[np.ndarray], offset: int = 0, count: int | None = None,
+                unscale: float = 1.0) -> float:
+    """sum of (g_i * unscale)^2 over [offset, offset+count) of the averaged gradient."""
+    grads = [np.ascontiguousarray(g) for g in grads]
+    code = _dtype_code(grads[0])
+    count = grads[0].size - offset if count is None else count
+    return float(lib().orc_grad_sqnorm(_ptr_table(grads), code, len(grads), offset, count,
+                                       unscale))
+
+
+def grad_scale(sqnorm: float, max_norm: float, unscale: float = 1.0) -> np.float32:
+    """fp32 multiplier unscale * min(1, max_norm / (sqrt(sqnorm) + 1e-6))."""
+    return np.float32(lib().orc_grad_scale(sqnorm, max_norm, unscale))
+
+
+def reduce_adamw_range(grads: Sequence[np.ndarray], offset: int, count: int, master, m, v, *,
+                       lr: float, beta1: float, beta2: float, eps: float, step: int,
+                       weight_decay: float = 0.0, gscale: float = 1.0):
+    """One AdamW step with the averaged gradient multiplied by gscale first."""
+    grads = [np.ascontiguousarray(g) for g in grads]
+    code = _dtype_code(grads[0])
+    for a in (master, m, v):
+        assert a.dtype == np.float32 and a.flags["C_CONTIGUOUS"] and a.size == count
+    out = np.empty(count, dtype=np.uint16)
+    _check_rc(lib().orc_reduce_adamw_range(_ptr_table(grads), code, len(grads), offset, count,
+                                           _ptr(master), _ptr(m), _ptr(v), _ptr(out), lr, beta1,
+                                           beta2, eps, weight_decay, gscale, step),
+              "reduce_adamw_range")
+    return out
 
 
 def threads_available() -> int:

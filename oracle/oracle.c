@@ -222,6 +222,51 @@ int orc_reduce_adam_gathered(const void *const *grads, int dtype, int n,
                                  lr, beta1, beta2, eps, weight_decay, step, 1);
 }
 
+/* ------------------------------------------------------------------ */
+/* Global-norm gradient clipping (the clipping config of the ZeRO-3     */
+/* answer's DeepSpeed example: gradient_clipping 1.0)                    */
+/* ------------------------------------------------------------------ */
+
+/* sum_i (g_i * unscale)^2 over elements [offset, offset+count), in fp64,
+ * g_i the fixed-order average above.  The global squared norm of a model is
+ * the sum of these over every rank's shard. */
+double orc_grad_sqnorm(const void *const *grads, int dtype, int n, int64_t offset,
+                       int64_t count, float unscale) {
+    double acc = 0.0;
+    for (int64_t j = 0; j < count; ++j) {
+        double x = (double)orc_average_one(grads, dtype, n, offset + j) * (double)unscale;
+        acc += x * x;
+    }
+    return acc;
+}
+
+/* The gradient multiplier: unscale * min(1, max_norm / (sqrt(sqnorm) + 1e-6))
+ * evaluated in fp64 and rounded once to fp32 (max_norm <= 0: no clipping). */
+float orc_grad_scale(double sqnorm, float max_norm, float unscale) {
+    double c = (double)unscale;
+    if (max_norm > 0.0f) {
+        double coef = (double)max_norm / (sqrt(sqnorm) + 1e-6);
+        if (coef < 1.0) c *= coef;
+    }
+    return (float)c;
+}
+
+/* One step with the averaged gradient multiplied by gscale first:
+ * g' = fl32(g * gscale), then (Adam)W as above. */
+int orc_reduce_adamw_range(const void *const *grads, int dtype, int n, int64_t offset,
+                           int64_t count, float *master, float *m, float *v, uint16_t *out,
+                           float lr, float beta1, float beta2, float eps, float weight_decay,
+                           float gscale, int64_t step) {
+    if (n < 1 || count < 0 || offset < 0 || step < 1) return -1;
+    orc_hyper h = make_hyper(lr, beta1, beta2, eps, weight_decay, step);
+    for (int64_t j = 0; j < count; ++j) {
+        float g = orc_average_one(grads, dtype, n, offset + j);
+        float gs = (float)((double)g * (double)gscale);
+        adam_one((double)gs, &master[j], &m[j], &v[j], out ? &out[j] : 0, &h);
+    }
+    return 0;
+}
+
 /* Average only (no optimizer), for pinning the reduce half on its own. */
 int orc_average(const void *const *grads, int dtype, int n, int64_t count,
                 float *g_out) {

@@ -76,13 +76,16 @@ def _f64(x):
 
 
 def oracle_trajectory(wl: Workload, local_idx: np.ndarray, t_first: int, t_last: int,
-                      grads_fn=None, init=None, hp=None) -> list[StepRef]:
+                      grads_fn=None, init=None, hp=None, weight_decay: float = 0.0,
+                      gscale_fn=None) -> list[StepRef]:
     """Run the oracle over steps t_first..t_last on the shard elements local_idx
     (0 <= j < S) and return every step's states and tolerances.
 
     grads_fn(r, t) -> gradient values at those elements (default: the seeded
     generator at flattened index shard_base + j); init -> (master, m, v)
-    (default: the seeded generator)."""
+    (default: the seeded generator).  weight_decay: AdamW decay; gscale_fn(t,
+    grads) -> the fp32 gradient multiplier of step t (clipping / unscaling),
+    computed by the oracle from that step's gradients."""
     hp = hp or dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps)
     gidx = wl.shard_base + np.asarray(local_idx, dtype=np.int64)
     if grads_fn is None:
@@ -101,8 +104,11 @@ def oracle_trajectory(wl: Workload, local_idx: np.ndarray, t_first: int, t_last:
     for t in range(t_first, t_last + 1):
         grads = [np.ascontiguousarray(grads_fn(r, t)) for r in range(wl.n_replicas)]
         g = oracle.average(grads)
+        if gscale_fn is not None:
+            c = np.float32(gscale_fn(t, grads))
+            g = (_f64(g) * np.float64(c)).astype(np.float32)
         th_prev, m_prev = _f64(master), _f64(m)
-        out = oracle.adam(g, master, m, v, step=t, **hp)
+        out = oracle.adam(g, master, m, v, step=t, weight_decay=weight_decay, **hp)
         bc1 = 1.0 - b1 ** t
         bc2 = 1.0 - b2 ** t
         scale_m = np.maximum.reduce([np.abs(b1 * m_prev), np.abs((1.0 - b1) * _f64(g)),

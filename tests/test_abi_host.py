@@ -157,3 +157,37 @@ def test_bucket_entries_reject_bad_arguments(dp):
     assert dp.dpopt_reduce_adam_buckets([G[0], MASTER + 16], 0, 2, [0], [100], *args) == 1
     # n_replicas beyond the limit
     assert dp.dpopt_reduce_adam_buckets(G[:64] * 2, 0, 65, [0], [10], *args) == 2
+
+
+def test_sqnorm_scratch_bytes(dp):
+    assert dp.dpopt_grad_sqnorm_scratch_bytes(0, 1) == (0, 8)
+    assert dp.dpopt_grad_sqnorm_scratch_bytes(65536, 1) == (0, 16)
+    assert dp.dpopt_grad_sqnorm_scratch_bytes(65537, 1) == (0, 24)
+    assert dp.dpopt_grad_sqnorm_scratch_bytes(1_093_750_000, 274)[1] == 8 * (16690 + 274)
+    assert dp.dpopt_grad_sqnorm_scratch_bytes(-1, 1)[0] == dp.DPOPT_ERR_INVALID_ARG
+
+
+def test_sqnorm_and_adamw_reject_bad_arguments(dp):
+    SQ, SCR = 0xD0_0000_0000, 0xE0_0000_0000
+    ok = dict(grads=G[:2], dt=0, n=2, numel=2 * 70000, rank=0, un=0.0, out=SQ, scr=SCR, nbytes=16)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return dp.dpopt_grad_sqnorm(a["grads"], a["dt"], a["n"], a["numel"], a["rank"], a["un"],
+                                    a["out"], a["scr"], a["nbytes"], 0)
+    assert call(out=0) == 1
+    assert call(out=SQ + 4) == 1
+    assert call(scr=0) == 1
+    assert call(nbytes=8) == 1                   # 70000 elements need two partials
+    assert call(un=-1.0) == 1
+    assert call(un=float("nan")) == 1
+    assert call(out=SCR + 8) == 1                # output inside the partials
+    assert call(grads=[SQ - 16, G[1]]) == 1      # gradients overlap the output
+    assert call(numel=7) == 1
+    assert call(n=65, grads=G[:64] + [G[0]]) == 2
+    opt = dp.StepOptions(-0.1, 0.0, None, 0.0)
+    assert dp.dpopt_reduce_adamw(G[:4], 0, 4, 4096, 0, 1024, MASTER, M, V, OUT, *HP, 1, opt, 0) == 1
+    opt = dp.StepOptions(0.01, 1.0, None, 0.0)   # clipping without a norm pointer
+    assert dp.dpopt_reduce_adamw(G[:4], 0, 4, 4096, 0, 1024, MASTER, M, V, OUT, *HP, 1, opt, 0) == 1
+    opt = dp.StepOptions(0.01, 1.0, SQ + 3, 0.0)  # misaligned norm pointer
+    assert dp.dpopt_reduce_adamw(G[:4], 0, 4, 4096, 0, 1024, MASTER, M, V, OUT, *HP, 1, opt, 0) == 1

@@ -31,6 +31,10 @@ MUTANTS = {
     "bf16 truncation": ("lower > 0x8000u ||", "0 &&"),
     "weight decay on the new theta": ("h->lr * h->weight_decay * th;",
                                       "h->lr * h->weight_decay * (th - delta);"),
+    "clip coefficient not clamped to 1": ("if (coef < 1.0) c *= coef;", "c *= coef;"),
+    "clip on the squared norm": ("max_norm / (sqrt(sqnorm) + 1e-6);", "max_norm / (sqnorm + 1e-6);"),
+    "unscale not applied in the norm": ("* (double)unscale;\n        acc += x * x;",
+                                        ";\n        acc += x * x;"),
 }
 
 PIN_FUNCS = [
@@ -44,6 +48,8 @@ PIN_FUNCS = [
     (pins.test_adamw_matches_torch_optim_adamw_float64, {}),
     (pins.test_first_step_closed_form, {}),
     (pins.test_constant_gradient_closed_form, {}),
+    (pins.test_sqnorm_matches_exact_rational_sum_of_squares, {}),
+    (pins.test_clipping_matches_torch_clip_grad_norm, {}),
 ]
 
 
@@ -64,7 +70,7 @@ def _load(path):
 def test_planted_mistake_is_caught(name, tmp_path):
     old, new = MUTANTS[name]
     src = open(SRC, encoding="utf-8").read()
-    assert src.count(old) >= 1, f"mutation anchor not found: {old!r}"
+    assert src.count(old) == 1, f"mutation anchor must occur exactly once: {old!r}"
     mutant_c = tmp_path / "oracle_mutant.c"
     mutant_c.write_text(src.replace(old, new, 1), encoding="utf-8")
     so = tmp_path / "liboracle_mutant.so"

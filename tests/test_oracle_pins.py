@@ -384,3 +384,61 @@ def test_eight_a100s_hold_the_conservative_70b_replica():
     # "Почему training 70B ...", §2: at least 8 x A100 80 GB = 640 GB >= 560 GB
     total = oracle.state_bytes(70e9, 1, 1, 0)
     assert 8 * 80e9 >= total and 8 * 80e9 == 640e9
+
+
+# ---------------------------------------------------------------------------
+# gradient clipping (AdamW + global-norm clipping row)
+# ---------------------------------------------------------------------------
+
+def test_sqnorm_matches_exact_rational_sum_of_squares():
+    rng = np.random.default_rng(21)
+    n, count = 3, 300
+    grads = [rand_bf16(rng, count, -12, 2) for _ in range(n)]
+    g = oracle.average(grads)
+    want = sum(Fraction(float(x)) ** 2 for x in g)
+    got = oracle.grad_sqnorm(grads)
+    assert abs(Fraction(got) - want) <= want * Fraction(1, 2 ** 45)
+    # unscale by a power of two scales the squared norm exactly by its square
+    assert oracle.grad_sqnorm(grads, unscale=0.25) == got / 16
+
+
+def test_clipping_matches_torch_clip_grad_norm():
+    """torch.nn.utils.clip_grad_norm_ (library, float64) on the averaged gradient of
+    two 'shards' gives the same total norm and, after fp32 rounding, the same
+    clipped gradient as the oracle."""
+    rng = np.random.default_rng(22)
+    n, numel = 4, 8000
+    grads = [rand_bf16(rng, numel, -10, 0) for _ in range(n)]
+    g = oracle.average(grads).astype(np.float64)
+    for max_norm in (1e-3, 1.0, 1e6):
+        t = torch.from_numpy(g.copy()).requires_grad_()
+        t.grad = torch.from_numpy(g.copy())
+        total = float(torch.nn.utils.clip_grad_norm_([t], max_norm))
+        sq = oracle.grad_sqnorm(grads, 0, numel // 2) + oracle.grad_sqnorm(grads, numel // 2,
+                                                                           numel // 2)
+        assert np.sqrt(sq) == pytest.approx(total, rel=1e-14)
+        c = oracle.grad_scale(sq, max_norm)
+        ours = (g.astype(np.float32).astype(np.float64) * np.float64(c)).astype(np.float32)
+        ref = t.grad.numpy()
+        np.testing.assert_allclose(ours, ref, rtol=3 * U, atol=0)
+        if max_norm >= 1e6:
+            assert c == np.float32(1.0)
+
+
+def test_clipped_adamw_step_equals_adamw_on_the_clipped_gradient():
+    rng = np.random.default_rng(23)
+    n, count = 2, 1000
+    grads = [rand_bf16(rng, count, -12, 0) for _ in range(n)]
+    th0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    c = oracle.grad_scale(oracle.grad_sqnorm(grads), 0.05)
+    assert c < 1
+    a = [th0.copy(), np.zeros(count, np.float32), np.zeros(count, np.float32)]
+    out_a = oracle.reduce_adamw_range(grads, 0, count, *a, lr=1e-3, beta1=0.9, beta2=0.999,
+                                      eps=1e-8, step=1, weight_decay=0.01, gscale=float(c))
+    g = (oracle.average(grads).astype(np.float64) * np.float64(c)).astype(np.float32)
+    b = [th0.copy(), np.zeros(count, np.float32), np.zeros(count, np.float32)]
+    out_b = oracle.adam(g, *b, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, step=1,
+                        weight_decay=0.01)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    np.testing.assert_array_equal(out_a, out_b)

@@ -6,8 +6,9 @@ fails loudly; there is no CPU or PyTorch fallback.
 """
 from .binding import *  # noqa: F401,F403
 from .binding import (  # noqa: F401
-    DpoptError, EXPORTED, LIB_PATH, kernel_policy, reduce_adam, reduce_adam_bucket,
-    reduce_adam_buckets, stream_status,
+    DpoptError, EXPORTED, LIB_PATH, StepOptions, grad_sqnorm, grad_sqnorm_buckets, kernel_policy,
+    reduce_adam, reduce_adam_bucket, reduce_adam_buckets, reduce_adamw, reduce_adamw_buckets,
+    step_options, stream_status,
 )
 
 __version__ = "0.1.0"

@@ -43,6 +43,15 @@ _F = ctypes.c_float
 _PP = ctypes.POINTER(ctypes.c_void_p)
 _PI64 = ctypes.POINTER(ctypes.c_int64)
 
+
+class StepOptions(ctypes.Structure):
+    """dpopt_step_options (include/dpopt.h)."""
+    _fields_ = [("weight_decay", ctypes.c_float), ("max_grad_norm", ctypes.c_float),
+                ("grad_sqnorm", ctypes.c_void_p), ("grad_unscale", ctypes.c_float)]
+
+
+_POPT = ctypes.POINTER(StepOptions)
+
 _SIGS = {
     "dpopt_reduce_adam": ([_PP, _I, _I64, _I, _I64, _P, _P, _P, _P, _F, _F, _F, _F, _I64, _P], _I),
     "dpopt_reduce_adam_ex": ([_PP, _I, _I, _I64, _I, _I64, _P, _P, _P, _P, _F, _F, _F, _F, _I64,
@@ -59,6 +68,13 @@ _SIGS = {
     "dpopt_state_bytes": ([_I64, _I, _I, _I, ctypes.POINTER(ctypes.c_double)], _I),
     "dpopt_version": ([], ctypes.c_char_p),
     "dpopt_launch_count": ([], _I64),
+    "dpopt_reduce_adamw": ([_PP, _I, _I, _I64, _I, _I64, _P, _P, _P, _P, _F, _F, _F, _F, _I64,
+                            _POPT, _P], _I),
+    "dpopt_reduce_adamw_buckets": ([_PP, _I, _I, _PI64, _PI64, _I64, _P, _P, _P, _P, _F, _F, _F,
+                                    _F, _I64, _POPT, _P], _I),
+    "dpopt_grad_sqnorm": ([_PP, _I, _I, _I64, _I, _F, _P, _P, _I64, _P], _I),
+    "dpopt_grad_sqnorm_buckets": ([_PP, _I, _I, _PI64, _PI64, _I64, _F, _P, _P, _I64, _P], _I),
+    "dpopt_grad_sqnorm_scratch_bytes": ([_I64, _I64, _PI64], _I),
     "dpopt_set_kernel_policy": ([_I], _I),
     "dpopt_get_kernel_policy": ([], _I),
     "dpopt_selftest_wait_timeout": ([_I64, _P], _I),
@@ -138,6 +154,56 @@ def dpopt_reduce_adam_buckets(slice_table: Sequence[int], grad_dtype: int, n_rep
     return _lib.dpopt_reduce_adam_buckets(_ptr_array(slice_table), grad_dtype, n_replicas, offs,
                                           lns, nb, master, m, v, param_bf16_out, lr, beta1, beta2,
                                           eps, step, stream)
+
+
+def _opts(opts):
+    return ctypes.byref(opts) if opts is not None else None
+
+
+def dpopt_reduce_adamw(grads: Sequence[int], grad_dtype: int, n_replicas: int, numel: int,
+                       shard_rank: int, bucket_elems: int, master: int, m: int, v: int,
+                       param_bf16_out: int, lr: float, beta1: float, beta2: float, eps: float,
+                       step: int, opts: StepOptions | None, stream: int = 0) -> int:
+    return _lib.dpopt_reduce_adamw(_ptr_array(grads) if grads is not None else None, grad_dtype,
+                                   n_replicas, numel, shard_rank, bucket_elems, master, m, v,
+                                   param_bf16_out, lr, beta1, beta2, eps, step, _opts(opts),
+                                   stream)
+
+
+def dpopt_reduce_adamw_buckets(slice_table: Sequence[int], grad_dtype: int, n_replicas: int,
+                               offsets: Sequence[int], lens: Sequence[int], master: int, m: int,
+                               v: int, param_bf16_out: int, lr: float, beta1: float, beta2: float,
+                               eps: float, step: int, opts: StepOptions | None,
+                               stream: int = 0) -> int:
+    nb = len(offsets)
+    return _lib.dpopt_reduce_adamw_buckets(
+        _ptr_array(slice_table), grad_dtype, n_replicas, (ctypes.c_int64 * nb)(*offsets),
+        (ctypes.c_int64 * nb)(*lens), nb, master, m, v, param_bf16_out, lr, beta1, beta2, eps,
+        step, _opts(opts), stream)
+
+
+def dpopt_grad_sqnorm(grads: Sequence[int], grad_dtype: int, n_replicas: int, numel: int,
+                      shard_rank: int, grad_unscale: float, sqnorm_out: int, scratch: int,
+                      scratch_bytes: int, stream: int = 0) -> int:
+    return _lib.dpopt_grad_sqnorm(_ptr_array(grads) if grads is not None else None, grad_dtype,
+                                  n_replicas, numel, shard_rank, grad_unscale, sqnorm_out, scratch,
+                                  scratch_bytes, stream)
+
+
+def dpopt_grad_sqnorm_buckets(slice_table: Sequence[int], grad_dtype: int, n_replicas: int,
+                              offsets: Sequence[int], lens: Sequence[int], grad_unscale: float,
+                              sqnorm_out: int, scratch: int, scratch_bytes: int,
+                              stream: int = 0) -> int:
+    nb = len(offsets)
+    return _lib.dpopt_grad_sqnorm_buckets(
+        _ptr_array(slice_table), grad_dtype, n_replicas, (ctypes.c_int64 * nb)(*offsets),
+        (ctypes.c_int64 * nb)(*lens), nb, grad_unscale, sqnorm_out, scratch, scratch_bytes, stream)
+
+
+def dpopt_grad_sqnorm_scratch_bytes(elems: int, n_buckets: int = 1) -> tuple[int, int]:
+    out = ctypes.c_int64(0)
+    rc = _lib.dpopt_grad_sqnorm_scratch_bytes(elems, n_buckets, ctypes.byref(out))
+    return rc, out.value
 
 
 def dpopt_stream_status(stream: int = 0) -> int:
@@ -239,6 +305,60 @@ def reduce_adam_buckets(bucket_slices, offsets, master, m, v, param_bf16_out, *,
                                    m.data_ptr(), v.data_ptr(), param_bf16_out.data_ptr(), lr,
                                    beta1, beta2, eps, step, _stream_handle(stream))
     _check(rc, "dpopt_reduce_adam_buckets")
+
+
+def step_options(weight_decay: float = 0.0, max_grad_norm: float = 0.0, grad_sqnorm=None,
+                 grad_unscale: float = 0.0) -> StepOptions:
+    """Build a dpopt_step_options; grad_sqnorm is a 1-element float64 device tensor."""
+    return StepOptions(weight_decay, max_grad_norm,
+                       grad_sqnorm.data_ptr() if grad_sqnorm is not None else None, grad_unscale)
+
+
+def reduce_adamw(grads, shard_rank: int, bucket_elems: int, master, m, v, param_bf16_out, *,
+                 lr: float, beta1: float, beta2: float, eps: float, step: int,
+                 opts: StepOptions | None, stream=None) -> None:
+    dt = _grad_dtype(grads[0])
+    rc = dpopt_reduce_adamw([g.data_ptr() for g in grads], dt, len(grads), grads[0].numel(),
+                            shard_rank, bucket_elems, master.data_ptr(), m.data_ptr(), v.data_ptr(),
+                            param_bf16_out.data_ptr(), lr, beta1, beta2, eps, step, opts,
+                            _stream_handle(stream))
+    _check(rc, "dpopt_reduce_adamw")
+
+
+def reduce_adamw_buckets(bucket_slices, offsets, master, m, v, param_bf16_out, *, lr: float,
+                         beta1: float, beta2: float, eps: float, step: int,
+                         opts: StepOptions | None, stream=None) -> None:
+    n = len(bucket_slices[0])
+    dt = _grad_dtype(bucket_slices[0][0])
+    table = [t.data_ptr() for row in bucket_slices for t in row]
+    lens = [row[0].numel() for row in bucket_slices]
+    rc = dpopt_reduce_adamw_buckets(table, dt, n, list(offsets), lens, master.data_ptr(),
+                                    m.data_ptr(), v.data_ptr(), param_bf16_out.data_ptr(), lr,
+                                    beta1, beta2, eps, step, opts, _stream_handle(stream))
+    _check(rc, "dpopt_reduce_adamw_buckets")
+
+
+def grad_sqnorm(grads, shard_rank: int, sqnorm_out, scratch, *, grad_unscale: float = 0.0,
+                stream=None) -> None:
+    """sqnorm_out: 1-element float64 device tensor; scratch: device tensor of at least
+    dpopt_grad_sqnorm_scratch_bytes(S) bytes."""
+    dt = _grad_dtype(grads[0])
+    rc = dpopt_grad_sqnorm([g.data_ptr() for g in grads], dt, len(grads), grads[0].numel(),
+                           shard_rank, grad_unscale, sqnorm_out.data_ptr(), scratch.data_ptr(),
+                           scratch.numel() * scratch.element_size(), _stream_handle(stream))
+    _check(rc, "dpopt_grad_sqnorm")
+
+
+def grad_sqnorm_buckets(bucket_slices, offsets, sqnorm_out, scratch, *, grad_unscale: float = 0.0,
+                        stream=None) -> None:
+    n = len(bucket_slices[0])
+    dt = _grad_dtype(bucket_slices[0][0])
+    table = [t.data_ptr() for row in bucket_slices for t in row]
+    lens = [row[0].numel() for row in bucket_slices]
+    rc = dpopt_grad_sqnorm_buckets(table, dt, n, list(offsets), lens, grad_unscale,
+                                   sqnorm_out.data_ptr(), scratch.data_ptr(),
+                                   scratch.numel() * scratch.element_size(), _stream_handle(stream))
+    _check(rc, "dpopt_grad_sqnorm_buckets")
 
 
 def stream_status(stream=None) -> None:

@@ -82,6 +82,11 @@ Hyper make_hyper(float lr, float beta1, float beta2, float eps, int64_t step, in
   h.eps = eps;
   h.n_f = (float)n;
   h.inv_n = ((n & (n - 1)) == 0) ? (float)(1.0 / n) : 0.f;
+  h.k_hi = 1.f;
+  h.k_lo = 0.f;
+  h.sqnorm = nullptr;
+  h.max_norm = 0.0;
+  h.unscale = 1.f;
   return h;
 }
 
@@ -130,13 +135,14 @@ int check_states(float* master, float* m, float* v, void* out, int64_t lo_elem, 
   return DPOPT_OK;
 }
 
-int check_grad(const void* p, int64_t len, size_t esize, const Range st[4]) {
+int check_grad(const void* p, int64_t len, size_t esize, const Range* avoid, int navoid) {
   if (!p) return fail(DPOPT_ERR_INVALID_ARG, "null gradient pointer");
   if ((uintptr_t)p % esize) return fail(DPOPT_ERR_INVALID_ARG, "misaligned gradient pointer");
   Range g{(uintptr_t)p, (uintptr_t)p + (uintptr_t)len * esize};
-  for (int i = 0; i < 4; ++i)
-    if (overlaps(g, st[i]))
-      return fail(DPOPT_ERR_INVALID_ARG, "a gradient buffer overlaps a state or output array");
+  for (int i = 0; i < navoid; ++i)
+    if (overlaps(g, avoid[i]))
+      return fail(DPOPT_ERR_INVALID_ARG, "a gradient buffer overlaps a state, output or scratch "
+                                         "range");
   return DPOPT_OK;
 }
 
@@ -169,9 +175,9 @@ struct SegDesc {
   int64_t len;
 };
 
-template <int NR, int GK, int PACK, int MS, int MP>
+template <int NR, int GK, int PACK, bool EXT, int MS, int MP>
 int launch_one(const LaunchParams<MS, MP>& p, cudaStream_t stream) {
-  auto kern = reduce_adam_ldg_kernel<NR, GK, PACK, MS, MP>;
+  auto kern = reduce_adam_ldg_kernel<NR, GK, PACK, EXT, MS, MP>;
   int sms = 0;
   int rc = sm_count(&sms);
   if (rc) return rc;
@@ -196,39 +202,43 @@ int launch_one(const LaunchParams<MS, MP>& p, cudaStream_t stream) {
 // Kernel choice by measurement on GB300: the scalar-lane body for N <= 8
 // (optimizer arithmetic dominates), the packed f32x2 body above (the replica
 // sum dominates); N in {1, 2, 4, 8} get a fully unrolled replica loop.
-template <int GK, int MS, int MP>
+template <int GK, bool EXT, int MS, int MP>
 int dispatch_gk(const LaunchParams<MS, MP>& p, cudaStream_t stream) {
   const int n = p.n_rep;
   if constexpr (MS == kSmallSegs) {
     switch (n) {
-      case 1: return launch_one<1, GK, 0>(p, stream);
-      case 2: return launch_one<2, GK, 0>(p, stream);
-      case 4: return launch_one<4, GK, 0>(p, stream);
-      case 8: return launch_one<8, GK, 0>(p, stream);
+      case 1: return launch_one<1, GK, 0, EXT>(p, stream);
+      case 2: return launch_one<2, GK, 0, EXT>(p, stream);
+      case 4: return launch_one<4, GK, 0, EXT>(p, stream);
+      case 8: return launch_one<8, GK, 0, EXT>(p, stream);
       default: break;
     }
   }
-  if (n <= 8) return launch_one<0, GK, 0>(p, stream);
-  return launch_one<0, GK, 1>(p, stream);
+  if (n <= 8) return launch_one<0, GK, 0, EXT>(p, stream);
+  return launch_one<0, GK, 1, EXT>(p, stream);
 }
 
 template <int MS, int MP>
-int dispatch(const LaunchParams<MS, MP>& p, int grad_dtype, cudaStream_t stream) {
-  if (grad_dtype == DPOPT_GRAD_BF16) return dispatch_gk<0>(p, stream);
-  return dispatch_gk<1>(p, stream);
+int dispatch(const LaunchParams<MS, MP>& p, int grad_dtype, bool ext, cudaStream_t stream) {
+  if (grad_dtype == DPOPT_GRAD_BF16)
+    return ext ? dispatch_gk<0, true>(p, stream) : dispatch_gk<0, false>(p, stream);
+  return ext ? dispatch_gk<1, true>(p, stream) : dispatch_gk<1, false>(p, stream);
 }
 
-// Fill and launch one LaunchParams from segments [s0, s1).
+// Fill the segment table of one LaunchParams from segments [s0, s1);
+// `unit` is the element count one index of Seg::first_group stands for (8 for
+// the update's groups, kNormChunk for the norm's chunks).  Returns the index
+// total (0 when every segment is empty).
 template <int MS, int MP>
-int run_segments(LaunchParams<MS, MP>& p, const SegDesc* segs, int s0, int s1, int n,
-                 cudaStream_t stream, int grad_dtype) {
-  int64_t groups = 0;
+int64_t fill_segments(LaunchParams<MS, MP>& p, const SegDesc* segs, int s0, int s1, int n,
+                      int64_t unit) {
+  int64_t units = 0;
   int nseg = 0;
   for (int s = s0; s < s1; ++s) {
     const SegDesc& d = segs[s];
     if (d.len == 0) continue;
     Seg& sg = p.seg[nseg];
-    sg.first_group = groups;
+    sg.first_group = units;
     sg.state_off = d.state_off;
     sg.len = d.len;
     sg.ptr_base = nseg * n;
@@ -239,15 +249,21 @@ int run_segments(LaunchParams<MS, MP>& p, const SegDesc* segs, int s0, int s1, i
       vec = vec && aligned16(d.ptrs[r]);
     }
     sg.vec = vec ? 1 : 0;
-    groups += (d.len + kGroup - 1) / kGroup;
+    units += (d.len + unit - 1) / unit;
     ++nseg;
   }
-  if (nseg == 0) return DPOPT_OK;
-  p.seg[nseg].first_group = groups;
+  p.seg[nseg].first_group = units;
   p.seg[nseg].len = 0;
   p.nseg = nseg;
-  p.total_groups = groups;
-  return dispatch(p, grad_dtype, stream);
+  p.total_groups = units;
+  return units;
+}
+
+template <int MS, int MP>
+int run_segments(LaunchParams<MS, MP>& p, const SegDesc* segs, int s0, int s1, int n,
+                 cudaStream_t stream, int grad_dtype, bool ext) {
+  if (fill_segments(p, segs, s0, s1, n, kGroup) == 0) return DPOPT_OK;
+  return dispatch(p, grad_dtype, ext, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -356,9 +372,9 @@ bool use_tma(const SegDesc* segs, int s0, int s1, int n, int grad_dtype, float* 
 }
 
 int run(const SegDesc* segs, int nsegs, int grad_dtype, int n, float* master, float* m, float* v,
-        void* out, const Hyper& h, cudaStream_t stream) {
+        void* out, const Hyper& h, bool ext, cudaStream_t stream) {
   if (nsegs == 1) {
-    if (use_tma(segs, 0, 1, n, grad_dtype, master, m, v, out)) {
+    if (!ext && use_tma(segs, 0, 1, n, grad_dtype, master, m, v, out)) {
       SmallTma p{};
       p.h = h;
       p.master = master; p.m = m; p.v = v; p.out = (uint16_t*)out;
@@ -369,13 +385,13 @@ int run(const SegDesc* segs, int nsegs, int grad_dtype, int n, float* master, fl
     p.h = h;
     p.master = master; p.m = m; p.v = v; p.out = (uint16_t*)out;
     p.n_rep = n;
-    return run_segments(p, segs, 0, 1, n, stream, grad_dtype);
+    return run_segments(p, segs, 0, 1, n, stream, grad_dtype, ext);
   }
   const int per_launch = std::min(kBigSegs, kBigPtrs / n);
   for (int s0 = 0; s0 < nsegs; s0 += per_launch) {
     const int s1 = std::min(nsegs, s0 + per_launch);
     int rc;
-    if (use_tma(segs, s0, s1, n, grad_dtype, master, m, v, out)) {
+    if (!ext && use_tma(segs, s0, s1, n, grad_dtype, master, m, v, out)) {
       static thread_local BigTma p;  // 20 KB: kept off the stack
       std::memset(&p, 0, sizeof p);
       p.h = h;
@@ -388,10 +404,70 @@ int run(const SegDesc* segs, int nsegs, int grad_dtype, int n, float* master, fl
       p.h = h;
       p.master = master; p.m = m; p.v = v; p.out = (uint16_t*)out;
       p.n_rep = n;
-      rc = run_segments(p, segs, s0, s1, n, stream, grad_dtype);
+      rc = run_segments(p, segs, s0, s1, n, stream, grad_dtype, ext);
     }
     if (rc) return rc;
   }
+  return DPOPT_OK;
+}
+
+// ---------------------------------------------------------------------------
+// squared-norm pre-pass
+// ---------------------------------------------------------------------------
+
+int64_t norm_chunks(const SegDesc* segs, int nsegs) {
+  int64_t c = 0;
+  for (int s = 0; s < nsegs; ++s) c += (segs[s].len + kNormChunk - 1) / kNormChunk;
+  return c;
+}
+
+template <int MS, int MP>
+int launch_sqnorm(LaunchParams<MS, MP>& p, int64_t nchunks, double* partials, int grad_dtype,
+                  cudaStream_t stream) {
+  int sms = 0;
+  int rc = sm_count(&sms);
+  if (rc) return rc;
+  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nchunks, (int64_t)sms * 4));
+  if (grad_dtype == DPOPT_GRAD_BF16)
+    grad_sqnorm_kernel<0, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks);
+  else
+    grad_sqnorm_kernel<1, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  ++g_launches;
+  return DPOPT_OK;
+}
+
+// Squared norm of segments [0, nsegs) into *out (device), partials in scratch.
+int run_sqnorm(const SegDesc* segs, int nsegs, int grad_dtype, int n, const Hyper& h,
+               double* partials, double* out, cudaStream_t stream) {
+  const int per_launch = nsegs == 1 ? 1 : std::min(kBigSegs, kBigPtrs / n);
+  int64_t done = 0;
+  for (int s0 = 0; s0 < nsegs; s0 += per_launch) {
+    const int s1 = std::min(nsegs, s0 + per_launch);
+    int64_t chunks;
+    int rc;
+    if (nsegs == 1) {
+      SmallParams p{};
+      p.h = h;
+      p.n_rep = n;
+      chunks = fill_segments(p, segs, s0, s1, n, kNormChunk);
+      rc = chunks ? launch_sqnorm(p, chunks, partials + done, grad_dtype, stream) : DPOPT_OK;
+    } else {
+      static thread_local BigParams p;
+      std::memset(&p, 0, sizeof p);
+      p.h = h;
+      p.n_rep = n;
+      chunks = fill_segments(p, segs, s0, s1, n, kNormChunk);
+      rc = chunks ? launch_sqnorm(p, chunks, partials + done, grad_dtype, stream) : DPOPT_OK;
+    }
+    if (rc) return rc;
+    done += chunks;
+  }
+  sqnorm_finish_kernel<<<1, kThreads, 0, stream>>>(partials, done, out);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  ++g_launches;
   return DPOPT_OK;
 }
 
@@ -402,10 +478,16 @@ using namespace dpopt;
 
 extern "C" {
 
-int dpopt_reduce_adam_ex(const void* const* grads, int grad_dtype, int n_replicas, int64_t numel,
-                         int shard_rank, int64_t bucket_elems, float* master_f32, float* m_f32,
-                         float* v_f32, void* param_bf16_out, float lr, float beta1, float beta2,
-                         float eps, int64_t step, dpopt_stream_t stream) {
+}  // extern "C"
+
+namespace dpopt {
+namespace {
+
+// The segments of a full-buffer call (one: the whole shard), checked.  `avoid`
+// lists extra ranges the gradients must not overlap (states, outputs, scratch).
+int build_full(const void* const* grads, int grad_dtype, int n_replicas, int64_t numel,
+               int shard_rank, int64_t bucket_elems, const Range* avoid, int navoid,
+               const void* ptrs_out[DPOPT_MAX_REPLICAS], int64_t* S_out) {
   int rc = check_replicas(n_replicas, grad_dtype);
   if (rc) return rc;
   if (!grads) return fail(DPOPT_ERR_INVALID_ARG, "grads must be non-null");
@@ -414,29 +496,188 @@ int dpopt_reduce_adam_ex(const void* const* grads, int grad_dtype, int n_replica
   if (shard_rank < 0 || shard_rank >= n_replicas)
     return fail(DPOPT_ERR_INVALID_ARG, "shard_rank must lie in [0, n_replicas)");
   if (bucket_elems < 1) return fail(DPOPT_ERR_INVALID_ARG, "bucket_elems must be >= 1");
-  rc = check_hyper(lr, beta1, beta2, eps, step);
-  if (rc) return rc;
   const int64_t S = numel / n_replicas;
   const int64_t base = (int64_t)shard_rank * S;
   const size_t esize = grad_dtype == DPOPT_GRAD_BF16 ? 2 : 4;
+  *S_out = S;
   if (S == 0) return DPOPT_OK;
-  Range st[4];
-  rc = check_states(master_f32, m_f32, v_f32, param_bf16_out, 0, S, st);
-  if (rc) return rc;
-  const void* ptrs[DPOPT_MAX_REPLICAS];
   for (int r = 0; r < n_replicas; ++r) {
     if (!grads[r]) return fail(DPOPT_ERR_INVALID_ARG, "null gradient pointer");
-    ptrs[r] = (const char*)grads[r] + (size_t)base * esize;
-    rc = check_grad(ptrs[r], S, esize, st);
+    ptrs_out[r] = (const char*)grads[r] + (size_t)base * esize;
+    rc = check_grad(ptrs_out[r], S, esize, avoid, navoid);
     if (rc) return rc;
   }
-  // Every contribution is resident and the buckets tile the shard contiguously,
-  // so the whole shard is one segment: bucket_elems changes neither the
-  // addresses nor the result, only what the bucket iterator reports.
-  SegDesc seg{ptrs, 0, S};
+  return DPOPT_OK;
+}
+
+// The segments of a batched-bucket call, checked; lo/hi receive the span of
+// shard elements they update.
+int build_buckets(const void* const* slice_table, int grad_dtype, int n_replicas,
+                  const int64_t* offsets, const int64_t* lens, int64_t n_buckets,
+                  std::vector<SegDesc>& segs, int64_t* lo_out, int64_t* hi_out) {
+  int rc = check_replicas(n_replicas, grad_dtype);
+  if (rc) return rc;
+  if (n_buckets < 0) return fail(DPOPT_ERR_INVALID_ARG, "n_buckets must be >= 0");
+  segs.clear();
+  *lo_out = *hi_out = 0;
+  if (n_buckets == 0) return DPOPT_OK;
+  if (!slice_table || !offsets || !lens)
+    return fail(DPOPT_ERR_INVALID_ARG, "slice_table, offsets and lens must be non-null");
+  if (n_buckets > (int64_t)1 << 30) return fail(DPOPT_ERR_UNSUPPORTED, "too many buckets");
+  int64_t lo = INT64_MAX, hi = 0;
+  std::vector<std::pair<int64_t, int64_t>> spans;
+  spans.reserve((size_t)n_buckets);
+  for (int64_t b = 0; b < n_buckets; ++b) {
+    if (offsets[b] < 0 || lens[b] < 0 || offsets[b] > INT64_MAX - lens[b])
+      return fail(DPOPT_ERR_INVALID_ARG, "bucket %lld: bad offset/len", (long long)b);
+    if (lens[b] == 0) continue;
+    lo = std::min(lo, offsets[b]);
+    hi = std::max(hi, offsets[b] + lens[b]);
+    spans.emplace_back(offsets[b], offsets[b] + lens[b]);
+  }
+  if (spans.empty()) return DPOPT_OK;
+  std::sort(spans.begin(), spans.end());
+  for (size_t i = 1; i < spans.size(); ++i)
+    if (spans[i].first < spans[i - 1].second)
+      return fail(DPOPT_ERR_INVALID_ARG, "buckets overlap");
+  segs.reserve((size_t)n_buckets);
+  for (int64_t b = 0; b < n_buckets; ++b) {
+    if (lens[b] == 0) continue;
+    segs.push_back(SegDesc{slice_table + b * n_replicas, offsets[b], lens[b]});
+  }
+  *lo_out = lo;
+  *hi_out = hi;
+  return DPOPT_OK;
+}
+
+int check_bucket_grads(const std::vector<SegDesc>& segs, int n, int grad_dtype, const Range* avoid,
+                       int navoid) {
+  const size_t esize = grad_dtype == DPOPT_GRAD_BF16 ? 2 : 4;
+  for (const SegDesc& d : segs)
+    for (int r = 0; r < n; ++r) {
+      int rc = check_grad(d.ptrs[r], d.len, esize, avoid, navoid);
+      if (rc) return rc;
+    }
+  return DPOPT_OK;
+}
+
+// Step options (null: plain Adam) -> the EXT fields of Hyper.  Returns
+// whether the extended kernel is needed.
+int apply_options(const dpopt_step_options* o, float lr, Hyper& h, bool* ext) {
+  *ext = false;
+  if (!o) return DPOPT_OK;
+  if (!std::isfinite(o->weight_decay) || o->weight_decay < 0.f)
+    return fail(DPOPT_ERR_INVALID_ARG, "weight_decay must be finite and >= 0");
+  if (!std::isfinite(o->max_grad_norm) || o->max_grad_norm < 0.f)
+    return fail(DPOPT_ERR_INVALID_ARG, "max_grad_norm must be finite and >= 0");
+  if (!std::isfinite(o->grad_unscale) || o->grad_unscale < 0.f)
+    return fail(DPOPT_ERR_INVALID_ARG, "grad_unscale must be finite and >= 0");
+  if (o->max_grad_norm > 0.f) {
+    if (!o->grad_sqnorm || ((uintptr_t)o->grad_sqnorm & 7u))
+      return fail(DPOPT_ERR_INVALID_ARG, "clipping needs an 8-byte aligned grad_sqnorm");
+    h.sqnorm = o->grad_sqnorm;
+    h.max_norm = (double)o->max_grad_norm;
+  }
+  const double k = 1.0 - (double)lr * (double)o->weight_decay;
+  h.k_hi = (float)k;
+  h.k_lo = (float)(k - (double)h.k_hi);
+  h.unscale = o->grad_unscale == 0.f ? 1.f : o->grad_unscale;
+  *ext = true;
+  return DPOPT_OK;
+}
+
+int full_impl(const void* const* grads, int grad_dtype, int n_replicas, int64_t numel,
+              int shard_rank, int64_t bucket_elems, float* master, float* m, float* v, void* out,
+              float lr, float beta1, float beta2, float eps, int64_t step,
+              const dpopt_step_options* opts, cudaStream_t stream) {
+  int rc = check_replicas(n_replicas, grad_dtype);
+  if (rc) return rc;
+  rc = check_hyper(lr, beta1, beta2, eps, step);
+  if (rc) return rc;
   Hyper h = make_hyper(lr, beta1, beta2, eps, step, n_replicas);
-  return run(&seg, 1, grad_dtype, n_replicas, master_f32, m_f32, v_f32, param_bf16_out, h,
-             (cudaStream_t)stream);
+  bool ext = false;
+  rc = apply_options(opts, lr, h, &ext);
+  if (rc) return rc;
+  if (numel > 0 && numel % n_replicas == 0 && numel / n_replicas > 0) {
+    Range st[4];
+    rc = check_states(master, m, v, out, 0, numel / n_replicas, st);
+    if (rc) return rc;
+    const void* ptrs[DPOPT_MAX_REPLICAS];
+    int64_t S = 0;
+    rc = build_full(grads, grad_dtype, n_replicas, numel, shard_rank, bucket_elems, st, 4, ptrs,
+                    &S);
+    if (rc) return rc;
+    // Every contribution is resident and the buckets tile the shard
+    // contiguously, so the whole shard is one segment: bucket_elems changes
+    // neither the addresses nor the result, only what the iterator reports.
+    SegDesc seg{ptrs, 0, S};
+    return run(&seg, 1, grad_dtype, n_replicas, master, m, v, out, h, ext, stream);
+  }
+  const void* ptrs[DPOPT_MAX_REPLICAS];
+  int64_t S = 0;
+  return build_full(grads, grad_dtype, n_replicas, numel, shard_rank, bucket_elems, nullptr, 0,
+                    ptrs, &S);
+}
+
+int buckets_impl(const void* const* slice_table, int grad_dtype, int n_replicas,
+                 const int64_t* offsets, const int64_t* lens, int64_t n_buckets, float* master,
+                 float* m, float* v, void* out, float lr, float beta1, float beta2, float eps,
+                 int64_t step, const dpopt_step_options* opts, cudaStream_t stream) {
+  int rc = check_replicas(n_replicas, grad_dtype);
+  if (rc) return rc;
+  rc = check_hyper(lr, beta1, beta2, eps, step);
+  if (rc) return rc;
+  Hyper h = make_hyper(lr, beta1, beta2, eps, step, n_replicas);
+  bool ext = false;
+  rc = apply_options(opts, lr, h, &ext);
+  if (rc) return rc;
+  std::vector<SegDesc> segs;
+  int64_t lo = 0, hi = 0;
+  rc = build_buckets(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets, segs, &lo, &hi);
+  if (rc || segs.empty()) return rc;
+  Range st[4];
+  rc = check_states(master, m, v, out, lo, hi, st);
+  if (rc) return rc;
+  rc = check_bucket_grads(segs, n_replicas, grad_dtype, st, 4);
+  if (rc) return rc;
+  return run(segs.data(), (int)segs.size(), grad_dtype, n_replicas, master, m, v, out, h, ext,
+             stream);
+}
+
+int check_norm_outputs(double* sqnorm_out, void* scratch, int64_t scratch_bytes, int64_t chunks,
+                       Range avoid[2]) {
+  if (!sqnorm_out || ((uintptr_t)sqnorm_out & 7u))
+    return fail(DPOPT_ERR_INVALID_ARG, "sqnorm_out must be a non-null, 8-byte aligned pointer");
+  if (chunks > 0 && (!scratch || ((uintptr_t)scratch & 7u)))
+    return fail(DPOPT_ERR_INVALID_ARG, "scratch must be a non-null, 8-byte aligned pointer");
+  if (scratch_bytes < chunks * 8)
+    return fail(DPOPT_ERR_INVALID_ARG, "scratch holds %lld bytes, %lld needed",
+                (long long)scratch_bytes, (long long)(chunks * 8));
+  avoid[0] = {(uintptr_t)sqnorm_out, (uintptr_t)(sqnorm_out + 1)};
+  avoid[1] = {(uintptr_t)scratch, (uintptr_t)scratch + (uintptr_t)(chunks * 8)};
+  if (chunks > 0 && overlaps(avoid[0], avoid[1]))
+    return fail(DPOPT_ERR_INVALID_ARG, "sqnorm_out lies inside the scratch partials");
+  return DPOPT_OK;
+}
+
+int finish_empty_norm(double* sqnorm_out, cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(sqnorm_out, 0, sizeof(double), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  return DPOPT_OK;
+}
+
+}  // namespace
+}  // namespace dpopt
+
+extern "C" {
+
+int dpopt_reduce_adam_ex(const void* const* grads, int grad_dtype, int n_replicas, int64_t numel,
+                         int shard_rank, int64_t bucket_elems, float* master_f32, float* m_f32,
+                         float* v_f32, void* param_bf16_out, float lr, float beta1, float beta2,
+                         float eps, int64_t step, dpopt_stream_t stream) {
+  return full_impl(grads, grad_dtype, n_replicas, numel, shard_rank, bucket_elems, master_f32,
+                   m_f32, v_f32, param_bf16_out, lr, beta1, beta2, eps, step, nullptr,
+                   (cudaStream_t)stream);
 }
 
 int dpopt_reduce_adam(const void* const* grads, int n_replicas, int64_t numel, int shard_rank,
@@ -446,6 +687,16 @@ int dpopt_reduce_adam(const void* const* grads, int n_replicas, int64_t numel, i
   return dpopt_reduce_adam_ex(grads, DPOPT_GRAD_BF16, n_replicas, numel, shard_rank, bucket_elems,
                               master_f32, m_f32, v_f32, param_bf16_out, lr, beta1, beta2, eps,
                               step, stream);
+}
+
+int dpopt_reduce_adamw(const void* const* grads, int grad_dtype, int n_replicas, int64_t numel,
+                       int shard_rank, int64_t bucket_elems, float* master_f32, float* m_f32,
+                       float* v_f32, void* param_bf16_out, float lr, float beta1, float beta2,
+                       float eps, int64_t step, const dpopt_step_options* opts,
+                       dpopt_stream_t stream) {
+  return full_impl(grads, grad_dtype, n_replicas, numel, shard_rank, bucket_elems, master_f32,
+                   m_f32, v_f32, param_bf16_out, lr, beta1, beta2, eps, step, opts,
+                   (cudaStream_t)stream);
 }
 
 int dpopt_bucket_count(int64_t shard_elems, int64_t bucket_elems, int64_t* count_out) {
@@ -473,49 +724,78 @@ int dpopt_reduce_adam_buckets(const void* const* slice_table, int grad_dtype, in
                               float* master_f32, float* m_f32, float* v_f32, void* param_bf16_out,
                               float lr, float beta1, float beta2, float eps, int64_t step,
                               dpopt_stream_t stream) {
+  return buckets_impl(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets, master_f32,
+                      m_f32, v_f32, param_bf16_out, lr, beta1, beta2, eps, step, nullptr,
+                      (cudaStream_t)stream);
+}
+
+int dpopt_reduce_adamw_buckets(const void* const* slice_table, int grad_dtype, int n_replicas,
+                               const int64_t* offsets, const int64_t* lens, int64_t n_buckets,
+                               float* master_f32, float* m_f32, float* v_f32,
+                               void* param_bf16_out, float lr, float beta1, float beta2, float eps,
+                               int64_t step, const dpopt_step_options* opts,
+                               dpopt_stream_t stream) {
+  return buckets_impl(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets, master_f32,
+                      m_f32, v_f32, param_bf16_out, lr, beta1, beta2, eps, step, opts,
+                      (cudaStream_t)stream);
+}
+
+int dpopt_grad_sqnorm_scratch_bytes(int64_t elems, int64_t n_buckets, int64_t* bytes_out) {
+  if (!bytes_out || elems < 0 || n_buckets < 0)
+    return fail(DPOPT_ERR_INVALID_ARG, "grad_sqnorm_scratch_bytes: invalid argument");
+  *bytes_out = 8 * ((elems + kNormChunk - 1) / kNormChunk + n_buckets);
+  return DPOPT_OK;
+}
+
+int dpopt_grad_sqnorm(const void* const* grads, int grad_dtype, int n_replicas, int64_t numel,
+                      int shard_rank, float grad_unscale, double* sqnorm_out, void* scratch,
+                      int64_t scratch_bytes, dpopt_stream_t stream) {
   int rc = check_replicas(n_replicas, grad_dtype);
   if (rc) return rc;
-  if (n_buckets < 0) return fail(DPOPT_ERR_INVALID_ARG, "n_buckets must be >= 0");
-  rc = check_hyper(lr, beta1, beta2, eps, step);
+  if (!std::isfinite(grad_unscale) || grad_unscale < 0.f)
+    return fail(DPOPT_ERR_INVALID_ARG, "grad_unscale must be finite and >= 0");
+  if (numel < 0 || numel % n_replicas != 0)
+    return fail(DPOPT_ERR_INVALID_ARG, "numel must be >= 0 and a multiple of n_replicas");
+  const int64_t S = numel / n_replicas;
+  const int64_t chunks = (S + kNormChunk - 1) / kNormChunk;
+  Range avoid[2];
+  rc = check_norm_outputs(sqnorm_out, scratch, scratch_bytes, chunks, avoid);
   if (rc) return rc;
-  if (n_buckets == 0) return DPOPT_OK;
-  if (!slice_table || !offsets || !lens)
-    return fail(DPOPT_ERR_INVALID_ARG, "slice_table, offsets and lens must be non-null");
-  if (n_buckets > (int64_t)1 << 30) return fail(DPOPT_ERR_UNSUPPORTED, "too many buckets");
-  const size_t esize = grad_dtype == DPOPT_GRAD_BF16 ? 2 : 4;
-  int64_t lo = INT64_MAX, hi = 0;
-  std::vector<std::pair<int64_t, int64_t>> spans;
-  spans.reserve((size_t)n_buckets);
-  for (int64_t b = 0; b < n_buckets; ++b) {
-    if (offsets[b] < 0 || lens[b] < 0 || offsets[b] > INT64_MAX - lens[b])
-      return fail(DPOPT_ERR_INVALID_ARG, "bucket %lld: bad offset/len", (long long)b);
-    if (lens[b] == 0) continue;
-    lo = std::min(lo, offsets[b]);
-    hi = std::max(hi, offsets[b] + lens[b]);
-    spans.emplace_back(offsets[b], offsets[b] + lens[b]);
-  }
-  if (spans.empty()) return DPOPT_OK;
-  std::sort(spans.begin(), spans.end());
-  for (size_t i = 1; i < spans.size(); ++i)
-    if (spans[i].first < spans[i - 1].second)
-      return fail(DPOPT_ERR_INVALID_ARG, "buckets overlap");
-  Range st[4];
-  rc = check_states(master_f32, m_f32, v_f32, param_bf16_out, lo, hi, st);
+  const void* ptrs[DPOPT_MAX_REPLICAS];
+  int64_t S2 = 0;
+  rc = build_full(grads, grad_dtype, n_replicas, numel, shard_rank, 1, avoid, chunks ? 2 : 1,
+                  ptrs, &S2);
   if (rc) return rc;
+  if (S == 0) return finish_empty_norm(sqnorm_out, (cudaStream_t)stream);
+  Hyper h = make_hyper(1.f, 0.f, 0.f, 0.f, 1, n_replicas);
+  h.unscale = grad_unscale == 0.f ? 1.f : grad_unscale;
+  SegDesc seg{ptrs, 0, S};
+  return run_sqnorm(&seg, 1, grad_dtype, n_replicas, h, (double*)scratch, sqnorm_out,
+                    (cudaStream_t)stream);
+}
+
+int dpopt_grad_sqnorm_buckets(const void* const* slice_table, int grad_dtype, int n_replicas,
+                              const int64_t* offsets, const int64_t* lens, int64_t n_buckets,
+                              float grad_unscale, double* sqnorm_out, void* scratch,
+                              int64_t scratch_bytes, dpopt_stream_t stream) {
+  if (!std::isfinite(grad_unscale) || grad_unscale < 0.f)
+    return fail(DPOPT_ERR_INVALID_ARG, "grad_unscale must be finite and >= 0");
   std::vector<SegDesc> segs;
-  segs.reserve((size_t)n_buckets);
-  for (int64_t b = 0; b < n_buckets; ++b) {
-    if (lens[b] == 0) continue;
-    const void* const* row = slice_table + b * n_replicas;
-    for (int r = 0; r < n_replicas; ++r) {
-      rc = check_grad(row[r], lens[b], esize, st);
-      if (rc) return rc;
-    }
-    segs.push_back(SegDesc{row, offsets[b], lens[b]});
-  }
-  Hyper h = make_hyper(lr, beta1, beta2, eps, step, n_replicas);
-  return run(segs.data(), (int)segs.size(), grad_dtype, n_replicas, master_f32, m_f32, v_f32,
-             param_bf16_out, h, (cudaStream_t)stream);
+  int64_t lo = 0, hi = 0;
+  int rc = build_buckets(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets, segs, &lo,
+                         &hi);
+  if (rc) return rc;
+  const int64_t chunks = norm_chunks(segs.data(), (int)segs.size());
+  Range avoid[2];
+  rc = check_norm_outputs(sqnorm_out, scratch, scratch_bytes, chunks, avoid);
+  if (rc) return rc;
+  rc = check_bucket_grads(segs, n_replicas, grad_dtype, avoid, chunks ? 2 : 1);
+  if (rc) return rc;
+  if (segs.empty()) return finish_empty_norm(sqnorm_out, (cudaStream_t)stream);
+  Hyper h = make_hyper(1.f, 0.f, 0.f, 0.f, 1, n_replicas);
+  h.unscale = grad_unscale == 0.f ? 1.f : grad_unscale;
+  return run_sqnorm(segs.data(), (int)segs.size(), grad_dtype, n_replicas, h, (double*)scratch,
+                    sqnorm_out, (cudaStream_t)stream);
 }
 
 int dpopt_reduce_adam_bucket(const void* const* grad_slices, int grad_dtype, int n_replicas,

@@ -201,9 +201,9 @@ struct GroupOut {
 
 // Scalar-lane form: 8 elements per thread, one element per operation.  Fewer
 // register pairings; faster when the optimizer arithmetic dominates (small N).
-template <int NR, int GK, class Src>
+template <int NR, int GK, bool EXT, class Src>
 __device__ __forceinline__ void group_vec_x1(const Src& src, int n, const Hyper& h,
-                                             const GroupOut& o) {
+                                             const GroupOut& o, float gscale) {
   float th[kGroup], mm[kGroup], vv[kGroup];
   {
     float4 a = src.state(0, 0), b = src.state(0, 1);
@@ -255,7 +255,8 @@ __device__ __forceinline__ void group_vec_x1(const Src& src, int n, const Hyper&
 #pragma unroll
   for (int k = 0; k < kGroup; ++k) {
     float g = acc[k].average(h);
-    adam_update(g, th[k], mm[k], vv[k], h);
+    if constexpr (EXT) g = __fmul_rn(g, gscale);
+    adam_update<EXT>(g, th[k], mm[k], vv[k], h);
   }
   st_stream16(o.master, th[0], th[1], th[2], th[3]);
   st_stream16(o.master + 4, th[4], th[5], th[6], th[7]);
@@ -269,9 +270,9 @@ __device__ __forceinline__ void group_vec_x1(const Src& src, int n, const Hyper&
 
 // Packed form: 4 element pairs per thread, every operation on f32x2 lanes.
 // Pays off when the replica sum dominates (large N).
-template <int NR, int GK, class Src>
+template <int NR, int GK, bool EXT, class Src>
 __device__ __forceinline__ void group_vec_x2(const Src& src, int n, const Hyper& h,
-                                             const GroupOut& o) {
+                                             const GroupOut& o, float gscale) {
   constexpr int P = kGroup / 2;  // element pairs per group
   float2 th[P], mm[P], vv[P];
   {
@@ -346,7 +347,8 @@ __device__ __forceinline__ void group_vec_x2(const Src& src, int n, const Hyper&
 #pragma unroll
   for (int j = 0; j < P; ++j) {
     float2 g = acc[j].average(h);
-    adam_update(g, th[j], mm[j], vv[j], h);
+    if constexpr (EXT) g = vmul(g, splat<float2>(gscale));
+    adam_update<EXT>(g, th[j], mm[j], vv[j], h);
   }
   st_stream16(o.master, th[0].x, th[0].y, th[1].x, th[1].y);
   st_stream16(o.master + 4, th[2].x, th[2].y, th[3].x, th[3].y);
@@ -362,8 +364,9 @@ __device__ __forceinline__ void group_vec_x2(const Src& src, int n, const Hyper&
 // a partial or unaligned group, one element at a time
 // ---------------------------------------------------------------------------
 
-template <int GK, class LP, class SegT>
-__device__ __noinline__ void group_scalar(const LP& p, const SegT& sg, int64_t e0, int count) {
+template <int GK, bool EXT, class LP, class SegT>
+__device__ __noinline__ void group_scalar(const LP& p, const SegT& sg, int64_t e0, int count,
+                                          float gscale) {
   const void* const* gp = p.gptr + sg.ptr_base;
   const int n = p.n_rep;
   for (int k = 0; k < count; ++k) {
@@ -373,7 +376,9 @@ __device__ __noinline__ void group_scalar(const LP& p, const SegT& sg, int64_t e
     acc.init(ld_grad1<GK>(gp[0], e));
     for (int r = 1; r < n; ++r) acc.add(ld_grad1<GK>(gp[r], e));
     float th = p.master[so], mm = p.m[so], vv = p.v[so];
-    adam_update(acc.average(p.h), th, mm, vv, p.h);
+    float g = acc.average(p.h);
+    if constexpr (EXT) g = __fmul_rn(g, gscale);
+    adam_update<EXT>(g, th, mm, vv, p.h);
     p.master[so] = th;
     p.m[so] = mm;
     p.v[so] = vv;
@@ -385,17 +390,20 @@ __device__ __noinline__ void group_scalar(const LP& p, const SegT& sg, int64_t e
 // the kernel
 // ---------------------------------------------------------------------------
 
-// Resident CTAs per SM the packed form's register budget is sized for: 4 x 256
-// threads (<= 64 registers) with an unrolled replica count, 2 for a runtime one.
+// Resident CTAs per SM the register budget is sized for: 4 x 256 threads
+// (<= 64 registers) with an unrolled replica count; the runtime-count bodies
+// take what they need (2 CTAs for the packed one).
 template <int NR, int PACK>
 constexpr int min_ctas() { return NR > 0 ? 4 : (PACK ? 2 : 1); }
 
 // PACK selects the lane form of the vector body (0: scalar, 1: f32x2); the
-// two forms give identical bits, so the choice is made by speed alone.
-template <int NR, int GK, int PACK, int MAXSEG, int MAXPTR>
+// two forms give identical bits, so the choice is made by speed alone.  EXT
+// adds the AdamW decay and the gradient multiplier (clipping, unscaling).
+template <int NR, int GK, int PACK, bool EXT, int MAXSEG, int MAXPTR>
 __global__ void __launch_bounds__(kThreads, min_ctas<NR, PACK>())
     reduce_adam_ldg_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p) {
   const uint64_t pol = evict_first_policy();
+  const float gscale = EXT ? grad_scale_of(p.h) : 1.f;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int si = 0;
   for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < p.total_groups;
@@ -409,12 +417,99 @@ __global__ void __launch_bounds__(kThreads, min_ctas<NR, PACK>())
       const GlobalSource<GK> src{p.gptr + sg.ptr_base, e0, {p.master + so, p.m + so, p.v + so},
                                  pol};
       const GroupOut o{p.master + so, p.m + so, p.v + so, p.out + so};
-      if constexpr (PACK) group_vec_x2<NR, GK>(src, p.n_rep, p.h, o);
-      else group_vec_x1<NR, GK>(src, p.n_rep, p.h, o);
+      if constexpr (PACK) group_vec_x2<NR, GK, EXT>(src, p.n_rep, p.h, o, gscale);
+      else group_vec_x1<NR, GK, EXT>(src, p.n_rep, p.h, o, gscale);
     } else {
-      group_scalar<GK>(p, sg, e0, (int)(rem < kGroup ? rem : kGroup));
+      group_scalar<GK, EXT>(p, sg, e0, (int)(rem < kGroup ? rem : kGroup), gscale);
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// squared L2 norm of the averaged gradient (the clipping pre-pass)
+// ---------------------------------------------------------------------------
+
+// Elements per partial sum.  Fixed, so the partition -- and therefore the
+// fp64 rounding of the total -- does not depend on the grid or the GPU.
+constexpr int kNormChunk = 65536;
+
+// One partial per chunk: sum over the chunk's elements, in element order per
+// thread and a fixed tree across threads, of (g * unscale)^2 in fp64, where g
+// is the same fixed-order average the step uses.  Seg::first_group holds the
+// segment's first chunk here.
+template <int GK, int MAXSEG, int MAXPTR>
+__global__ void __launch_bounds__(kThreads)
+    grad_sqnorm_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p, double* partials,
+                       int64_t nchunks) {
+  __shared__ double red[kThreads];
+  const uint64_t pol = evict_first_policy();
+  const double us = (double)p.h.unscale;
+  int si = 0;
+  for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+    while (c >= p.seg[si + 1].first_group) ++si;
+    const Seg& sg = p.seg[si];
+    const int64_t c0 = (c - sg.first_group) * (int64_t)kNormChunk;
+    const void* const* gp = p.gptr + sg.ptr_base;
+    double acc = 0.0;
+    for (int k = threadIdx.x; k < kNormChunk / kGroup; k += kThreads) {
+      const int64_t e0 = c0 + (int64_t)k * kGroup;
+      if (e0 >= sg.len) break;
+      const int64_t rem = sg.len - e0;
+      float g[kGroup];
+      int cnt = kGroup;
+      if (sg.vec && rem >= kGroup) {
+        CompSum<float> cs[kGroup];
+        GradLoad<GK> gl;
+        gl.load(gp[0], e0, pol);
+#pragma unroll
+        for (int j = 0; j < kGroup; ++j) cs[j].init(gl.get(j));
+        for (int r = 1; r < p.n_rep; ++r) {
+          gl.load(gp[r], e0, pol);
+#pragma unroll
+          for (int j = 0; j < kGroup; ++j) cs[j].add(gl.get(j));
+        }
+#pragma unroll
+        for (int j = 0; j < kGroup; ++j) g[j] = cs[j].average(p.h);
+      } else {
+        cnt = (int)(rem < kGroup ? rem : kGroup);
+        for (int j = 0; j < cnt; ++j) {
+          CompSum<float> cs;
+          cs.init(ld_grad1<GK>(gp[0], e0 + j));
+          for (int r = 1; r < p.n_rep; ++r) cs.add(ld_grad1<GK>(gp[r], e0 + j));
+          g[j] = cs.average(p.h);
+        }
+      }
+      for (int j = 0; j < cnt; ++j) {
+        const double x = __dmul_rn((double)g[j], us);
+        acc = __fma_rn(x, x, acc);
+      }
+    }
+    red[threadIdx.x] = acc;
+    __syncthreads();
+#pragma unroll
+    for (int w = kThreads / 2; w > 0; w >>= 1) {
+      if (threadIdx.x < w) red[threadIdx.x] = __dadd_rn(red[threadIdx.x], red[threadIdx.x + w]);
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) partials[c] = red[0];
+    __syncthreads();
+  }
+}
+
+// Sum of the partials in a fixed order: strided per thread, then a fixed tree.
+__global__ void __launch_bounds__(kThreads)
+    sqnorm_finish_kernel(const double* partials, int64_t nchunks, double* out) {
+  __shared__ double red[kThreads];
+  double acc = 0.0;
+  for (int64_t c = threadIdx.x; c < nchunks; c += kThreads) acc = __dadd_rn(acc, partials[c]);
+  red[threadIdx.x] = acc;
+  __syncthreads();
+#pragma unroll
+  for (int w = kThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] = __dadd_rn(red[threadIdx.x], red[threadIdx.x + w]);
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *out = red[0];
 }
 
 }  // namespace dpopt

@@ -41,8 +41,27 @@ struct Hyper {
   float eps;
   float inv_n;         // 1/N when N is a power of two (exact scaling), else 0
   float n_f;           // N
+  float k_hi, k_lo;    // 1 - lr*weight_decay (AdamW), used by the extended step only
+  // gradient scale of the extended step: g <- fl32(g * c), c an fp32 scalar
+  // computed once per launch from these (see grad_scale_of)
+  const double* sqnorm;  // device: squared global L2 norm of the averaged gradient, or null
+  double max_norm;       // clip threshold (used when sqnorm is non-null)
+  float unscale;         // multiplier applied first (1/loss scale; 1 when unused)
   float pad_;
 };
+
+// The extended step's gradient multiplier: c = unscale * min(1, max_norm /
+// (sqrt(sqnorm) + 1e-6)), evaluated in fp64 and rounded once to fp32.
+// The same value in every thread (one device scalar read).
+__device__ __forceinline__ float grad_scale_of(const Hyper& h) {
+  double c = (double)h.unscale;
+  if (h.sqnorm != nullptr) {
+    const double nrm = __dsqrt_rn(*h.sqnorm);
+    const double coef = __ddiv_rn(h.max_norm, __dadd_rn(nrm, 1e-6));
+    if (coef < 1.0) c = __dmul_rn(c, coef);
+  }
+  return __double2float_rn(c);
+}
 
 // ---------------------------------------------------------------------------
 // lane-generic IEEE operations (round to nearest even)
@@ -170,18 +189,22 @@ __device__ __forceinline__ V moment2(V v, V g, const Hyper& h) {
   return r;
 }
 
-// theta' = theta - lr * (m'/bc1) / (sqrt(v'/bc2) + eps), the plain fp32 form,
-// used for non-finite inputs or results.
+// theta' = k*theta - lr * (m'/bc1) / (sqrt(v'/bc2) + eps), the plain fp32 form
+// (k = 1 - lr*weight_decay, 1 for plain Adam), used for non-finite inputs or
+// results.
 __device__ __noinline__ float master_update_plain(float theta, float m_new, float v_new,
-                                                  float a_hi, float b_hi, float eps) {
+                                                  float a_hi, float b_hi, float eps, float k) {
   float d = __fadd_rn(__fmul_rn(__fsqrt_rn(v_new), b_hi), eps);
   float delta = __fdiv_rn(__fmul_rn(a_hi, m_new), d);
-  return __fsub_rn(theta, delta);
+  return __fsub_rn(__fmul_rn(theta, k), delta);
 }
 
 // theta' = theta - a*m' / (b*sqrt(v') + eps) with a = lr/bc1, b = 1/sqrt(bc2),
-// the quotient carried as q + q_lo and the subtraction rounded once.
-template <class V>
+// the quotient carried as q + q_lo and the subtraction rounded once.  With
+// EXT the decoupled weight decay of AdamW (Loshchilov & Hutter 2019) is
+// folded in: theta' = k*theta - a*m'/(...), k = 1 - lr*weight_decay carried
+// as a (hi, lo) pair and k*theta as an exact product.
+template <class V, bool EXT>
 __device__ __forceinline__ V master_update(V theta, V m_new, V v_new, const Hyper& h) {
   constexpr int L = Lanes<V>::n;
   // sqrt(v') as s + s_lo: approximate reciprocal square root, one correction
@@ -219,23 +242,32 @@ __device__ __forceinline__ V master_update(V theta, V m_new, V v_new, const Hype
   V r = vfma(vneg(q), D, n);
   r = vfma(vneg(q), D_lo, vadd(r, n_lo));
   V q_lo = vmul(r, rD);
-  // theta - (q + q_lo), rounded once
-  V t, te;
-  two_sum(theta, vneg(q), t, te);
-  V th = vadd(t, vadd(te, vneg(q_lo)));
+  // (k*)theta - (q + q_lo), rounded once
+  V t, te, th;
+  if constexpr (EXT) {
+    const V kh = splat<V>(h.k_hi), kl = splat<V>(h.k_lo);
+    V P = vmul(theta, kh);
+    V Pe = vfma(theta, kl, vfma(theta, kh, vneg(P)));
+    two_sum(P, vneg(q), t, te);
+    th = vadd(t, vadd(vadd(te, Pe), vneg(q_lo)));
+  } else {
+    two_sum(theta, vneg(q), t, te);
+    th = vadd(t, vadd(te, vneg(q_lo)));
+  }
 #pragma unroll
   for (int i = 0; i < L; ++i)
     if (!finite(Lanes<V>::get(th, i)) || !finite(Lanes<V>::get(q_lo, i)))
-      Lanes<V>::at(th, i) = master_update_plain(Lanes<V>::get(theta, i), Lanes<V>::get(m_new, i),
-                                                Lanes<V>::get(v_new, i), h.a_hi, h.b_hi, h.eps);
+      Lanes<V>::at(th, i) =
+          master_update_plain(Lanes<V>::get(theta, i), Lanes<V>::get(m_new, i),
+                              Lanes<V>::get(v_new, i), h.a_hi, h.b_hi, h.eps, EXT ? h.k_hi : 1.f);
   return th;
 }
 
 // The single-lane form of master_update, written with a branch instead of
 // lane selects (fewer live registers); the same operations on every element.
-template <>
-__device__ __forceinline__ float master_update<float>(float theta, float m_new, float v_new,
-                                                      const Hyper& h) {
+template <bool EXT>
+__device__ __forceinline__ float master_update_x1(float theta, float m_new, float v_new,
+                                                  const Hyper& h) {
   float s, s_lo;
   if (v_new >= 0x1p-100f && v_new <= 3.402823466e38f) {
     float y = rsqrt_approx(v_new);
@@ -259,20 +291,28 @@ __device__ __forceinline__ float master_update<float>(float theta, float m_new, 
   float r = __fmaf_rn(-q, D, n);
   r = __fmaf_rn(-q, D_lo, __fadd_rn(r, n_lo));
   float q_lo = __fmul_rn(r, rD);
-  float t, te;
-  two_sum(theta, -q, t, te);
-  float th = __fadd_rn(t, __fadd_rn(te, -q_lo));
+  float t, te, th;
+  if constexpr (EXT) {
+    float P = __fmul_rn(theta, h.k_hi);
+    float Pe = __fmaf_rn(theta, h.k_lo, __fmaf_rn(theta, h.k_hi, -P));
+    two_sum(P, -q, t, te);
+    th = __fadd_rn(t, __fadd_rn(__fadd_rn(te, Pe), -q_lo));
+  } else {
+    two_sum(theta, -q, t, te);
+    th = __fadd_rn(t, __fadd_rn(te, -q_lo));
+  }
   if (!finite(th) || !finite(q_lo))
-    th = master_update_plain(theta, m_new, v_new, h.a_hi, h.b_hi, h.eps);
+    th = master_update_plain(theta, m_new, v_new, h.a_hi, h.b_hi, h.eps, EXT ? h.k_hi : 1.f);
   return th;
 }
 
 // One step after the reduce: updates theta, m, v in place.
-template <class V>
+template <bool EXT, class V>
 __device__ __forceinline__ void adam_update(V g, V& theta, V& m, V& v, const Hyper& h) {
   m = moment1(m, g, h);
   v = moment2(v, g, h);
-  theta = master_update(theta, m, v, h);
+  if constexpr (Lanes<V>::n == 1) theta = master_update_x1<EXT>(theta, m, v, h);
+  else theta = master_update<V, EXT>(theta, m, v, h);
 }
 
 // bf16 bits of x, round to nearest, ties to even (PTX cvt.rn.bf16.f32).

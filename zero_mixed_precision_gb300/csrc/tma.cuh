@@ -202,8 +202,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                                    {sx, sx + kTmaTile * 4u, sx + kTmaTile * 8u}};
         const int64_t so = sg.state_off + e0 + (int64_t)c * kGroup;
         const GroupOut o{p.master + so, p.m + so, p.v + so, p.out + so};
-        if constexpr (PACK) group_vec_x2<NR, GK>(src, n, p.h, o);
-        else group_vec_x1<NR, GK>(src, n, p.h, o);
+        if constexpr (PACK) group_vec_x2<NR, GK, false>(src, n, p.h, o, 1.f);
+        else group_vec_x1<NR, GK, false>(src, n, p.h, o, 1.f);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     if (c == 0) {
       for (int j = blockIdx.x; j < p.nseg; j += gridDim.x) {
         const TmaSeg& sg = p.seg[j];
-        if (sg.len > sg.body) group_scalar<GK>(p, sg, sg.body, (int)(sg.len - sg.body));
+        if (sg.len > sg.body) group_scalar<GK, false>(p, sg, sg.body, (int)(sg.len - sg.body), 1.f);
       }
     }
   }
