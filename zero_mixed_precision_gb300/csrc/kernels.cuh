@@ -199,24 +199,11 @@ struct GroupOut {
 // one 8-element group, vector path
 // ---------------------------------------------------------------------------
 
-// Scalar-lane form: 8 elements per thread, one element per operation.  Fewer
-// register pairings; faster when the optimizer arithmetic dominates (small N).
-template <int NR, int GK, bool EXT, class Src>
-__device__ __forceinline__ void group_vec_x1(const Src& src, int n, const Hyper& h,
-                                             const GroupOut& o, float gscale) {
-  float th[kGroup], mm[kGroup], vv[kGroup];
-  {
-    float4 a = src.state(0, 0), b = src.state(0, 1);
-    th[0] = a.x; th[1] = a.y; th[2] = a.z; th[3] = a.w;
-    th[4] = b.x; th[5] = b.y; th[6] = b.z; th[7] = b.w;
-    a = src.state(1, 0); b = src.state(1, 1);
-    mm[0] = a.x; mm[1] = a.y; mm[2] = a.z; mm[3] = a.w;
-    mm[4] = b.x; mm[5] = b.y; mm[6] = b.z; mm[7] = b.w;
-    a = src.state(2, 0); b = src.state(2, 1);
-    vv[0] = a.x; vv[1] = a.y; vv[2] = a.z; vv[3] = a.w;
-    vv[4] = b.x; vv[5] = b.y; vv[6] = b.z; vv[7] = b.w;
-  }
-  CompSum<float> acc[kGroup];
+// The fixed-order compensated replica sum of one 8-element group (scalar
+// lanes), shared by the step and the squared-norm pre-pass so both see the
+// same bits of g.
+template <int NR, int GK, class Src>
+__device__ __forceinline__ void reduce_group_x1(const Src& src, int n, CompSum<float> (&acc)[kGroup]) {
   if constexpr (NR > 0) {
     GradLoad<GK> gl[NR];
 #pragma unroll
@@ -252,6 +239,27 @@ __device__ __forceinline__ void group_vec_x1(const Src& src, int n, const Hyper&
       }
     }
   }
+}
+
+// Scalar-lane form: 8 elements per thread, one element per operation.  Fewer
+// register pairings; faster when the optimizer arithmetic dominates (small N).
+template <int NR, int GK, bool EXT, class Src>
+__device__ __forceinline__ void group_vec_x1(const Src& src, int n, const Hyper& h,
+                                             const GroupOut& o, float gscale) {
+  float th[kGroup], mm[kGroup], vv[kGroup];
+  {
+    float4 a = src.state(0, 0), b = src.state(0, 1);
+    th[0] = a.x; th[1] = a.y; th[2] = a.z; th[3] = a.w;
+    th[4] = b.x; th[5] = b.y; th[6] = b.z; th[7] = b.w;
+    a = src.state(1, 0); b = src.state(1, 1);
+    mm[0] = a.x; mm[1] = a.y; mm[2] = a.z; mm[3] = a.w;
+    mm[4] = b.x; mm[5] = b.y; mm[6] = b.z; mm[7] = b.w;
+    a = src.state(2, 0); b = src.state(2, 1);
+    vv[0] = a.x; vv[1] = a.y; vv[2] = a.z; vv[3] = a.w;
+    vv[4] = b.x; vv[5] = b.y; vv[6] = b.z; vv[7] = b.w;
+  }
+  CompSum<float> acc[kGroup];
+  reduce_group_x1<NR, GK>(src, n, acc);
 #pragma unroll
   for (int k = 0; k < kGroup; ++k) {
     float g = acc[k].average(h);
@@ -433,24 +441,26 @@ __global__ void __launch_bounds__(kThreads, min_ctas<NR, PACK>())
 // fp64 rounding of the total -- does not depend on the grid or the GPU.
 constexpr int kNormChunk = 65536;
 
-// One partial per chunk: sum over the chunk's elements, in element order per
-// thread and a fixed tree across threads, of (g * unscale)^2 in fp64, where g
-// is the same fixed-order average the step uses.  Seg::first_group holds the
-// segment's first chunk here.
+// One partial per chunk: sum over the chunk's elements of x^2, x = fl32(g *
+// unscale) (exact for a power-of-two unscale) with g the same fixed-order
+// average the step uses.  Each thread accumulates its elements in order as an
+// fp32 pair (TwoProd for each square, TwoSum into the sum: about 2^-44
+// relative), then the threads' sums are added in fp64 over a fixed tree.
+// Seg::first_group holds the segment's first chunk here.
 template <int GK, int MAXSEG, int MAXPTR>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
     grad_sqnorm_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p, double* partials,
                        int64_t nchunks) {
   __shared__ double red[kThreads];
   const uint64_t pol = evict_first_policy();
-  const double us = (double)p.h.unscale;
+  const float us = p.h.unscale;
   int si = 0;
   for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
     while (c >= p.seg[si + 1].first_group) ++si;
     const Seg& sg = p.seg[si];
     const int64_t c0 = (c - sg.first_group) * (int64_t)kNormChunk;
     const void* const* gp = p.gptr + sg.ptr_base;
-    double acc = 0.0;
+    float hi = 0.f, lo = 0.f;  // double-float running sum of the squares
     for (int k = threadIdx.x; k < kNormChunk / kGroup; k += kThreads) {
       const int64_t e0 = c0 + (int64_t)k * kGroup;
       if (e0 >= sg.len) break;
@@ -458,16 +468,9 @@ __global__ void __launch_bounds__(kThreads)
       float g[kGroup];
       int cnt = kGroup;
       if (sg.vec && rem >= kGroup) {
+        const GlobalSource<GK> src{gp, e0, {nullptr, nullptr, nullptr}, pol};
         CompSum<float> cs[kGroup];
-        GradLoad<GK> gl;
-        gl.load(gp[0], e0, pol);
-#pragma unroll
-        for (int j = 0; j < kGroup; ++j) cs[j].init(gl.get(j));
-        for (int r = 1; r < p.n_rep; ++r) {
-          gl.load(gp[r], e0, pol);
-#pragma unroll
-          for (int j = 0; j < kGroup; ++j) cs[j].add(gl.get(j));
-        }
+        reduce_group_x1<0, GK>(src, p.n_rep, cs);
 #pragma unroll
         for (int j = 0; j < kGroup; ++j) g[j] = cs[j].average(p.h);
       } else {
@@ -479,11 +482,21 @@ __global__ void __launch_bounds__(kThreads)
           g[j] = cs.average(p.h);
         }
       }
-      for (int j = 0; j < cnt; ++j) {
-        const double x = __dmul_rn((double)g[j], us);
-        acc = __fma_rn(x, x, acc);
+#pragma unroll
+      for (int j = 0; j < kGroup; ++j) {
+        if (j < cnt) {
+          // x^2 exactly as p2 + pe (TwoProd), added with TwoSum
+          const float x = __fmul_rn(g[j], us);
+          const float p2 = __fmul_rn(x, x);
+          const float pe = __fmaf_rn(x, x, -p2);
+          float t, e;
+          two_sum(hi, p2, t, e);
+          hi = t;
+          lo = __fadd_rn(lo, __fadd_rn(e, pe));
+        }
       }
     }
+    const double acc = __dadd_rn((double)hi, (double)lo);
     red[threadIdx.x] = acc;
     __syncthreads();
 #pragma unroll
