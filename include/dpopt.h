@@ -219,6 +219,27 @@ int dpopt_grad_sqnorm_buckets(const void *const *slice_table, int grad_dtype, in
                               float grad_unscale, double *sqnorm_out, void *scratch,
                               int64_t scratch_bytes, dpopt_stream_t stream);
 
+/* dpopt_grad_sqnorm without a scratch buffer.  Not part of the method on the
+ * source pages (they have no counterpart): it serves callers that cannot call
+ * cudaMalloc for the step's scratch -- code whose device memory is all owned by
+ * another allocator (a framework's caching allocator that has reserved the
+ * GPU), or that must not trigger the device-wide synchronisation cudaMalloc /
+ * cudaFree can cause in the middle of a training step.  The chunk partials go
+ * to an array built into the library: 32768 fp64 values (256 KB) on every
+ * device that loads the library, held until the process exits, which limits a
+ * shard to 2^31 elements (DPOPT_ERR_UNSUPPORTED beyond that, with a message
+ * from dpopt_last_error()).  It allocates nothing and calls no allocating
+ * routine.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  Every call on a device shares the one array, and each
+ * call writes every partial it reads, so no state carries over between calls;
+ * but calls that can run at the same time on the GPU (other streams, other host
+ * threads) race on it -- serialise them.  Arguments, result and other errors
+ * as for dpopt_grad_sqnorm. */
+int dpopt_grad_sqnorm_noalloc(const void *const *grads, int grad_dtype, int n_replicas,
+                              int64_t numel, int shard_rank, float grad_unscale,
+                              double *sqnorm_out, dpopt_stream_t stream);
+
 /* Scratch bytes dpopt_grad_sqnorm{,_buckets} need for `elems` gradient elements
  * per replica cut into n_buckets buckets (use n_buckets = 1 for the full-buffer
  * form): 8 * (ceil(elems / 65536) + n_buckets).  Host-only. */

@@ -75,6 +75,7 @@ _SIGS = {
     "dpopt_grad_sqnorm": ([_PP, _I, _I, _I64, _I, _F, _P, _P, _I64, _P], _I),
     "dpopt_grad_sqnorm_buckets": ([_PP, _I, _I, _PI64, _PI64, _I64, _F, _P, _P, _I64, _P], _I),
     "dpopt_grad_sqnorm_scratch_bytes": ([_I64, _I64, _PI64], _I),
+    "dpopt_grad_sqnorm_noalloc": ([_PP, _I, _I, _I64, _I, _F, _P, _P], _I),
     "dpopt_set_kernel_policy": ([_I], _I),
     "dpopt_get_kernel_policy": ([], _I),
     "dpopt_selftest_wait_timeout": ([_I64, _P], _I),
@@ -198,6 +199,14 @@ def dpopt_grad_sqnorm_buckets(slice_table: Sequence[int], grad_dtype: int, n_rep
     return _lib.dpopt_grad_sqnorm_buckets(
         _ptr_array(slice_table), grad_dtype, n_replicas, (ctypes.c_int64 * nb)(*offsets),
         (ctypes.c_int64 * nb)(*lens), nb, grad_unscale, sqnorm_out, scratch, scratch_bytes, stream)
+
+
+def dpopt_grad_sqnorm_noalloc(grads: Sequence[int], grad_dtype: int, n_replicas: int,
+                              numel: int, shard_rank: int, grad_unscale: float, sqnorm_out: int,
+                              stream: int = 0) -> int:
+    return _lib.dpopt_grad_sqnorm_noalloc(_ptr_array(grads) if grads is not None else None,
+                                          grad_dtype, n_replicas, numel, shard_rank, grad_unscale,
+                                          sqnorm_out, stream)
 
 
 def dpopt_grad_sqnorm_scratch_bytes(elems: int, n_buckets: int = 1) -> tuple[int, int]:

@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "dpopt.h"
@@ -666,6 +667,39 @@ int finish_empty_norm(double* sqnorm_out, cudaStream_t stream) {
   return DPOPT_OK;
 }
 
+// ---------------------------------------------------------------------------
+// allocation-free squared norm: partials in a fixed device array
+// ---------------------------------------------------------------------------
+
+// Chunk partials for dpopt_grad_sqnorm_noalloc: one fp64 per 65536-element
+// chunk, so shards of up to kNoAllocMaxChunks * 65536 = 2^31 elements.  The
+// array is part of the library image: every device that loads the library
+// holds these 256 KB until the process exits.
+constexpr int64_t kNoAllocMaxChunks = 32768;
+static __device__ __align__(256) double g_noalloc_partials[kNoAllocMaxChunks];
+
+// Device address of g_noalloc_partials on the current device.  In host code
+// the array's name only stands for the symbol, so the address is looked up
+// once per device (with that device current) and cached.
+std::once_flag g_noalloc_once[kMaxDevices];
+double* g_noalloc_addr[kMaxDevices];
+cudaError_t g_noalloc_err[kMaxDevices];
+
+int noalloc_partials(double** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DPOPT_ERR_UNSUPPORTED, "device index too large");
+  std::call_once(g_noalloc_once[dev], [dev] {
+    void* ptr = nullptr;
+    g_noalloc_err[dev] = cudaGetSymbolAddress(&ptr, g_noalloc_partials);
+    g_noalloc_addr[dev] = static_cast<double*>(ptr);
+  });
+  if (g_noalloc_err[dev] != cudaSuccess) return cuda_fail(g_noalloc_err[dev], "cudaGetSymbolAddress");
+  *out = g_noalloc_addr[dev];
+  return DPOPT_OK;
+}
+
 }  // namespace
 }  // namespace dpopt
 
@@ -771,6 +805,46 @@ int dpopt_grad_sqnorm(const void* const* grads, int grad_dtype, int n_replicas, 
   h.unscale = grad_unscale == 0.f ? 1.f : grad_unscale;
   SegDesc seg{ptrs, 0, S};
   return run_sqnorm(&seg, 1, grad_dtype, n_replicas, h, (double*)scratch, sqnorm_out,
+                    (cudaStream_t)stream);
+}
+
+// Same result as dpopt_grad_sqnorm, for callers that cannot hand the library
+// a scratch buffer: the chunk partials live in g_noalloc_partials.  Nothing
+// there has to start at zero -- each call writes every partial it later reads.
+// All calls on a device share that one array, so calls whose kernels may run
+// at the same time on the GPU (different streams, other host threads) race.
+int dpopt_grad_sqnorm_noalloc(const void* const* grads, int grad_dtype, int n_replicas,
+                              int64_t numel, int shard_rank, float grad_unscale,
+                              double* sqnorm_out, dpopt_stream_t stream) {
+  int rc = check_replicas(n_replicas, grad_dtype);
+  if (rc) return rc;
+  if (!std::isfinite(grad_unscale) || grad_unscale < 0.f)
+    return fail(DPOPT_ERR_INVALID_ARG, "grad_unscale must be finite and >= 0");
+  if (numel < 0 || numel % n_replicas != 0)
+    return fail(DPOPT_ERR_INVALID_ARG, "numel must be >= 0 and a multiple of n_replicas");
+  const int64_t S = numel / n_replicas;
+  const int64_t chunks = (S + kNormChunk - 1) / kNormChunk;
+  if (chunks > kNoAllocMaxChunks)
+    return fail(DPOPT_ERR_UNSUPPORTED,
+                "dpopt_grad_sqnorm_noalloc: a shard of %lld elements needs %lld partials; the "
+                "built-in array holds %lld (shards up to %lld elements)",
+                (long long)S, (long long)chunks, (long long)kNoAllocMaxChunks,
+                (long long)(kNoAllocMaxChunks * kNormChunk));
+  if (!sqnorm_out || ((uintptr_t)sqnorm_out & 7u))
+    return fail(DPOPT_ERR_INVALID_ARG, "sqnorm_out must be a non-null, 8-byte aligned pointer");
+  Range avoid[1] = {{(uintptr_t)sqnorm_out, (uintptr_t)(sqnorm_out + 1)}};
+  const void* ptrs[DPOPT_MAX_REPLICAS];
+  int64_t S2 = 0;
+  rc = build_full(grads, grad_dtype, n_replicas, numel, shard_rank, 1, avoid, 1, ptrs, &S2);
+  if (rc) return rc;
+  if (S == 0) return finish_empty_norm(sqnorm_out, (cudaStream_t)stream);
+  double* partials = nullptr;
+  rc = noalloc_partials(&partials);
+  if (rc) return rc;
+  Hyper h = make_hyper(1.f, 0.f, 0.f, 0.f, 1, n_replicas);
+  h.unscale = grad_unscale == 0.f ? 1.f : grad_unscale;
+  SegDesc seg{ptrs, 0, S};
+  return run_sqnorm(&seg, 1, grad_dtype, n_replicas, h, partials, sqnorm_out,
                     (cudaStream_t)stream);
 }
 
