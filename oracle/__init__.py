@@ -30,6 +30,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
 GRAD_BF16 = 0
 GRAD_F32 = 1
+GRAD_F16 = 2
 
 
 def build_command() -> list[str]:
@@ -72,6 +73,8 @@ def lib() -> ctypes.CDLL:
         L.orc_f32_to_bf16_array.restype = None
         L.orc_threads_available.argtypes = []
         L.orc_threads_available.restype = I
+        L.orc_f16_to_f64_array.argtypes = [P, I64, P]
+        L.orc_f16_to_f64_array.restype = None
         L.orc_grad_sqnorm.argtypes = [P, I, I, I64, I64, F]
         L.orc_grad_sqnorm.restype = ctypes.c_double
         L.orc_grad_scale.argtypes = [ctypes.c_double, F, F]
@@ -86,12 +89,23 @@ def lib() -> ctypes.CDLL:
 # array marshalling
 # ---------------------------------------------------------------------------
 
+class F16Bits(np.ndarray):
+    """uint16 array holding binary16 bit patterns (plain uint16 arrays are read
+    as bf16)."""
+
+
+def as_f16_bits(a: np.ndarray) -> "F16Bits":
+    return np.ascontiguousarray(a, dtype=np.uint16).view(F16Bits)
+
+
 def _dtype_code(arr: np.ndarray) -> int:
+    if isinstance(arr, F16Bits):
+        return GRAD_F16
     if arr.dtype == np.uint16:
         return GRAD_BF16
     if arr.dtype == np.float32:
         return GRAD_F32
-    raise TypeError(f"gradients must be bf16 bit patterns (uint16) or float32, got {arr.dtype}")
+    raise TypeError(f"gradients must be bf16/fp16 bit patterns (uint16) or float32, got {arr.dtype}")
 
 
 def _ptr(a: np.ndarray) -> int:
@@ -120,6 +134,14 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
         return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+def f16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of binary16 bit patterns to float64."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(b.shape, dtype=np.float64)
+    lib().orc_f16_to_f64_array(_ptr(b), b.size, _ptr(out))
+    return out
+
+
 def f32_to_bf16(x: np.ndarray) -> np.ndarray:
     """Round-to-nearest-even bf16 bit patterns of a float32 array."""
     x = np.ascontiguousarray(x, dtype=np.float32)
@@ -128,9 +150,14 @@ def f32_to_bf16(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def _contig(g: np.ndarray) -> np.ndarray:
+    c = np.ascontiguousarray(g)
+    return c.view(F16Bits) if isinstance(g, F16Bits) else c
+
+
 def average(grads: Sequence[np.ndarray]) -> np.ndarray:
     """Fixed-order (ascending replica) average of N equal-length gradient arrays."""
-    grads = [np.ascontiguousarray(g) for g in grads]
+    grads = [_contig(g) for g in grads]
     n = len(grads)
     count = grads[0].size
     code = _dtype_code(grads[0])
@@ -160,7 +187,7 @@ def reduce_adam_range(grads: Sequence[np.ndarray], offset: int, count: int, mast
     """Average N flattened replica buffers over [offset, offset+count) and apply
     one Adam step to the count-element states (in place).  Returns the bf16
     working copy."""
-    grads = [np.ascontiguousarray(g) for g in grads]
+    grads = [_contig(g) for g in grads]
     code = _dtype_code(grads[0])
     for g in grads:
         assert _dtype_code(g) == code and g.size >= offset + count
@@ -190,7 +217,7 @@ def reduce_adam_shard(grads: Sequence[np.ndarray], numel: int, shard_rank: int, 
 def grad_sqnorm(grads: Sequence[np.ndarray], offset: int = 0, count: int | None = None,
                 unscale: float = 1.0) -> float:
     """sum of (g_i * unscale)^2 over [offset, offset+count) of the averaged gradient."""
-    grads = [np.ascontiguousarray(g) for g in grads]
+    grads = [_contig(g) for g in grads]
     code = _dtype_code(grads[0])
     count = grads[0].size - offset if count is None else count
     return float(lib().orc_grad_sqnorm(_ptr_table(grads), code, len(grads), offset, count,
@@ -206,7 +233,7 @@ def reduce_adamw_range(grads: Sequence[np.ndarray], offset: int, count: int, mas
                        lr: float, beta1: float, beta2: float, eps: float, step: int,
                        weight_decay: float = 0.0, gscale: float = 1.0):
     """One AdamW step with the averaged gradient multiplied by gscale first."""
-    grads = [np.ascontiguousarray(g) for g in grads]
+    grads = [_contig(g) for g in grads]
     code = _dtype_code(grads[0])
     for a in (master, m, v):
         assert a.dtype == np.float32 and a.flags["C_CONTIGUOUS"] and a.size == count
@@ -294,3 +321,67 @@ def state_bytes(psi: int | float, variant: int, n_dp: int, zero_stage: int) -> f
     """Total model-state bytes held by one device (sum of state_components)."""
     c = state_components(psi, variant, n_dp, zero_stage)
     return c["params"] + c["grads"] + c["optimizer"]
+
+
+# ---------------------------------------------------------------------------
+# dynamic loss scaling (the fp16 block of the ZeRO-3 answer's DeepSpeed config:
+# loss_scale 0 = dynamic, initial_scale_power 16, loss_scale_window 1000,
+# hysteresis 2, min_loss_scale 1).  The pages give only the keys; the reading:
+#   - a step overflows when any averaged gradient element of any rank is not
+#     finite (its global squared norm is then not finite);
+#   - an overflowing step is skipped: no state changes, the step count stays;
+#     the run of clean steps restarts; every `hysteresis`-th overflow since the
+#     scale last changed halves the scale (never below min_scale);
+#   - a clean step is applied to g / scale; after `window` clean steps in a row
+#     the scale doubles.
+# ---------------------------------------------------------------------------
+
+class LossScaler:
+    def __init__(self, init_scale: float = 2.0 ** 16, window: int = 1000, hysteresis: int = 2,
+                 min_scale: float = 1.0):
+        self.scale = float(init_scale)
+        self.window = int(window)
+        self.hysteresis = int(hysteresis)
+        self.min_scale = float(min_scale)
+        self.good_steps = 0
+        self.hysteresis_left = int(hysteresis)
+        self.step = 0          # optimizer steps taken
+        self.skipped = 0
+
+    def update(self, overflow: bool) -> None:
+        if overflow:
+            self.skipped += 1
+            self.good_steps = 0
+            self.hysteresis_left -= 1
+            if self.hysteresis_left <= 0:
+                self.scale = max(self.scale / 2.0, self.min_scale)
+                self.hysteresis_left = self.hysteresis
+        else:
+            self.step += 1
+            self.good_steps += 1
+            if self.good_steps >= self.window:
+                self.scale *= 2.0
+                self.good_steps = 0
+                self.hysteresis_left = self.hysteresis
+
+
+def amp_step(all_grads, shard_offset: int, shard_len: int, master, m, v, scaler: LossScaler, *,
+             lr: float, beta1: float, beta2: float, eps: float, weight_decay: float = 0.0,
+             max_grad_norm: float = 0.0):
+    """One mixed-precision step with dynamic loss scaling on one rank's shard.
+
+    all_grads: the N replica buffers (scaled gradients, e.g. fp16) over the whole
+    model, so the global norm and the overflow decision see every rank.  Updates
+    master/m/v in place unless the step overflows; updates the scaler.  Returns
+    (bf16 working copy or None if skipped, overflow)."""
+    unscale = 1.0 / scaler.scale
+    sq = grad_sqnorm(all_grads, 0, all_grads[0].size, unscale)
+    overflow = not np.isfinite(sq)
+    out = None
+    if not overflow:
+        gscale = grad_scale(sq, max_grad_norm, unscale)
+        out = reduce_adamw_range(all_grads, shard_offset, shard_len, master, m, v, lr=lr,
+                                 beta1=beta1, beta2=beta2, eps=eps, step=scaler.step + 1,
+                                 weight_decay=weight_decay, gscale=float(gscale))
+    scaler.update(overflow)
+    return out, overflow

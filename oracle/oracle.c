@@ -85,16 +85,34 @@ uint16_t orc_f32_to_bf16_rne(float x) {
     return (uint16_t)upper;
 }
 
+/* IEEE-754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction
+ * bits.  Exponent field 0 holds zero and the subnormals f * 2^-24, field 31
+ * the infinities and NaNs; otherwise the value is (1024 + f) * 2^(e - 25). */
+double orc_f16_to_f64(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int f = h & 0x3FF;
+    double x;
+    if (e == 0) x = ldexp((double)f, -24);
+    else if (e == 31) x = f ? NAN : INFINITY;
+    else x = ldexp((double)(1024 + f), e - 25);
+    return sign ? -x : x;
+}
+
 /* ------------------------------------------------------------------ */
 /* Reduce: fixed-order average of N replica gradients                   */
 /* ------------------------------------------------------------------ */
 
 #define ORC_GRAD_BF16 0
 #define ORC_GRAD_F32 1
+#define ORC_GRAD_F16 2
 
 static double grad_at(const void *buf, int dtype, int64_t i) {
     if (dtype == ORC_GRAD_BF16) {
         return orc_bf16_to_f64(((const uint16_t *)buf)[i]);
+    }
+    if (dtype == ORC_GRAD_F16) {
+        return orc_f16_to_f64(((const uint16_t *)buf)[i]);
     }
     return (double)((const float *)buf)[i];
 }
@@ -180,7 +198,7 @@ int orc_reduce_adam_range(const void *const *grads, int dtype, int n,
                           float beta1, float beta2, float eps,
                           float weight_decay, int64_t step, int nthreads) {
     if (n < 1 || count < 0 || offset < 0 || step < 1) return -1;
-    if (dtype != ORC_GRAD_BF16 && dtype != ORC_GRAD_F32) return -1;
+    if (dtype != ORC_GRAD_BF16 && dtype != ORC_GRAD_F32 && dtype != ORC_GRAD_F16) return -1;
     orc_hyper h = make_hyper(lr, beta1, beta2, eps, weight_decay, step);
 #ifdef _OPENMP
     if (nthreads < 1) nthreads = 1;
@@ -265,6 +283,11 @@ int orc_reduce_adamw_range(const void *const *grads, int dtype, int n, int64_t o
         adam_one((double)gs, &master[j], &m[j], &v[j], out ? &out[j] : 0, &h);
     }
     return 0;
+}
+
+/* Widen an array of binary16 bit patterns (pinned against a library). */
+void orc_f16_to_f64_array(const uint16_t *h, int64_t count, double *out) {
+    for (int64_t j = 0; j < count; ++j) out[j] = orc_f16_to_f64(h[j]);
 }
 
 /* Average only (no optimizer), for pinning the reduce half on its own. */

@@ -28,6 +28,7 @@ _DEV_LIB = os.path.join(_HERE, "libsynth_dev.so")
 
 KIND_BF16 = 0
 KIND_F32 = 1
+KIND_F16 = 2
 
 
 def host_build_command() -> list[str]:
@@ -91,8 +92,8 @@ def _dist_args(d: Dist):
 
 def host_fill(kind: int, start: int, count: int, seed: int, stream: int, dist: Dist) -> np.ndarray:
     """Elements start .. start+count-1 of one stream, as uint16 bf16 bits
-    (kind 0) or float32 (kind 1)."""
-    out = np.empty(count, dtype=np.uint16 if kind == KIND_BF16 else np.float32)
+    (kind 0), float32 (kind 1) or uint16 fp16 bits (kind 2)."""
+    out = np.empty(count, dtype=np.float32 if kind == KIND_F32 else np.uint16)
     if count:
         _host_lib().syn_fill(out.ctypes.data, kind, start, count, seed, stream, *_dist_args(dist))
     return out
@@ -101,7 +102,7 @@ def host_fill(kind: int, start: int, count: int, seed: int, stream: int, dist: D
 def host_gather(kind: int, idx: np.ndarray, seed: int, stream: int, dist: Dist) -> np.ndarray:
     """Elements idx[k] of one stream."""
     idx = np.ascontiguousarray(idx, dtype=np.int64)
-    out = np.empty(idx.size, dtype=np.uint16 if kind == KIND_BF16 else np.float32)
+    out = np.empty(idx.size, dtype=np.float32 if kind == KIND_F32 else np.uint16)
     if idx.size:
         _host_lib().syn_gather(out.ctypes.data, kind, idx.ctypes.data, idx.size, seed, stream,
                                *_dist_args(dist))

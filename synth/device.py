@@ -25,15 +25,12 @@ class DeviceWorkload:
         self.wl = wl
         self.device = torch.device(device)
         S, n = wl.shard_elems, wl.n_replicas
-        gdt = torch.bfloat16 if wl.grad_kind == 0 else torch.float32
+        gdt = {0: torch.bfloat16, 1: torch.float32, 2: torch.float16}[wl.grad_kind]
         glen = wl.numel if wl.layout == "full" else S
         self.grads = [torch.empty(glen, dtype=gdt, device=self.device) for _ in range(n)]
         if wl.layout == "full":
             for g in self.grads:
-                if wl.grad_kind == 0:
-                    g.view(torch.int16).fill_(BF16_NAN)
-                else:
-                    g.fill_(float("nan"))
+                g.fill_(float("nan"))
         self.master = torch.empty(S, dtype=torch.float32, device=self.device)
         self.m = torch.empty(S, dtype=torch.float32, device=self.device)
         self.v = torch.empty(S, dtype=torch.float32, device=self.device)
@@ -59,7 +56,7 @@ class DeviceWorkload:
     def fill_grads(self, t: int) -> None:
         """Step t's gradients of every replica (the rank's shard range only)."""
         wl, S = self.wl, self.wl.shard_elems
-        esize = 2 if wl.grad_kind == 0 else 4
+        esize = wl.grad_bytes()
         off = wl.shard_base if wl.layout == "full" else 0
         for r, g in enumerate(self.grads):
             synth.device_fill(g.data_ptr() + off * esize, wl.grad_kind, wl.shard_base, S, wl.seed,

@@ -21,7 +21,9 @@
  *   outlier     : draw j = 6, top 53 bits * 2^-53 < p  -> x *= outlier_scale
  *   x           = mu + sigma * z   (two roundings, never fused), |x| if asked
  *   fp32 value  = x rounded to nearest binary32; bf16 value = that binary32
- *                 rounded to nearest-even bf16.
+ *                 rounded to nearest-even bf16; fp16 value = that binary32
+ *                 rounded to nearest-even binary16 (subnormals kept, overflow
+ *                 to infinity).
  * z is therefore exact; only mu + sigma*z rounds.
  *
  * Build: cc -O2 -ffp-contract=off -fPIC -shared synth.c
@@ -80,7 +82,35 @@ static uint16_t syn_bf16_rne(float f) {
     return (uint16_t)up;
 }
 
-/* out[k] = value of element start+k, k < count.  kind 0: bf16, 1: fp32. */
+/* binary32 -> binary16, round to nearest even.  The binary16 value of a
+ * binary32 f is f's significand cut to 11 bits (fewer for subnormal results)
+ * at the bit position set by f's exponent; the cut-off bits decide the
+ * rounding as usual: above half up, below half down, exactly half to even. */
+static uint16_t syn_f16_rne(float f) {
+    uint32_t b;
+    memcpy(&b, &f, 4);
+    uint32_t sign = (b >> 16) & 0x8000u;
+    uint32_t ex = (b >> 23) & 0xFFu;
+    uint32_t man = b & 0x7FFFFFu;
+    if (ex == 0xFFu) return (uint16_t)(sign | 0x7C00u | (man ? 0x200u : 0u));
+    int e = (int)ex - 127;                 /* unbiased exponent */
+    if (e > 15) return (uint16_t)(sign | 0x7C00u);
+    if (ex == 0 || e < -25) return (uint16_t)sign; /* |f| < 2^-25 rounds to zero */
+    uint32_t sig = man | 0x800000u;        /* 24-bit significand, value sig * 2^(e-23) */
+    int shift;                             /* bits of sig to drop */
+    uint32_t base;                         /* exponent field of the result */
+    if (e >= -14) { shift = 13; base = (uint32_t)(e + 15) << 10; sig &= 0x7FFFFFu; sig |= 0x800000u; }
+    else { shift = 13 + (-14 - e); base = 0; }
+    uint32_t kept = sig >> shift;
+    uint32_t rest = sig & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1);
+    if (e >= -14) kept &= 0x3FFu;          /* the implicit bit lives in the exponent field */
+    uint32_t r = base + kept;
+    if (rest > half || (rest == half && (kept & 1u))) r += 1u;  /* carries into the exponent */
+    return (uint16_t)(sign | r);
+}
+
+/* out[k] = value of element start+k, k < count.  kind 0: bf16, 1: fp32, 2: fp16. */
 void syn_fill(void *out, int kind, int64_t start, int64_t count, uint64_t seed,
               uint64_t stream, double mu, double sigma, double outlier_p,
               double outlier_scale, int absval) {
@@ -89,6 +119,7 @@ void syn_fill(void *out, int kind, int64_t start, int64_t count, uint64_t seed,
     for (int64_t k = 0; k < count; ++k) {
         float f = (float)syn_value(key, (uint64_t)(start + k), &d);
         if (kind == 0) ((uint16_t *)out)[k] = syn_bf16_rne(f);
+        else if (kind == 2) ((uint16_t *)out)[k] = syn_f16_rne(f);
         else ((float *)out)[k] = f;
     }
 }
@@ -102,6 +133,7 @@ void syn_gather(void *out, int kind, const int64_t *idx, int64_t count,
     for (int64_t k = 0; k < count; ++k) {
         float f = (float)syn_value(key, (uint64_t)idx[k], &d);
         if (kind == 0) ((uint16_t *)out)[k] = syn_bf16_rne(f);
+        else if (kind == 2) ((uint16_t *)out)[k] = syn_f16_rne(f);
         else ((float *)out)[k] = f;
     }
 }

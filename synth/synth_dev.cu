@@ -9,6 +9,7 @@
 // explicitly rounded intrinsics so that no multiply-add is fused and the
 // result matches the host bit-for-bit.
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace {
@@ -61,6 +62,7 @@ __global__ void fill_kernel(void* out, int kind, int64_t start, int64_t count,
   for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < count; k += stride) {
     float f = __double2float_rn(value_at(key, (uint64_t)(start + k), d));
     if (kind == 0) static_cast<uint16_t*>(out)[k] = bf16_rne_bits(f);
+    else if (kind == 2) static_cast<uint16_t*>(out)[k] = __half_as_ushort(__float2half_rn(f));
     else static_cast<float*>(out)[k] = f;
   }
 }
@@ -68,7 +70,7 @@ __global__ void fill_kernel(void* out, int kind, int64_t start, int64_t count,
 }  // namespace
 
 // Fill `count` elements of device buffer `out` (bf16 when kind == 0, fp32
-// when kind == 1) with elements start .. start+count-1 of stream (seed,
+// when kind == 1, fp16 when kind == 2) with elements start .. start+count-1 of stream (seed,
 // stream).  Returns a cudaError_t value (0 on success).  Asynchronous on
 // `stream_handle` (a cudaStream_t).
 extern "C" int syn_fill_device(void* out, int kind, int64_t start, int64_t count,
@@ -76,7 +78,7 @@ extern "C" int syn_fill_device(void* out, int kind, int64_t start, int64_t count
                                double outlier_p, double outlier_scale, int absval,
                                void* stream_handle) {
   if (count <= 0) return 0;
-  if (out == nullptr || (kind != 0 && kind != 1)) return (int)cudaErrorInvalidValue;
+  if (out == nullptr || kind < 0 || kind > 2) return (int)cudaErrorInvalidValue;
   uint64_t key = mix64(seed * kGamma + mix64(stream + 0x632BE59BD9B4E019ull));
   Dist d{mu, sigma, outlier_p, outlier_scale, absval};
   int dev = 0, sms = 0;

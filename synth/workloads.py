@@ -54,7 +54,7 @@ class Workload:
     v_dist: Optional[Dist]
     steps: int                            # measured Adam steps
     warmup_steps: int = 0                 # steps run before the measured ones
-    grad_kind: int = 0                    # 0 bf16, 1 fp32
+    grad_kind: int = 0                    # 0 bf16, 1 fp32, 2 fp16
     layout: str = "full"                  # "full": N full buffers; "slices": N shard slices
     lr: float = 1e-3
     beta1: float = 0.9
@@ -71,7 +71,7 @@ class Workload:
         return self.shard_rank * self.shard_elems
 
     def grad_bytes(self) -> int:
-        return 2 if self.grad_kind == 0 else 4
+        return 4 if self.grad_kind == 1 else 2
 
     def bytes_per_param(self) -> int:
         # N gradient reads + master/m/v read and write (24) + bf16 write (2)

@@ -34,15 +34,19 @@ FLT_MIN = float(np.finfo(np.float32).tiny)
 # inputs
 # ---------------------------------------------------------------------------
 
+def _typed(wl: Workload, a: np.ndarray) -> np.ndarray:
+    return oracle.as_f16_bits(a) if wl.grad_kind == synth.KIND_F16 else a
+
+
 def grad_host(wl: Workload, r: int, t: int, idx: np.ndarray) -> np.ndarray:
     """Replica r's gradient of step t at flattened replica-buffer indices idx."""
-    return synth.host_gather(wl.grad_kind, idx, wl.seed, stream_id(STREAM_GRAD, r, t),
-                             wl.grad_dist(r))
+    return _typed(wl, synth.host_gather(wl.grad_kind, idx, wl.seed,
+                                        stream_id(STREAM_GRAD, r, t), wl.grad_dist(r)))
 
 
 def grad_host_range(wl: Workload, r: int, t: int, start: int, count: int) -> np.ndarray:
-    return synth.host_fill(wl.grad_kind, start, count, wl.seed, stream_id(STREAM_GRAD, r, t),
-                           wl.grad_dist(r))
+    return _typed(wl, synth.host_fill(wl.grad_kind, start, count, wl.seed,
+                                      stream_id(STREAM_GRAD, r, t), wl.grad_dist(r)))
 
 
 def states_host(wl: Workload, gidx: np.ndarray):
@@ -75,6 +79,44 @@ def _f64(x):
     return np.asarray(x, dtype=np.float64)
 
 
+class _Tolerance:
+    """Running tolerance allowances of one trajectory (see the module doc)."""
+
+    def __init__(self, size: int, hp: dict):
+        self.b1 = float(np.float32(hp["beta1"]))
+        self.b2 = float(np.float32(hp["beta2"]))
+        self.lr = float(np.float32(hp["lr"]))
+        self.eps = float(np.float32(hp["eps"]))
+        self.acc_m = np.zeros(size)
+        self.acc_v = np.zeros(size)
+        self.acc_t = np.zeros(size)
+
+    def step(self, t, g, th_prev, m_prev, master, m, v):
+        b1, b2, lr, eps = self.b1, self.b2, self.lr, self.eps
+        bc1 = 1.0 - b1 ** t
+        bc2 = 1.0 - b2 ** t
+        scale_m = np.maximum.reduce([np.abs(b1 * m_prev), np.abs((1.0 - b1) * _f64(g)),
+                                     np.abs(_f64(m))])
+        self.acc_m += scale_m
+        self.acc_v += _f64(v)
+        with np.errstate(all="ignore"):
+            D = np.sqrt(_f64(v) / bc2) + eps
+            a = lr / bc1
+            delta = a * _f64(m) / D
+            delta_m = a * self.acc_m / D
+            delta_v = np.abs(delta) * self.acc_v / np.maximum(2.0 * _f64(v), FLT_MIN)
+        scale_t = np.maximum.reduce([np.abs(th_prev), np.abs(_f64(master)), np.abs(delta),
+                                     delta_m, np.minimum(delta_v, np.abs(delta) * 8)])
+        scale_t = np.where(np.isfinite(scale_t), scale_t, 0.0)
+        self.acc_t += scale_t
+
+    def ref(self, t, master, m, v, out) -> "StepRef":
+        return StepRef(t, master.copy(), m.copy(), v.copy(), out,
+                       REL_TOL * np.maximum(self.acc_t, FLT_MIN),
+                       REL_TOL * np.maximum(self.acc_m, FLT_MIN),
+                       REL_TOL * np.maximum(self.acc_v, FLT_MIN))
+
+
 def oracle_trajectory(wl: Workload, local_idx: np.ndarray, t_first: int, t_last: int,
                       grads_fn=None, init=None, hp=None, weight_decay: float = 0.0,
                       gscale_fn=None) -> list[StepRef]:
@@ -93,43 +135,50 @@ def oracle_trajectory(wl: Workload, local_idx: np.ndarray, t_first: int, t_last:
             return grad_host(wl, r, t, gidx)
     master, m, v = init if init is not None else states_host(wl, gidx)
     master, m, v = master.copy(), m.copy(), v.copy()
-    b1 = float(np.float32(hp["beta1"]))
-    b2 = float(np.float32(hp["beta2"]))
-    lr = float(np.float32(hp["lr"]))
-    eps = float(np.float32(hp["eps"]))
-    acc_m = np.zeros(master.size)
-    acc_v = np.zeros(master.size)
-    acc_t = np.zeros(master.size)
+    tol = _Tolerance(master.size, hp)
     refs = []
     for t in range(t_first, t_last + 1):
-        grads = [np.ascontiguousarray(grads_fn(r, t)) for r in range(wl.n_replicas)]
+        grads = [grads_fn(r, t) for r in range(wl.n_replicas)]
         g = oracle.average(grads)
         if gscale_fn is not None:
             c = np.float32(gscale_fn(t, grads))
             g = (_f64(g) * np.float64(c)).astype(np.float32)
         th_prev, m_prev = _f64(master), _f64(m)
         out = oracle.adam(g, master, m, v, step=t, weight_decay=weight_decay, **hp)
-        bc1 = 1.0 - b1 ** t
-        bc2 = 1.0 - b2 ** t
-        scale_m = np.maximum.reduce([np.abs(b1 * m_prev), np.abs((1.0 - b1) * _f64(g)),
-                                     np.abs(_f64(m))])
-        acc_m += scale_m
-        acc_v += _f64(v)
-        with np.errstate(all="ignore"):
-            D = np.sqrt(_f64(v) / bc2) + eps
-            a = lr / bc1
-            delta = a * _f64(m) / D
-            delta_m = a * acc_m / D
-            delta_v = np.abs(delta) * acc_v / np.maximum(2.0 * _f64(v), FLT_MIN)
-        scale_t = np.maximum.reduce([np.abs(th_prev), np.abs(_f64(master)), np.abs(delta),
-                                     delta_m, np.minimum(delta_v, np.abs(delta) * 8)])
-        scale_t = np.where(np.isfinite(scale_t), scale_t, 0.0)
-        acc_t += scale_t
-        refs.append(StepRef(t, master.copy(), m.copy(), v.copy(), out,
-                            REL_TOL * np.maximum(acc_t, FLT_MIN),
-                            REL_TOL * np.maximum(acc_m, FLT_MIN),
-                            REL_TOL * np.maximum(acc_v, FLT_MIN)))
+        tol.step(t, g, th_prev, m_prev, master, m, v)
+        refs.append(tol.ref(t, master, m, v, out))
     return refs
+
+
+def oracle_amp_trajectory(wl: Workload, iters: int, full_grads_fn, scaler, *,
+                          weight_decay: float = 0.0, max_grad_norm: float = 0.0, hp=None):
+    """Loss-scaled run of the oracle over every element of the shard: at each
+    iteration k (1-based) full_grads_fn(k) gives the N whole replica buffers
+    (scaled gradients); the oracle decides overflow from the global norm,
+    skips or steps, and advances the scaler.  Returns per iteration
+    (StepRef, overflow, scale_after, optimizer_steps_after)."""
+    hp = hp or dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps)
+    S, base = wl.shard_elems, wl.shard_base
+    master, m, v = states_host(wl, base + np.arange(S, dtype=np.int64))
+    tol = _Tolerance(S, hp)
+    out = oracle.f32_to_bf16(master)
+    res = []
+    for k in range(1, iters + 1):
+        full = full_grads_fn(k)
+        unscale = 1.0 / scaler.scale
+        sq = oracle.grad_sqnorm(full, 0, full[0].size, unscale)
+        overflow = not np.isfinite(sq)
+        if not overflow:
+            c = oracle.grad_scale(sq, max_grad_norm, unscale)
+            g = (_f64(oracle.average([x[base:base + S] for x in full])) * np.float64(c)).astype(
+                np.float32)
+            th_prev, m_prev = _f64(master), _f64(m)
+            t = scaler.step + 1
+            out = oracle.adam(g, master, m, v, step=t, weight_decay=weight_decay, **hp)
+            tol.step(t, g, th_prev, m_prev, master, m, v)
+        scaler.update(overflow)
+        res.append((tol.ref(scaler.step, master, m, v, out), overflow, scaler.scale, scaler.step))
+    return res
 
 
 # ---------------------------------------------------------------------------

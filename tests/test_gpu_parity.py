@@ -39,7 +39,8 @@ def f32(t: torch.Tensor) -> np.ndarray:
 
 def to_dev_grad(a: np.ndarray, dev="cuda") -> torch.Tensor:
     if a.dtype == np.uint16:
-        return torch.from_numpy(a.view(np.int16).copy()).to(dev).view(torch.bfloat16)
+        dt = torch.float16 if isinstance(a, oracle.F16Bits) else torch.bfloat16
+        return torch.from_numpy(np.asarray(a).view(np.int16).copy()).to(dev).view(dt)
     return torch.from_numpy(a.copy()).to(dev)
 
 
@@ -61,6 +62,8 @@ def _host_full_buffers(wl, t):
     for r in range(wl.n_replicas):
         if wl.grad_kind == 0:
             buf = np.full(wl.numel, 0x7FC0, dtype=np.uint16)
+        elif wl.grad_kind == 2:
+            buf = oracle.as_f16_bits(np.full(wl.numel, 0x7E00, dtype=np.uint16))
         else:
             buf = np.full(wl.numel, np.nan, dtype=np.float32)
         buf[wl.shard_base:wl.shard_base + wl.shard_elems] = grad_host_range(

@@ -442,3 +442,85 @@ def test_clipped_adamw_step_equals_adamw_on_the_clipped_gradient():
     for x, y in zip(a, b):
         np.testing.assert_array_equal(x, y)
     np.testing.assert_array_equal(out_a, out_b)
+
+
+# ---------------------------------------------------------------------------
+# fp16 gradients (fp16 + dynamic loss scaling row)
+# ---------------------------------------------------------------------------
+
+def test_f16_widening_matches_numpy_float16():
+    h = np.arange(0, 65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.f16_to_f64(h)
+    ref = h.view(np.float16).astype(np.float64)
+    fin = np.isfinite(ref)
+    np.testing.assert_array_equal(ours[fin], ref[fin])
+    assert np.all(np.isnan(ours[np.isnan(ref)]))
+    np.testing.assert_array_equal(ours[np.isinf(ref)], ref[np.isinf(ref)])
+
+
+def test_f16_average_equals_exact_rational_average():
+    rng = np.random.default_rng(31)
+    n, count = 5, 400
+    bits = [rng.integers(0, 0x7C00, count).astype(np.uint16) | (rng.integers(0, 2, count) << 15)
+            .astype(np.uint16) for _ in range(n)]
+    got = oracle.average([oracle.as_f16_bits(b) for b in bits])
+    for j in range(count):
+        s = sum(Fraction(float(np.uint16(b[j]).view(np.float16))) for b in bits)
+        assert got[j] == np.float32(frac_to_f32(Fraction(frac_to_f32(s)) / n))
+
+
+def test_loss_scaler_follows_the_worked_trajectory():
+    rows = []
+    with open(os.path.join(GOLDEN, "loss_scale_trajectory.txt"), encoding="utf-8") as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            rows.append(line.split())
+    cfg = rows[0]
+    assert cfg[0] == "config"
+    sc = oracle.LossScaler(float(cfg[1]), int(cfg[2]), int(cfg[3]), float(cfg[4]))
+    for r in rows[1:]:
+        sc.update(bool(int(r[0])))
+        assert (sc.scale, sc.good_steps, sc.hysteresis_left, sc.step) == (
+            float(r[1]), int(r[2]), int(r[3]), int(r[4])), r
+
+
+def test_amp_step_on_power_of_two_scaled_fp16_grads_equals_the_unscaled_step():
+    """Loss scaling by 2^k is exact on fp16 gradients that stay in range, so the
+    unscaled step sees exactly the gradients of an unscaled run."""
+    rng = np.random.default_rng(33)
+    n, numel = 4, 4000
+    raw = [(rng.standard_normal(numel) * 1e-3).astype(np.float16) for _ in range(n)]
+    scaled = [oracle.as_f16_bits((r.astype(np.float32) * 1024).astype(np.float16).view(np.uint16))
+              for r in raw]
+    plain = [oracle.as_f16_bits(r.view(np.uint16)) for r in raw]
+    # the scaled values are exactly 1024x the raw ones
+    np.testing.assert_array_equal(oracle.f16_to_f64(scaled[0]), 1024 * raw[0].astype(np.float64))
+    th0 = (rng.standard_normal(numel // n) * 0.02).astype(np.float32)
+    a = [th0.copy(), np.zeros(th0.size, np.float32), np.zeros(th0.size, np.float32)]
+    sc = oracle.LossScaler(1024.0, 1000, 2, 1.0)
+    out_a, ovf = oracle.amp_step(scaled, 0, th0.size, *a, sc, lr=1e-3, beta1=0.9, beta2=0.999,
+                                 eps=1e-8, weight_decay=0.01, max_grad_norm=1.0)
+    assert not ovf and sc.step == 1
+    b = [th0.copy(), np.zeros(th0.size, np.float32), np.zeros(th0.size, np.float32)]
+    sc1 = oracle.LossScaler(1.0, 1000, 2, 1.0)
+    out_b, _ = oracle.amp_step(plain, 0, th0.size, *b, sc1, lr=1e-3, beta1=0.9, beta2=0.999,
+                               eps=1e-8, weight_decay=0.01, max_grad_norm=1.0)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    np.testing.assert_array_equal(out_a, out_b)
+
+
+def test_amp_step_skips_on_overflow_and_leaves_the_states_alone():
+    rng = np.random.default_rng(34)
+    n, numel = 2, 1000
+    g = [oracle.as_f16_bits((rng.standard_normal(numel) * 10).astype(np.float16).view(np.uint16))
+         for _ in range(n)]
+    g[1][777] = 0x7C00  # +Inf in one replica, in another rank's shard
+    th0 = (rng.standard_normal(500) * 0.02).astype(np.float32)
+    st = [th0.copy(), np.ones(500, np.float32), np.ones(500, np.float32)]
+    sc = oracle.LossScaler(65536.0, 1000, 1, 1.0)
+    out, ovf = oracle.amp_step(g, 0, 500, *st, sc, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8)
+    assert ovf and out is None and sc.step == 0 and sc.skipped == 1 and sc.scale == 32768.0
+    np.testing.assert_array_equal(st[0], th0)
+    assert np.all(st[1] == 1) and np.all(st[2] == 1)

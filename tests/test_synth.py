@@ -40,3 +40,14 @@ def test_bf16_kind_is_the_rounded_fp32_kind():
     import torch
     ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     np.testing.assert_array_equal(h, ref)
+
+
+def test_fp16_kind_is_the_rounded_fp32_kind():
+    """The host's binary16 rounding against numpy's (library), over the whole
+    binary16 range: normal, subnormal, underflow to zero, overflow to Inf."""
+    for sigma in (1e-3, 1.0, 3e3, 1e5, 1e-6, 1e-8):
+        d = synth.Dist(0.0, sigma, outlier_p=0.05, outlier_scale=100.0)
+        f = synth.host_fill(1, 0, 50_000, 3, 4, d)
+        h = synth.host_fill(2, 0, 50_000, 3, 4, d)
+        ref = f.astype(np.float16).view(np.uint16)
+        np.testing.assert_array_equal(h, ref)

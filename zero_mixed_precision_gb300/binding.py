@@ -22,6 +22,7 @@ DPOPT_ERR_CUDA = 3
 DPOPT_ERR_TIMEOUT = 4
 DPOPT_GRAD_BF16 = 0
 DPOPT_GRAD_F32 = 1
+DPOPT_GRAD_F16 = 2
 DPOPT_MAX_REPLICAS = 64
 DPOPT_KERNEL_AUTO = 0
 DPOPT_KERNEL_DIRECT = 1
@@ -52,6 +53,22 @@ class StepOptions(ctypes.Structure):
 
 _POPT = ctypes.POINTER(StepOptions)
 
+
+class LossScaleState(ctypes.Structure):
+    """dpopt_loss_scale_state (device-resident; this is its host-side layout)."""
+    _fields_ = [("scale", ctypes.c_float), ("good_steps", ctypes.c_int32),
+                ("hysteresis_left", ctypes.c_int32), ("last_overflow", ctypes.c_int32),
+                ("step", ctypes.c_int64), ("skipped", ctypes.c_int64)]
+
+
+class LossScaleConfig(ctypes.Structure):
+    """dpopt_loss_scale_config."""
+    _fields_ = [("init_scale", ctypes.c_float), ("window", ctypes.c_int32),
+                ("hysteresis", ctypes.c_int32), ("min_scale", ctypes.c_float)]
+
+
+_PCFG = ctypes.POINTER(LossScaleConfig)
+
 _SIGS = {
     "dpopt_reduce_adam": ([_PP, _I, _I64, _I, _I64, _P, _P, _P, _P, _F, _F, _F, _F, _I64, _P], _I),
     "dpopt_reduce_adam_ex": ([_PP, _I, _I, _I64, _I, _I64, _P, _P, _P, _P, _F, _F, _F, _F, _I64,
@@ -76,6 +93,10 @@ _SIGS = {
     "dpopt_grad_sqnorm_buckets": ([_PP, _I, _I, _PI64, _PI64, _I64, _F, _P, _P, _I64, _P], _I),
     "dpopt_grad_sqnorm_scratch_bytes": ([_I64, _I64, _PI64], _I),
     "dpopt_grad_sqnorm_noalloc": ([_PP, _I, _I, _I64, _I, _F, _P, _P], _I),
+    "dpopt_loss_scale_init": ([_P, _PCFG, _P], _I),
+    "dpopt_amp_sqnorm": ([_PP, _I, _I, _I64, _I, _P, _P, _P, _I64, _P], _I),
+    "dpopt_amp_step": ([_PP, _I, _I, _I64, _I, _I64, _P, _P, _P, _P, _F, _F, _F, _F, _F, _F, _P, _P,
+                        _PCFG, _P], _I),
     "dpopt_set_kernel_policy": ([_I], _I),
     "dpopt_get_kernel_policy": ([], _I),
     "dpopt_selftest_wait_timeout": ([_I64, _P], _I),
@@ -215,6 +236,29 @@ def dpopt_grad_sqnorm_scratch_bytes(elems: int, n_buckets: int = 1) -> tuple[int
     return rc, out.value
 
 
+def dpopt_loss_scale_init(state: int, cfg: LossScaleConfig | None, stream: int = 0) -> int:
+    return _lib.dpopt_loss_scale_init(state, ctypes.byref(cfg) if cfg is not None else None,
+                                      stream)
+
+
+def dpopt_amp_sqnorm(grads: Sequence[int], grad_dtype: int, n_replicas: int, numel: int,
+                     shard_rank: int, state: int, sqnorm_out: int, scratch: int,
+                     scratch_bytes: int, stream: int = 0) -> int:
+    return _lib.dpopt_amp_sqnorm(_ptr_array(grads), grad_dtype, n_replicas, numel, shard_rank,
+                                 state, sqnorm_out, scratch, scratch_bytes, stream)
+
+
+def dpopt_amp_step(grads: Sequence[int], grad_dtype: int, n_replicas: int, numel: int,
+                   shard_rank: int, bucket_elems: int, master: int, m: int, v: int,
+                   param_bf16_out: int, lr: float, beta1: float, beta2: float, eps: float,
+                   weight_decay: float, max_grad_norm: float, global_sqnorm: int, state: int,
+                   cfg: LossScaleConfig | None, stream: int = 0) -> int:
+    return _lib.dpopt_amp_step(_ptr_array(grads), grad_dtype, n_replicas, numel, shard_rank,
+                               bucket_elems, master, m, v, param_bf16_out, lr, beta1, beta2, eps,
+                               weight_decay, max_grad_norm, global_sqnorm, state,
+                               ctypes.byref(cfg) if cfg is not None else None, stream)
+
+
 def dpopt_stream_status(stream: int = 0) -> int:
     return _lib.dpopt_stream_status(stream)
 
@@ -268,7 +312,9 @@ def _grad_dtype(t) -> int:
         return DPOPT_GRAD_BF16
     if t.dtype == torch.float32:
         return DPOPT_GRAD_F32
-    raise TypeError(f"gradients must be bfloat16 or float32, got {t.dtype}")
+    if t.dtype == torch.float16:
+        return DPOPT_GRAD_F16
+    raise TypeError(f"gradients must be bfloat16, float16 or float32, got {t.dtype}")
 
 
 def _stream_handle(stream) -> int:
@@ -368,6 +414,43 @@ def grad_sqnorm_buckets(bucket_slices, offsets, sqnorm_out, scratch, *, grad_uns
                                    sqnorm_out.data_ptr(), scratch.data_ptr(),
                                    scratch.numel() * scratch.element_size(), _stream_handle(stream))
     _check(rc, "dpopt_grad_sqnorm_buckets")
+
+
+def loss_scale_init(state, init_scale: float = 65536.0, window: int = 1000, hysteresis: int = 2,
+                    min_scale: float = 1.0, stream=None) -> LossScaleConfig:
+    """state: a device tensor of at least 32 bytes (e.g. torch.zeros(4, dtype=torch.int64)).
+    Returns the config to pass to amp_step."""
+    cfg = LossScaleConfig(init_scale, window, hysteresis, min_scale)
+    _check(dpopt_loss_scale_init(state.data_ptr(), cfg, _stream_handle(stream)),
+           "dpopt_loss_scale_init")
+    return cfg
+
+
+def read_loss_scale(state) -> LossScaleState:
+    """Copy the device state to the host (synchronises)."""
+    raw = state.detach().cpu().numpy().tobytes()[:ctypes.sizeof(LossScaleState)]
+    return LossScaleState.from_buffer_copy(raw)
+
+
+def amp_sqnorm(grads, shard_rank: int, state, sqnorm_out, scratch, stream=None) -> None:
+    dt = _grad_dtype(grads[0])
+    rc = dpopt_amp_sqnorm([g.data_ptr() for g in grads], dt, len(grads), grads[0].numel(),
+                          shard_rank, state.data_ptr(), sqnorm_out.data_ptr(), scratch.data_ptr(),
+                          scratch.numel() * scratch.element_size(), _stream_handle(stream))
+    _check(rc, "dpopt_amp_sqnorm")
+
+
+def amp_step(grads, shard_rank: int, bucket_elems: int, master, m, v, param_bf16_out, *,
+             lr: float, beta1: float, beta2: float, eps: float, weight_decay: float,
+             max_grad_norm: float, global_sqnorm, state, cfg: LossScaleConfig,
+             stream=None) -> None:
+    dt = _grad_dtype(grads[0])
+    rc = dpopt_amp_step([g.data_ptr() for g in grads], dt, len(grads), grads[0].numel(),
+                        shard_rank, bucket_elems, master.data_ptr(), m.data_ptr(), v.data_ptr(),
+                        param_bf16_out.data_ptr(), lr, beta1, beta2, eps, weight_decay,
+                        max_grad_norm, global_sqnorm.data_ptr(), state.data_ptr(), cfg,
+                        _stream_handle(stream))
+    _check(rc, "dpopt_amp_step")
 
 
 def stream_status(stream=None) -> None:

@@ -88,6 +88,8 @@ Hyper make_hyper(float lr, float beta1, float beta2, float eps, int64_t step, in
   h.sqnorm = nullptr;
   h.max_norm = 0.0;
   h.unscale = 1.f;
+  h.lr = lr;
+  h.scale_dev = nullptr;
   return h;
 }
 
@@ -106,7 +108,8 @@ int check_replicas(int n_replicas, int grad_dtype) {
   if (n_replicas < 1) return fail(DPOPT_ERR_INVALID_ARG, "n_replicas must be >= 1");
   if (n_replicas > DPOPT_MAX_REPLICAS)
     return fail(DPOPT_ERR_UNSUPPORTED, "n_replicas %d exceeds %d", n_replicas, DPOPT_MAX_REPLICAS);
-  if (grad_dtype != DPOPT_GRAD_BF16 && grad_dtype != DPOPT_GRAD_F32)
+  if (grad_dtype != DPOPT_GRAD_BF16 && grad_dtype != DPOPT_GRAD_F32 &&
+      grad_dtype != DPOPT_GRAD_F16)
     return fail(DPOPT_ERR_INVALID_ARG, "unknown grad_dtype %d", grad_dtype);
   return DPOPT_OK;
 }
@@ -223,6 +226,8 @@ template <int MS, int MP>
 int dispatch(const LaunchParams<MS, MP>& p, int grad_dtype, bool ext, cudaStream_t stream) {
   if (grad_dtype == DPOPT_GRAD_BF16)
     return ext ? dispatch_gk<0, true>(p, stream) : dispatch_gk<0, false>(p, stream);
+  if (grad_dtype == DPOPT_GRAD_F16)
+    return ext ? dispatch_gk<2, true>(p, stream) : dispatch_gk<2, false>(p, stream);
   return ext ? dispatch_gk<1, true>(p, stream) : dispatch_gk<1, false>(p, stream);
 }
 
@@ -315,8 +320,8 @@ int dispatch_tma_gk(const TmaParams<MS, MP>& p, cudaStream_t stream) {
 // pointer 16-byte aligned and the replica count within its shared memory.
 bool tma_eligible(const SegDesc* segs, int s0, int s1, int n, int grad_dtype, float* master,
                   float* m, float* v, void* out) {
-  if (n > kTmaMaxReplicas) return false;
-  const uint32_t gsize = grad_dtype == DPOPT_GRAD_BF16 ? 2u : 4u;
+  if (n > kTmaMaxReplicas || grad_dtype == DPOPT_GRAD_F16) return false;
+  const uint32_t gsize = grad_dtype == DPOPT_GRAD_F32 ? 4u : 2u;
   if (2u * (uint32_t)kTmaTile * ((uint32_t)n * gsize + 12u) > kTmaSmemBudget) return false;
   for (int s = s0; s < s1; ++s) {
     const SegDesc& d = segs[s];
@@ -333,7 +338,7 @@ bool tma_eligible(const SegDesc* segs, int s0, int s1, int n, int grad_dtype, fl
 template <int MS, int MP>
 int run_segments_tma(TmaParams<MS, MP>& p, const SegDesc* segs, int s0, int s1, int n,
                      cudaStream_t stream, int grad_dtype) {
-  const uint32_t gsize = grad_dtype == DPOPT_GRAD_BF16 ? 2u : 4u;
+  const uint32_t gsize = grad_dtype == DPOPT_GRAD_F32 ? 4u : 2u;
   int64_t tiles = 0;
   int nseg = 0;
   for (int s = s0; s < s1; ++s) {
@@ -431,6 +436,8 @@ int launch_sqnorm(LaunchParams<MS, MP>& p, int64_t nchunks, double* partials, in
   const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nchunks, (int64_t)sms * 4));
   if (grad_dtype == DPOPT_GRAD_BF16)
     grad_sqnorm_kernel<0, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks);
+  else if (grad_dtype == DPOPT_GRAD_F16)
+    grad_sqnorm_kernel<2, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks);
   else
     grad_sqnorm_kernel<1, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks);
   cudaError_t e = cudaGetLastError();
@@ -499,7 +506,7 @@ int build_full(const void* const* grads, int grad_dtype, int n_replicas, int64_t
   if (bucket_elems < 1) return fail(DPOPT_ERR_INVALID_ARG, "bucket_elems must be >= 1");
   const int64_t S = numel / n_replicas;
   const int64_t base = (int64_t)shard_rank * S;
-  const size_t esize = grad_dtype == DPOPT_GRAD_BF16 ? 2 : 4;
+  const size_t esize = grad_dtype == DPOPT_GRAD_F32 ? 4 : 2;
   *S_out = S;
   if (S == 0) return DPOPT_OK;
   for (int r = 0; r < n_replicas; ++r) {
@@ -553,7 +560,7 @@ int build_buckets(const void* const* slice_table, int grad_dtype, int n_replicas
 
 int check_bucket_grads(const std::vector<SegDesc>& segs, int n, int grad_dtype, const Range* avoid,
                        int navoid) {
-  const size_t esize = grad_dtype == DPOPT_GRAD_BF16 ? 2 : 4;
+  const size_t esize = grad_dtype == DPOPT_GRAD_F32 ? 4 : 2;
   for (const SegDesc& d : segs)
     for (int r = 0; r < n; ++r) {
       int rc = check_grad(d.ptrs[r], d.len, esize, avoid, navoid);
@@ -664,6 +671,73 @@ int check_norm_outputs(double* sqnorm_out, void* scratch, int64_t scratch_bytes,
 int finish_empty_norm(double* sqnorm_out, cudaStream_t stream) {
   cudaError_t e = cudaMemsetAsync(sqnorm_out, 0, sizeof(double), stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  return DPOPT_OK;
+}
+
+// ---------------------------------------------------------------------------
+// mixed-precision step with dynamic loss scaling
+// ---------------------------------------------------------------------------
+
+static_assert(sizeof(LossScaleState) == sizeof(dpopt_loss_scale_state), "state layout");
+static_assert(sizeof(LossScaleConfig) == sizeof(dpopt_loss_scale_config), "config layout");
+
+int check_scale_config(const dpopt_loss_scale_config* cfg, LossScaleConfig* out) {
+  if (!cfg) return fail(DPOPT_ERR_INVALID_ARG, "loss-scale config must be non-null");
+  if (!std::isfinite(cfg->init_scale) || cfg->init_scale <= 0.f || cfg->window < 1 ||
+      cfg->hysteresis < 1 || !std::isfinite(cfg->min_scale) || cfg->min_scale <= 0.f)
+    return fail(DPOPT_ERR_INVALID_ARG,
+                "loss-scale config: scales must be finite and > 0, window and hysteresis >= 1");
+  *out = LossScaleConfig{cfg->init_scale, cfg->window, cfg->hysteresis, cfg->min_scale};
+  return DPOPT_OK;
+}
+
+int check_state_ptr(const void* st) {
+  if (!st || ((uintptr_t)st & 7u))
+    return fail(DPOPT_ERR_INVALID_ARG, "loss-scale state must be a non-null, 8-byte aligned pointer");
+  return DPOPT_OK;
+}
+
+template <int GK, int PACK, int MS, int MP>
+int launch_amp(const LaunchParams<MS, MP>& p, const LossScaleState* st, const double* sq,
+               cudaStream_t stream) {
+  auto kern = reduce_adam_amp_kernel<GK, PACK, MS, MP>;
+  int sms = 0;
+  int rc = sm_count(&sms);
+  if (rc) return rc;
+  static std::atomic<int> per_sm{0};
+  int bps = per_sm.load(std::memory_order_relaxed);
+  if (bps == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, kThreads, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (bps < 1) bps = 1;
+    per_sm.store(bps, std::memory_order_relaxed);
+  }
+  const int64_t want = (p.total_groups + kThreads - 1) / kThreads;
+  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * bps));
+  kern<<<grid, kThreads, 0, stream>>>(p, st, sq);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  ++g_launches;
+  return DPOPT_OK;
+}
+
+template <int MS, int MP>
+int dispatch_amp(const LaunchParams<MS, MP>& p, int grad_dtype, const LossScaleState* st,
+                 const double* sq, cudaStream_t stream) {
+  const bool pack = p.n_rep > 8;
+  if (grad_dtype == DPOPT_GRAD_F16)
+    return pack ? launch_amp<2, 1>(p, st, sq, stream) : launch_amp<2, 0>(p, st, sq, stream);
+  if (grad_dtype == DPOPT_GRAD_BF16)
+    return pack ? launch_amp<0, 1>(p, st, sq, stream) : launch_amp<0, 0>(p, st, sq, stream);
+  return pack ? launch_amp<1, 1>(p, st, sq, stream) : launch_amp<1, 0>(p, st, sq, stream);
+}
+
+int launch_scale_update(LossScaleState* st, const double* sq, const LossScaleConfig& cfg,
+                        cudaStream_t stream) {
+  loss_scale_update_kernel<<<1, 32, 0, stream>>>(st, sq, cfg);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  ++g_launches;
   return DPOPT_OK;
 }
 
@@ -884,6 +958,104 @@ int dpopt_reduce_adam_bucket(const void* const* grad_slices, int grad_dtype, int
   return dpopt_reduce_adam_buckets(grad_slices, grad_dtype, n_replicas, &shard_offset, &len, 1,
                                    master_f32, m_f32, v_f32, param_bf16_out, lr, beta1, beta2, eps,
                                    step, stream);
+}
+
+int dpopt_loss_scale_init(dpopt_loss_scale_state* state, const dpopt_loss_scale_config* cfg,
+                          dpopt_stream_t stream) {
+  int rc = check_state_ptr(state);
+  if (rc) return rc;
+  LossScaleConfig c;
+  rc = check_scale_config(cfg, &c);
+  if (rc) return rc;
+  loss_scale_init_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((LossScaleState*)state, c);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  ++g_launches;
+  return DPOPT_OK;
+}
+
+int dpopt_amp_sqnorm(const void* const* grads, int grad_dtype, int n_replicas, int64_t numel,
+                     int shard_rank, const dpopt_loss_scale_state* state, double* sqnorm_out,
+                     void* scratch, int64_t scratch_bytes, dpopt_stream_t stream) {
+  int rc = check_replicas(n_replicas, grad_dtype);
+  if (rc) return rc;
+  rc = check_state_ptr(state);
+  if (rc) return rc;
+  if (numel < 0 || numel % n_replicas != 0)
+    return fail(DPOPT_ERR_INVALID_ARG, "numel must be >= 0 and a multiple of n_replicas");
+  const int64_t S = numel / n_replicas;
+  const int64_t chunks = (S + kNormChunk - 1) / kNormChunk;
+  Range avoid[2];
+  rc = check_norm_outputs(sqnorm_out, scratch, scratch_bytes, chunks, avoid);
+  if (rc) return rc;
+  const void* ptrs[DPOPT_MAX_REPLICAS];
+  int64_t S2 = 0;
+  rc = build_full(grads, grad_dtype, n_replicas, numel, shard_rank, 1, avoid, chunks ? 2 : 1,
+                  ptrs, &S2);
+  if (rc) return rc;
+  if (S == 0) return finish_empty_norm(sqnorm_out, (cudaStream_t)stream);
+  Hyper h = make_hyper(1.f, 0.f, 0.f, 0.f, 1, n_replicas);
+  h.scale_dev = &((const LossScaleState*)state)->scale;
+  SegDesc seg{ptrs, 0, S};
+  return run_sqnorm(&seg, 1, grad_dtype, n_replicas, h, (double*)scratch, sqnorm_out,
+                    (cudaStream_t)stream);
+}
+
+int dpopt_amp_step(const void* const* grads, int grad_dtype, int n_replicas, int64_t numel,
+                   int shard_rank, int64_t bucket_elems, float* master_f32, float* m_f32,
+                   float* v_f32, void* param_bf16_out, float lr, float beta1, float beta2,
+                   float eps, float weight_decay, float max_grad_norm,
+                   const double* global_sqnorm, dpopt_loss_scale_state* state,
+                   const dpopt_loss_scale_config* cfg, dpopt_stream_t stream) {
+  int rc = check_replicas(n_replicas, grad_dtype);
+  if (rc) return rc;
+  rc = check_hyper(lr, beta1, beta2, eps, 1);
+  if (rc) return rc;
+  rc = check_state_ptr(state);
+  if (rc) return rc;
+  LossScaleConfig c;
+  rc = check_scale_config(cfg, &c);
+  if (rc) return rc;
+  if (!global_sqnorm || ((uintptr_t)global_sqnorm & 7u))
+    return fail(DPOPT_ERR_INVALID_ARG, "global_sqnorm must be a non-null, 8-byte aligned pointer");
+  Hyper h = make_hyper(lr, beta1, beta2, eps, 1, n_replicas);
+  dpopt_step_options o{weight_decay, max_grad_norm, global_sqnorm, 0.f};
+  bool ext = false;
+  rc = apply_options(&o, lr, h, &ext);
+  if (rc) return rc;
+  h.max_norm = (double)max_grad_norm;
+  if (numel < 0 || numel % n_replicas != 0 || numel == 0) {
+    const void* ptrs[DPOPT_MAX_REPLICAS];
+    int64_t S = 0;
+    rc = build_full(grads, grad_dtype, n_replicas, numel, shard_rank, bucket_elems, nullptr, 0,
+                    ptrs, &S);
+    if (rc) return rc;
+    return launch_scale_update((LossScaleState*)state, global_sqnorm, c, (cudaStream_t)stream);
+  }
+  const int64_t S = numel / n_replicas;
+  Range st[5];
+  rc = check_states(master_f32, m_f32, v_f32, param_bf16_out, 0, S, st);
+  if (rc) return rc;
+  st[4] = {(uintptr_t)state, (uintptr_t)state + sizeof(dpopt_loss_scale_state)};
+  for (int i = 0; i < 4; ++i)
+    if (overlaps(st[4], st[i]))
+      return fail(DPOPT_ERR_INVALID_ARG, "the loss-scale state overlaps a state or output array");
+  const void* ptrs[DPOPT_MAX_REPLICAS];
+  int64_t S2 = 0;
+  rc = build_full(grads, grad_dtype, n_replicas, numel, shard_rank, bucket_elems, st, 5, ptrs,
+                  &S2);
+  if (rc) return rc;
+  SmallParams p{};
+  p.h = h;
+  p.master = master_f32; p.m = m_f32; p.v = v_f32; p.out = (uint16_t*)param_bf16_out;
+  p.n_rep = n_replicas;
+  SegDesc seg{ptrs, 0, S};
+  if (fill_segments(p, &seg, 0, 1, n_replicas, kGroup) > 0) {
+    rc = dispatch_amp(p, grad_dtype, (const LossScaleState*)state, global_sqnorm,
+                      (cudaStream_t)stream);
+    if (rc) return rc;
+  }
+  return launch_scale_update((LossScaleState*)state, global_sqnorm, c, (cudaStream_t)stream);
 }
 
 int dpopt_stream_status(dpopt_stream_t stream) {

@@ -144,11 +144,38 @@ struct GradLoad<1> {
   }
 };
 
+// fp16: binary16 words; widening to fp32 is exact (PTX cvt.f32.f16).
+__device__ __forceinline__ float f16_to_f32(uint32_t bits16) {
+  float f;
+  asm("{ .reg .b16 h; cvt.u16.u32 h, %1; cvt.f32.f16 %0, h; }" : "=f"(f) : "r"(bits16));
+  return f;
+}
+
+template <>
+struct GradLoad<2> {
+  uint4 w;
+  __device__ __forceinline__ void load(const void* base, int64_t e0, uint64_t pol) {
+    w = ld_grad16(static_cast<const uint16_t*>(base) + e0, pol);
+  }
+  __device__ __forceinline__ void load_shared(uint32_t saddr) { w = ld_shared16(saddr); }
+  __device__ __forceinline__ void zero() { w = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ float get(int k) const {
+    uint32_t x = (k < 2) ? w.x : (k < 4) ? w.y : (k < 6) ? w.z : w.w;
+    return f16_to_f32((k & 1) ? (x >> 16) : (x & 0xFFFFu));
+  }
+  __device__ __forceinline__ float2 pair(int j) const {
+    uint32_t x = j == 0 ? w.x : j == 1 ? w.y : j == 2 ? w.z : w.w;
+    return make_float2(f16_to_f32(x & 0xFFFFu), f16_to_f32(x >> 16));
+  }
+};
+
 template <int GK>
 __device__ __forceinline__ float ld_grad1(const void* base, int64_t e) {
-  if (GK == 0) {
+  if constexpr (GK == 0) {
     uint16_t h = static_cast<const uint16_t*>(base)[e];
     return __uint_as_float(((uint32_t)h) << 16);
+  } else if constexpr (GK == 2) {
+    return f16_to_f32(static_cast<const uint16_t*>(base)[e]);
   } else {
     return static_cast<const float*>(base)[e];
   }
@@ -373,8 +400,8 @@ __device__ __forceinline__ void group_vec_x2(const Src& src, int n, const Hyper&
 // ---------------------------------------------------------------------------
 
 template <int GK, bool EXT, class LP, class SegT>
-__device__ __noinline__ void group_scalar(const LP& p, const SegT& sg, int64_t e0, int count,
-                                          float gscale) {
+__device__ __noinline__ void group_scalar(const LP& p, const Hyper& h, const SegT& sg, int64_t e0,
+                                          int count, float gscale) {
   const void* const* gp = p.gptr + sg.ptr_base;
   const int n = p.n_rep;
   for (int k = 0; k < count; ++k) {
@@ -384,9 +411,9 @@ __device__ __noinline__ void group_scalar(const LP& p, const SegT& sg, int64_t e
     acc.init(ld_grad1<GK>(gp[0], e));
     for (int r = 1; r < n; ++r) acc.add(ld_grad1<GK>(gp[r], e));
     float th = p.master[so], mm = p.m[so], vv = p.v[so];
-    float g = acc.average(p.h);
+    float g = acc.average(h);
     if constexpr (EXT) g = __fmul_rn(g, gscale);
-    adam_update<EXT>(g, th, mm, vv, p.h);
+    adam_update<EXT>(g, th, mm, vv, h);
     p.master[so] = th;
     p.m[so] = mm;
     p.v[so] = vv;
@@ -404,14 +431,10 @@ __device__ __noinline__ void group_scalar(const LP& p, const SegT& sg, int64_t e
 template <int NR, int PACK>
 constexpr int min_ctas() { return NR > 0 ? 4 : (PACK ? 2 : 1); }
 
-// PACK selects the lane form of the vector body (0: scalar, 1: f32x2); the
-// two forms give identical bits, so the choice is made by speed alone.  EXT
-// adds the AdamW decay and the gradient multiplier (clipping, unscaling).
-template <int NR, int GK, int PACK, bool EXT, int MAXSEG, int MAXPTR>
-__global__ void __launch_bounds__(kThreads, min_ctas<NR, PACK>())
-    reduce_adam_ldg_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p) {
+// The grid-stride walk over the 8-element groups of every segment.
+template <int NR, int GK, int PACK, bool EXT, class LP>
+__device__ __forceinline__ void step_loop(const LP& p, const Hyper& h, float gscale) {
   const uint64_t pol = evict_first_policy();
-  const float gscale = EXT ? grad_scale_of(p.h) : 1.f;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int si = 0;
   for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < p.total_groups;
@@ -425,12 +448,119 @@ __global__ void __launch_bounds__(kThreads, min_ctas<NR, PACK>())
       const GlobalSource<GK> src{p.gptr + sg.ptr_base, e0, {p.master + so, p.m + so, p.v + so},
                                  pol};
       const GroupOut o{p.master + so, p.m + so, p.v + so, p.out + so};
-      if constexpr (PACK) group_vec_x2<NR, GK, EXT>(src, p.n_rep, p.h, o, gscale);
-      else group_vec_x1<NR, GK, EXT>(src, p.n_rep, p.h, o, gscale);
+      if constexpr (PACK) group_vec_x2<NR, GK, EXT>(src, p.n_rep, h, o, gscale);
+      else group_vec_x1<NR, GK, EXT>(src, p.n_rep, h, o, gscale);
     } else {
-      group_scalar<GK, EXT>(p, sg, e0, (int)(rem < kGroup ? rem : kGroup), gscale);
+      group_scalar<GK, EXT>(p, h, sg, e0, (int)(rem < kGroup ? rem : kGroup), gscale);
     }
   }
+}
+
+// PACK selects the lane form of the vector body (0: scalar, 1: f32x2); the
+// two forms give identical bits, so the choice is made by speed alone.  EXT
+// adds the AdamW decay and the gradient multiplier (clipping, unscaling).
+template <int NR, int GK, int PACK, bool EXT, int MAXSEG, int MAXPTR>
+__global__ void __launch_bounds__(kThreads, min_ctas<NR, PACK>())
+    reduce_adam_ldg_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p) {
+  const float gscale = EXT ? grad_scale_of(p.h) : 1.f;
+  step_loop<NR, GK, PACK, EXT>(p, p.h, gscale);
+}
+
+// ---------------------------------------------------------------------------
+// mixed-precision step with dynamic loss scaling
+// ---------------------------------------------------------------------------
+
+// Device-resident loss-scale state (the layout of dpopt_loss_scale_state).
+struct LossScaleState {
+  float scale;
+  int32_t good_steps;
+  int32_t hysteresis_left;
+  int32_t last_overflow;
+  int64_t step;
+  int64_t skipped;
+};
+
+struct LossScaleConfig {
+  float init_scale;
+  int32_t window;
+  int32_t hysteresis;
+  float min_scale;
+};
+
+// The step of a loss-scaled run: skipped entirely when the global squared norm
+// of the unscaled gradient is not finite (an overflow somewhere); otherwise
+// the bias corrections of step state->step + 1 and the multiplier 1/scale
+// (times the clip coefficient) are formed here, from device state, so no host
+// synchronisation is needed between steps.
+template <int GK, int PACK, int MAXSEG, int MAXPTR>
+__global__ void __launch_bounds__(kThreads, PACK ? 2 : 1)
+    reduce_adam_amp_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p,
+                           const LossScaleState* state, const double* sqnorm) {
+  __shared__ Hyper hs;
+  __shared__ int skip;
+  if (threadIdx.x == 0) {
+    Hyper h = p.h;
+    const double sq = *sqnorm;
+    skip = isfinite(sq) ? 0 : 1;
+    const LossScaleState st = *state;
+    const double t = (double)(st.step + 1);
+    const double bc1 = 1.0 - pow((double)h.beta1, t);
+    const double bc2 = 1.0 - pow((double)h.beta2, t);
+    const double a = (double)h.lr / bc1;
+    const double b = 1.0 / sqrt(bc2);
+    h.a_hi = __double2float_rn(a);
+    h.a_lo = __double2float_rn(a - (double)h.a_hi);
+    h.b_hi = __double2float_rn(b);
+    h.b_lo = __double2float_rn(b - (double)h.b_hi);
+    h.unscale = __fdiv_rn(1.f, st.scale);
+    h.sqnorm = sqnorm;
+    hs = h;
+  }
+  __syncthreads();
+  if (skip) return;
+  const float gscale = grad_scale_of(hs);
+  step_loop<0, GK, PACK, true>(p, hs, gscale);
+}
+
+__global__ void loss_scale_init_kernel(LossScaleState* st, LossScaleConfig cfg) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  LossScaleState s;
+  s.scale = cfg.init_scale;
+  s.good_steps = 0;
+  s.hysteresis_left = cfg.hysteresis;
+  s.last_overflow = 0;
+  s.step = 0;
+  s.skipped = 0;
+  *st = s;
+}
+
+// After a step: skip bookkeeping, halving on every hysteresis-th overflow since
+// the scale last changed (not below min_scale), doubling after `window` clean
+// steps in a row.
+__global__ void loss_scale_update_kernel(LossScaleState* st, const double* sqnorm,
+                                         LossScaleConfig cfg) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  LossScaleState s = *st;
+  const bool overflow = !isfinite(*sqnorm);
+  s.last_overflow = overflow ? 1 : 0;
+  if (overflow) {
+    s.skipped += 1;
+    s.good_steps = 0;
+    s.hysteresis_left -= 1;
+    if (s.hysteresis_left <= 0) {
+      s.scale = fmaxf(s.scale * 0.5f, cfg.min_scale);
+      s.hysteresis_left = cfg.hysteresis;
+    }
+  } else {
+    s.step += 1;
+    s.good_steps += 1;
+    if (s.good_steps >= cfg.window) {
+      s.scale = s.scale * 2.0f;
+      s.good_steps = 0;
+      s.hysteresis_left = cfg.hysteresis;
+    }
+  }
+  *st = s;
 }
 
 // ---------------------------------------------------------------------------
@@ -453,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                        int64_t nchunks) {
   __shared__ double red[kThreads];
   const uint64_t pol = evict_first_policy();
-  const float us = p.h.unscale;
+  const float us = p.h.scale_dev ? __fdiv_rn(1.f, *p.h.scale_dev) : p.h.unscale;
   int si = 0;
   for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
     while (c >= p.seg[si + 1].first_group) ++si;

@@ -45,9 +45,10 @@ struct Hyper {
   // gradient scale of the extended step: g <- fl32(g * c), c an fp32 scalar
   // computed once per launch from these (see grad_scale_of)
   const double* sqnorm;  // device: squared global L2 norm of the averaged gradient, or null
-  double max_norm;       // clip threshold (used when sqnorm is non-null)
+  double max_norm;       // clip threshold (clipping when > 0 and sqnorm is non-null)
   float unscale;         // multiplier applied first (1/loss scale; 1 when unused)
-  float pad_;
+  float lr;              // learning rate (for bias corrections formed on the device)
+  const float* scale_dev;  // device loss scale: the norm pre-pass unscales by 1/*scale_dev
 };
 
 // The extended step's gradient multiplier: c = unscale * min(1, max_norm /
@@ -55,7 +56,7 @@ struct Hyper {
 // The same value in every thread (one device scalar read).
 __device__ __forceinline__ float grad_scale_of(const Hyper& h) {
   double c = (double)h.unscale;
-  if (h.sqnorm != nullptr) {
+  if (h.sqnorm != nullptr && h.max_norm > 0.0) {
     const double nrm = __dsqrt_rn(*h.sqnorm);
     const double coef = __ddiv_rn(h.max_norm, __dadd_rn(nrm, 1e-6));
     if (coef < 1.0) c = __dmul_rn(c, coef);

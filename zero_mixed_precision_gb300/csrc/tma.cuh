@@ -212,7 +212,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     if (c == 0) {
       for (int j = blockIdx.x; j < p.nseg; j += gridDim.x) {
         const TmaSeg& sg = p.seg[j];
-        if (sg.len > sg.body) group_scalar<GK, false>(p, sg, sg.body, (int)(sg.len - sg.body), 1.f);
+        if (sg.len > sg.body)
+          group_scalar<GK, false>(p, p.h, sg, sg.body, (int)(sg.len - sg.body), 1.f);
       }
     }
   }
