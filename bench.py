@@ -56,9 +56,12 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", choices=("auto", "direct", "bulk"), default="auto",
                     help="kernel policy of the library (both give identical results)")
-    ap.add_argument("--optimizer", choices=("adam", "adamw_clip"), default="adam",
+    ap.add_argument("--optimizer", choices=("adam", "adamw_clip", "adam_allgather"),
+                    default="adam",
                     help="adam: the fused reduce + Adam step; adamw_clip: the squared-norm "
-                         "pre-pass then the clipped AdamW step (weight_decay 0.01, clip 1.0)")
+                         "pre-pass then the clipped AdamW step (weight_decay 0.01, clip 1.0); "
+                         "adam_allgather: the step then the ZeRO-3 all-gather of the bf16 "
+                         "shard into N replica parameter buffers")
     return ap.parse_args(argv)
 
 
@@ -304,8 +307,15 @@ def run_ours(args, wl):
         scratch = torch.empty(dp.dpopt_grad_sqnorm_scratch_bytes(S, nb)[1] // 8 + 1,
                               dtype=torch.float64, device=device)
         opts = dp.step_options(weight_decay=0.01, max_grad_norm=1.0, grad_sqnorm=sqn)
+    if args.optimizer == "adam_allgather":
+        param_reps = [torch.empty(S * n, dtype=torch.bfloat16, device=device) for _ in range(n)]
     if wl.layout == "full":
-        if args.optimizer == "adamw_clip":
+        if args.optimizer == "adam_allgather":
+            def step(t):
+                dp.reduce_adam(dev.grads, wl.shard_rank, wl.bucket_elems, dev.master, dev.m,
+                               dev.v, dev.out, step=t, stream=stream, **hp)
+                dp.allgather_bf16(dev.out, wl.shard_rank, param_reps, stream=stream)
+        elif args.optimizer == "adamw_clip":
             def step(t):
                 dp.grad_sqnorm(dev.grads, wl.shard_rank, sqn, scratch, stream=stream)
                 dp.reduce_adamw(dev.grads, wl.shard_rank, wl.bucket_elems, dev.master, dev.m,
@@ -315,6 +325,8 @@ def run_ours(args, wl):
                 dp.reduce_adam(dev.grads, wl.shard_rank, wl.bucket_elems, dev.master, dev.m,
                                dev.v, dev.out, step=t, stream=stream, **hp)
     else:  # gradients delivered as per-bucket slices of the rank's shard
+        if args.optimizer == "adam_allgather":
+            raise SystemExit("adam_allgather runs on the full-buffer workloads")
         buckets = dev.bucket_slices()
         rows, offs = [b for _, b in buckets], [o for o, _ in buckets]
         if args.optimizer == "adamw_clip":
@@ -415,6 +427,8 @@ def _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks
     n, bpp = wl.n_replicas, wl.bytes_per_param()
     if args.optimizer == "adamw_clip":   # the norm pre-pass reads the N gradients once more
         bpp += wl.grad_bytes() * wl.n_replicas
+    elif args.optimizer == "adam_allgather":   # read the bf16 shard, write N copies
+        bpp += 2 + 2 * wl.n_replicas
     ms_per_step = elapsed_ms / K
     value = throughput(world, S, K, elapsed_ms)
     peak, peak_kind = load_peaks()

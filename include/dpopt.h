@@ -304,6 +304,26 @@ int dpopt_amp_step(const void *const *grads, int grad_dtype, int n_replicas, int
                    const double *global_sqnorm, dpopt_loss_scale_state *state,
                    const dpopt_loss_scale_config *cfg, dpopt_stream_t stream);
 
+/* ------------------------------------------------------------------------- */
+/* ZeRO-3 parameter all-gather                                                */
+/* ------------------------------------------------------------------------- */
+
+/* Write this rank's bf16 shard into every replica's parameter buffer
+ * ("Почему training 70B ...", section 5: before each layer's forward and backward
+ * the full parameters are all-gathered from the ranks' shards).  With every
+ * replica resident the gather is a local broadcast:
+ *   param_replicas[r][shard_rank*shard_elems + i] = shard_bf16[i],  r < n_replicas.
+ *  shard_bf16      DEVICE pointer to shard_elems bf16 values (e.g. param_bf16_out of
+ *                  a step); a replica whose destination is this very range is skipped.
+ *  param_replicas  HOST array of n_replicas DEVICE pointers, each to a flat bf16
+ *                  buffer of at least n_replicas*shard_elems elements.
+ * Calling it for every shard_rank gives every replica the full updated vector.
+ * Errors: DPOPT_ERR_INVALID_ARG for null or misaligned pointers, a rank outside
+ * [0, n_replicas), destinations overlapping the shard or one another;
+ * DPOPT_ERR_UNSUPPORTED for n_replicas > DPOPT_MAX_REPLICAS. */
+int dpopt_allgather_bf16(const void *shard_bf16, int64_t shard_elems, int shard_rank,
+                         void *const *param_replicas, int n_replicas, dpopt_stream_t stream);
+
 /* Wait for `stream`, then return and clear the current device's status word:
  * DPOPT_OK, or DPOPT_ERR_TIMEOUT if a bounded device-side wait gave up since the
  * last call, or DPOPT_ERR_CUDA if the wait itself failed. */

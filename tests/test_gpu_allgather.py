@@ -1,0 +1,87 @@
+"""ZeRO-3 parameter all-gather on one GPU: after every rank's shard step and
+all-gather, every replica's bf16 parameters equal the data-parallel update."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import zero_mixed_precision_gb300 as dp
+    from tests.test_gpu_parity import _host_full_buffers, _small_workload, to_dev_grad, u16
+else:
+    dp = None
+
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8)
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+@pytest.mark.parametrize("n,S", [(4, 50_000), (3, 7), (8, 10_001), (64, 2_048)])
+def test_every_replica_ends_with_the_data_parallel_parameters(n, S):
+    _need_gpu()
+    numel = n * S
+    wl = _small_workload(n, S, rank=0)
+    rng = np.random.default_rng(n * S)
+    gh = [oracle.f32_to_bf16((rng.standard_normal(numel) * 1e-3).astype(np.float32))
+          for _ in range(n)]
+    th0 = (rng.standard_normal(numel) * 0.02).astype(np.float32)
+    grads = [to_dev_grad(g) for g in gh]
+    replicas = [torch.full((numel,), float("nan"), dtype=torch.bfloat16, device="cuda")
+                for _ in range(n)]
+    for r in range(n):   # every rank: its shard's step, then the all-gather of its shard
+        st = [torch.from_numpy(th0[r * S:(r + 1) * S].copy()).cuda(),
+              torch.zeros(S, device="cuda"), torch.zeros(S, device="cuda")]
+        out = torch.empty(S, dtype=torch.bfloat16, device="cuda")
+        dp.reduce_adam(grads, r, S, *st, out, step=1, **HP)
+        dp.allgather_bf16(out, r, replicas)
+    dp.stream_status()
+    # the oracle's data-parallel update of the whole vector
+    m = np.zeros(numel, np.float32)
+    v = np.zeros(numel, np.float32)
+    th = th0.copy()
+    want = oracle.reduce_adam_range(gh, 0, numel, th, m, v, step=1, **HP)
+    for rep in replicas:
+        got = u16(rep)
+        d = np.abs(parity.bf16_ordered(got) - parity.bf16_ordered(want))
+        assert d.max() <= 1 and np.mean(got == want) > 0.999
+
+
+def test_unaligned_and_self_aliased_destinations():
+    _need_gpu()
+    n, S = 3, 1001
+    base = [torch.zeros(n * S + 8, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    reps = [b[1:1 + n * S] for b in base]          # 2-byte aligned only: scalar path
+    shard = torch.arange(S, dtype=torch.float32, device="cuda").to(torch.bfloat16)
+    dp.allgather_bf16(shard, 2, reps)
+    # the shard already in replica 1's slot is skipped, the others are written
+    reps[1][2 * S:3 * S] = shard
+    dp.allgather_bf16(reps[1][2 * S:3 * S], 2, reps)
+    dp.stream_status()
+    want = u16(shard)
+    for rep in reps:
+        np.testing.assert_array_equal(u16(rep[2 * S:3 * S]), want)
+        assert not rep[:2 * S].float().any()
+    for b in base:
+        assert b[0].item() == 0 and not b[1 + n * S:].float().any()
+
+
+def test_allgather_rejects_bad_arguments():
+    _need_gpu()
+    x = torch.zeros(100, dtype=torch.bfloat16, device="cuda")
+    reps = [torch.zeros(200, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    P = x.data_ptr()
+    R = [r.data_ptr() for r in reps]
+    assert dp.dpopt_allgather_bf16(P, 100, 2, R, 2, 0) == dp.DPOPT_ERR_INVALID_ARG
+    assert dp.dpopt_allgather_bf16(P, 100, 0, [R[0], R[0] + 20], 2, 0) == dp.DPOPT_ERR_INVALID_ARG
+    assert dp.dpopt_allgather_bf16(R[0] + 10, 100, 0, R, 2, 0) == dp.DPOPT_ERR_INVALID_ARG
+    assert dp.dpopt_allgather_bf16(P + 1, 100, 0, R, 2, 0) == dp.DPOPT_ERR_INVALID_ARG
+    assert dp.dpopt_allgather_bf16(P, 100, 0, R, 65, 0) == dp.DPOPT_ERR_UNSUPPORTED

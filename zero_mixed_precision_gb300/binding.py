@@ -97,6 +97,7 @@ _SIGS = {
     "dpopt_amp_sqnorm": ([_PP, _I, _I, _I64, _I, _P, _P, _P, _I64, _P], _I),
     "dpopt_amp_step": ([_PP, _I, _I, _I64, _I, _I64, _P, _P, _P, _P, _F, _F, _F, _F, _F, _F, _P, _P,
                         _PCFG, _P], _I),
+    "dpopt_allgather_bf16": ([_P, _I64, _I, _PP, _I, _P], _I),
     "dpopt_set_kernel_policy": ([_I], _I),
     "dpopt_get_kernel_policy": ([], _I),
     "dpopt_selftest_wait_timeout": ([_I64, _P], _I),
@@ -257,6 +258,13 @@ def dpopt_amp_step(grads: Sequence[int], grad_dtype: int, n_replicas: int, numel
                                bucket_elems, master, m, v, param_bf16_out, lr, beta1, beta2, eps,
                                weight_decay, max_grad_norm, global_sqnorm, state,
                                ctypes.byref(cfg) if cfg is not None else None, stream)
+
+
+def dpopt_allgather_bf16(shard_bf16: int, shard_elems: int, shard_rank: int,
+                         param_replicas: Sequence[int], n_replicas: int, stream: int = 0) -> int:
+    return _lib.dpopt_allgather_bf16(shard_bf16, shard_elems, shard_rank,
+                                     _ptr_array(param_replicas) if param_replicas is not None
+                                     else None, n_replicas, stream)
 
 
 def dpopt_stream_status(stream: int = 0) -> int:
@@ -451,6 +459,15 @@ def amp_step(grads, shard_rank: int, bucket_elems: int, master, m, v, param_bf16
                         max_grad_norm, global_sqnorm.data_ptr(), state.data_ptr(), cfg,
                         _stream_handle(stream))
     _check(rc, "dpopt_amp_step")
+
+
+def allgather_bf16(shard_bf16, shard_rank: int, param_replicas, stream=None) -> None:
+    """Write the bf16 shard tensor into every replica's flat bf16 parameter tensor
+    at the shard's position."""
+    rc = dpopt_allgather_bf16(shard_bf16.data_ptr(), shard_bf16.numel(), shard_rank,
+                              [t.data_ptr() for t in param_replicas], len(param_replicas),
+                              _stream_handle(stream))
+    _check(rc, "dpopt_allgather_bf16")
 
 
 def stream_status(stream=None) -> None:

@@ -13,6 +13,7 @@
 #include <vector>
 
 #include "dpopt.h"
+#include "gather.cuh"
 #include "kernels.cuh"
 #include "tma.cuh"
 
@@ -1056,6 +1057,56 @@ int dpopt_amp_step(const void* const* grads, int grad_dtype, int n_replicas, int
     if (rc) return rc;
   }
   return launch_scale_update((LossScaleState*)state, global_sqnorm, c, (cudaStream_t)stream);
+}
+
+int dpopt_allgather_bf16(const void* shard_bf16, int64_t shard_elems, int shard_rank,
+                         void* const* param_replicas, int n_replicas, dpopt_stream_t stream) {
+  if (n_replicas < 1) return fail(DPOPT_ERR_INVALID_ARG, "n_replicas must be >= 1");
+  if (n_replicas > DPOPT_MAX_REPLICAS)
+    return fail(DPOPT_ERR_UNSUPPORTED, "n_replicas %d exceeds %d", n_replicas, DPOPT_MAX_REPLICAS);
+  if (shard_elems < 0) return fail(DPOPT_ERR_INVALID_ARG, "shard_elems must be >= 0");
+  if (shard_rank < 0 || shard_rank >= n_replicas)
+    return fail(DPOPT_ERR_INVALID_ARG, "shard_rank must lie in [0, n_replicas)");
+  if (shard_elems == 0) return DPOPT_OK;
+  if (!shard_bf16 || !param_replicas)
+    return fail(DPOPT_ERR_INVALID_ARG, "shard_bf16 and param_replicas must be non-null");
+  if ((uintptr_t)shard_bf16 & 1u) return fail(DPOPT_ERR_INVALID_ARG, "misaligned shard pointer");
+  GatherParams p{};
+  p.src = static_cast<const uint16_t*>(shard_bf16);
+  p.len = shard_elems;
+  const uintptr_t bytes = (uintptr_t)shard_elems * 2u;
+  const Range src{(uintptr_t)shard_bf16, (uintptr_t)shard_bf16 + bytes};
+  Range dst[DPOPT_MAX_REPLICAS];
+  bool vec = ((uintptr_t)shard_bf16 & 15u) == 0;
+  int nd = 0;
+  for (int r = 0; r < n_replicas; ++r) {
+    if (!param_replicas[r]) return fail(DPOPT_ERR_INVALID_ARG, "null replica pointer");
+    if ((uintptr_t)param_replicas[r] & 1u)
+      return fail(DPOPT_ERR_INVALID_ARG, "misaligned replica pointer");
+    uint16_t* d = static_cast<uint16_t*>(param_replicas[r]) + (int64_t)shard_rank * shard_elems;
+    const Range dr{(uintptr_t)d, (uintptr_t)d + bytes};
+    if ((const void*)d == shard_bf16) continue;  // the shard already sits in this replica
+    if (overlaps(dr, src))
+      return fail(DPOPT_ERR_INVALID_ARG, "a replica's destination overlaps the shard");
+    for (int j = 0; j < nd; ++j)
+      if (overlaps(dr, dst[j])) return fail(DPOPT_ERR_INVALID_ARG, "replica destinations overlap");
+    dst[nd] = dr;
+    p.dst[nd++] = d;
+    vec = vec && (((uintptr_t)d & 15u) == 0);
+  }
+  p.n_dst = nd;
+  p.vec = vec ? 1 : 0;
+  if (nd == 0) return DPOPT_OK;
+  int sms = 0;
+  int rc = sm_count(&sms);
+  if (rc) return rc;
+  const int64_t want = (shard_elems + (int64_t)kThreads * kGroup - 1) / ((int64_t)kThreads * kGroup);
+  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * 8));
+  allgather_bf16_kernel<<<grid, kThreads, 0, (cudaStream_t)stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  ++g_launches;
+  return DPOPT_OK;
 }
 
 int dpopt_stream_status(dpopt_stream_t stream) {
