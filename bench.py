@@ -51,6 +51,10 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="gpt2s",
                     help="tiny | gpt2s | 1p3b | 70b_shard (parity configs; gpt2s is the default)")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--overlap", action="store_true",
+                    help="measure bucket-as-ready overlap: gradients produced bucket by bucket on "
+                         "one stream (last bucket first), stepped on another as each is ready")
+    ap.add_argument("--bucket-elems", type=int, default=0, help="override the bucket size")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -468,12 +472,91 @@ def _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks
     return line
 
 
+def run_overlap(args, wl):
+    """Bucket-as-ready against produce-then-step, on one GPU, one line of JSON."""
+    import torch
+    from dataclasses import replace
+
+    import synth
+    import zero_mixed_precision_gb300 as dp
+    from synth.device import DeviceWorkload
+
+    torch.cuda.set_device(0)
+    if args.bucket_elems:
+        wl = replace(wl, bucket_elems=args.bucket_elems)
+    wl = replace(wl, layout="slices")
+    dev = DeviceWorkload(wl)
+    dev.fill_states()
+    buckets = dev.bucket_slices()
+    rows, offs = [s for _, s in buckets], [o for o, _ in buckets]
+    hp = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps)
+    P, C = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def produce(t, stream, events=None):
+        for b in reversed(range(len(buckets))):
+            off, sl = buckets[b]
+            for r, x in enumerate(sl):
+                synth.device_fill(x.data_ptr(), wl.grad_kind, wl.shard_base + off, x.numel(),
+                                  wl.seed, synth.stream_id(synth.STREAM_GRAD, r, t),
+                                  wl.grad_dist(r), stream.cuda_stream)
+            if events is not None:
+                events[b].record(stream)
+
+    def timed(fn, reps):
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(P)
+        C.wait_stream(P)
+        for k in range(reps):
+            fn(k)
+        P.wait_stream(C)
+        t1.record(P)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / reps
+
+    reps = max(1, args.steps)
+    for k in range(args.warmup):
+        produce(1, P)
+        dp.reduce_adam_buckets(rows, offs, dev.master, dev.m, dev.v, dev.out, step=k + 1,
+                               stream=P, **hp)
+    t_prod = timed(lambda k: produce(k + 2, P), reps)
+    t_step = timed(lambda k: dp.reduce_adam_buckets(rows, offs, dev.master, dev.m, dev.v, dev.out,
+                                                    step=k + 1, stream=C, **hp), reps)
+
+    def serial(k):
+        produce(k + 2, P)
+        dp.reduce_adam_buckets(rows, offs, dev.master, dev.m, dev.v, dev.out, step=k + 1,
+                               stream=P, **hp)
+    t_serial = timed(serial, reps)
+    evs = [torch.cuda.Event() for _ in buckets]
+
+    def overlapped(k):
+        produce(k + 2, P, evs)
+        dp.reduce_adam_buckets_when_ready(rows, offs, evs, dev.master, dev.m, dev.v, dev.out,
+                                          step=k + 1, stream=C, **hp)
+        P.wait_stream(C)   # the next step's backward starts after this step's update
+    t_over = timed(overlapped, reps)
+    dp.stream_status(C)
+    hidden = (t_serial - t_over) / t_step if t_step > 0 else 0.0
+    return {"metric": "bucket-as-ready overlap of the step with gradient production",
+            "workload": wl.name, "n_replicas": wl.n_replicas, "shard_params": wl.shard_elems,
+            "buckets": len(buckets), "bucket_elems": wl.bucket_elems, "steps": reps,
+            "ms_produce": t_prod, "ms_step": t_step, "ms_produce_then_step": t_serial,
+            "ms_when_ready": t_over, "fraction_of_step_hidden": hidden,
+            "producer": "seeded generator kernels writing each bucket's N slices, last bucket "
+                        "first, on a second stream (a stand-in for the backward pass)"}
+
+
 def main(argv=None):
     args = parse_args(argv)
     import synth
     if args.workload not in synth.WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}")
     wl = synth.WORKLOADS[args.workload]
+    if args.overlap:
+        print(json.dumps(run_overlap(args, wl)), flush=True)
+        return
     if args.impl == "reference":
         line = run_reference(args, wl)
     else:

@@ -64,9 +64,11 @@
 extern "C" {
 #endif
 
-/* Same type as cudaStream_t, declared without the CUDA headers. */
+/* Same types as cudaStream_t and cudaEvent_t, declared without the CUDA headers. */
 struct CUstream_st;
 typedef struct CUstream_st *dpopt_stream_t;
+struct CUevent_st;
+typedef struct CUevent_st *dpopt_event_t;
 
 typedef enum {
     DPOPT_OK = 0,
@@ -323,6 +325,28 @@ int dpopt_amp_step(const void *const *grads, int grad_dtype, int n_replicas, int
  * DPOPT_ERR_UNSUPPORTED for n_replicas > DPOPT_MAX_REPLICAS. */
 int dpopt_allgather_bf16(const void *shard_bf16, int64_t shard_elems, int shard_rank,
                          void *const *param_replicas, int n_replicas, dpopt_stream_t stream);
+
+/* Bucket-as-ready: the batched-bucket step with one launch per bucket, each made
+ * to wait on the stream for that bucket's readiness event first.  The producer
+ * of the gradients (a backward pass on another stream, last layer first) records
+ * ready[b] when bucket b's slices are complete, so the step of early buckets runs
+ * while later ones are still being produced -- the one-GPU counterpart of
+ * starting each bucket's reduction as soon as its gradients exist instead of
+ * after the whole backward pass ("Глава 4.4", section 7: overlap of communication
+ * with computation; the ZeRO-3 answer's overlap_comm; the DP page's gradient
+ * hooks that launch a non-blocking all-reduce per parameter).
+ *  ready  HOST array of n_buckets events (cudaEvent_t); a NULL entry means the
+ *         bucket is ready already.  Buckets run in array order.
+ * Other arguments and errors as for dpopt_reduce_adam_buckets, plus
+ * DPOPT_ERR_CUDA if waiting on an event fails.  Results equal the batched
+ * entry's bit for bit. */
+int dpopt_reduce_adam_buckets_when_ready(const void *const *slice_table, int grad_dtype,
+                                         int n_replicas, const int64_t *offsets,
+                                         const int64_t *lens, int64_t n_buckets,
+                                         const dpopt_event_t *ready, float *master_f32,
+                                         float *m_f32, float *v_f32, void *param_bf16_out,
+                                         float lr, float beta1, float beta2, float eps,
+                                         int64_t step, dpopt_stream_t stream);
 
 /* Wait for `stream`, then return and clear the current device's status word:
  * DPOPT_OK, or DPOPT_ERR_TIMEOUT if a bounded device-side wait gave up since the

@@ -1,0 +1,95 @@
+"""Bucket-as-ready: buckets produced on one stream (a stand-in backward pass,
+last bucket first) are stepped on another as each one's event fires; the
+result equals the batched step bit for bit and matches the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from synth.device import DeviceWorkload
+from tests import parity
+from tests.parity import oracle_trajectory
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import zero_mixed_precision_gb300 as dp
+    from tests.test_gpu_parity import f32, u16
+else:
+    dp = None
+
+
+def _wl():
+    return synth.Workload(name="overlap", n_replicas=4, numel=4 * 3_000_001, shard_rank=2,
+                          bucket_elems=400_000, seed=51, grad_dist=lambda r: synth.Dist(0.0, 1e-3),
+                          master_dist=synth.Dist(0.0, 0.02), m_dist=None, v_dist=None, steps=2,
+                          layout="slices")
+
+
+def _produce(dev, wl, t, stream, events):
+    """Fill step t's gradients bucket by bucket, last bucket first, recording
+    each bucket's event on `stream` when its N slices are written."""
+    buckets = dev.bucket_slices()
+    for b in reversed(range(len(buckets))):
+        off, sl = buckets[b]
+        for r, x in enumerate(sl):
+            synth.device_fill(x.data_ptr(), wl.grad_kind, wl.shard_base + off, x.numel(), wl.seed,
+                              synth.stream_id(synth.STREAM_GRAD, r, t), wl.grad_dist(r),
+                              stream.cuda_stream)
+        events[b].record(stream)
+    return buckets
+
+
+def test_when_ready_equals_the_batched_step_and_the_oracle():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    wl = _wl()
+    hp = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps)
+    producer, consumer = torch.cuda.Stream(), torch.cuda.Stream()
+    results = []
+    for mode in ("ready", "batched"):
+        dev = DeviceWorkload(wl)
+        dev.fill_states()
+        torch.cuda.synchronize()
+        for t in (1, 2):
+            nb = -(-wl.shard_elems // wl.bucket_elems)
+            events = [torch.cuda.Event() for _ in range(nb)]
+            buckets = _produce(dev, wl, t, producer, events)
+            rows, offs = [s for _, s in buckets], [o for o, _ in buckets]
+            if mode == "ready":
+                dp.reduce_adam_buckets_when_ready(rows, offs, events, dev.master, dev.m, dev.v,
+                                                  dev.out, step=t, stream=consumer, **hp)
+            else:
+                consumer.wait_stream(producer)
+                dp.reduce_adam_buckets(rows, offs, dev.master, dev.m, dev.v, dev.out, step=t,
+                                       stream=consumer, **hp)
+            consumer.synchronize()
+            dp.stream_status(consumer)
+        results.append([f32(dev.master), f32(dev.m), f32(dev.v), u16(dev.out)])
+    for a, b in zip(*results):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+    rng = np.random.default_rng(5)
+    idx = np.unique(np.concatenate([rng.integers(0, wl.shard_elems, 20_000),
+                                    np.arange(wl.shard_elems - 100, wl.shard_elems)]))
+    refs = oracle_trajectory(wl, idx, 1, 2)
+    parity.check(refs[-1], *(x[idx] for x in results[0]), where="when_ready")
+
+
+def test_null_events_mean_ready_now():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    wl = _wl()
+    dev = DeviceWorkload(wl)
+    dev.fill_states()
+    dev.fill_grads(1)
+    buckets = dev.bucket_slices()
+    rows, offs = [s for _, s in buckets], [o for o, _ in buckets]
+    dp.reduce_adam_buckets_when_ready(rows, offs, [None] * len(rows), dev.master, dev.m, dev.v,
+                                      dev.out, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2,
+                                      eps=wl.eps, step=1)
+    dp.stream_status()
+    refs = oracle_trajectory(wl, np.arange(0, wl.shard_elems, 997), 1, 1)
+    parity.check(refs[0], f32(dev.master)[::997], f32(dev.m)[::997], f32(dev.v)[::997],
+                 u16(dev.out)[::997], where="null events")

@@ -98,6 +98,8 @@ _SIGS = {
     "dpopt_amp_step": ([_PP, _I, _I, _I64, _I, _I64, _P, _P, _P, _P, _F, _F, _F, _F, _F, _F, _P, _P,
                         _PCFG, _P], _I),
     "dpopt_allgather_bf16": ([_P, _I64, _I, _PP, _I, _P], _I),
+    "dpopt_reduce_adam_buckets_when_ready": ([_PP, _I, _I, _PI64, _PI64, _I64, _PP, _P, _P, _P,
+                                              _P, _F, _F, _F, _F, _I64, _P], _I),
     "dpopt_set_kernel_policy": ([_I], _I),
     "dpopt_get_kernel_policy": ([], _I),
     "dpopt_selftest_wait_timeout": ([_I64, _P], _I),
@@ -258,6 +260,19 @@ def dpopt_amp_step(grads: Sequence[int], grad_dtype: int, n_replicas: int, numel
                                bucket_elems, master, m, v, param_bf16_out, lr, beta1, beta2, eps,
                                weight_decay, max_grad_norm, global_sqnorm, state,
                                ctypes.byref(cfg) if cfg is not None else None, stream)
+
+
+def dpopt_reduce_adam_buckets_when_ready(slice_table: Sequence[int], grad_dtype: int,
+                                         n_replicas: int, offsets: Sequence[int],
+                                         lens: Sequence[int], ready: Sequence[int], master: int,
+                                         m: int, v: int, param_bf16_out: int, lr: float,
+                                         beta1: float, beta2: float, eps: float, step: int,
+                                         stream: int = 0) -> int:
+    nb = len(offsets)
+    return _lib.dpopt_reduce_adam_buckets_when_ready(
+        _ptr_array(slice_table), grad_dtype, n_replicas, (ctypes.c_int64 * nb)(*offsets),
+        (ctypes.c_int64 * nb)(*lens), nb, _ptr_array(ready), master, m, v, param_bf16_out, lr,
+        beta1, beta2, eps, step, stream)
 
 
 def dpopt_allgather_bf16(shard_bf16: int, shard_elems: int, shard_rank: int,
@@ -459,6 +474,22 @@ def amp_step(grads, shard_rank: int, bucket_elems: int, master, m, v, param_bf16
                         max_grad_norm, global_sqnorm.data_ptr(), state.data_ptr(), cfg,
                         _stream_handle(stream))
     _check(rc, "dpopt_amp_step")
+
+
+def reduce_adam_buckets_when_ready(bucket_slices, offsets, ready_events, master, m, v,
+                                  param_bf16_out, *, lr: float, beta1: float, beta2: float,
+                                  eps: float, step: int, stream=None) -> None:
+    """ready_events: one torch.cuda.Event (already recorded) or None per bucket."""
+    n = len(bucket_slices[0])
+    dt = _grad_dtype(bucket_slices[0][0])
+    table = [t.data_ptr() for row in bucket_slices for t in row]
+    lens = [row[0].numel() for row in bucket_slices]
+    ready = [e.cuda_event if e is not None else 0 for e in ready_events]
+    rc = dpopt_reduce_adam_buckets_when_ready(table, dt, n, list(offsets), lens, ready,
+                                              master.data_ptr(), m.data_ptr(), v.data_ptr(),
+                                              param_bf16_out.data_ptr(), lr, beta1, beta2, eps,
+                                              step, _stream_handle(stream))
+    _check(rc, "dpopt_reduce_adam_buckets_when_ready")
 
 
 def allgather_bf16(shard_bf16, shard_rank: int, param_replicas, stream=None) -> None:

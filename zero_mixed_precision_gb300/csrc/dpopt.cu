@@ -1059,6 +1059,44 @@ int dpopt_amp_step(const void* const* grads, int grad_dtype, int n_replicas, int
   return launch_scale_update((LossScaleState*)state, global_sqnorm, c, (cudaStream_t)stream);
 }
 
+int dpopt_reduce_adam_buckets_when_ready(const void* const* slice_table, int grad_dtype,
+                                         int n_replicas, const int64_t* offsets,
+                                         const int64_t* lens, int64_t n_buckets,
+                                         const dpopt_event_t* ready, float* master_f32,
+                                         float* m_f32, float* v_f32, void* param_bf16_out,
+                                         float lr, float beta1, float beta2, float eps,
+                                         int64_t step, dpopt_stream_t stream) {
+  int rc = check_replicas(n_replicas, grad_dtype);
+  if (rc) return rc;
+  rc = check_hyper(lr, beta1, beta2, eps, step);
+  if (rc) return rc;
+  if (n_buckets > 0 && !ready) return fail(DPOPT_ERR_INVALID_ARG, "ready must be non-null");
+  std::vector<SegDesc> segs;
+  int64_t lo = 0, hi = 0;
+  rc = build_buckets(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets, segs, &lo, &hi);
+  if (rc || segs.empty()) return rc;
+  Range st[4];
+  rc = check_states(master_f32, m_f32, v_f32, param_bf16_out, lo, hi, st);
+  if (rc) return rc;
+  rc = check_bucket_grads(segs, n_replicas, grad_dtype, st, 4);
+  if (rc) return rc;
+  const Hyper h = make_hyper(lr, beta1, beta2, eps, step, n_replicas);
+  // one launch per bucket, each behind its own readiness event, in bucket order
+  size_t si = 0;
+  for (int64_t b = 0; b < n_buckets; ++b) {
+    if (lens[b] == 0) continue;
+    if (ready[b]) {
+      cudaError_t e = cudaStreamWaitEvent((cudaStream_t)stream, (cudaEvent_t)ready[b], 0);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+    }
+    rc = run(&segs[si], 1, grad_dtype, n_replicas, master_f32, m_f32, v_f32, param_bf16_out, h,
+             false, (cudaStream_t)stream);
+    if (rc) return rc;
+    ++si;
+  }
+  return DPOPT_OK;
+}
+
 int dpopt_allgather_bf16(const void* shard_bf16, int64_t shard_elems, int shard_rank,
                          void* const* param_replicas, int n_replicas, dpopt_stream_t stream) {
   if (n_replicas < 1) return fail(DPOPT_ERR_INVALID_ARG, "n_replicas must be >= 1");
