@@ -531,9 +531,12 @@ def run_overlap(args, wl):
     t_serial = timed(serial, reps)
     evs = [torch.cuda.Event() for _ in buckets]
 
+    # buckets listed in the order they become ready (the producer goes last to first)
+    rrows, roffs, revs = rows[::-1], offs[::-1], evs[::-1]
+
     def overlapped(k):
         produce(k + 2, P, evs)
-        dp.reduce_adam_buckets_when_ready(rows, offs, evs, dev.master, dev.m, dev.v, dev.out,
+        dp.reduce_adam_buckets_when_ready(rrows, roffs, revs, dev.master, dev.m, dev.v, dev.out,
                                           step=k + 1, stream=C, **hp)
         P.wait_stream(C)   # the next step's backward starts after this step's update
     t_over = timed(overlapped, reps)

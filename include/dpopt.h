@@ -336,7 +336,8 @@ int dpopt_allgather_bf16(const void *shard_bf16, int64_t shard_elems, int shard_
  * with computation; the ZeRO-3 answer's overlap_comm; the DP page's gradient
  * hooks that launch a non-blocking all-reduce per parameter).
  *  ready  HOST array of n_buckets events (cudaEvent_t); a NULL entry means the
- *         bucket is ready already.  Buckets run in array order.
+ *         bucket is ready already.  Buckets run in array order, so list them in the
+ *         order their gradients become ready (a backward pass: last bucket first).
  * Other arguments and errors as for dpopt_reduce_adam_buckets, plus
  * DPOPT_ERR_CUDA if waiting on an event fails.  Results equal the batched
  * entry's bit for bit. */

@@ -58,9 +58,10 @@ def test_when_ready_equals_the_batched_step_and_the_oracle():
             events = [torch.cuda.Event() for _ in range(nb)]
             buckets = _produce(dev, wl, t, producer, events)
             rows, offs = [s for _, s in buckets], [o for o, _ in buckets]
-            if mode == "ready":
-                dp.reduce_adam_buckets_when_ready(rows, offs, events, dev.master, dev.m, dev.v,
-                                                  dev.out, step=t, stream=consumer, **hp)
+            if mode == "ready":   # in readiness order: last bucket first
+                dp.reduce_adam_buckets_when_ready(rows[::-1], offs[::-1], events[::-1],
+                                                  dev.master, dev.m, dev.v, dev.out, step=t,
+                                                  stream=consumer, **hp)
             else:
                 consumer.wait_stream(producer)
                 dp.reduce_adam_buckets(rows, offs, dev.master, dev.m, dev.v, dev.out, step=t,
