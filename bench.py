@@ -55,6 +55,10 @@ def parse_args(argv=None):
                     help="measure bucket-as-ready overlap: gradients produced bucket by bucket on "
                          "one stream (last bucket first), stepped on another as each is ready")
     ap.add_argument("--bucket-elems", type=int, default=0, help="override the bucket size")
+    ap.add_argument("--sweep", action="store_true",
+                    help="the size sweep: S in {1M, 16M, 256M, 1B} x N in {1, 2, 8, 32, 64} x "
+                         "{bf16, fp32} gradients, one JSON line per cell")
+    ap.add_argument("--sweep-sizes", default="", help="comma-separated S values (default all)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -551,6 +555,82 @@ def run_overlap(args, wl):
                         "first, on a second stream (a stand-in for the backward pass)"}
 
 
+def run_sweep(args):
+    """One line per sweep cell: N slices of S elements (one bucket), one step
+    per rep.  Cells whose working set is under 512 MB would sit in the 129 MB L2
+    between reps, so a 1 GB buffer is written before each rep and only the step
+    is timed (flagged); cells that do not fit the free memory are skipped."""
+    import torch
+
+    import synth
+    import zero_mixed_precision_gb300 as dp
+    from synth.device import DeviceWorkload, workload_bytes
+
+    torch.cuda.set_device(0)
+    peak, peak_kind = load_peaks()
+    sizes = ([int(x) for x in args.sweep_sizes.split(",")] if args.sweep_sizes
+             else list(synth.SWEEP_SIZES))
+    flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    for kind in (0, 1):
+        for S in sizes:
+            for n in synth.SWEEP_REPLICAS:
+                wl = synth.sweep_cell(S, n, kind)
+                need = workload_bytes(wl)
+                free, _ = torch.cuda.mem_get_info()
+                line = {"cell": wl.name, "shard_params": S, "n_replicas": n,
+                        "grad_dtype": "bf16" if kind == 0 else "fp32",
+                        "bytes_per_param": wl.bytes_per_param()}
+                if need + (4 << 30) > free:
+                    line.update(skipped=f"needs {need / 1e9:.1f} GB, {free / 1e9:.1f} GB free")
+                    print(json.dumps(line), flush=True)
+                    continue
+                dev = DeviceWorkload(wl)
+                dev.fill_states()
+                dev.fill_grads(1)
+                rows, offs = [dev.shard_slices()], [0]
+                hp = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps)
+                step_bytes = S * wl.bytes_per_param()
+                l2_flush = step_bytes < (512 << 20)
+                reps = int(min(200, max(3, 1.3e12 / max(step_bytes, 1))))
+                for t in range(1, 4):
+                    dp.reduce_adam_buckets(rows, offs, dev.master, dev.m, dev.v, dev.out, step=t,
+                                           **hp)
+                torch.cuda.synchronize()
+                if l2_flush:
+                    tot = 0.0
+                    for k in range(reps):
+                        flush.fill_(k & 0xFF)
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record()
+                        dp.reduce_adam_buckets(rows, offs, dev.master, dev.m, dev.v, dev.out,
+                                               step=4 + k, **hp)
+                        e1.record()
+                        torch.cuda.synchronize()
+                        tot += e0.elapsed_time(e1)
+                    ms = tot / reps
+                else:
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    for k in range(reps):
+                        dp.reduce_adam_buckets(rows, offs, dev.master, dev.m, dev.v, dev.out,
+                                               step=4 + k, **hp)
+                    e1.record()
+                    torch.cuda.synchronize()
+                    ms = e0.elapsed_time(e1) / reps
+                dp.stream_status()
+                gbs = step_bytes / (ms / 1e3) / 1e9
+                line.update(ms_per_step=ms, g_params_per_s=S / (ms / 1e3) / 1e9, hbm_gbs=gbs,
+                            frac_of_measured=gbs / peak, frac_of_8tbs=gbs / 8000.0,
+                            peak_source=peak_kind, reps=reps,
+                            l2="flushed before each rep (1 GB write), step timed alone: not a "
+                               "roofline figure" if l2_flush else "working set above L2")
+                print(json.dumps(line), flush=True)
+                del dev
+                torch.cuda.empty_cache()
+
+
 def main(argv=None):
     args = parse_args(argv)
     import synth
@@ -559,6 +639,9 @@ def main(argv=None):
     wl = synth.WORKLOADS[args.workload]
     if args.overlap:
         print(json.dumps(run_overlap(args, wl)), flush=True)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
     if args.impl == "reference":
         line = run_reference(args, wl)
