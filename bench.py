@@ -627,7 +627,7 @@ def run_sweep(args):
                             l2="flushed before each rep (1 GB write), step timed alone: not a "
                                "roofline figure" if l2_flush else "working set above L2")
                 print(json.dumps(line), flush=True)
-                del dev
+                del dev, rows, offs
                 torch.cuda.empty_cache()
 
 

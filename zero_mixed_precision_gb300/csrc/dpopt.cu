@@ -428,6 +428,20 @@ int64_t norm_chunks(const SegDesc* segs, int nsegs) {
   return c;
 }
 
+// Unrolled replica loops for N in {1, 2, 4, 8} (fewer registers, four CTAs
+// per SM), a runtime loop otherwise.  The accumulation order is the same.
+template <int GK, int MS, int MP>
+void sqnorm_launch_gk(const LaunchParams<MS, MP>& p, unsigned grid, double* partials,
+                      int64_t nchunks, cudaStream_t stream) {
+  switch (p.n_rep) {
+    case 1: grad_sqnorm_kernel<1, GK, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks); return;
+    case 2: grad_sqnorm_kernel<2, GK, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks); return;
+    case 4: grad_sqnorm_kernel<4, GK, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks); return;
+    case 8: grad_sqnorm_kernel<8, GK, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks); return;
+    default: grad_sqnorm_kernel<0, GK, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks);
+  }
+}
+
 template <int MS, int MP>
 int launch_sqnorm(LaunchParams<MS, MP>& p, int64_t nchunks, double* partials, int grad_dtype,
                   cudaStream_t stream) {
@@ -436,11 +450,11 @@ int launch_sqnorm(LaunchParams<MS, MP>& p, int64_t nchunks, double* partials, in
   if (rc) return rc;
   const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nchunks, (int64_t)sms * 4));
   if (grad_dtype == DPOPT_GRAD_BF16)
-    grad_sqnorm_kernel<0, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks);
+    sqnorm_launch_gk<0>(p, grid, partials, nchunks, stream);
   else if (grad_dtype == DPOPT_GRAD_F16)
-    grad_sqnorm_kernel<2, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks);
+    sqnorm_launch_gk<2>(p, grid, partials, nchunks, stream);
   else
-    grad_sqnorm_kernel<1, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks);
+    sqnorm_launch_gk<1>(p, grid, partials, nchunks, stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   ++g_launches;

@@ -577,8 +577,8 @@ constexpr int kNormChunk = 65536;
 // fp32 pair (TwoProd for each square, TwoSum into the sum: about 2^-44
 // relative), then the threads' sums are added in fp64 over a fixed tree.
 // Seg::first_group holds the segment's first chunk here.
-template <int GK, int MAXSEG, int MAXPTR>
-__global__ void __launch_bounds__(kThreads, 2)
+template <int NR, int GK, int MAXSEG, int MAXPTR>
+__global__ void __launch_bounds__(kThreads, NR > 0 ? 4 : 2)
     grad_sqnorm_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p, double* partials,
                        int64_t nchunks) {
   __shared__ double red[kThreads];
@@ -600,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (sg.vec && rem >= kGroup) {
         const GlobalSource<GK> src{gp, e0, {nullptr, nullptr, nullptr}, pol};
         CompSum<float> cs[kGroup];
-        reduce_group_x1<0, GK>(src, p.n_rep, cs);
+        reduce_group_x1<NR, GK>(src, p.n_rep, cs);
 #pragma unroll
         for (int j = 0; j < kGroup; ++j) g[j] = cs[j].average(p.h);
       } else {
