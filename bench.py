@@ -49,7 +49,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="gpt2s",
-                    help="tiny | gpt2s | 1p3b | 70b_shard (parity configs; gpt2s is the default)")
+                    help="tiny | gpt2s | 1p3b | 70b_shard | sweep_<S>_<N>_<bf16|fp32> "
+                         "(gpt2s is the default)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--overlap", action="store_true",
                     help="measure bucket-as-ready overlap: gradients produced bucket by bucket on "
@@ -631,12 +632,21 @@ def run_sweep(args):
                 torch.cuda.empty_cache()
 
 
+def resolve_workload(name: str):
+    """A named workload, or one sweep cell written sweep_<S>_<N>_<bf16|fp32>."""
+    import synth
+    if name in synth.WORKLOADS:
+        return synth.WORKLOADS[name]
+    parts = name.split("_")
+    if len(parts) == 4 and parts[0] == "sweep" and parts[3] in ("bf16", "fp32"):
+        return synth.sweep_cell(int(parts[1]), int(parts[2]), 0 if parts[3] == "bf16" else 1)
+    raise SystemExit(f"unknown workload {name}")
+
+
 def main(argv=None):
     args = parse_args(argv)
     import synth
-    if args.workload not in synth.WORKLOADS:
-        raise SystemExit(f"unknown workload {args.workload}")
-    wl = synth.WORKLOADS[args.workload]
+    wl = resolve_workload(args.workload)
     if args.overlap:
         print(json.dumps(run_overlap(args, wl)), flush=True)
         return
