@@ -39,7 +39,7 @@ if ROOT not in sys.path:
 METRIC = "G params/s updated and achieved HBM GB/s vs ~8 TB/s roofline, at N replicas"
 UNIT = "G params/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ("numerics.cuh", "kernels.cuh", "dpopt.cu")
+KERNEL_SOURCES = ("numerics.cuh", "kernels.cuh", "launch_gk.cu", "internal.h", "dpopt.cu")
 
 
 def parse_args(argv=None):

@@ -57,6 +57,22 @@ def test_sqnorm_matches_the_oracle(n, S, kind):
     assert torch.equal(a, out)
 
 
+@pytest.mark.parametrize("kind", [0, 1, 2])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8, 9])
+def test_sqnorm_every_unrolled_replica_count(n, kind):
+    """The norm pass has a kernel per N = 1..8 and a runtime-count one above."""
+    _need_gpu()
+    S = 140_003
+    wl = _small_workload(n, S, kind=kind, rank=0)
+    gh = _host_full_buffers(wl, 1)
+    grads = [to_dev_grad(g) for g in gh]
+    out = torch.zeros(1, dtype=torch.float64, device="cuda")
+    dp.grad_sqnorm(grads, wl.shard_rank, out, _scratch(S))
+    dp.stream_status()
+    want = oracle.grad_sqnorm(gh, wl.shard_base, S, 1.0)
+    assert float(out.item()) == pytest.approx(want, rel=4 * S * 2.0 ** -53, abs=1e-300)
+
+
 def test_sqnorm_over_bucket_slices_matches_full_buffer():
     _need_gpu()
     wl = _small_workload(4, 300_000, rank=1)
@@ -113,10 +129,12 @@ def _oracle_clipped(wl, steps, wd, max_norm, unscale=1.0):
                              weight_decay=wd, gscale_fn=gscale)
 
 
-@pytest.mark.parametrize("n,S", [(4, 50_000), (8, 20_001), (16, 9_999)])
+@pytest.mark.parametrize("n,S", [(1, 30_001), (2, 30_001), (3, 20_003), (4, 50_000),
+                                 (5, 12_007), (6, 10_001), (7, 9_001), (8, 20_001),
+                                 (16, 9_999)])
 def test_clipped_adamw_matches_the_oracle(n, S):
     _need_gpu()
-    wl = _small_workload(n, S, rank=1)
+    wl = _small_workload(n, S, rank=min(1, n - 1))
     # the averaged gradient's global norm is ~1e-3*sqrt(numel/n): clip to a tenth of it
     max_norm = float(1e-4 * np.sqrt(wl.numel))
     refs = _oracle_clipped(wl, (1, 2, 3), 0.01, max_norm)

@@ -27,7 +27,7 @@ def _need_gpu():
         pytest.skip("no CUDA device")
 
 
-@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 13, 64])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8, 13, 64])
 @pytest.mark.parametrize("S", [7, 4097, 100_003])
 def test_fp16_gradients_every_element(n, S):
     _need_gpu()

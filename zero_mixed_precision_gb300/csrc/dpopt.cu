@@ -1,5 +1,8 @@
 // dpopt.cu -- the C ABI (include/dpopt.h): argument checks, the step's
-// scalars, segment tables and kernel launches.  No memory is allocated here.
+// scalars, segment tables, the kernel choice and the small kernels (loss-scale
+// bookkeeping, the norm's final sum, the all-gather).  The step, loss-scaled
+// step and norm kernels live in launch_gk.cu, the bulk-copy kernel in tma.cu.
+// No memory is allocated here.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -13,33 +16,15 @@
 #include <vector>
 
 #include "dpopt.h"
+#include "control.cuh"
 #include "gather.cuh"
-#include "kernels.cuh"
-#include "tma.cuh"
+#include "internal.h"
 
 namespace dpopt {
 namespace {
 
-constexpr int kSmallSegs = 1;
-constexpr int kSmallPtrs = DPOPT_MAX_REPLICAS;
-constexpr int kBigSegs = 128;
-constexpr int kBigPtrs = 2048;
 constexpr int kMaxDevices = 64;
 
-using SmallParams = LaunchParams<kSmallSegs, kSmallPtrs>;
-using BigParams = LaunchParams<kBigSegs, kBigPtrs>;
-using SmallTma = TmaParams<kSmallSegs, kSmallPtrs>;
-using BigTma = TmaParams<kBigSegs, kBigPtrs>;
-static_assert(sizeof(BigParams) <= 32000, "kernel parameters must fit the 32 KB limit");
-static_assert(sizeof(BigTma) <= 32000, "kernel parameters must fit the 32 KB limit");
-
-// Bulk-copy kernel: shared memory budget for the stage ring of one CTA (two
-// CTAs of 8 consumer warps per SM measured best: 6386 GB/s at N = 4 against
-// 4687 GB/s for one CTA with five stages), the largest replica count it
-// serves, and how long one bounded wait may spin.
-constexpr uint32_t kTmaSmemBudget = 100 * 1024;
-constexpr int kTmaMaxReplicas = 16;
-constexpr long long kWaitLimitCycles = 2000000000LL;  // about one second
 // Under DPOPT_KERNEL_AUTO the bulk-copy kernel serves N up to this.  Measured
 // on GB300 the direct-load kernel is as fast or faster at every N (6400 vs
 // 6386 GB/s at N = 4, the only replica count where the bulk-copy ring fits two
@@ -50,6 +35,13 @@ std::atomic<int> g_policy{DPOPT_KERNEL_AUTO};
 
 thread_local char g_last_error[512];
 thread_local int64_t g_launches = 0;
+
+struct DeviceCache {
+  std::atomic<int> sms[kMaxDevices];
+};
+DeviceCache g_dev;
+
+}  // namespace
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -62,6 +54,25 @@ int fail(int code, const char* fmt, ...) {
 int cuda_fail(cudaError_t e, const char* what) {
   return fail(DPOPT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
+
+void count_launch() { ++g_launches; }
+
+int sm_count(int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DPOPT_ERR_UNSUPPORTED, "device index too large");
+  int s = g_dev.sms[dev].load(std::memory_order_relaxed);
+  if (s == 0) {
+    e = cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    g_dev.sms[dev].store(s, std::memory_order_relaxed);
+  }
+  *out = s;
+  return DPOPT_OK;
+}
+
+namespace {
 
 bool is_finite(float x) { return std::isfinite(x); }
 
@@ -151,94 +162,26 @@ int check_grad(const void* p, int64_t len, size_t esize, const Range* avoid, int
   return DPOPT_OK;
 }
 
-bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
-
-struct DeviceCache {
-  std::atomic<int> sms[kMaxDevices];
-};
-DeviceCache g_dev;
-
-int sm_count(int* out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kMaxDevices) return fail(DPOPT_ERR_UNSUPPORTED, "device index too large");
-  int s = g_dev.sms[dev].load(std::memory_order_relaxed);
-  if (s == 0) {
-    e = cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    g_dev.sms[dev].store(s, std::memory_order_relaxed);
-  }
-  *out = s;
-  return DPOPT_OK;
-}
-
-// One segment as the kernel sees it.
-struct SegDesc {
-  const void* const* ptrs;  // n_replicas gradient pointers at the segment start
-  int64_t state_off;
-  int64_t len;
-};
-
-template <int NR, int GK, int PACK, bool EXT, int MS, int MP>
-int launch_one(const LaunchParams<MS, MP>& p, cudaStream_t stream) {
-  auto kern = reduce_adam_ldg_kernel<NR, GK, PACK, EXT, MS, MP>;
-  int sms = 0;
-  int rc = sm_count(&sms);
-  if (rc) return rc;
-  static std::atomic<int> per_sm{0};
-  int bps = per_sm.load(std::memory_order_relaxed);
-  if (bps == 0) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, kThreads, 0);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-    if (bps < 1) bps = 1;
-    per_sm.store(bps, std::memory_order_relaxed);
-  }
-  int64_t want = (p.total_groups + kThreads - 1) / kThreads;
-  int64_t cap = (int64_t)sms * bps;
-  unsigned grid = (unsigned)std::max<int64_t>(1, std::min(want, cap));
-  kern<<<grid, kThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
-  ++g_launches;
-  return DPOPT_OK;
-}
-
-// Kernel choice by measurement on GB300: the scalar-lane body for N <= 8
-// (optimizer arithmetic dominates), the packed f32x2 body above (the replica
-// sum dominates); N in {1, 2, 4, 8} get a fully unrolled replica loop.
-template <int GK, bool EXT, int MS, int MP>
-int dispatch_gk(const LaunchParams<MS, MP>& p, cudaStream_t stream) {
-  const int n = p.n_rep;
-  if constexpr (MS == kSmallSegs) {
-    switch (n) {
-      case 1: return launch_one<1, GK, 0, EXT>(p, stream);
-      case 2: return launch_one<2, GK, 0, EXT>(p, stream);
-      case 4: return launch_one<4, GK, 0, EXT>(p, stream);
-      case 8: return launch_one<8, GK, 0, EXT>(p, stream);
-      default: break;
-    }
-  }
-  if (n <= 8) return launch_one<0, GK, 0, EXT>(p, stream);
-  return launch_one<0, GK, 1, EXT>(p, stream);
-}
-
+// The step for grad_dtype: the per-type launchers pick the kernel for N.
 template <int MS, int MP>
 int dispatch(const LaunchParams<MS, MP>& p, int grad_dtype, bool ext, cudaStream_t stream) {
-  if (grad_dtype == DPOPT_GRAD_BF16)
-    return ext ? dispatch_gk<0, true>(p, stream) : dispatch_gk<0, false>(p, stream);
-  if (grad_dtype == DPOPT_GRAD_F16)
-    return ext ? dispatch_gk<2, true>(p, stream) : dispatch_gk<2, false>(p, stream);
-  return ext ? dispatch_gk<1, true>(p, stream) : dispatch_gk<1, false>(p, stream);
+  if (grad_dtype == DPOPT_GRAD_BF16) return launch_step<0>(p, ext, stream);
+  if (grad_dtype == DPOPT_GRAD_F16) return launch_step<2>(p, ext, stream);
+  return launch_step<1>(p, ext, stream);
 }
 
 // Fill the segment table of one LaunchParams from segments [s0, s1);
 // `unit` is the element count one index of Seg::first_group stands for (8 for
-// the update's groups, kNormChunk for the norm's chunks).  Returns the index
+// the update's groups, kNormChunk for the norm's chunks).  A segment's vector
+// level: 2 when master/m/v (and fp32 gradients) are 32-byte aligned and
+// everything else 16-byte aligned (one 256-bit access per state array per
+// thread), 1 when everything is 16-byte aligned, else 0 (one element at a
+// time).  Null state pointers (the norm) count as aligned.  Returns the index
 // total (0 when every segment is empty).
 template <int MS, int MP>
 int64_t fill_segments(LaunchParams<MS, MP>& p, const SegDesc* segs, int s0, int s1, int n,
-                      int64_t unit) {
+                      int64_t unit, int grad_dtype) {
+  auto aligned32 = [](const void* q) { return ((uintptr_t)q & 31u) == 0; };
   int64_t units = 0;
   int nseg = 0;
   for (int s = s0; s < s1; ++s) {
@@ -249,13 +192,16 @@ int64_t fill_segments(LaunchParams<MS, MP>& p, const SegDesc* segs, int s0, int 
     sg.state_off = d.state_off;
     sg.len = d.len;
     sg.ptr_base = nseg * n;
-    bool vec = aligned16(p.master + d.state_off) && aligned16(p.m + d.state_off) &&
+    bool v16 = aligned16(p.master + d.state_off) && aligned16(p.m + d.state_off) &&
                aligned16(p.v + d.state_off) && aligned16(p.out + d.state_off);
+    bool v32 = aligned32(p.master + d.state_off) && aligned32(p.m + d.state_off) &&
+               aligned32(p.v + d.state_off);
     for (int r = 0; r < n; ++r) {
       p.gptr[nseg * n + r] = d.ptrs[r];
-      vec = vec && aligned16(d.ptrs[r]);
+      v16 = v16 && aligned16(d.ptrs[r]);
+      if (grad_dtype == DPOPT_GRAD_F32) v32 = v32 && aligned32(d.ptrs[r]);
     }
-    sg.vec = vec ? 1 : 0;
+    sg.vec = v16 ? (v32 ? 2 : 1) : 0;
     units += (d.len + unit - 1) / unit;
     ++nseg;
   }
@@ -269,102 +215,8 @@ int64_t fill_segments(LaunchParams<MS, MP>& p, const SegDesc* segs, int s0, int 
 template <int MS, int MP>
 int run_segments(LaunchParams<MS, MP>& p, const SegDesc* segs, int s0, int s1, int n,
                  cudaStream_t stream, int grad_dtype, bool ext) {
-  if (fill_segments(p, segs, s0, s1, n, kGroup) == 0) return DPOPT_OK;
+  if (fill_segments(p, segs, s0, s1, n, kGroup, grad_dtype) == 0) return DPOPT_OK;
   return dispatch(p, grad_dtype, ext, stream);
-}
-
-// ---------------------------------------------------------------------------
-// bulk-copy kernel launch
-// ---------------------------------------------------------------------------
-
-template <int NR, int GK, int PACK, int MS, int MP>
-int launch_tma(const TmaParams<MS, MP>& p, cudaStream_t stream) {
-  auto kern = reduce_adam_tma_kernel<NR, GK, PACK, MS, MP>;
-  const size_t dyn = (size_t)p.stages * p.stage_bytes;
-  static std::atomic<size_t> configured{0};
-  if (configured.load(std::memory_order_relaxed) < dyn) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kTmaSmemBudget + 1024));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-    configured.store(kTmaSmemBudget + 1024, std::memory_order_relaxed);
-  }
-  int sms = 0;
-  int rc = sm_count(&sms);
-  if (rc) return rc;
-  int bps = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, kTmaThreads, dyn);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-  if (bps < 1) return fail(DPOPT_ERR_UNSUPPORTED, "bulk-copy kernel does not fit an SM");
-  const int64_t want = std::max<int64_t>(p.total_tiles, (int64_t)p.nseg);
-  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * bps));
-  kern<<<grid, kTmaThreads, dyn, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
-  ++g_launches;
-  return DPOPT_OK;
-}
-
-template <int GK, int MS, int MP>
-int dispatch_tma_gk(const TmaParams<MS, MP>& p, cudaStream_t stream) {
-  switch (p.n_rep) {
-    case 1: return launch_tma<1, GK, 0>(p, stream);
-    case 2: return launch_tma<2, GK, 0>(p, stream);
-    case 4: return launch_tma<4, GK, 0>(p, stream);
-    case 8: return launch_tma<8, GK, 0>(p, stream);
-    default: break;
-  }
-  if (p.n_rep <= 8) return launch_tma<0, GK, 0>(p, stream);
-  return launch_tma<0, GK, 1>(p, stream);
-}
-
-// Whether segments [s0, s1) can go through the bulk-copy kernel: every
-// pointer 16-byte aligned and the replica count within its shared memory.
-bool tma_eligible(const SegDesc* segs, int s0, int s1, int n, int grad_dtype, float* master,
-                  float* m, float* v, void* out) {
-  if (n > kTmaMaxReplicas || grad_dtype == DPOPT_GRAD_F16) return false;
-  const uint32_t gsize = grad_dtype == DPOPT_GRAD_F32 ? 4u : 2u;
-  if (2u * (uint32_t)kTmaTile * ((uint32_t)n * gsize + 12u) > kTmaSmemBudget) return false;
-  for (int s = s0; s < s1; ++s) {
-    const SegDesc& d = segs[s];
-    if (d.len == 0) continue;
-    if (!aligned16(master + d.state_off) || !aligned16(m + d.state_off) ||
-        !aligned16(v + d.state_off) || !aligned16((uint16_t*)out + d.state_off))
-      return false;
-    for (int r = 0; r < n; ++r)
-      if (!aligned16(d.ptrs[r])) return false;
-  }
-  return true;
-}
-
-template <int MS, int MP>
-int run_segments_tma(TmaParams<MS, MP>& p, const SegDesc* segs, int s0, int s1, int n,
-                     cudaStream_t stream, int grad_dtype) {
-  const uint32_t gsize = grad_dtype == DPOPT_GRAD_F32 ? 4u : 2u;
-  int64_t tiles = 0;
-  int nseg = 0;
-  for (int s = s0; s < s1; ++s) {
-    const SegDesc& d = segs[s];
-    if (d.len == 0) continue;
-    TmaSeg& sg = p.seg[nseg];
-    sg.first_tile = tiles;
-    sg.state_off = d.state_off;
-    sg.len = d.len;
-    sg.body = d.len & ~(int64_t)(kGroup - 1);
-    sg.ptr_base = nseg * n;
-    for (int r = 0; r < n; ++r) p.gptr[nseg * n + r] = d.ptrs[r];
-    tiles += (sg.body + kTmaTile - 1) / kTmaTile;
-    ++nseg;
-  }
-  if (nseg == 0) return DPOPT_OK;
-  p.seg[nseg].first_tile = tiles;
-  p.nseg = nseg;
-  p.total_tiles = tiles;
-  p.stage_bytes = (uint32_t)kTmaTile * ((uint32_t)n * gsize + 12u);
-  p.stages = (int)std::min<uint32_t>(kTmaMaxStages, kTmaSmemBudget / p.stage_bytes);
-  p.wait_limit = kWaitLimitCycles;
-  if (p.stages < 2) return fail(DPOPT_ERR_UNSUPPORTED, "replica rows do not fit two stages");
-  if (grad_dtype == DPOPT_GRAD_BF16) return dispatch_tma_gk<0>(p, stream);
-  return dispatch_tma_gk<1>(p, stream);
 }
 
 // Kernel choice: the bulk-copy kernel where it applies and the policy allows,
@@ -381,13 +233,8 @@ bool use_tma(const SegDesc* segs, int s0, int s1, int n, int grad_dtype, float* 
 int run(const SegDesc* segs, int nsegs, int grad_dtype, int n, float* master, float* m, float* v,
         void* out, const Hyper& h, bool ext, cudaStream_t stream) {
   if (nsegs == 1) {
-    if (!ext && use_tma(segs, 0, 1, n, grad_dtype, master, m, v, out)) {
-      SmallTma p{};
-      p.h = h;
-      p.master = master; p.m = m; p.v = v; p.out = (uint16_t*)out;
-      p.n_rep = n;
-      return run_segments_tma(p, segs, 0, 1, n, stream, grad_dtype);
-    }
+    if (!ext && use_tma(segs, 0, 1, n, grad_dtype, master, m, v, out))
+      return run_tma(segs, 0, 1, n, grad_dtype, master, m, v, out, h, stream);
     SmallParams p{};
     p.h = h;
     p.master = master; p.m = m; p.v = v; p.out = (uint16_t*)out;
@@ -399,14 +246,9 @@ int run(const SegDesc* segs, int nsegs, int grad_dtype, int n, float* master, fl
     const int s1 = std::min(nsegs, s0 + per_launch);
     int rc;
     if (!ext && use_tma(segs, s0, s1, n, grad_dtype, master, m, v, out)) {
-      static thread_local BigTma p;  // 20 KB: kept off the stack
-      std::memset(&p, 0, sizeof p);
-      p.h = h;
-      p.master = master; p.m = m; p.v = v; p.out = (uint16_t*)out;
-      p.n_rep = n;
-      rc = run_segments_tma(p, segs, s0, s1, n, stream, grad_dtype);
+      rc = run_tma(segs, s0, s1, n, grad_dtype, master, m, v, out, h, stream);
     } else {
-      static thread_local BigParams p;
+      static thread_local BigParams p;  // 20 KB: kept off the stack
       std::memset(&p, 0, sizeof p);
       p.h = h;
       p.master = master; p.m = m; p.v = v; p.out = (uint16_t*)out;
@@ -428,37 +270,12 @@ int64_t norm_chunks(const SegDesc* segs, int nsegs) {
   return c;
 }
 
-// Unrolled replica loops for N in {1, 2, 4, 8} (fewer registers, four CTAs
-// per SM), a runtime loop otherwise.  The accumulation order is the same.
-template <int GK, int MS, int MP>
-void sqnorm_launch_gk(const LaunchParams<MS, MP>& p, unsigned grid, double* partials,
-                      int64_t nchunks, cudaStream_t stream) {
-  switch (p.n_rep) {
-    case 1: grad_sqnorm_kernel<1, GK, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks); return;
-    case 2: grad_sqnorm_kernel<2, GK, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks); return;
-    case 4: grad_sqnorm_kernel<4, GK, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks); return;
-    case 8: grad_sqnorm_kernel<8, GK, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks); return;
-    default: grad_sqnorm_kernel<0, GK, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks);
-  }
-}
-
 template <int MS, int MP>
 int launch_sqnorm(LaunchParams<MS, MP>& p, int64_t nchunks, double* partials, int grad_dtype,
                   cudaStream_t stream) {
-  int sms = 0;
-  int rc = sm_count(&sms);
-  if (rc) return rc;
-  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nchunks, (int64_t)sms * 4));
-  if (grad_dtype == DPOPT_GRAD_BF16)
-    sqnorm_launch_gk<0>(p, grid, partials, nchunks, stream);
-  else if (grad_dtype == DPOPT_GRAD_F16)
-    sqnorm_launch_gk<2>(p, grid, partials, nchunks, stream);
-  else
-    sqnorm_launch_gk<1>(p, grid, partials, nchunks, stream);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
-  ++g_launches;
-  return DPOPT_OK;
+  if (grad_dtype == DPOPT_GRAD_BF16) return launch_sqnorm_pass<0>(p, partials, nchunks, stream);
+  if (grad_dtype == DPOPT_GRAD_F16) return launch_sqnorm_pass<2>(p, partials, nchunks, stream);
+  return launch_sqnorm_pass<1>(p, partials, nchunks, stream);
 }
 
 // Squared norm of segments [0, nsegs) into *out (device), partials in scratch.
@@ -474,14 +291,14 @@ int run_sqnorm(const SegDesc* segs, int nsegs, int grad_dtype, int n, const Hype
       SmallParams p{};
       p.h = h;
       p.n_rep = n;
-      chunks = fill_segments(p, segs, s0, s1, n, kNormChunk);
+      chunks = fill_segments(p, segs, s0, s1, n, kNormChunk, grad_dtype);
       rc = chunks ? launch_sqnorm(p, chunks, partials + done, grad_dtype, stream) : DPOPT_OK;
     } else {
       static thread_local BigParams p;
       std::memset(&p, 0, sizeof p);
       p.h = h;
       p.n_rep = n;
-      chunks = fill_segments(p, segs, s0, s1, n, kNormChunk);
+      chunks = fill_segments(p, segs, s0, s1, n, kNormChunk, grad_dtype);
       rc = chunks ? launch_sqnorm(p, chunks, partials + done, grad_dtype, stream) : DPOPT_OK;
     }
     if (rc) return rc;
@@ -494,17 +311,6 @@ int run_sqnorm(const SegDesc* segs, int nsegs, int grad_dtype, int n, const Hype
   return DPOPT_OK;
 }
 
-}  // namespace
-}  // namespace dpopt
-
-using namespace dpopt;
-
-extern "C" {
-
-}  // extern "C"
-
-namespace dpopt {
-namespace {
 
 // The segments of a full-buffer call (one: the whole shard), checked.  `avoid`
 // lists extra ranges the gradients must not overlap (states, outputs, scratch).
@@ -712,39 +518,11 @@ int check_state_ptr(const void* st) {
   return DPOPT_OK;
 }
 
-template <int GK, int PACK, int MS, int MP>
-int launch_amp(const LaunchParams<MS, MP>& p, const LossScaleState* st, const double* sq,
-               cudaStream_t stream) {
-  auto kern = reduce_adam_amp_kernel<GK, PACK, MS, MP>;
-  int sms = 0;
-  int rc = sm_count(&sms);
-  if (rc) return rc;
-  static std::atomic<int> per_sm{0};
-  int bps = per_sm.load(std::memory_order_relaxed);
-  if (bps == 0) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, kThreads, 0);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-    if (bps < 1) bps = 1;
-    per_sm.store(bps, std::memory_order_relaxed);
-  }
-  const int64_t want = (p.total_groups + kThreads - 1) / kThreads;
-  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * bps));
-  kern<<<grid, kThreads, 0, stream>>>(p, st, sq);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
-  ++g_launches;
-  return DPOPT_OK;
-}
-
-template <int MS, int MP>
-int dispatch_amp(const LaunchParams<MS, MP>& p, int grad_dtype, const LossScaleState* st,
-                 const double* sq, cudaStream_t stream) {
-  const bool pack = p.n_rep > 8;
-  if (grad_dtype == DPOPT_GRAD_F16)
-    return pack ? launch_amp<2, 1>(p, st, sq, stream) : launch_amp<2, 0>(p, st, sq, stream);
-  if (grad_dtype == DPOPT_GRAD_BF16)
-    return pack ? launch_amp<0, 1>(p, st, sq, stream) : launch_amp<0, 0>(p, st, sq, stream);
-  return pack ? launch_amp<1, 1>(p, st, sq, stream) : launch_amp<1, 0>(p, st, sq, stream);
+int dispatch_amp(const SmallParams& p, int grad_dtype, const LossScaleState* st, const double* sq,
+                 cudaStream_t stream) {
+  if (grad_dtype == DPOPT_GRAD_F16) return launch_amp_step<2>(p, st, sq, stream);
+  if (grad_dtype == DPOPT_GRAD_BF16) return launch_amp_step<0>(p, st, sq, stream);
+  return launch_amp_step<1>(p, st, sq, stream);
 }
 
 int launch_scale_update(LossScaleState* st, const double* sq, const LossScaleConfig& cfg,
@@ -791,6 +569,8 @@ int noalloc_partials(double** out) {
 
 }  // namespace
 }  // namespace dpopt
+
+using namespace dpopt;
 
 extern "C" {
 
@@ -1065,7 +845,7 @@ int dpopt_amp_step(const void* const* grads, int grad_dtype, int n_replicas, int
   p.master = master_f32; p.m = m_f32; p.v = v_f32; p.out = (uint16_t*)param_bf16_out;
   p.n_rep = n_replicas;
   SegDesc seg{ptrs, 0, S};
-  if (fill_segments(p, &seg, 0, 1, n_replicas, kGroup) > 0) {
+  if (fill_segments(p, &seg, 0, 1, n_replicas, kGroup, grad_dtype) > 0) {
     rc = dispatch_amp(p, grad_dtype, (const LossScaleState*)state, global_sqnorm,
                       (cudaStream_t)stream);
     if (rc) return rc;
@@ -1164,16 +944,10 @@ int dpopt_allgather_bf16(const void* shard_bf16, int64_t shard_elems, int shard_
 int dpopt_stream_status(dpopt_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  unsigned int st = 0;
-  e = cudaMemcpyFromSymbol(&st, g_status, sizeof st);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol");
-  if (st != 0) {
-    const unsigned int zero = 0;
-    e = cudaMemcpyToSymbol(g_status, &zero, sizeof zero);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
-    return DPOPT_ERR_TIMEOUT;
-  }
-  return DPOPT_OK;
+  bool timed_out = false;
+  const int rc = take_wait_status(&timed_out);
+  if (rc) return rc;
+  return timed_out ? DPOPT_ERR_TIMEOUT : DPOPT_OK;
 }
 
 const char* dpopt_status_string(int status) {
@@ -1217,11 +991,7 @@ int dpopt_selftest_wait_timeout(int64_t limit_cycles, dpopt_stream_t stream) {
   if (limit_cycles < 1 || limit_cycles > kWaitLimitCycles)
     return fail(DPOPT_ERR_INVALID_ARG, "limit_cycles must lie in [1, %lld]",
                 (long long)kWaitLimitCycles);
-  selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((long long)limit_cycles);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
-  ++g_launches;
-  return DPOPT_OK;
+  return launch_selftest_wait((long long)limit_cycles, (cudaStream_t)stream);
 }
 
 const char* dpopt_version(void) { return "0.1.0"; }

@@ -21,16 +21,12 @@ namespace dpopt {
 constexpr int kGroup = 8;      // elements per thread per iteration
 constexpr int kThreads = 256;  // threads per CTA
 
-// Sticky per-device status word: bit 0 is set when a bounded device-side wait
-// gave up.  Read and cleared by dpopt_stream_status().
-__device__ unsigned int g_status;
-
 struct Seg {
   int64_t first_group;  // groups of all earlier segments (prefix sum)
   int64_t state_off;    // first shard element this segment updates
   int64_t len;          // elements
   int32_t ptr_base;     // index of replica 0's pointer in LaunchParams::gptr
-  int32_t vec;          // 1: every pointer of the segment is 16-byte aligned
+  int32_t vec;          // 2: 32-byte accesses apply (see fill_segments), 1: 16-byte, 0: scalar
 };
 
 template <int MAXSEG, int MAXPTR>
@@ -88,8 +84,31 @@ __device__ __forceinline__ void st_stream16u(void* p, uint32_t a, uint32_t b, ui
                : "memory");
 }
 
+// 32 bytes in one 256-bit access (sm_100 and later; the address must be
+// 32-byte aligned).  A warp then moves 1 KB of contiguous, whole 32-byte
+// sectors per instruction, where two 16-byte accesses per thread would each
+// touch every sector of that KB by halves.
+__device__ __forceinline__ void ld_state32(const float* p, float4& lo, float4& hi) {
+  asm("ld.global.nc.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=f"(lo.x), "=f"(lo.y), "=f"(lo.z), "=f"(lo.w), "=f"(hi.x), "=f"(hi.y), "=f"(hi.z),
+        "=f"(hi.w)
+      : "l"(p));
+}
+
+__device__ __forceinline__ void ld_grad32(const void* p, uint64_t pol, uint4& a, uint4& b) {
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+      : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+      : "l"(p), "l"(pol));
+}
+
+__device__ __forceinline__ void st_stream32(float* p, float4 lo, float4 hi) {
+  asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(lo.x),
+               "f"(lo.y), "f"(lo.z), "f"(lo.w), "f"(hi.x), "f"(hi.y), "f"(hi.z), "f"(hi.w)
+               : "memory");
+}
+
 // 8 gradient values of one replica as fp32.  GK 0: bf16 (one 16-byte load),
-// GK 1: fp32 (two 16-byte loads).
+// GK 1: fp32 (one 32-byte load, or two 16-byte ones: W), GK 2: fp16.
 template <int GK>
 struct GradLoad;
 
@@ -104,6 +123,7 @@ __device__ __forceinline__ uint4 ld_shared16(uint32_t saddr) {
 template <>
 struct GradLoad<0> {
   uint4 w;
+  template <int W = 16>
   __device__ __forceinline__ void load(const void* base, int64_t e0, uint64_t pol) {
     w = ld_grad16(static_cast<const uint16_t*>(base) + e0, pol);
   }
@@ -122,10 +142,15 @@ struct GradLoad<0> {
 template <>
 struct GradLoad<1> {
   uint4 a, b;
+  template <int W = 16>
   __device__ __forceinline__ void load(const void* base, int64_t e0, uint64_t pol) {
     const float* p = static_cast<const float*>(base) + e0;
-    a = ld_grad16(p, pol);
-    b = ld_grad16(p + 4, pol);
+    if constexpr (W == 32) {
+      ld_grad32(p, pol, a, b);
+    } else {
+      a = ld_grad16(p, pol);
+      b = ld_grad16(p + 4, pol);
+    }
   }
   __device__ __forceinline__ void load_shared(uint32_t saddr) {
     a = ld_shared16(saddr);
@@ -154,6 +179,7 @@ __device__ __forceinline__ float f16_to_f32(uint32_t bits16) {
 template <>
 struct GradLoad<2> {
   uint4 w;
+  template <int W = 16>
   __device__ __forceinline__ void load(const void* base, int64_t e0, uint64_t pol) {
     w = ld_grad16(static_cast<const uint16_t*>(base) + e0, pol);
   }
@@ -185,16 +211,24 @@ __device__ __forceinline__ float ld_grad1(const void* base, int64_t e) {
 // where one 8-element group's inputs come from, where its outputs go
 // ---------------------------------------------------------------------------
 
-// Inputs read straight from global memory (the direct-load kernel).
-template <int GK>
+// Inputs read straight from global memory (the direct-load kernel).  W: the
+// width of one state access (32: one 256-bit load per array, 16: two).
+template <int GK, int W = 16>
 struct GlobalSource {
   const void* const* gp;  // the segment's replica pointers
   int64_t e0;             // group's first element within the segment
   const float* st[3];     // master, m, v at the group's first element
   uint64_t pol;
-  __device__ __forceinline__ void grad(GradLoad<GK>& g, int r) const { g.load(gp[r], e0, pol); }
-  __device__ __forceinline__ float4 state(int a, int half) const {
-    return ld_state16(st[a] + 4 * half);
+  __device__ __forceinline__ void grad(GradLoad<GK>& g, int r) const {
+    g.template load<W>(gp[r], e0, pol);
+  }
+  __device__ __forceinline__ void state8(int a, float4& lo, float4& hi) const {
+    if constexpr (W == 32) {
+      ld_state32(st[a], lo, hi);
+    } else {
+      lo = ld_state16(st[a]);
+      hi = ld_state16(st[a] + 4);
+    }
   }
 };
 
@@ -207,20 +241,32 @@ struct SharedSource {
   __device__ __forceinline__ void grad(GradLoad<GK>& g, int r) const {
     g.load_shared(g0 + (uint32_t)r * rstride);
   }
-  __device__ __forceinline__ float4 state(int a, int half) const {
-    uint4 u = ld_shared16(st[a] + 16u * half);
-    return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
-                       __uint_as_float(u.w));
+  __device__ __forceinline__ void state8(int a, float4& lo, float4& hi) const {
+    const uint4 u = ld_shared16(st[a]), w = ld_shared16(st[a] + 16u);
+    lo = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                     __uint_as_float(u.w));
+    hi = make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                     __uint_as_float(w.w));
   }
 };
 
-// Outputs, at the group's first element.
-struct GroupOut {
+// Outputs, at the group's first element; W as for GlobalSource.
+template <int W = 16>
+struct GroupOutT {
   float* master;
   float* m;
   float* v;
   uint16_t* out;
+  __device__ __forceinline__ void put(float* p, float4 lo, float4 hi) const {
+    if constexpr (W == 32) {
+      st_stream32(p, lo, hi);
+    } else {
+      st_stream16(p, lo.x, lo.y, lo.z, lo.w);
+      st_stream16(p + 4, hi.x, hi.y, hi.z, hi.w);
+    }
+  }
 };
+using GroupOut = GroupOutT<16>;
 
 // ---------------------------------------------------------------------------
 // one 8-element group, vector path
@@ -270,18 +316,19 @@ __device__ __forceinline__ void reduce_group_x1(const Src& src, int n, CompSum<f
 
 // Scalar-lane form: 8 elements per thread, one element per operation.  Fewer
 // register pairings; faster when the optimizer arithmetic dominates (small N).
-template <int NR, int GK, bool EXT, class Src>
-__device__ __forceinline__ void group_vec_x1(const Src& src, int n, const Hyper& h,
-                                             const GroupOut& o, float gscale) {
+template <int NR, int GK, bool EXT, class Src, class Out>
+__device__ __forceinline__ void group_vec_x1(const Src& src, int n, const Hyper& h, const Out& o,
+                                             float gscale) {
   float th[kGroup], mm[kGroup], vv[kGroup];
   {
-    float4 a = src.state(0, 0), b = src.state(0, 1);
+    float4 a, b;
+    src.state8(0, a, b);
     th[0] = a.x; th[1] = a.y; th[2] = a.z; th[3] = a.w;
     th[4] = b.x; th[5] = b.y; th[6] = b.z; th[7] = b.w;
-    a = src.state(1, 0); b = src.state(1, 1);
+    src.state8(1, a, b);
     mm[0] = a.x; mm[1] = a.y; mm[2] = a.z; mm[3] = a.w;
     mm[4] = b.x; mm[5] = b.y; mm[6] = b.z; mm[7] = b.w;
-    a = src.state(2, 0); b = src.state(2, 1);
+    src.state8(2, a, b);
     vv[0] = a.x; vv[1] = a.y; vv[2] = a.z; vv[3] = a.w;
     vv[4] = b.x; vv[5] = b.y; vv[6] = b.z; vv[7] = b.w;
   }
@@ -293,31 +340,29 @@ __device__ __forceinline__ void group_vec_x1(const Src& src, int n, const Hyper&
     if constexpr (EXT) g = __fmul_rn(g, gscale);
     adam_update<EXT>(g, th[k], mm[k], vv[k], h);
   }
-  st_stream16(o.master, th[0], th[1], th[2], th[3]);
-  st_stream16(o.master + 4, th[4], th[5], th[6], th[7]);
-  st_stream16(o.m, mm[0], mm[1], mm[2], mm[3]);
-  st_stream16(o.m + 4, mm[4], mm[5], mm[6], mm[7]);
-  st_stream16(o.v, vv[0], vv[1], vv[2], vv[3]);
-  st_stream16(o.v + 4, vv[4], vv[5], vv[6], vv[7]);
+  o.put(o.master, make_float4(th[0], th[1], th[2], th[3]), make_float4(th[4], th[5], th[6], th[7]));
+  o.put(o.m, make_float4(mm[0], mm[1], mm[2], mm[3]), make_float4(mm[4], mm[5], mm[6], mm[7]));
+  o.put(o.v, make_float4(vv[0], vv[1], vv[2], vv[3]), make_float4(vv[4], vv[5], vv[6], vv[7]));
   st_stream16u(o.out, to_bf16x2(th[0], th[1]), to_bf16x2(th[2], th[3]),
                to_bf16x2(th[4], th[5]), to_bf16x2(th[6], th[7]));
 }
 
 // Packed form: 4 element pairs per thread, every operation on f32x2 lanes.
 // Pays off when the replica sum dominates (large N).
-template <int NR, int GK, bool EXT, class Src>
-__device__ __forceinline__ void group_vec_x2(const Src& src, int n, const Hyper& h,
-                                             const GroupOut& o, float gscale) {
+template <int NR, int GK, bool EXT, class Src, class Out>
+__device__ __forceinline__ void group_vec_x2(const Src& src, int n, const Hyper& h, const Out& o,
+                                             float gscale) {
   constexpr int P = kGroup / 2;  // element pairs per group
   float2 th[P], mm[P], vv[P];
   {
-    float4 a = src.state(0, 0), b = src.state(0, 1);
+    float4 a, b;
+    src.state8(0, a, b);
     th[0] = make_float2(a.x, a.y); th[1] = make_float2(a.z, a.w);
     th[2] = make_float2(b.x, b.y); th[3] = make_float2(b.z, b.w);
-    a = src.state(1, 0); b = src.state(1, 1);
+    src.state8(1, a, b);
     mm[0] = make_float2(a.x, a.y); mm[1] = make_float2(a.z, a.w);
     mm[2] = make_float2(b.x, b.y); mm[3] = make_float2(b.z, b.w);
-    a = src.state(2, 0); b = src.state(2, 1);
+    src.state8(2, a, b);
     vv[0] = make_float2(a.x, a.y); vv[1] = make_float2(a.z, a.w);
     vv[2] = make_float2(b.x, b.y); vv[3] = make_float2(b.z, b.w);
   }
@@ -385,12 +430,12 @@ __device__ __forceinline__ void group_vec_x2(const Src& src, int n, const Hyper&
     if constexpr (EXT) g = vmul(g, splat<float2>(gscale));
     adam_update<EXT>(g, th[j], mm[j], vv[j], h);
   }
-  st_stream16(o.master, th[0].x, th[0].y, th[1].x, th[1].y);
-  st_stream16(o.master + 4, th[2].x, th[2].y, th[3].x, th[3].y);
-  st_stream16(o.m, mm[0].x, mm[0].y, mm[1].x, mm[1].y);
-  st_stream16(o.m + 4, mm[2].x, mm[2].y, mm[3].x, mm[3].y);
-  st_stream16(o.v, vv[0].x, vv[0].y, vv[1].x, vv[1].y);
-  st_stream16(o.v + 4, vv[2].x, vv[2].y, vv[3].x, vv[3].y);
+  o.put(o.master, make_float4(th[0].x, th[0].y, th[1].x, th[1].y),
+        make_float4(th[2].x, th[2].y, th[3].x, th[3].y));
+  o.put(o.m, make_float4(mm[0].x, mm[0].y, mm[1].x, mm[1].y),
+        make_float4(mm[2].x, mm[2].y, mm[3].x, mm[3].y));
+  o.put(o.v, make_float4(vv[0].x, vv[0].y, vv[1].x, vv[1].y),
+        make_float4(vv[2].x, vv[2].y, vv[3].x, vv[3].y));
   st_stream16u(o.out, to_bf16x2(th[0].x, th[0].y), to_bf16x2(th[1].x, th[1].y),
                to_bf16x2(th[2].x, th[2].y), to_bf16x2(th[3].x, th[3].y));
 }
@@ -426,14 +471,18 @@ __device__ __noinline__ void group_scalar(const LP& p, const Hyper& h, const Seg
 // ---------------------------------------------------------------------------
 
 // Resident CTAs per SM the register budget is sized for: 4 x 256 threads
-// (<= 64 registers) with an unrolled replica count; the runtime-count bodies
-// take what they need (2 CTAs for the packed one).
+// (<= 64 registers) with an unrolled replica count (N <= 8); the runtime-count
+// bodies take what they need (2 CTAs for the packed one).
 template <int NR, int PACK>
 constexpr int min_ctas() { return NR > 0 ? 4 : (PACK ? 2 : 1); }
 
-// The grid-stride walk over the 8-element groups of every segment.
-template <int NR, int GK, int PACK, bool EXT, class LP>
+// The grid-stride walk over the 8-element groups of every segment.  W is the
+// width of one state access (32: one 256-bit access per array, for segments
+// of vector level 2; 16: two 16-byte accesses, level >= 1); other groups go
+// one element at a time.
+template <int NR, int GK, int PACK, bool EXT, int W, class LP>
 __device__ __forceinline__ void step_loop(const LP& p, const Hyper& h, float gscale) {
+  constexpr int kLevel = W == 32 ? 2 : 1;
   const uint64_t pol = evict_first_policy();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int si = 0;
@@ -443,11 +492,11 @@ __device__ __forceinline__ void step_loop(const LP& p, const Hyper& h, float gsc
     const Seg& sg = p.seg[si];
     const int64_t e0 = (gi - sg.first_group) * kGroup;
     const int64_t rem = sg.len - e0;
-    if (sg.vec && rem >= kGroup) {
-      const int64_t so = sg.state_off + e0;
-      const GlobalSource<GK> src{p.gptr + sg.ptr_base, e0, {p.master + so, p.m + so, p.v + so},
-                                 pol};
-      const GroupOut o{p.master + so, p.m + so, p.v + so, p.out + so};
+    const int64_t so = sg.state_off + e0;
+    if (sg.vec >= kLevel && rem >= kGroup) {
+      const GlobalSource<GK, W> src{p.gptr + sg.ptr_base, e0,
+                                    {p.master + so, p.m + so, p.v + so}, pol};
+      const GroupOutT<W> o{p.master + so, p.m + so, p.v + so, p.out + so};
       if constexpr (PACK) group_vec_x2<NR, GK, EXT>(src, p.n_rep, h, o, gscale);
       else group_vec_x1<NR, GK, EXT>(src, p.n_rep, h, o, gscale);
     } else {
@@ -459,11 +508,11 @@ __device__ __forceinline__ void step_loop(const LP& p, const Hyper& h, float gsc
 // PACK selects the lane form of the vector body (0: scalar, 1: f32x2); the
 // two forms give identical bits, so the choice is made by speed alone.  EXT
 // adds the AdamW decay and the gradient multiplier (clipping, unscaling).
-template <int NR, int GK, int PACK, bool EXT, int MAXSEG, int MAXPTR>
+template <int NR, int GK, int PACK, bool EXT, int W, int MAXSEG, int MAXPTR>
 __global__ void __launch_bounds__(kThreads, min_ctas<NR, PACK>())
     reduce_adam_ldg_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p) {
   const float gscale = EXT ? grad_scale_of(p.h) : 1.f;
-  step_loop<NR, GK, PACK, EXT>(p, p.h, gscale);
+  step_loop<NR, GK, PACK, EXT, W>(p, p.h, gscale);
 }
 
 // ---------------------------------------------------------------------------
@@ -492,11 +541,15 @@ struct LossScaleConfig {
 // the bias corrections of step state->step + 1 and the multiplier 1/scale
 // (times the clip coefficient) are formed here, from device state, so no host
 // synchronisation is needed between steps.
-template <int GK, int PACK, int MAXSEG, int MAXPTR>
-__global__ void __launch_bounds__(kThreads, PACK ? 2 : 1)
+template <int NR, int GK, int PACK, int W, int MAXSEG, int MAXPTR>
+__global__ void __launch_bounds__(kThreads, min_ctas<NR, PACK>())
     reduce_adam_amp_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p,
                            const LossScaleState* state, const double* sqnorm) {
-  __shared__ Hyper hs;
+  // Thread 0 forms the step's scalars once; every thread then takes a copy of
+  // the grid-constant Hyper with only those overwritten, so the untouched
+  // fields stay constant-bank operands instead of occupying registers.
+  __shared__ float s_ab[4];
+  __shared__ float s_gscale;
   __shared__ int skip;
   if (threadIdx.x == 0) {
     Hyper h = p.h;
@@ -508,59 +561,22 @@ __global__ void __launch_bounds__(kThreads, PACK ? 2 : 1)
     const double bc2 = 1.0 - pow((double)h.beta2, t);
     const double a = (double)h.lr / bc1;
     const double b = 1.0 / sqrt(bc2);
-    h.a_hi = __double2float_rn(a);
-    h.a_lo = __double2float_rn(a - (double)h.a_hi);
-    h.b_hi = __double2float_rn(b);
-    h.b_lo = __double2float_rn(b - (double)h.b_hi);
+    s_ab[0] = __double2float_rn(a);
+    s_ab[1] = __double2float_rn(a - (double)s_ab[0]);
+    s_ab[2] = __double2float_rn(b);
+    s_ab[3] = __double2float_rn(b - (double)s_ab[2]);
     h.unscale = __fdiv_rn(1.f, st.scale);
     h.sqnorm = sqnorm;
-    hs = h;
+    s_gscale = grad_scale_of(h);
   }
   __syncthreads();
   if (skip) return;
-  const float gscale = grad_scale_of(hs);
-  step_loop<0, GK, PACK, true>(p, hs, gscale);
-}
-
-__global__ void loss_scale_init_kernel(LossScaleState* st, LossScaleConfig cfg) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  LossScaleState s;
-  s.scale = cfg.init_scale;
-  s.good_steps = 0;
-  s.hysteresis_left = cfg.hysteresis;
-  s.last_overflow = 0;
-  s.step = 0;
-  s.skipped = 0;
-  *st = s;
-}
-
-// After a step: skip bookkeeping, halving on every hysteresis-th overflow since
-// the scale last changed (not below min_scale), doubling after `window` clean
-// steps in a row.
-__global__ void loss_scale_update_kernel(LossScaleState* st, const double* sqnorm,
-                                         LossScaleConfig cfg) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  LossScaleState s = *st;
-  const bool overflow = !isfinite(*sqnorm);
-  s.last_overflow = overflow ? 1 : 0;
-  if (overflow) {
-    s.skipped += 1;
-    s.good_steps = 0;
-    s.hysteresis_left -= 1;
-    if (s.hysteresis_left <= 0) {
-      s.scale = fmaxf(s.scale * 0.5f, cfg.min_scale);
-      s.hysteresis_left = cfg.hysteresis;
-    }
-  } else {
-    s.step += 1;
-    s.good_steps += 1;
-    if (s.good_steps >= cfg.window) {
-      s.scale = s.scale * 2.0f;
-      s.good_steps = 0;
-      s.hysteresis_left = cfg.hysteresis;
-    }
-  }
-  *st = s;
+  Hyper h = p.h;
+  h.a_hi = s_ab[0];
+  h.a_lo = s_ab[1];
+  h.b_hi = s_ab[2];
+  h.b_lo = s_ab[3];
+  step_loop<NR, GK, PACK, true, W>(p, h, s_gscale);
 }
 
 // ---------------------------------------------------------------------------
@@ -577,6 +593,17 @@ constexpr int kNormChunk = 65536;
 // fp32 pair (TwoProd for each square, TwoSum into the sum: about 2^-44
 // relative), then the threads' sums are added in fp64 over a fixed tree.
 // Seg::first_group holds the segment's first chunk here.
+// The averaged gradient of one aligned 8-element group, as the step forms it.
+template <int NR, int GK, int W>
+__device__ __forceinline__ void norm_group(const void* const* gp, int64_t e0, uint64_t pol, int n,
+                                           const Hyper& h, float (&g)[kGroup]) {
+  const GlobalSource<GK, W> src{gp, e0, {nullptr, nullptr, nullptr}, pol};
+  CompSum<float> cs[kGroup];
+  reduce_group_x1<NR, GK>(src, n, cs);
+#pragma unroll
+  for (int j = 0; j < kGroup; ++j) g[j] = cs[j].average(h);
+}
+
 template <int NR, int GK, int MAXSEG, int MAXPTR>
 __global__ void __launch_bounds__(kThreads, NR > 0 ? 4 : 2)
     grad_sqnorm_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p, double* partials,
@@ -597,12 +624,10 @@ __global__ void __launch_bounds__(kThreads, NR > 0 ? 4 : 2)
       const int64_t rem = sg.len - e0;
       float g[kGroup];
       int cnt = kGroup;
-      if (sg.vec && rem >= kGroup) {
-        const GlobalSource<GK> src{gp, e0, {nullptr, nullptr, nullptr}, pol};
-        CompSum<float> cs[kGroup];
-        reduce_group_x1<NR, GK>(src, p.n_rep, cs);
-#pragma unroll
-        for (int j = 0; j < kGroup; ++j) g[j] = cs[j].average(p.h);
+      if (GK == 1 && sg.vec == 2 && rem >= kGroup) {
+        norm_group<NR, GK, 32>(gp, e0, pol, p.n_rep, p.h, g);
+      } else if (sg.vec && rem >= kGroup) {
+        norm_group<NR, GK, 16>(gp, e0, pol, p.n_rep, p.h, g);
       } else {
         cnt = (int)(rem < kGroup ? rem : kGroup);
         for (int j = 0; j < cnt; ++j) {
@@ -637,22 +662,6 @@ __global__ void __launch_bounds__(kThreads, NR > 0 ? 4 : 2)
     if (threadIdx.x == 0) partials[c] = red[0];
     __syncthreads();
   }
-}
-
-// Sum of the partials in a fixed order: strided per thread, then a fixed tree.
-__global__ void __launch_bounds__(kThreads)
-    sqnorm_finish_kernel(const double* partials, int64_t nchunks, double* out) {
-  __shared__ double red[kThreads];
-  double acc = 0.0;
-  for (int64_t c = threadIdx.x; c < nchunks; c += kThreads) acc = __dadd_rn(acc, partials[c]);
-  red[threadIdx.x] = acc;
-  __syncthreads();
-#pragma unroll
-  for (int w = kThreads / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) red[threadIdx.x] = __dadd_rn(red[threadIdx.x], red[threadIdx.x + w]);
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) *out = red[0];
 }
 
 }  // namespace dpopt

@@ -1,0 +1,218 @@
+// launch_gk.cu -- the kernels of one gradient type and their launchers: the
+// fused reduce + Adam step, the loss-scaled step and the squared-norm pass.
+// The build compiles this file once per type (-DDPOPT_GK=0 bf16, 1 fp32,
+// 2 fp16), so the three instantiation sets compile in parallel.
+//
+// Replica counts 1..8 each get a kernel with the replica loop unrolled: at
+// most 64 registers, so four 256-thread CTAs share an SM and every thread has
+// all N of its gradient loads in flight at once.  Above 8 the runtime-count
+// packed body runs (two CTAs per SM).  The accumulation order is the same in
+// every form, so the choice changes speed only, never bits.
+//
+// State access width per kernel, by measurement on GB300 (256M-element
+// shards): one 256-bit access per state array and thread (W = 32: whole
+// sectors, half the load/store instructions) is faster where the arithmetic
+// per byte is highest -- bf16/fp16 gradients with N <= 3 (+5..7% at N = 2, 3)
+// and fp32 gradients with N <= 6 (+2..10%) -- and 2..4% slower above, where
+// its 8-register tuples cost spills; there two 16-byte accesses (W = 16) run.
+#include <algorithm>
+#include <atomic>
+
+#include "internal.h"
+
+#ifndef DPOPT_GK
+#error "compile with -DDPOPT_GK=0 (bf16), 1 (fp32) or 2 (fp16)"
+#endif
+
+// The helpers below live in a namespace of their own per gradient type: nvcc
+// names an anonymous namespace after the source file, and this file is
+// compiled three times into one library.
+#if DPOPT_GK == 0
+#define DPOPT_GK_NS gk_bf16
+#elif DPOPT_GK == 1
+#define DPOPT_GK_NS gk_f32
+#elif DPOPT_GK == 2
+#define DPOPT_GK_NS gk_f16
+#else
+#error "DPOPT_GK must be 0, 1 or 2"
+#endif
+
+namespace dpopt {
+namespace DPOPT_GK_NS {
+
+constexpr int kGK = DPOPT_GK;
+
+constexpr bool wide_states(int nr) { return nr >= 1 && (kGK == 1 ? nr <= 6 : nr <= 3); }
+
+// Whether every segment's vector level allows the 32-byte accesses (level 0
+// segments go one element at a time in either form).
+template <int MS, int MP>
+bool all_wide(const LaunchParams<MS, MP>& p) {
+  for (int s = 0; s < p.nseg; ++s)
+    if (p.seg[s].vec == 1) return false;
+  return true;
+}
+
+// Persistent grid: `want` CTAs of work, capped at the resident CTAs of every
+// SM (occupancy looked up once per kernel).
+template <class Kern>
+int persistent_grid(Kern kern, std::atomic<int>& per_sm, int64_t want, unsigned* grid) {
+  int sms = 0;
+  int rc = sm_count(&sms);
+  if (rc) return rc;
+  int bps = per_sm.load(std::memory_order_relaxed);
+  if (bps == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, kThreads, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (bps < 1) bps = 1;
+    per_sm.store(bps, std::memory_order_relaxed);
+  }
+  *grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * bps));
+  return DPOPT_OK;
+}
+
+int launched() {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  count_launch();
+  return DPOPT_OK;
+}
+
+// ---------------------------------------------------------------------------
+// the step
+// ---------------------------------------------------------------------------
+
+template <int NR, int PACK, bool EXT, int W, int MS, int MP>
+int step_kernel(const LaunchParams<MS, MP>& p, cudaStream_t stream) {
+  auto kern = reduce_adam_ldg_kernel<NR, kGK, PACK, EXT, W, MS, MP>;
+  static std::atomic<int> per_sm{0};
+  unsigned grid = 0;
+  int rc = persistent_grid(kern, per_sm, (p.total_groups + kThreads - 1) / kThreads, &grid);
+  if (rc) return rc;
+  kern<<<grid, kThreads, 0, stream>>>(p);
+  return launched();
+}
+
+// Unrolled kernel for NR replicas in its measured width; a 32-byte kernel
+// whose segments are not all 32-byte aligned hands over to the runtime-count
+// 16-byte kernel.
+template <int NR, bool EXT, int MS, int MP>
+int step_nr(const LaunchParams<MS, MP>& p, cudaStream_t s) {
+  if constexpr (wide_states(NR)) {
+    if (all_wide(p)) return step_kernel<NR, 0, EXT, 32>(p, s);
+    return step_kernel<0, 1, EXT, 16>(p, s);
+  } else {
+    return step_kernel<NR, 0, EXT, 16>(p, s);
+  }
+}
+
+template <bool EXT, int MS, int MP>
+int step_n(const LaunchParams<MS, MP>& p, cudaStream_t s) {
+  switch (p.n_rep) {
+    case 1: return step_nr<1, EXT>(p, s);
+    case 2: return step_nr<2, EXT>(p, s);
+    case 3: return step_nr<3, EXT>(p, s);
+    case 4: return step_nr<4, EXT>(p, s);
+    case 5: return step_nr<5, EXT>(p, s);
+    case 6: return step_nr<6, EXT>(p, s);
+    case 7: return step_nr<7, EXT>(p, s);
+    case 8: return step_nr<8, EXT>(p, s);
+    default: return step_kernel<0, 1, EXT, 16>(p, s);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the loss-scaled step
+// ---------------------------------------------------------------------------
+
+template <int NR, int PACK, int W, int MS, int MP>
+int amp_kernel(const LaunchParams<MS, MP>& p, const LossScaleState* st, const double* sq,
+               cudaStream_t stream) {
+  auto kern = reduce_adam_amp_kernel<NR, kGK, PACK, W, MS, MP>;
+  static std::atomic<int> per_sm{0};
+  unsigned grid = 0;
+  int rc = persistent_grid(kern, per_sm, (p.total_groups + kThreads - 1) / kThreads, &grid);
+  if (rc) return rc;
+  kern<<<grid, kThreads, 0, stream>>>(p, st, sq);
+  return launched();
+}
+
+template <int NR, int MS, int MP>
+int amp_nr(const LaunchParams<MS, MP>& p, const LossScaleState* st, const double* sq,
+           cudaStream_t s) {
+  if constexpr (wide_states(NR)) {
+    if (all_wide(p)) return amp_kernel<NR, 0, 32>(p, st, sq, s);
+    return amp_kernel<0, 1, 16>(p, st, sq, s);
+  } else {
+    return amp_kernel<NR, 0, 16>(p, st, sq, s);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the squared-norm pass: one CTA per 65536-element chunk, four per SM
+// ---------------------------------------------------------------------------
+
+template <int NR, int MS, int MP>
+int norm_kernel(const LaunchParams<MS, MP>& p, double* partials, int64_t nchunks,
+                cudaStream_t stream) {
+  int sms = 0;
+  int rc = sm_count(&sms);
+  if (rc) return rc;
+  const unsigned grid =
+      (unsigned)std::max<int64_t>(1, std::min<int64_t>(nchunks, (int64_t)sms * 4));
+  grad_sqnorm_kernel<NR, kGK, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks);
+  return launched();
+}
+
+}  // namespace DPOPT_GK_NS
+
+using DPOPT_GK_NS::kGK;
+
+template <int G, int MS, int MP>
+int launch_step(const LaunchParams<MS, MP>& p, bool ext, cudaStream_t stream) {
+  static_assert(G == kGK, "launch_step instantiated for another gradient type");
+  return ext ? DPOPT_GK_NS::step_n<true>(p, stream) : DPOPT_GK_NS::step_n<false>(p, stream);
+}
+
+template <int G, int MS, int MP>
+int launch_amp_step(const LaunchParams<MS, MP>& p, const LossScaleState* state,
+                    const double* sqnorm, cudaStream_t stream) {
+  static_assert(G == kGK, "launch_amp_step instantiated for another gradient type");
+  switch (p.n_rep) {
+    case 1: return DPOPT_GK_NS::amp_nr<1>(p, state, sqnorm, stream);
+    case 2: return DPOPT_GK_NS::amp_nr<2>(p, state, sqnorm, stream);
+    case 3: return DPOPT_GK_NS::amp_nr<3>(p, state, sqnorm, stream);
+    case 4: return DPOPT_GK_NS::amp_nr<4>(p, state, sqnorm, stream);
+    case 5: return DPOPT_GK_NS::amp_nr<5>(p, state, sqnorm, stream);
+    case 6: return DPOPT_GK_NS::amp_nr<6>(p, state, sqnorm, stream);
+    case 7: return DPOPT_GK_NS::amp_nr<7>(p, state, sqnorm, stream);
+    case 8: return DPOPT_GK_NS::amp_nr<8>(p, state, sqnorm, stream);
+    default: return DPOPT_GK_NS::amp_kernel<0, 1, 16>(p, state, sqnorm, stream);
+  }
+}
+
+template <int G, int MS, int MP>
+int launch_sqnorm_pass(const LaunchParams<MS, MP>& p, double* partials, int64_t nchunks,
+                       cudaStream_t stream) {
+  static_assert(G == kGK, "launch_sqnorm_pass instantiated for another gradient type");
+  switch (p.n_rep) {
+    case 1: return DPOPT_GK_NS::norm_kernel<1>(p, partials, nchunks, stream);
+    case 2: return DPOPT_GK_NS::norm_kernel<2>(p, partials, nchunks, stream);
+    case 3: return DPOPT_GK_NS::norm_kernel<3>(p, partials, nchunks, stream);
+    case 4: return DPOPT_GK_NS::norm_kernel<4>(p, partials, nchunks, stream);
+    case 5: return DPOPT_GK_NS::norm_kernel<5>(p, partials, nchunks, stream);
+    case 6: return DPOPT_GK_NS::norm_kernel<6>(p, partials, nchunks, stream);
+    case 7: return DPOPT_GK_NS::norm_kernel<7>(p, partials, nchunks, stream);
+    case 8: return DPOPT_GK_NS::norm_kernel<8>(p, partials, nchunks, stream);
+    default: return DPOPT_GK_NS::norm_kernel<0>(p, partials, nchunks, stream);
+  }
+}
+
+template int launch_step<kGK>(const SmallParams&, bool, cudaStream_t);
+template int launch_step<kGK>(const BigParams&, bool, cudaStream_t);
+template int launch_amp_step<kGK>(const SmallParams&, const LossScaleState*, const double*,
+                                  cudaStream_t);
+template int launch_sqnorm_pass<kGK>(const SmallParams&, double*, int64_t, cudaStream_t);
+template int launch_sqnorm_pass<kGK>(const BigParams&, double*, int64_t, cudaStream_t);
+
+}  // namespace dpopt

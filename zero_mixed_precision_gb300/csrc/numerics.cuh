@@ -193,7 +193,7 @@ __device__ __forceinline__ V moment2(V v, V g, const Hyper& h) {
 // theta' = k*theta - lr * (m'/bc1) / (sqrt(v'/bc2) + eps), the plain fp32 form
 // (k = 1 - lr*weight_decay, 1 for plain Adam), used for non-finite inputs or
 // results.
-__device__ __noinline__ float master_update_plain(float theta, float m_new, float v_new,
+static __device__ __noinline__ float master_update_plain(float theta, float m_new, float v_new,
                                                   float a_hi, float b_hi, float eps, float k) {
   float d = __fadd_rn(__fmul_rn(__fsqrt_rn(v_new), b_hi), eps);
   float delta = __fdiv_rn(__fmul_rn(a_hi, m_new), d);

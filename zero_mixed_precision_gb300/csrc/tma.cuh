@@ -22,6 +22,10 @@
 
 namespace dpopt {
 
+// Sticky status word of this library image: bit 0 is set when a bounded
+// device-side wait gave up.  Read and cleared by dpopt_stream_status().
+__device__ unsigned int g_status;
+
 constexpr int kTmaConsumerWarps = 8;
 constexpr int kTmaThreads = 32 * (kTmaConsumerWarps + 1);
 constexpr int kTmaTile = kTmaConsumerWarps * 32 * kGroup;  // elements per tile (2048)
