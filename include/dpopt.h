@@ -375,11 +375,12 @@ int dpopt_state_bytes(int64_t psi, int variant, int n_dp, int zero_stage, double
 
 /* Which kernel carries the step (process-wide; default DPOPT_KERNEL_AUTO).
  *  DPOPT_KERNEL_AUTO    the faster of the two for the replica count, by measurement
- *  DPOPT_KERNEL_DIRECT  direct 16-byte loads from global memory into registers
+ *  DPOPT_KERNEL_DIRECT  direct vector loads from global memory into registers
  *  DPOPT_KERNEL_BULK    bulk copies (TMA) into a shared-memory ring, where it applies
- *                       (every pointer 16-byte aligned, two stages of 2048 elements fit
- *                       100 KB of shared memory: bf16 N <= 6, fp32 N <= 3); other calls
- *                       still take the direct-load kernel
+ *                       (master/m/v 32-byte aligned, every other pointer 16-byte
+ *                       aligned, two stages of 2048 elements fit 100 KB of shared
+ *                       memory: bf16 N <= 6, fp32 N <= 3); other calls still take
+ *                       the direct-load kernel
  * Both kernels give bitwise identical results.  Errors: DPOPT_ERR_INVALID_ARG for an
  * unknown value. */
 typedef enum { DPOPT_KERNEL_AUTO = 0, DPOPT_KERNEL_DIRECT = 1, DPOPT_KERNEL_BULK = 2 } dpopt_kernel_policy;

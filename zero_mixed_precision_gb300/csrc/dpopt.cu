@@ -25,11 +25,16 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-// Under DPOPT_KERNEL_AUTO the bulk-copy kernel serves N up to this.  Measured
-// on GB300 the direct-load kernel is as fast or faster at every N (6400 vs
-// 6386 GB/s at N = 4, the only replica count where the bulk-copy ring fits two
-// CTAs per SM), so AUTO always picks it.
-constexpr int kTmaAutoMaxReplicas = 0;
+// Under DPOPT_KERNEL_AUTO the bulk-copy kernel carries the step where it
+// measured faster than the direct-load kernel on GB300 (256M-element shards):
+// bf16 N = 3 (6444 against 6041 GB/s), fp32 N = 2 (6501 against 6145) and
+// fp32 N = 3 (6615 against 6360).  Elsewhere the direct-load kernel is as fast
+// or faster (bf16 N = 1: 6473 against 6006; bf16 N = 4..6 by 0..4%).
+bool auto_bulk(int n, int grad_dtype) {
+  if (grad_dtype == DPOPT_GRAD_BF16) return n == 3;
+  if (grad_dtype == DPOPT_GRAD_F32) return n == 2 || n == 3;
+  return false;
+}
 
 std::atomic<int> g_policy{DPOPT_KERNEL_AUTO};
 
@@ -227,7 +232,7 @@ bool use_tma(const SegDesc* segs, int s0, int s1, int n, int grad_dtype, float* 
   if (pol == DPOPT_KERNEL_DIRECT) return false;
   if (!tma_eligible(segs, s0, s1, n, grad_dtype, master, m, v, out)) return false;
   if (pol == DPOPT_KERNEL_BULK) return true;
-  return n <= kTmaAutoMaxReplicas;
+  return auto_bulk(n, grad_dtype);
 }
 
 int run(const SegDesc* segs, int nsegs, int grad_dtype, int n, float* master, float* m, float* v,

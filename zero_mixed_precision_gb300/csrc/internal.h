@@ -56,8 +56,9 @@ template <int GK, int MS, int MP>
 int launch_sqnorm_pass(const LaunchParams<MS, MP>& p, double* partials, int64_t nchunks,
                        cudaStream_t stream);
 
-// Bulk-copy kernel (tma.cu).  tma_eligible: every pointer 16-byte aligned,
-// a supported gradient type and the replica rows within the stage budget.
+// Bulk-copy kernel (tma.cu).  tma_eligible: master/m/v 32-byte aligned, the
+// other pointers 16-byte aligned, a supported gradient type and two stages of
+// replica rows within the shared-memory budget.
 bool tma_eligible(const SegDesc* segs, int s0, int s1, int n, int grad_dtype, const float* master,
                   const float* m, const float* v, const void* out);
 int run_tma(const SegDesc* segs, int s0, int s1, int n, int grad_dtype, float* master, float* m,

@@ -16,13 +16,14 @@ static_assert(sizeof(BigTma) <= 32000, "kernel parameters must fit the 32 KB lim
 
 // Shared memory budget for the stage ring of one CTA (two CTAs of 8 consumer
 // warps per SM measured best: 6386 GB/s at N = 4 against 4687 GB/s for one
-// CTA with five stages) and the largest replica count the ring serves.
+// CTA with five stages).  Two stages of 2048 elements fit for bf16 N <= 6
+// and fp32 N <= 3; each of those replica counts has its own kernel.
 constexpr uint32_t kTmaSmemBudget = 100 * 1024;
-constexpr int kTmaMaxReplicas = 16;
+constexpr int kTmaMaxReplicas = 6;
 
-template <int NR, int GK, int PACK, int MS, int MP>
+template <int NR, int GK, int W, int MS, int MP>
 int launch_tma(const TmaParams<MS, MP>& p, cudaStream_t stream) {
-  auto kern = reduce_adam_tma_kernel<NR, GK, PACK, MS, MP>;
+  auto kern = reduce_adam_tma_kernel<NR, GK, W, MS, MP>;
   const size_t dyn = (size_t)p.stages * p.stage_bytes;
   static std::atomic<size_t> configured{0};
   if (configured.load(std::memory_order_relaxed) < dyn) {
@@ -47,17 +48,29 @@ int launch_tma(const TmaParams<MS, MP>& p, cudaStream_t stream) {
   return DPOPT_OK;
 }
 
+// Width of the consumers' state stores, by measurement on GB300 (256M-element
+// shards): 256-bit stores for bf16 N <= 3 (6444 against 6059 GB/s at N = 3)
+// and fp32 N = 1; two 16-byte stores above (bf16 N = 4: 6625 against 6356,
+// fp32 N = 3: 6615 against 6432).
+constexpr int tma_width(int gk, int nr) { return (gk == 0 ? nr <= 3 : nr <= 1) ? 32 : 16; }
+
 template <int GK, int MS, int MP>
 int dispatch_tma_gk(const TmaParams<MS, MP>& p, cudaStream_t stream) {
   switch (p.n_rep) {
-    case 1: return launch_tma<1, GK, 0>(p, stream);
-    case 2: return launch_tma<2, GK, 0>(p, stream);
-    case 4: return launch_tma<4, GK, 0>(p, stream);
-    case 8: return launch_tma<8, GK, 0>(p, stream);
+    case 1: return launch_tma<1, GK, tma_width(GK, 1)>(p, stream);
+    case 2: return launch_tma<2, GK, tma_width(GK, 2)>(p, stream);
+    case 3: return launch_tma<3, GK, tma_width(GK, 3)>(p, stream);
     default: break;
   }
-  if (p.n_rep <= 8) return launch_tma<0, GK, 0>(p, stream);
-  return launch_tma<0, GK, 1>(p, stream);
+  if constexpr (GK == 0) {
+    switch (p.n_rep) {
+      case 4: return launch_tma<4, GK, tma_width(GK, 4)>(p, stream);
+      case 5: return launch_tma<5, GK, tma_width(GK, 5)>(p, stream);
+      case 6: return launch_tma<6, GK, tma_width(GK, 6)>(p, stream);
+      default: break;
+    }
+  }
+  return fail(DPOPT_ERR_UNSUPPORTED, "bulk-copy kernel: no ring for %d replicas", p.n_rep);
 }
 
 template <int MS, int MP>
@@ -108,11 +121,12 @@ bool tma_eligible(const SegDesc* segs, int s0, int s1, int n, int grad_dtype, co
   if (n > kTmaMaxReplicas || grad_dtype == DPOPT_GRAD_F16) return false;
   const uint32_t gsize = grad_dtype == DPOPT_GRAD_F32 ? 4u : 2u;
   if (2u * (uint32_t)kTmaTile * ((uint32_t)n * gsize + 12u) > kTmaSmemBudget) return false;
+  auto aligned32 = [](const void* q) { return ((uintptr_t)q & 31u) == 0; };
   for (int s = s0; s < s1; ++s) {
     const SegDesc& d = segs[s];
     if (d.len == 0) continue;
-    if (!aligned16(master + d.state_off) || !aligned16(m + d.state_off) ||
-        !aligned16(v + d.state_off) || !aligned16((const uint16_t*)out + d.state_off))
+    if (!aligned32(master + d.state_off) || !aligned32(m + d.state_off) ||
+        !aligned32(v + d.state_off) || !aligned16((const uint16_t*)out + d.state_off))
       return false;
     for (int r = 0; r < n; ++r)
       if (!aligned16(d.ptrs[r])) return false;

@@ -123,16 +123,20 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int NR, int GK, int PACK, int MAXSEG, int MAXPTR>
+// NR: the replica count (the ring holds two stages of N replica rows only
+// for small N, so every eligible N has its own kernel).  W: the width of one
+// state store to global memory (32: one 256-bit store per array and thread).
+template <int NR, int GK, int W, int MAXSEG, int MAXPTR>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     reduce_adam_tma_kernel(const __grid_constant__ TmaParams<MAXSEG, MAXPTR> p) {
+  static_assert(NR >= 1, "one kernel per replica count");
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full_bar[kTmaMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kTmaMaxStages];
 
   constexpr uint32_t gsize = GK == 0 ? 2u : 4u;
   const int S = p.stages;
-  const int n = NR > 0 ? NR : p.n_rep;
+  constexpr int n = NR;
   const uint32_t row_bytes = (uint32_t)kTmaTile * gsize;     // one replica's row of a tile
   const uint32_t state_base = (uint32_t)n * row_bytes;      // master row, then m, then v
   const uint32_t smem0 = smem_u32(smem);
@@ -205,9 +209,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         const SharedSource<GK> src{sb + (uint32_t)c * kGroup * gsize, row_bytes,
                                    {sx, sx + kTmaTile * 4u, sx + kTmaTile * 8u}};
         const int64_t so = sg.state_off + e0 + (int64_t)c * kGroup;
-        const GroupOut o{p.master + so, p.m + so, p.v + so, p.out + so};
-        if constexpr (PACK) group_vec_x2<NR, GK, false>(src, n, p.h, o, 1.f);
-        else group_vec_x1<NR, GK, false>(src, n, p.h, o, 1.f);
+        const GroupOutT<W> o{p.master + so, p.m + so, p.v + so, p.out + so};
+        group_vec_x1<NR, GK, false>(src, n, p.h, o, 1.f);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
