@@ -23,6 +23,7 @@ bounded samples of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -39,7 +40,9 @@ if ROOT not in sys.path:
 METRIC = "G params/s updated and achieved HBM GB/s vs ~8 TB/s roofline, at N replicas"
 UNIT = "G params/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ("numerics.cuh", "kernels.cuh", "launch_gk.cu", "internal.h", "dpopt.cu")
+# the step kernel's device code and its per-N form table (a traffic figure is
+# void once these change; launch plumbing lives elsewhere)
+KERNEL_SOURCES = ("numerics.cuh", "kernels.cuh")
 
 
 def parse_args(argv=None):
@@ -65,12 +68,14 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", choices=("auto", "direct", "bulk"), default="auto",
                     help="kernel policy of the library (both give identical results)")
-    ap.add_argument("--optimizer", choices=("adam", "adamw_clip", "adam_allgather"),
+    ap.add_argument("--optimizer", choices=("adam", "adamw_clip", "adam_allgather", "amp"),
                     default="adam",
                     help="adam: the fused reduce + Adam step; adamw_clip: the squared-norm "
                          "pre-pass then the clipped AdamW step (weight_decay 0.01, clip 1.0); "
                          "adam_allgather: the step then the ZeRO-3 all-gather of the bf16 "
-                         "shard into N replica parameter buffers")
+                         "shard into N replica parameter buffers; amp: fp16 gradients with "
+                         "dynamic loss scaling -- the unscaled squared-norm pre-pass, then the "
+                         "loss-scaled, clipped AdamW step and the device-side scale update")
     return ap.parse_args(argv)
 
 
@@ -233,7 +238,7 @@ def config_of(wl, kernel=None):
     return {"workload": f"{wl.name}: {wl.numel:,} params per replica buffer, N={wl.n_replicas} "
                         f"replicas, rank {wl.shard_rank} shard of {wl.shard_elems:,} params, "
                         f"{wl.bucket_elems:,}-element buckets, "
-                        f"{'bf16' if wl.grad_kind == 0 else 'fp32'} gradients",
+                        f"{('bf16', 'fp32', 'fp16')[wl.grad_kind]} gradients",
             "n_replicas": wl.n_replicas, "numel": wl.numel, "shard_params": wl.shard_elems,
             "bucket_elems": wl.bucket_elems,
             "bytes_per_param": wl.bytes_per_param(),
@@ -297,6 +302,10 @@ def run_ours(args, wl):
     if world > 1:
         dist.init_process_group("nccl", device_id=device)
     wl = rank_workload(wl, rank)
+    if args.optimizer == "amp":
+        if wl.layout != "full":
+            raise SystemExit("amp runs on the full-buffer workloads")
+        wl = dataclasses.replace(wl, grad_kind=2)   # fp16 gradients, the loss-scaled recipe
     dp.dpopt_set_kernel_policy({"auto": dp.DPOPT_KERNEL_AUTO, "direct": dp.DPOPT_KERNEL_DIRECT,
                                 "bulk": dp.DPOPT_KERNEL_BULK}[args.kernel])
     S, n = wl.shard_elems, wl.n_replicas
@@ -318,12 +327,24 @@ def run_ours(args, wl):
         opts = dp.step_options(weight_decay=0.01, max_grad_norm=1.0, grad_sqnorm=sqn)
     if args.optimizer == "adam_allgather":
         param_reps = [torch.empty(S * n, dtype=torch.bfloat16, device=device) for _ in range(n)]
+    if args.optimizer == "amp":
+        sqn = torch.zeros(1, dtype=torch.float64, device=device)
+        scratch = torch.empty(dp.dpopt_grad_sqnorm_scratch_bytes(S, 1)[1] // 8 + 1,
+                              dtype=torch.float64, device=device)
+        ls_state = torch.zeros(4, dtype=torch.int64, device=device)
+        ls_cfg = dp.loss_scale_init(ls_state, init_scale=1024.0, window=1000, stream=stream)
     if wl.layout == "full":
         if args.optimizer == "adam_allgather":
             def step(t):
                 dp.reduce_adam(dev.grads, wl.shard_rank, wl.bucket_elems, dev.master, dev.m,
                                dev.v, dev.out, step=t, stream=stream, **hp)
                 dp.allgather_bf16(dev.out, wl.shard_rank, param_reps, stream=stream)
+        elif args.optimizer == "amp":
+            def step(t):   # t is implied: the device state counts the steps taken
+                dp.amp_sqnorm(dev.grads, wl.shard_rank, ls_state, sqn, scratch, stream=stream)
+                dp.amp_step(dev.grads, wl.shard_rank, wl.bucket_elems, dev.master, dev.m,
+                            dev.v, dev.out, weight_decay=0.01, max_grad_norm=1.0,
+                            global_sqnorm=sqn, state=ls_state, cfg=ls_cfg, stream=stream, **hp)
         elif args.optimizer == "adamw_clip":
             def step(t):
                 dp.grad_sqnorm(dev.grads, wl.shard_rank, sqn, scratch, stream=stream)
@@ -434,7 +455,7 @@ def _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks
             dist.destroy_process_group()
         return None
     n, bpp = wl.n_replicas, wl.bytes_per_param()
-    if args.optimizer == "adamw_clip":   # the norm pre-pass reads the N gradients once more
+    if args.optimizer in ("adamw_clip", "amp"):   # the norm pre-pass reads the N gradients again
         bpp += wl.grad_bytes() * wl.n_replicas
     elif args.optimizer == "adam_allgather":   # read the bf16 shard, write N copies
         bpp += 2 + 2 * wl.n_replicas

@@ -19,6 +19,7 @@
 #include "control.cuh"
 #include "gather.cuh"
 #include "internal.h"
+#include "norm.cuh"
 
 namespace dpopt {
 namespace {

@@ -8,17 +8,14 @@
 // all N of its gradient loads in flight at once.  Above 8 the runtime-count
 // packed body runs (two CTAs per SM).  The accumulation order is the same in
 // every form, so the choice changes speed only, never bits.
+
 //
-// State access width per kernel, by measurement on GB300 (256M-element
-// shards): one 256-bit access per state array and thread (W = 32: whole
-// sectors, half the load/store instructions) is faster where the arithmetic
-// per byte is highest -- bf16/fp16 gradients with N <= 3 (+5..7% at N = 2, 3)
-// and fp32 gradients with N <= 6 (+2..10%) -- and 2..4% slower above, where
-// its 8-register tuples cost spills; there two 16-byte accesses (W = 16) run.
+// The state access width of each kernel is wide_states() (kernels.cuh).
 #include <algorithm>
 #include <atomic>
 
 #include "internal.h"
+#include "norm.cuh"
 
 #ifndef DPOPT_GK
 #error "compile with -DDPOPT_GK=0 (bf16), 1 (fp32) or 2 (fp16)"
@@ -42,7 +39,7 @@ namespace DPOPT_GK_NS {
 
 constexpr int kGK = DPOPT_GK;
 
-constexpr bool wide_states(int nr) { return nr >= 1 && (kGK == 1 ? nr <= 6 : nr <= 3); }
+constexpr bool wide_states(int nr) { return dpopt::wide_states(kGK, nr); }
 
 // Whether every segment's vector level allows the 32-byte accesses (level 0
 // segments go one element at a time in either form).
