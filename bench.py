@@ -76,6 +76,11 @@ def parse_args(argv=None):
                          "shard into N replica parameter buffers; amp: fp16 gradients with "
                          "dynamic loss scaling -- the unscaled squared-norm pre-pass, then the "
                          "loss-scaled, clipped AdamW step and the device-side scale update")
+    ap.add_argument("--clip-path", choices=("stored", "fused"), default="stored",
+                    help="adamw_clip / amp on full-buffer workloads: 'stored' -- the norm pass "
+                         "also stores the averaged gradient (the reduced gradient shard) and the "
+                         "step reads it as one fp32 replica; 'fused' -- the step reads the N "
+                         "replicas again.  Both give the same bits.")
     return ap.parse_args(argv)
 
 
@@ -327,6 +332,9 @@ def run_ours(args, wl):
         opts = dp.step_options(weight_decay=0.01, max_grad_norm=1.0, grad_sqnorm=sqn)
     if args.optimizer == "adam_allgather":
         param_reps = [torch.empty(S * n, dtype=torch.bfloat16, device=device) for _ in range(n)]
+    stored = args.clip_path == "stored" and wl.layout == "full"
+    if args.optimizer in ("adamw_clip", "amp") and stored:
+        avg = torch.empty(S, dtype=torch.float32, device=device)
     if args.optimizer == "amp":
         sqn = torch.zeros(1, dtype=torch.float64, device=device)
         scratch = torch.empty(dp.dpopt_grad_sqnorm_scratch_bytes(S, 1)[1] // 8 + 1,
@@ -339,12 +347,25 @@ def run_ours(args, wl):
                 dp.reduce_adam(dev.grads, wl.shard_rank, wl.bucket_elems, dev.master, dev.m,
                                dev.v, dev.out, step=t, stream=stream, **hp)
                 dp.allgather_bf16(dev.out, wl.shard_rank, param_reps, stream=stream)
-        elif args.optimizer == "amp":
+        elif args.optimizer == "amp" and stored:
             def step(t):   # t is implied: the device state counts the steps taken
+                dp.amp_average_sqnorm(dev.grads, wl.shard_rank, ls_state, avg, sqn, scratch,
+                                      stream=stream)
+                dp.amp_step([avg], 0, wl.bucket_elems, dev.master, dev.m, dev.v, dev.out,
+                            weight_decay=0.01, max_grad_norm=1.0, global_sqnorm=sqn,
+                            state=ls_state, cfg=ls_cfg, stream=stream, **hp)
+        elif args.optimizer == "amp":
+            def step(t):
                 dp.amp_sqnorm(dev.grads, wl.shard_rank, ls_state, sqn, scratch, stream=stream)
                 dp.amp_step(dev.grads, wl.shard_rank, wl.bucket_elems, dev.master, dev.m,
                             dev.v, dev.out, weight_decay=0.01, max_grad_norm=1.0,
                             global_sqnorm=sqn, state=ls_state, cfg=ls_cfg, stream=stream, **hp)
+        elif args.optimizer == "adamw_clip" and stored:
+            def step(t):
+                dp.grad_average_sqnorm(dev.grads, wl.shard_rank, avg, sqn, scratch,
+                                       stream=stream)
+                dp.reduce_adamw([avg], 0, wl.bucket_elems, dev.master, dev.m, dev.v, dev.out,
+                                step=t, opts=opts, stream=stream, **hp)
         elif args.optimizer == "adamw_clip":
             def step(t):
                 dp.grad_sqnorm(dev.grads, wl.shard_rank, sqn, scratch, stream=stream)
@@ -415,7 +436,7 @@ def run_ours(args, wl):
         # (pinned host copies of the inputs would not fit sensibly; the end-to-end
         # figure is taken for the default fused step)
         return _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks,
-                       None, None)
+                       None, None, stored)
     hs = [torch.empty(S, dtype=dev.grads[0].dtype, pin_memory=True) for _ in range(n)]
     for h, g in zip(hs, dev.shard_slices()):
         h.copy_(g)
@@ -444,18 +465,22 @@ def run_ours(args, wl):
     grads = [h.view(torch.int16).numpy().view("uint16") if h.dtype == torch.bfloat16
              else h.numpy() for h in hs]
     return _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks, e2e,
-                   grads)
+                   grads, stored)
 
 
 def _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks, e2e,
-            host_grads):
+            host_grads, stored=False):
     import torch.distributed as dist
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return None
     n, bpp = wl.n_replicas, wl.bytes_per_param()
-    if args.optimizer in ("adamw_clip", "amp"):   # the norm pre-pass reads the N gradients again
+    if args.optimizer in ("adamw_clip", "amp") and stored:
+        # norm pass: the N replicas read, the fp32 average written (4 B); the step
+        # reads that average (4 B) in place of the N replicas: g*N + 34 in all
+        bpp += 8
+    elif args.optimizer in ("adamw_clip", "amp"):   # the norm pre-pass reads the N gradients again
         bpp += wl.grad_bytes() * wl.n_replicas
     elif args.optimizer == "adam_allgather":   # read the bf16 shard, write N copies
         bpp += 2 + 2 * wl.n_replicas
@@ -470,7 +495,9 @@ def _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded counter-based generator, generated in HBM)",
         "config": {**config_of(wl, args.kernel), "optimizer": args.optimizer,
-                   "bytes_per_param": bpp},
+                   "bytes_per_param": bpp,
+                   **({"clip_path": "stored" if stored else "fused"}
+                      if args.optimizer in ("adamw_clip", "amp") else {})},
         "hbm_gbs": S * bpp / (ms_per_step / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth",

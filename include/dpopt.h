@@ -204,7 +204,7 @@ int dpopt_reduce_adamw_buckets(const void *const *slice_table, int grad_dtype, i
 /* Squared L2 norm of this shard's averaged gradient (the clipping pre-pass):
  *   *sqnorm_out = sum_i (g_i * grad_unscale)^2      (fp64, DEVICE pointer)
  * with g_i the same fixed-order average the step computes.  Partial sums over
- * fixed 65536-element chunks go to `scratch` (a DEVICE buffer the caller owns,
+ * fixed 4096-element chunks go to `scratch` (a DEVICE buffer the caller owns,
  * at least dpopt_grad_sqnorm_scratch_bytes() bytes, 8-byte aligned) and are
  * added in chunk order, so the result is bitwise reproducible and does not
  * depend on the GPU's SM count.  Arguments as for dpopt_reduce_adam_ex;
@@ -228,7 +228,7 @@ int dpopt_grad_sqnorm_buckets(const void *const *slice_table, int grad_dtype, in
  * another allocator (a framework's caching allocator that has reserved the
  * GPU), or that must not trigger the device-wide synchronisation cudaMalloc /
  * cudaFree can cause in the middle of a training step.  The chunk partials go
- * to an array built into the library: 32768 fp64 values (256 KB) on every
+ * to an array built into the library: 524288 fp64 values (4 MB) on every
  * device that loads the library, held until the process exits, which limits a
  * shard to 2^31 elements (DPOPT_ERR_UNSUPPORTED beyond that, with a message
  * from dpopt_last_error()).  It allocates nothing and calls no allocating
@@ -243,9 +243,29 @@ int dpopt_grad_sqnorm_noalloc(const void *const *grads, int grad_dtype, int n_re
                               int64_t numel, int shard_rank, float grad_unscale,
                               double *sqnorm_out, dpopt_stream_t stream);
 
+/* dpopt_grad_sqnorm that also stores the shard's averaged gradient -- the
+ * reduced gradient partition a reduce-scatter leaves on each rank in ZeRO's
+ * stage 2 ("ZeRO: Memory Optimizations Toward Training Trillion Parameter
+ * Models", Pos+g): avg_out[i] = g_i for i = 0 .. S-1 (S = numel / n_replicas),
+ * the fixed-order average of element i of this rank's shard in fp32, before
+ * grad_unscale -- the same g the fused step forms.  avg_out is a DEVICE buffer
+ * of S floats that the caller owns, 4-byte aligned (16- or 32-byte alignment
+ * lets the kernel store vectors), overlapping neither the gradients nor
+ * sqnorm_out nor scratch.  A following step can read the average instead of
+ * the N replicas: dpopt_reduce_adamw(&avg_out, DPOPT_GRAD_F32, 1, S, 0, ...)
+ * (or dpopt_amp_step with the same arguments) gives bit for bit the states
+ * that the fused call on the N replicas gives, moving 4 + 26 bytes per
+ * parameter in that pass instead of 2N + 26.  Errors: as for
+ * dpopt_grad_sqnorm, and DPOPT_ERR_INVALID_ARG for a null, misaligned or
+ * overlapping avg_out. */
+int dpopt_grad_average_sqnorm(const void *const *grads, int grad_dtype, int n_replicas,
+                              int64_t numel, int shard_rank, float grad_unscale, float *avg_out,
+                              double *sqnorm_out, void *scratch, int64_t scratch_bytes,
+                              dpopt_stream_t stream);
+
 /* Scratch bytes dpopt_grad_sqnorm{,_buckets} need for `elems` gradient elements
  * per replica cut into n_buckets buckets (use n_buckets = 1 for the full-buffer
- * form): 8 * (ceil(elems / 65536) + n_buckets).  Host-only. */
+ * form): 8 * (ceil(elems / 4096) + n_buckets).  Host-only. */
 int dpopt_grad_sqnorm_scratch_bytes(int64_t elems, int64_t n_buckets, int64_t *bytes_out);
 
 /* ------------------------------------------------------------------------- */
@@ -292,6 +312,14 @@ int dpopt_loss_scale_init(dpopt_loss_scale_state *state, const dpopt_loss_scale_
 int dpopt_amp_sqnorm(const void *const *grads, int grad_dtype, int n_replicas, int64_t numel,
                      int shard_rank, const dpopt_loss_scale_state *state, double *sqnorm_out,
                      void *scratch, int64_t scratch_bytes, dpopt_stream_t stream);
+
+/* dpopt_amp_sqnorm that also stores the averaged gradient (before the unscale)
+ * in avg_out, as dpopt_grad_average_sqnorm does; dpopt_amp_step on
+ * (&avg_out, DPOPT_GRAD_F32, 1, S, 0, ...) then gives the fused step's states. */
+int dpopt_amp_average_sqnorm(const void *const *grads, int grad_dtype, int n_replicas,
+                             int64_t numel, int shard_rank, const dpopt_loss_scale_state *state,
+                             float *avg_out, double *sqnorm_out, void *scratch,
+                             int64_t scratch_bytes, dpopt_stream_t stream);
 
 /* One loss-scaled step of this rank's shard (full-buffer layout, arguments as for
  * dpopt_reduce_adam_ex): if *global_sqnorm is finite, AdamW (weight_decay) on the

@@ -161,9 +161,10 @@ def test_bucket_entries_reject_bad_arguments(dp):
 
 def test_sqnorm_scratch_bytes(dp):
     assert dp.dpopt_grad_sqnorm_scratch_bytes(0, 1) == (0, 8)
-    assert dp.dpopt_grad_sqnorm_scratch_bytes(65536, 1) == (0, 16)
-    assert dp.dpopt_grad_sqnorm_scratch_bytes(65537, 1) == (0, 24)
-    assert dp.dpopt_grad_sqnorm_scratch_bytes(1_093_750_000, 274)[1] == 8 * (16690 + 274)
+    assert dp.dpopt_grad_sqnorm_scratch_bytes(65536, 1) == (0, 8 * (65536 // 4096 + 1))
+    assert dp.dpopt_grad_sqnorm_scratch_bytes(4097, 0) == (0, 16)
+    assert dp.dpopt_grad_sqnorm_scratch_bytes(65537, 1) == (0, 8 * (17 + 1))
+    assert dp.dpopt_grad_sqnorm_scratch_bytes(1_093_750_000, 274)[1] == 8 * (267_029 + 274)
     assert dp.dpopt_grad_sqnorm_scratch_bytes(-1, 1)[0] == dp.DPOPT_ERR_INVALID_ARG
 
 
@@ -185,6 +186,18 @@ def test_sqnorm_and_adamw_reject_bad_arguments(dp):
     assert call(grads=[SQ - 16, G[1]]) == 1      # gradients overlap the output
     assert call(numel=7) == 1
     assert call(n=65, grads=G[:64] + [G[0]]) == 2
+    AVG = 0xC0_0000_0000
+
+    def call_avg(avg, **kw):
+        a = dict(ok, **kw)
+        return dp.dpopt_grad_average_sqnorm(a["grads"], a["dt"], a["n"], a["numel"], a["rank"],
+                                            a["un"], avg, a["out"], a["scr"], a["nbytes"], 0)
+    assert call_avg(0) == 1                      # no destination for the average
+    assert call_avg(AVG + 2) == 1                # not 4-byte aligned
+    assert call_avg(SCR - 16) == 1               # overlaps the partials
+    assert call_avg(SQ - 64) == 1                # overlaps the norm output
+    assert call_avg(G[0] - 8) == 1               # overlaps a gradient
+    assert call_avg(AVG, nbytes=8) == 1          # the norm's own checks still apply
     opt = dp.StepOptions(-0.1, 0.0, None, 0.0)
     assert dp.dpopt_reduce_adamw(G[:4], 0, 4, 4096, 0, 1024, MASTER, M, V, OUT, *HP, 1, opt, 0) == 1
     opt = dp.StepOptions(0.01, 1.0, None, 0.0)   # clipping without a norm pointer

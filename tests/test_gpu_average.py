@@ -1,0 +1,199 @@
+"""The stored averaged gradient (the reduced gradient shard of ZeRO stage 2) on
+the GPU: the average the norm pass writes agrees with the oracle's fixed-order
+average, and the two-pass path -- norm pass storing the average, then the step
+reading it as one fp32 replica -- gives bit for bit the states of the fused
+path that reads the N replicas in the step, for clipped AdamW and for the
+loss-scaled fp16 step (overflow skips included)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.parity import grad_host_range
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import zero_mixed_precision_gb300 as dp
+    from tests.test_gpu_amp import _amp_workload
+    from tests.test_gpu_parity import _small_workload, f32, to_dev_grad, u16
+    from tests import parity
+else:
+    dp = None
+
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8)
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _scratch(S):
+    rc, nbytes = dp.dpopt_grad_sqnorm_scratch_bytes(S, 1)
+    assert rc == 0
+    return torch.empty(max(1, nbytes // 8), dtype=torch.float64, device="cuda")
+
+
+def _full_grads(wl, t):
+    return [grad_host_range(wl, r, t, 0, wl.numel) for r in range(wl.n_replicas)]
+
+
+def _ulp_diff(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    ia = a.view(np.int32).astype(np.int64)
+    ib = b.view(np.int32).astype(np.int64)
+    ia = np.where(ia < 0, -(ia & 0x7FFFFFFF), ia)
+    ib = np.where(ib < 0, -(ib & 0x7FFFFFFF), ib)
+    return np.abs(ia - ib)
+
+
+@pytest.mark.parametrize("n,S,kind", [(1, 9, 0), (2, 20_011, 0), (3, 70_001, 1), (4, 100_003, 0),
+                                      (8, 50_000, 2), (13, 30_001, 0)])
+def test_stored_average_matches_the_oracle(n, S, kind):
+    _need_gpu()
+    wl = _small_workload(n, S, kind=kind, rank=n - 1)
+    gh = _full_grads(wl, 1)
+    grads = [to_dev_grad(g) for g in gh]
+    avg = torch.full((S,), float("nan"), device="cuda")
+    sq = torch.zeros(1, dtype=torch.float64, device="cuda")
+    sq_ref = torch.zeros(1, dtype=torch.float64, device="cuda")
+    scratch = _scratch(S)
+    dp.grad_average_sqnorm(grads, wl.shard_rank, avg, sq, scratch)
+    dp.grad_sqnorm(grads, wl.shard_rank, sq_ref, scratch)
+    dp.stream_status()
+    # the norm is the one grad_sqnorm gives, bit for bit
+    assert torch.equal(sq, sq_ref)
+    # the average: fp64 sum in replica order, rounded to fp32, divided by N (the
+    # oracle's definition); the compensated fp32 sum rounds the same way except
+    # where the exact sum sits within ~2^-48 of a rounding boundary
+    want = oracle.average([g[wl.shard_base:wl.shard_base + S] for g in gh])
+    got = f32(avg)
+    d = _ulp_diff(got, want)
+    assert np.all(np.isfinite(got))
+    assert d.max() <= 1
+    assert (d == 0).mean() > 0.999
+
+
+def _two_pass_clip(wl, steps, wd, max_norm, unscale, stored):
+    S = wl.shard_elems
+    master, m, v = parity.states_host(wl, wl.shard_base + np.arange(S))
+    dm, dmm, dv = (torch.from_numpy(x.copy()).cuda() for x in (master, m, v))
+    dout = torch.empty(S, dtype=torch.bfloat16, device="cuda")
+    part = torch.zeros(wl.n_replicas, dtype=torch.float64, device="cuda")
+    total = torch.zeros(1, dtype=torch.float64, device="cuda")
+    scratch = _scratch(S)
+    avgs = [torch.empty(S, device="cuda") for _ in range(wl.n_replicas)]
+    for t in steps:
+        grads = [to_dev_grad(g) for g in _full_grads(wl, t)]
+        for r in range(wl.n_replicas):
+            if stored:
+                dp.grad_average_sqnorm(grads, r, avgs[r], part[r:r + 1], scratch,
+                                       grad_unscale=unscale)
+            else:
+                dp.grad_sqnorm(grads, r, part[r:r + 1], scratch, grad_unscale=unscale)
+        torch.sum(part, dim=0, keepdim=True, out=total)
+        opts = dp.step_options(weight_decay=wd, max_grad_norm=max_norm, grad_sqnorm=total,
+                               grad_unscale=unscale)
+        if stored:   # the rank's stored average as a single fp32 replica
+            dp.reduce_adamw([avgs[wl.shard_rank]], 0, S, dm, dmm, dv, dout, step=t, opts=opts,
+                            **HP)
+        else:
+            dp.reduce_adamw(grads, wl.shard_rank, S, dm, dmm, dv, dout, step=t, opts=opts, **HP)
+    dp.stream_status()
+    return f32(dm), f32(dmm), f32(dv), u16(dout)
+
+
+@pytest.mark.parametrize("n,S,kind", [(1, 30_001, 0), (3, 20_003, 0), (4, 50_000, 0),
+                                      (4, 40_000, 1), (8, 20_001, 2), (13, 9_999, 0)])
+def test_two_pass_clipped_adamw_equals_the_fused_path(n, S, kind):
+    _need_gpu()
+    wl = _small_workload(n, S, kind=kind, rank=min(1, n - 1))
+    max_norm = float(1e-4 * np.sqrt(wl.numel))   # clips: a tenth of the norm
+    a = _two_pass_clip(wl, (1, 2, 3), 0.01, max_norm, 0.0, stored=True)
+    b = _two_pass_clip(wl, (1, 2, 3), 0.01, max_norm, 0.0, stored=False)
+    for x, y in zip(a, b):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+def test_two_pass_with_unscale_equals_the_fused_path():
+    _need_gpu()
+    wl = _small_workload(4, 30_000, rank=2)
+    a = _two_pass_clip(wl, (1, 2), 0.01, 1e-3, 2.0 ** -7, stored=True)
+    b = _two_pass_clip(wl, (1, 2), 0.01, 1e-3, 2.0 ** -7, stored=False)
+    for x, y in zip(a, b):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+@pytest.mark.parametrize("max_norm", [0.0, 1.0])
+def test_two_pass_loss_scaled_run_equals_the_fused_path(max_norm):
+    """Ten loss-scaled iterations with overflows at 4, 6, 7 (as in the fused
+    test): the stored-average path skips, rescales and steps exactly as the
+    fused path."""
+    _need_gpu()
+    n, S = 4, 20_000
+    wl = _amp_workload(n, S)
+    inject = {4: (2, 3 * S + 11, 0x7C00), 6: (0, 5, 0xFC00), 7: (3, S - 1, 0x7E00)}
+
+    def full(k):
+        bufs = [grad_host_range(wl, r, k, 0, wl.numel) for r in range(n)]
+        if k in inject:
+            r, i, bits = inject[k]
+            bufs[r][i] = bits
+        return bufs
+
+    def run(stored):
+        master, m, v = parity.states_host(wl, wl.shard_base + np.arange(S))
+        dm, dmm, dv = (torch.from_numpy(x.copy()).cuda() for x in (master, m, v))
+        dout = torch.zeros(S, dtype=torch.bfloat16, device="cuda")
+        state = torch.zeros(4, dtype=torch.int64, device="cuda")
+        cfg = dp.loss_scale_init(state, init_scale=1024.0, window=3, hysteresis=2, min_scale=1.0)
+        scratch = _scratch(S)
+        part = torch.zeros(n, dtype=torch.float64, device="cuda")
+        total = torch.zeros(1, dtype=torch.float64, device="cuda")
+        avgs = [torch.empty(S, device="cuda") for _ in range(n)]
+        trail = []
+        for k in range(1, 11):
+            grads = [to_dev_grad(b) for b in full(k)]
+            for r in range(n):
+                if stored:
+                    dp.amp_average_sqnorm(grads, r, state, avgs[r], part[r:r + 1], scratch)
+                else:
+                    dp.amp_sqnorm(grads, r, state, part[r:r + 1], scratch)
+            torch.sum(part, dim=0, keepdim=True, out=total)
+            src = [avgs[wl.shard_rank]] if stored else grads
+            rank = 0 if stored else wl.shard_rank
+            dp.amp_step(src, rank, S, dm, dmm, dv, dout, weight_decay=0.01,
+                        max_grad_norm=max_norm, global_sqnorm=total, state=state, cfg=cfg, **HP)
+            st = dp.read_loss_scale(state)
+            trail.append((st.scale, st.step, st.skipped, st.last_overflow))
+        dp.stream_status()
+        return trail, (f32(dm), f32(dmm), f32(dv), u16(dout))
+
+    ta, a = run(True)
+    tb, b = run(False)
+    assert ta == tb
+    assert ta[-1][2] == 3
+    for x, y in zip(a, b):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+def test_stored_average_argument_checks():
+    _need_gpu()
+    wl = _small_workload(2, 1000)
+    grads = [to_dev_grad(g) for g in _full_grads(wl, 1)]
+    sq = torch.zeros(1, dtype=torch.float64, device="cuda")
+    scratch = _scratch(1000)
+    avg = torch.empty(1001, device="cuda")
+    ptrs = [g.data_ptr() for g in grads]
+    nb = scratch.numel() * 8
+    ok = dp.dpopt_grad_average_sqnorm(ptrs, 0, 2, 2000, 1, 0.0, avg.data_ptr(), sq.data_ptr(),
+                                      scratch.data_ptr(), nb, 0)
+    assert ok == dp.DPOPT_OK
+    # null, misaligned, overlapping the scratch, overlapping a gradient
+    for bad in (0, avg.data_ptr() + 2, scratch.data_ptr(), grads[0].data_ptr()):
+        rc = dp.dpopt_grad_average_sqnorm(ptrs, 0, 2, 2000, 1, 0.0, bad, sq.data_ptr(),
+                                          scratch.data_ptr(), nb, 0)
+        assert rc == dp.DPOPT_ERR_INVALID_ARG, bad
+    dp.stream_status()

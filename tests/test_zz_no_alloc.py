@@ -67,7 +67,7 @@ def test_noalloc_matches_the_scratch_entry_point_twice_in_a_row(n, S, dtype, uns
 def test_noalloc_rejects_shards_beyond_its_array():
     dp = _lib()
     fake = [0x10_0000_0000 + r * 0x1_0000_0000_00 for r in range(2)]
-    too_big = 2 * (32768 * 65536 + 1)        # one element past 2^31 per shard
+    too_big = 2 * ((1 << 31) + 1)            # one element past 2^31 per shard
     rc = dp.dpopt_grad_sqnorm_noalloc(fake, dp.DPOPT_GRAD_BF16, 2, too_big, 0, 0.0,
                                       0xF0_0000_0000, 0)
     assert rc == dp.DPOPT_ERR_UNSUPPORTED

@@ -93,8 +93,10 @@ _SIGS = {
     "dpopt_grad_sqnorm_buckets": ([_PP, _I, _I, _PI64, _PI64, _I64, _F, _P, _P, _I64, _P], _I),
     "dpopt_grad_sqnorm_scratch_bytes": ([_I64, _I64, _PI64], _I),
     "dpopt_grad_sqnorm_noalloc": ([_PP, _I, _I, _I64, _I, _F, _P, _P], _I),
+    "dpopt_grad_average_sqnorm": ([_PP, _I, _I, _I64, _I, _F, _P, _P, _P, _I64, _P], _I),
     "dpopt_loss_scale_init": ([_P, _PCFG, _P], _I),
     "dpopt_amp_sqnorm": ([_PP, _I, _I, _I64, _I, _P, _P, _P, _I64, _P], _I),
+    "dpopt_amp_average_sqnorm": ([_PP, _I, _I, _I64, _I, _P, _P, _P, _P, _I64, _P], _I),
     "dpopt_amp_step": ([_PP, _I, _I, _I64, _I, _I64, _P, _P, _P, _P, _F, _F, _F, _F, _F, _F, _P, _P,
                         _PCFG, _P], _I),
     "dpopt_allgather_bf16": ([_P, _I64, _I, _PP, _I, _P], _I),
@@ -231,6 +233,23 @@ def dpopt_grad_sqnorm_noalloc(grads: Sequence[int], grad_dtype: int, n_replicas:
     return _lib.dpopt_grad_sqnorm_noalloc(_ptr_array(grads) if grads is not None else None,
                                           grad_dtype, n_replicas, numel, shard_rank, grad_unscale,
                                           sqnorm_out, stream)
+
+
+def dpopt_grad_average_sqnorm(grads: Sequence[int], grad_dtype: int, n_replicas: int,
+                              numel: int, shard_rank: int, grad_unscale: float, avg_out: int,
+                              sqnorm_out: int, scratch: int, scratch_bytes: int,
+                              stream: int = 0) -> int:
+    return _lib.dpopt_grad_average_sqnorm(_ptr_array(grads) if grads is not None else None,
+                                          grad_dtype, n_replicas, numel, shard_rank, grad_unscale,
+                                          avg_out, sqnorm_out, scratch, scratch_bytes, stream)
+
+
+def dpopt_amp_average_sqnorm(grads: Sequence[int], grad_dtype: int, n_replicas: int, numel: int,
+                             shard_rank: int, state: int, avg_out: int, sqnorm_out: int,
+                             scratch: int, scratch_bytes: int, stream: int = 0) -> int:
+    return _lib.dpopt_amp_average_sqnorm(_ptr_array(grads) if grads is not None else None,
+                                         grad_dtype, n_replicas, numel, shard_rank, state,
+                                         avg_out, sqnorm_out, scratch, scratch_bytes, stream)
 
 
 def dpopt_grad_sqnorm_scratch_bytes(elems: int, n_buckets: int = 1) -> tuple[int, int]:
@@ -425,6 +444,29 @@ def grad_sqnorm(grads, shard_rank: int, sqnorm_out, scratch, *, grad_unscale: fl
                            shard_rank, grad_unscale, sqnorm_out.data_ptr(), scratch.data_ptr(),
                            scratch.numel() * scratch.element_size(), _stream_handle(stream))
     _check(rc, "dpopt_grad_sqnorm")
+
+
+def grad_average_sqnorm(grads, shard_rank: int, avg_out, sqnorm_out, scratch, *,
+                        grad_unscale: float = 0.0, stream=None) -> None:
+    """grad_sqnorm that also writes the shard's fixed-order average gradient to
+    avg_out (float32 device tensor of S = numel / N elements)."""
+    dt = _grad_dtype(grads[0])
+    rc = dpopt_grad_average_sqnorm([g.data_ptr() for g in grads], dt, len(grads),
+                                   grads[0].numel(), shard_rank, grad_unscale, avg_out.data_ptr(),
+                                   sqnorm_out.data_ptr(), scratch.data_ptr(),
+                                   scratch.numel() * scratch.element_size(),
+                                   _stream_handle(stream))
+    _check(rc, "dpopt_grad_average_sqnorm")
+
+
+def amp_average_sqnorm(grads, shard_rank: int, state, avg_out, sqnorm_out, scratch,
+                       stream=None) -> None:
+    dt = _grad_dtype(grads[0])
+    rc = dpopt_amp_average_sqnorm([g.data_ptr() for g in grads], dt, len(grads),
+                                  grads[0].numel(), shard_rank, state.data_ptr(),
+                                  avg_out.data_ptr(), sqnorm_out.data_ptr(), scratch.data_ptr(),
+                                  scratch.numel() * scratch.element_size(), _stream_handle(stream))
+    _check(rc, "dpopt_amp_average_sqnorm")
 
 
 def grad_sqnorm_buckets(bucket_slices, offsets, sqnorm_out, scratch, *, grad_unscale: float = 0.0,

@@ -48,20 +48,29 @@ __global__ void loss_scale_update_kernel(LossScaleState* st, const double* sqnor
   *st = s;
 }
 
-// Sum of the partials in a fixed order: strided per thread, then a fixed tree.
-__global__ void __launch_bounds__(kThreads)
-    sqnorm_finish_kernel(const double* partials, int64_t nchunks, double* out) {
-  __shared__ double red[kThreads];
-  double acc = 0.0;
-  for (int64_t c = threadIdx.x; c < nchunks; c += kThreads) acc = __dadd_rn(acc, partials[c]);
-  red[threadIdx.x] = acc;
-  __syncthreads();
+// Sum of the chunk partials (double-float pairs) in a fixed order: strided
+// over 1024 threads, a shuffle tree in each warp, the warps' sums in warp
+// order; the final pair is added once in fp64.
+constexpr int kFinishThreads = 1024;
+
+__global__ void __launch_bounds__(kFinishThreads)
+    sqnorm_finish_kernel(const DFloat* partials, int64_t nchunks, double* out) {
+  __shared__ DFloat warp_sum[kFinishThreads / 32];
+  DFloat acc{0.f, 0.f};
+  for (int64_t c = threadIdx.x; c < nchunks; c += kFinishThreads) acc = df_add(acc, partials[c]);
 #pragma unroll
-  for (int w = kThreads / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) red[threadIdx.x] = __dadd_rn(red[threadIdx.x], red[threadIdx.x + w]);
-    __syncthreads();
+  for (int off = 16; off > 0; off >>= 1) {
+    const DFloat o{__shfl_down_sync(0xffffffffu, acc.hi, off),
+                   __shfl_down_sync(0xffffffffu, acc.lo, off)};
+    acc = df_add(acc, o);
   }
-  if (threadIdx.x == 0) *out = red[0];
+  if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    DFloat tot = warp_sum[0];
+    for (int w = 1; w < kFinishThreads / 32; ++w) tot = df_add(tot, warp_sum[w]);
+    *out = __dadd_rn((double)tot.hi, (double)tot.lo);
+  }
 }
 
 }  // namespace dpopt

@@ -28,13 +28,11 @@ constexpr int kMaxDevices = 64;
 
 // Under DPOPT_KERNEL_AUTO the bulk-copy kernel carries the step where it
 // measured faster than the direct-load kernel on GB300 (256M-element shards):
-// bf16 N = 3 (6444 against 6041 GB/s), fp32 N = 2 (6501 against 6145) and
-// fp32 N = 3 (6615 against 6360).  Elsewhere the direct-load kernel is as fast
-// or faster (bf16 N = 1: 6473 against 6006; bf16 N = 4..6 by 0..4%).
+// fp32 N = 2 (6431 against 6163 GB/s) and fp32 N = 3 (6567 against 6218).
+// Elsewhere the direct-load kernel is as fast or faster (bf16 N = 3: 6475
+// against 6436; bf16 N = 1: 6439 against 6006; bf16 N = 4..6 by 0..4%).
 bool auto_bulk(int n, int grad_dtype) {
-  if (grad_dtype == DPOPT_GRAD_BF16) return n == 3;
-  if (grad_dtype == DPOPT_GRAD_F32) return n == 2 || n == 3;
-  return false;
+  return grad_dtype == DPOPT_GRAD_F32 && (n == 2 || n == 3);
 }
 
 std::atomic<int> g_policy{DPOPT_KERNEL_AUTO};
@@ -278,15 +276,20 @@ int64_t norm_chunks(const SegDesc* segs, int nsegs) {
 
 template <int MS, int MP>
 int launch_sqnorm(LaunchParams<MS, MP>& p, int64_t nchunks, double* partials, int grad_dtype,
-                  cudaStream_t stream) {
-  if (grad_dtype == DPOPT_GRAD_BF16) return launch_sqnorm_pass<0>(p, partials, nchunks, stream);
-  if (grad_dtype == DPOPT_GRAD_F16) return launch_sqnorm_pass<2>(p, partials, nchunks, stream);
-  return launch_sqnorm_pass<1>(p, partials, nchunks, stream);
+                  bool store_average, cudaStream_t stream) {
+  if (grad_dtype == DPOPT_GRAD_BF16)
+    return launch_sqnorm_pass<0>(p, partials, nchunks, store_average, stream);
+  if (grad_dtype == DPOPT_GRAD_F16)
+    return launch_sqnorm_pass<2>(p, partials, nchunks, store_average, stream);
+  return launch_sqnorm_pass<1>(p, partials, nchunks, store_average, stream);
 }
 
 // Squared norm of segments [0, nsegs) into *out (device), partials in scratch.
+// avg_out (one segment only): also store each element's average there.
 int run_sqnorm(const SegDesc* segs, int nsegs, int grad_dtype, int n, const Hyper& h,
-               double* partials, double* out, cudaStream_t stream) {
+               double* partials, double* out, cudaStream_t stream, float* avg_out = nullptr) {
+  if (avg_out && nsegs != 1)
+    return fail(DPOPT_ERR_UNSUPPORTED, "the averaged gradient is stored for one segment only");
   const int per_launch = nsegs == 1 ? 1 : std::min(kBigSegs, kBigPtrs / n);
   int64_t done = 0;
   for (int s0 = 0; s0 < nsegs; s0 += per_launch) {
@@ -297,20 +300,26 @@ int run_sqnorm(const SegDesc* segs, int nsegs, int grad_dtype, int n, const Hype
       SmallParams p{};
       p.h = h;
       p.n_rep = n;
+      p.master = avg_out;  // the average's destination (null: norm only)
       chunks = fill_segments(p, segs, s0, s1, n, kNormChunk, grad_dtype);
-      rc = chunks ? launch_sqnorm(p, chunks, partials + done, grad_dtype, stream) : DPOPT_OK;
+      rc = chunks ? launch_sqnorm(p, chunks, partials + done, grad_dtype, avg_out != nullptr,
+                                  stream)
+                  : DPOPT_OK;
     } else {
       static thread_local BigParams p;
       std::memset(&p, 0, sizeof p);
       p.h = h;
       p.n_rep = n;
       chunks = fill_segments(p, segs, s0, s1, n, kNormChunk, grad_dtype);
-      rc = chunks ? launch_sqnorm(p, chunks, partials + done, grad_dtype, stream) : DPOPT_OK;
+      rc = chunks ? launch_sqnorm(p, chunks, partials + done, grad_dtype, false, stream)
+                  : DPOPT_OK;
     }
     if (rc) return rc;
     done += chunks;
   }
-  sqnorm_finish_kernel<<<1, kThreads, 0, stream>>>(partials, done, out);
+  // each chunk's partial is a double-float pair in its 8-byte slot
+  sqnorm_finish_kernel<<<1, kFinishThreads, 0, stream>>>(reinterpret_cast<const DFloat*>(partials),
+                                                         done, out);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   ++g_launches;
@@ -501,6 +510,47 @@ int finish_empty_norm(double* sqnorm_out, cudaStream_t stream) {
   return DPOPT_OK;
 }
 
+// The full-buffer squared norm: with `state` the unscale is 1/state->scale
+// (read on the device), else grad_unscale (0: 1); with avg_out each element's
+// average is also stored there (S floats, 4-byte aligned; the vector paths
+// want 16 or 32 bytes).
+int full_norm_impl(const void* const* grads, int grad_dtype, int n_replicas, int64_t numel,
+                   int shard_rank, float grad_unscale, const LossScaleState* state,
+                   float* avg_out, double* sqnorm_out, void* scratch, int64_t scratch_bytes,
+                   cudaStream_t stream) {
+  int rc = check_replicas(n_replicas, grad_dtype);
+  if (rc) return rc;
+  if (!std::isfinite(grad_unscale) || grad_unscale < 0.f)
+    return fail(DPOPT_ERR_INVALID_ARG, "grad_unscale must be finite and >= 0");
+  if (numel < 0 || numel % n_replicas != 0)
+    return fail(DPOPT_ERR_INVALID_ARG, "numel must be >= 0 and a multiple of n_replicas");
+  const int64_t S = numel / n_replicas;
+  const int64_t chunks = (S + kNormChunk - 1) / kNormChunk;
+  Range avoid[3];
+  rc = check_norm_outputs(sqnorm_out, scratch, scratch_bytes, chunks, avoid);
+  if (rc) return rc;
+  int navoid = chunks ? 2 : 1;
+  if (avg_out && S > 0) {
+    if ((uintptr_t)avg_out & 3u) return fail(DPOPT_ERR_INVALID_ARG, "avg_out must be 4-byte aligned");
+    const Range a{(uintptr_t)avg_out, (uintptr_t)(avg_out + S)};
+    for (int i = 0; i < navoid; ++i)
+      if (overlaps(a, avoid[i]))
+        return fail(DPOPT_ERR_INVALID_ARG, "avg_out overlaps sqnorm_out or the scratch partials");
+    avoid[navoid++] = a;
+  }
+  const void* ptrs[DPOPT_MAX_REPLICAS];
+  int64_t S2 = 0;
+  rc = build_full(grads, grad_dtype, n_replicas, numel, shard_rank, 1, avoid, navoid, ptrs, &S2);
+  if (rc) return rc;
+  if (S == 0) return finish_empty_norm(sqnorm_out, stream);
+  Hyper h = make_hyper(1.f, 0.f, 0.f, 0.f, 1, n_replicas);
+  h.unscale = grad_unscale == 0.f ? 1.f : grad_unscale;
+  if (state) h.scale_dev = &state->scale;
+  SegDesc seg{ptrs, 0, S};
+  return run_sqnorm(&seg, 1, grad_dtype, n_replicas, h, (double*)scratch, sqnorm_out, stream,
+                    avg_out);
+}
+
 // ---------------------------------------------------------------------------
 // mixed-precision step with dynamic loss scaling
 // ---------------------------------------------------------------------------
@@ -544,11 +594,12 @@ int launch_scale_update(LossScaleState* st, const double* sq, const LossScaleCon
 // allocation-free squared norm: partials in a fixed device array
 // ---------------------------------------------------------------------------
 
-// Chunk partials for dpopt_grad_sqnorm_noalloc: one fp64 per 65536-element
-// chunk, so shards of up to kNoAllocMaxChunks * 65536 = 2^31 elements.  The
+// Chunk partials for dpopt_grad_sqnorm_noalloc: one fp64 per 4096-element
+// chunk, so shards of up to kNoAllocMaxChunks * 4096 = 2^31 elements.  The
 // array is part of the library image: every device that loads the library
-// holds these 256 KB until the process exits.
-constexpr int64_t kNoAllocMaxChunks = 32768;
+// holds these 4 MB until the process exits.
+constexpr int64_t kNoAllocMaxChunks = 524288;
+static_assert(kNoAllocMaxChunks * kNormChunk == (int64_t)1 << 31, "noalloc covers 2^31 elements");
 static __device__ __align__(256) double g_noalloc_partials[kNoAllocMaxChunks];
 
 // Device address of g_noalloc_partials on the current device.  In host code
@@ -659,28 +710,17 @@ int dpopt_grad_sqnorm_scratch_bytes(int64_t elems, int64_t n_buckets, int64_t* b
 int dpopt_grad_sqnorm(const void* const* grads, int grad_dtype, int n_replicas, int64_t numel,
                       int shard_rank, float grad_unscale, double* sqnorm_out, void* scratch,
                       int64_t scratch_bytes, dpopt_stream_t stream) {
-  int rc = check_replicas(n_replicas, grad_dtype);
-  if (rc) return rc;
-  if (!std::isfinite(grad_unscale) || grad_unscale < 0.f)
-    return fail(DPOPT_ERR_INVALID_ARG, "grad_unscale must be finite and >= 0");
-  if (numel < 0 || numel % n_replicas != 0)
-    return fail(DPOPT_ERR_INVALID_ARG, "numel must be >= 0 and a multiple of n_replicas");
-  const int64_t S = numel / n_replicas;
-  const int64_t chunks = (S + kNormChunk - 1) / kNormChunk;
-  Range avoid[2];
-  rc = check_norm_outputs(sqnorm_out, scratch, scratch_bytes, chunks, avoid);
-  if (rc) return rc;
-  const void* ptrs[DPOPT_MAX_REPLICAS];
-  int64_t S2 = 0;
-  rc = build_full(grads, grad_dtype, n_replicas, numel, shard_rank, 1, avoid, chunks ? 2 : 1,
-                  ptrs, &S2);
-  if (rc) return rc;
-  if (S == 0) return finish_empty_norm(sqnorm_out, (cudaStream_t)stream);
-  Hyper h = make_hyper(1.f, 0.f, 0.f, 0.f, 1, n_replicas);
-  h.unscale = grad_unscale == 0.f ? 1.f : grad_unscale;
-  SegDesc seg{ptrs, 0, S};
-  return run_sqnorm(&seg, 1, grad_dtype, n_replicas, h, (double*)scratch, sqnorm_out,
-                    (cudaStream_t)stream);
+  return full_norm_impl(grads, grad_dtype, n_replicas, numel, shard_rank, grad_unscale, nullptr,
+                        nullptr, sqnorm_out, scratch, scratch_bytes, (cudaStream_t)stream);
+}
+
+int dpopt_grad_average_sqnorm(const void* const* grads, int grad_dtype, int n_replicas,
+                              int64_t numel, int shard_rank, float grad_unscale, float* avg_out,
+                              double* sqnorm_out, void* scratch, int64_t scratch_bytes,
+                              dpopt_stream_t stream) {
+  if (!avg_out) return fail(DPOPT_ERR_INVALID_ARG, "avg_out must be non-null");
+  return full_norm_impl(grads, grad_dtype, n_replicas, numel, shard_rank, grad_unscale, nullptr,
+                        avg_out, sqnorm_out, scratch, scratch_bytes, (cudaStream_t)stream);
 }
 
 // Same result as dpopt_grad_sqnorm, for callers that cannot hand the library
@@ -778,28 +818,23 @@ int dpopt_loss_scale_init(dpopt_loss_scale_state* state, const dpopt_loss_scale_
 int dpopt_amp_sqnorm(const void* const* grads, int grad_dtype, int n_replicas, int64_t numel,
                      int shard_rank, const dpopt_loss_scale_state* state, double* sqnorm_out,
                      void* scratch, int64_t scratch_bytes, dpopt_stream_t stream) {
-  int rc = check_replicas(n_replicas, grad_dtype);
+  int rc = check_state_ptr(state);
   if (rc) return rc;
-  rc = check_state_ptr(state);
+  return full_norm_impl(grads, grad_dtype, n_replicas, numel, shard_rank, 0.f,
+                        (const LossScaleState*)state, nullptr, sqnorm_out, scratch,
+                        scratch_bytes, (cudaStream_t)stream);
+}
+
+int dpopt_amp_average_sqnorm(const void* const* grads, int grad_dtype, int n_replicas,
+                             int64_t numel, int shard_rank, const dpopt_loss_scale_state* state,
+                             float* avg_out, double* sqnorm_out, void* scratch,
+                             int64_t scratch_bytes, dpopt_stream_t stream) {
+  int rc = check_state_ptr(state);
   if (rc) return rc;
-  if (numel < 0 || numel % n_replicas != 0)
-    return fail(DPOPT_ERR_INVALID_ARG, "numel must be >= 0 and a multiple of n_replicas");
-  const int64_t S = numel / n_replicas;
-  const int64_t chunks = (S + kNormChunk - 1) / kNormChunk;
-  Range avoid[2];
-  rc = check_norm_outputs(sqnorm_out, scratch, scratch_bytes, chunks, avoid);
-  if (rc) return rc;
-  const void* ptrs[DPOPT_MAX_REPLICAS];
-  int64_t S2 = 0;
-  rc = build_full(grads, grad_dtype, n_replicas, numel, shard_rank, 1, avoid, chunks ? 2 : 1,
-                  ptrs, &S2);
-  if (rc) return rc;
-  if (S == 0) return finish_empty_norm(sqnorm_out, (cudaStream_t)stream);
-  Hyper h = make_hyper(1.f, 0.f, 0.f, 0.f, 1, n_replicas);
-  h.scale_dev = &((const LossScaleState*)state)->scale;
-  SegDesc seg{ptrs, 0, S};
-  return run_sqnorm(&seg, 1, grad_dtype, n_replicas, h, (double*)scratch, sqnorm_out,
-                    (cudaStream_t)stream);
+  if (!avg_out) return fail(DPOPT_ERR_INVALID_ARG, "avg_out must be non-null");
+  return full_norm_impl(grads, grad_dtype, n_replicas, numel, shard_rank, 0.f,
+                        (const LossScaleState*)state, avg_out, sqnorm_out, scratch, scratch_bytes,
+                        (cudaStream_t)stream);
 }
 
 int dpopt_amp_step(const void* const* grads, int grad_dtype, int n_replicas, int64_t numel,

@@ -52,9 +52,11 @@ int launch_step(const LaunchParams<MS, MP>& p, bool ext, cudaStream_t stream);
 template <int GK, int MS, int MP>
 int launch_amp_step(const LaunchParams<MS, MP>& p, const LossScaleState* state,
                     const double* sqnorm, cudaStream_t stream);
+// store_average: also write each element's average to p.master (one
+// segment only).
 template <int GK, int MS, int MP>
 int launch_sqnorm_pass(const LaunchParams<MS, MP>& p, double* partials, int64_t nchunks,
-                       cudaStream_t stream);
+                       bool store_average, cudaStream_t stream);
 
 // Bulk-copy kernel (tma.cu).  tma_eligible: master/m/v 32-byte aligned, the
 // other pointers 16-byte aligned, a supported gradient type and two stages of

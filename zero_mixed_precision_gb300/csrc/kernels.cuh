@@ -107,6 +107,19 @@ __device__ __forceinline__ void st_stream32(float* p, float4 lo, float4 hi) {
                : "memory");
 }
 
+// Stores that keep the line in L2 (a value the next kernel reads back).
+__device__ __forceinline__ void st_global16(float* p, float4 a) {
+  asm volatile("st.global.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(a.x), "f"(a.y), "f"(a.z),
+               "f"(a.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_global32(float* p, float4 lo, float4 hi) {
+  asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(lo.x),
+               "f"(lo.y), "f"(lo.z), "f"(lo.w), "f"(hi.x), "f"(hi.y), "f"(hi.z), "f"(hi.w)
+               : "memory");
+}
+
 // 8 gradient values of one replica as fp32.  GK 0: bf16 (one 16-byte load),
 // GK 1: fp32 (one 32-byte load, or two 16-byte ones: W), GK 2: fp16.
 template <int GK>
@@ -478,14 +491,22 @@ constexpr int min_ctas() { return NR > 0 ? 4 : (PACK ? 2 : 1); }
 
 // State access width of the unrolled kernels, by measurement on GB300
 // (256M-element shards): one 256-bit access per state array and thread
-// (W = 32: whole sectors, half the load/store instructions) is faster where
-// the arithmetic per byte is highest -- bf16/fp16 gradients with N <= 3
-// (+5..7% at N = 2, 3) and fp32 gradients with N <= 6 (+2..10%) -- and 2..4%
-// slower above, where its 8-register tuples cost spills; there two 16-byte
-// accesses (W = 16) run.  gk: 0 bf16, 1 fp32, 2 fp16.
+// (W = 32: whole sectors, half the load/store instructions) is faster for
+// fp32 gradients at every N <= 8 (+0..8%) and for bf16/fp16 gradients with
+// N <= 3 (N = 2: 6395 against 5601 GB/s); for bf16/fp16 N >= 4 two 16-byte
+// accesses (W = 16) are faster (N = 4: 6627 against 6363).  gk: 0 bf16,
+// 1 fp32, 2 fp16.
 constexpr bool wide_states(int gk, int nr) {
-  return nr >= 1 && (gk == 1 ? nr <= 6 : nr <= 3);
+  return nr >= 1 && (gk == 1 ? nr <= 8 : nr <= 3);
 }
+
+// Resident CTAs per SM of a 256-bit kernel: its accesses need aligned
+// 8-register tuples, and at four CTAs (64 registers) most forms spill, so
+// they run three (up to 85 registers; bf16 N = 2: 6395 against 5884 GB/s,
+// fp32 N = 5: 6722 against 6240).  bf16/fp16 with one replica fits 64
+// registers without spills and keeps four (6439 against 5925).
+template <int NR, int GK>
+constexpr int wide_ctas() { return (NR == 1 && GK != 1) ? 4 : 3; }
 
 // The grid-stride walk over the 8-element groups of every segment.  W is the
 // width of one state access (32: one 256-bit access per array, for segments
@@ -520,7 +541,7 @@ __device__ __forceinline__ void step_loop(const LP& p, const Hyper& h, float gsc
 // two forms give identical bits, so the choice is made by speed alone.  EXT
 // adds the AdamW decay and the gradient multiplier (clipping, unscaling).
 template <int NR, int GK, int PACK, bool EXT, int W, int MAXSEG, int MAXPTR>
-__global__ void __launch_bounds__(kThreads, min_ctas<NR, PACK>())
+__global__ void __launch_bounds__(kThreads, W == 32 ? wide_ctas<NR, GK>() : min_ctas<NR, PACK>())
     reduce_adam_ldg_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p) {
   const float gscale = EXT ? grad_scale_of(p.h) : 1.f;
   step_loop<NR, GK, PACK, EXT, W>(p, p.h, gscale);
@@ -552,8 +573,12 @@ struct LossScaleConfig {
 // the bias corrections of step state->step + 1 and the multiplier 1/scale
 // (times the clip coefficient) are formed here, from device state, so no host
 // synchronisation is needed between steps.
+// The 256-bit forms run three CTAs per SM at every N (up to 85 registers): the
+// per-step scalars held in registers make even the one-replica form spill at
+// four (loss-scaled gpt2s step through the stored average: 130.7 against
+// 122.2 G params/s).
 template <int NR, int GK, int PACK, int W, int MAXSEG, int MAXPTR>
-__global__ void __launch_bounds__(kThreads, min_ctas<NR, PACK>())
+__global__ void __launch_bounds__(kThreads, W == 32 ? 3 : min_ctas<NR, PACK>())
     reduce_adam_amp_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p,
                            const LossScaleState* state, const double* sqnorm) {
   // Thread 0 forms the step's scalars once; every thread then takes a copy of

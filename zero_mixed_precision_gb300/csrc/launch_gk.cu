@@ -134,6 +134,10 @@ int amp_kernel(const LaunchParams<MS, MP>& p, const LossScaleState* st, const do
   return launched();
 }
 
+// The loss-scaled kernels take the same widths as the step: their 256-bit
+// forms spill 16..60 bytes at 64 registers (the per-step scalars sit in
+// registers), yet measured faster than the 16-byte ones (fp32 N = 1: 5134
+// against 4990 GB/s for the whole two-pass step).
 template <int NR, int MS, int MP>
 int amp_nr(const LaunchParams<MS, MP>& p, const LossScaleState* st, const double* sq,
            cudaStream_t s) {
@@ -146,19 +150,32 @@ int amp_nr(const LaunchParams<MS, MP>& p, const LossScaleState* st, const double
 }
 
 // ---------------------------------------------------------------------------
-// the squared-norm pass: one CTA per 65536-element chunk, four per SM
+// the squared-norm pass: one CTA per chunk, the hardware scheduler filling
+// the SMs (a CTA loops over further chunks only beyond 2^24 of them)
 // ---------------------------------------------------------------------------
 
-template <int NR, int MS, int MP>
+template <int NR, bool STORE, int MS, int MP>
 int norm_kernel(const LaunchParams<MS, MP>& p, double* partials, int64_t nchunks,
                 cudaStream_t stream) {
-  int sms = 0;
-  int rc = sm_count(&sms);
-  if (rc) return rc;
-  const unsigned grid =
-      (unsigned)std::max<int64_t>(1, std::min<int64_t>(nchunks, (int64_t)sms * 4));
-  grad_sqnorm_kernel<NR, kGK, MS, MP><<<grid, kThreads, 0, stream>>>(p, partials, nchunks);
+  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nchunks, 1 << 24));
+  grad_sqnorm_kernel<NR, kGK, STORE, MS, MP><<<grid, kThreads, 0, stream>>>(
+      p, reinterpret_cast<DFloat*>(partials), nchunks);
   return launched();
+}
+
+template <bool STORE, int MS, int MP>
+int norm_n(const LaunchParams<MS, MP>& p, double* partials, int64_t nchunks, cudaStream_t s) {
+  switch (p.n_rep) {
+    case 1: return norm_kernel<1, STORE>(p, partials, nchunks, s);
+    case 2: return norm_kernel<2, STORE>(p, partials, nchunks, s);
+    case 3: return norm_kernel<3, STORE>(p, partials, nchunks, s);
+    case 4: return norm_kernel<4, STORE>(p, partials, nchunks, s);
+    case 5: return norm_kernel<5, STORE>(p, partials, nchunks, s);
+    case 6: return norm_kernel<6, STORE>(p, partials, nchunks, s);
+    case 7: return norm_kernel<7, STORE>(p, partials, nchunks, s);
+    case 8: return norm_kernel<8, STORE>(p, partials, nchunks, s);
+    default: return norm_kernel<0, STORE>(p, partials, nchunks, s);
+  }
 }
 
 }  // namespace DPOPT_GK_NS
@@ -190,26 +207,18 @@ int launch_amp_step(const LaunchParams<MS, MP>& p, const LossScaleState* state,
 
 template <int G, int MS, int MP>
 int launch_sqnorm_pass(const LaunchParams<MS, MP>& p, double* partials, int64_t nchunks,
-                       cudaStream_t stream) {
+                       bool store_average, cudaStream_t stream) {
   static_assert(G == kGK, "launch_sqnorm_pass instantiated for another gradient type");
-  switch (p.n_rep) {
-    case 1: return DPOPT_GK_NS::norm_kernel<1>(p, partials, nchunks, stream);
-    case 2: return DPOPT_GK_NS::norm_kernel<2>(p, partials, nchunks, stream);
-    case 3: return DPOPT_GK_NS::norm_kernel<3>(p, partials, nchunks, stream);
-    case 4: return DPOPT_GK_NS::norm_kernel<4>(p, partials, nchunks, stream);
-    case 5: return DPOPT_GK_NS::norm_kernel<5>(p, partials, nchunks, stream);
-    case 6: return DPOPT_GK_NS::norm_kernel<6>(p, partials, nchunks, stream);
-    case 7: return DPOPT_GK_NS::norm_kernel<7>(p, partials, nchunks, stream);
-    case 8: return DPOPT_GK_NS::norm_kernel<8>(p, partials, nchunks, stream);
-    default: return DPOPT_GK_NS::norm_kernel<0>(p, partials, nchunks, stream);
-  }
+  if (!store_average) return DPOPT_GK_NS::norm_n<false>(p, partials, nchunks, stream);
+  if constexpr (MS == kSmallSegs) return DPOPT_GK_NS::norm_n<true>(p, partials, nchunks, stream);
+  return fail(DPOPT_ERR_UNSUPPORTED, "the averaged gradient is stored for one segment only");
 }
 
 template int launch_step<kGK>(const SmallParams&, bool, cudaStream_t);
 template int launch_step<kGK>(const BigParams&, bool, cudaStream_t);
 template int launch_amp_step<kGK>(const SmallParams&, const LossScaleState*, const double*,
                                   cudaStream_t);
-template int launch_sqnorm_pass<kGK>(const SmallParams&, double*, int64_t, cudaStream_t);
-template int launch_sqnorm_pass<kGK>(const BigParams&, double*, int64_t, cudaStream_t);
+template int launch_sqnorm_pass<kGK>(const SmallParams&, double*, int64_t, bool, cudaStream_t);
+template int launch_sqnorm_pass<kGK>(const BigParams&, double*, int64_t, bool, cudaStream_t);
 
 }  // namespace dpopt

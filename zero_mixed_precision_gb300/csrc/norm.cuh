@@ -13,9 +13,13 @@ namespace dpopt {
 // squared L2 norm of the averaged gradient (the clipping pre-pass)
 // ---------------------------------------------------------------------------
 
-// Elements per partial sum.  Fixed, so the partition -- and therefore the
-// fp64 rounding of the total -- does not depend on the grid or the GPU.
-constexpr int kNormChunk = 65536;
+// Elements per partial sum: two 8-element groups per thread of a 256-thread
+// CTA.  Fixed, so the partition -- and therefore the fp64 rounding of the
+// total -- does not depend on the grid or the GPU; small, so that one CTA per
+// chunk keeps every SM busy to the end (a 65536-element chunk per CTA left
+// the last wave a quarter empty: 3.55 TB/s at N = 4).
+constexpr int kNormChunk = 4096;
+static_assert(sizeof(DFloat) == sizeof(double), "a chunk partial fills one 8-byte scratch slot");
 
 // The averaged gradient of one aligned 8-element group, as the step forms it.
 template <int NR, int GK, int W>
@@ -31,14 +35,23 @@ __device__ __forceinline__ void norm_group(const void* const* gp, int64_t e0, ui
 // One partial per chunk: sum over the chunk's elements of x^2, x = fl32(g *
 // unscale) (exact for a power-of-two unscale) with g the same fixed-order
 // average the step uses.  Each thread accumulates its elements in order as an
-// fp32 pair (TwoProd for each square, TwoSum into the sum: about 2^-44
-// relative), then the threads' sums are added in fp64 over a fixed tree.
-// Seg::first_group holds the segment's first chunk here.
-template <int NR, int GK, int MAXSEG, int MAXPTR>
-__global__ void __launch_bounds__(kThreads, NR > 0 ? 4 : 2)
-    grad_sqnorm_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p, double* partials,
+// fp32 pair (TwoProd for each square, TwoSum into the sum), then the threads'
+// pairs are added over a fixed tree of double-float additions -- a shuffle
+// tree inside each warp, then the warps' sums in warp order -- and the chunk's
+// pair is stored (8 bytes per chunk).  No fp64 arithmetic: on GB300 an fp64
+// tree per 4096-element chunk kept the fp64 pipe half busy.  Seg::first_group
+// holds the segment's first chunk here.
+//
+// STORE: the pass also writes each element's average g (fp32, before the
+// unscale) to p.master[state_off + e] -- the reduced gradient shard -- so that
+// a following step can read 4 bytes per element instead of N replicas.
+// Five CTAs per SM for N <= 4 (at most 48 registers, no spills; six spilled),
+// four above.
+template <int NR, int GK, bool STORE, int MAXSEG, int MAXPTR>
+__global__ void __launch_bounds__(kThreads, NR > 0 ? (NR <= 4 ? 5 : 4) : 2)
+    grad_sqnorm_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p, DFloat* partials,
                        int64_t nchunks) {
-  __shared__ double red[kThreads];
+  __shared__ DFloat warp_sum[kThreads / 32];
   const uint64_t pol = evict_first_policy();
   const float us = p.h.scale_dev ? __fdiv_rn(1.f, *p.h.scale_dev) : p.h.unscale;
   int si = 0;
@@ -54,6 +67,7 @@ __global__ void __launch_bounds__(kThreads, NR > 0 ? 4 : 2)
       const int64_t rem = sg.len - e0;
       float g[kGroup];
       int cnt = kGroup;
+      float* const avg = STORE ? p.master + sg.state_off + e0 : nullptr;
       if (GK == 1 && sg.vec == 2 && rem >= kGroup) {
         norm_group<NR, GK, 32>(gp, e0, pol, p.n_rep, p.h, g);
       } else if (sg.vec && rem >= kGroup) {
@@ -65,6 +79,18 @@ __global__ void __launch_bounds__(kThreads, NR > 0 ? 4 : 2)
           cs.init(ld_grad1<GK>(gp[0], e0 + j));
           for (int r = 1; r < p.n_rep; ++r) cs.add(ld_grad1<GK>(gp[r], e0 + j));
           g[j] = cs.average(p.h);
+        }
+      }
+      if constexpr (STORE) {
+        const float4 lo4 = make_float4(g[0], g[1], g[2], g[3]);
+        const float4 hi4 = make_float4(g[4], g[5], g[6], g[7]);
+        if (sg.vec == 2 && cnt == kGroup) {
+          st_global32(avg, lo4, hi4);
+        } else if (sg.vec && cnt == kGroup) {
+          st_global16(avg, lo4);
+          st_global16(avg + 4, hi4);
+        } else {
+          for (int j = 0; j < cnt; ++j) avg[j] = g[j];
         }
       }
 #pragma unroll
@@ -81,16 +107,22 @@ __global__ void __launch_bounds__(kThreads, NR > 0 ? 4 : 2)
         }
       }
     }
-    const double acc = __dadd_rn((double)hi, (double)lo);
-    red[threadIdx.x] = acc;
-    __syncthreads();
+    DFloat acc{hi, lo};
 #pragma unroll
-    for (int w = kThreads / 2; w > 0; w >>= 1) {
-      if (threadIdx.x < w) red[threadIdx.x] = __dadd_rn(red[threadIdx.x], red[threadIdx.x + w]);
-      __syncthreads();
+    for (int off = 16; off > 0; off >>= 1) {
+      const DFloat o{__shfl_down_sync(0xffffffffu, acc.hi, off),
+                     __shfl_down_sync(0xffffffffu, acc.lo, off)};
+      acc = df_add(acc, o);
     }
-    if (threadIdx.x == 0) partials[c] = red[0];
+    if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = acc;
     __syncthreads();
+    if (threadIdx.x == 0) {
+      DFloat tot = warp_sum[0];
+#pragma unroll
+      for (int w = 1; w < kThreads / 32; ++w) tot = df_add(tot, warp_sum[w]);
+      partials[c] = tot;
+    }
+    __syncthreads();  // warp_sum is rewritten for the next chunk
   }
 }
 

@@ -116,6 +116,23 @@ __device__ __forceinline__ void two_sum(V a, V b, V& s, V& e) {
   e = vadd(vadd(a, vneg(ap)), vadd(b, vneg(bp)));
 }
 
+// A double-float: hi + lo with |lo| <= ulp(hi)/2, about 48 significant bits.
+struct DFloat {
+  float hi, lo;
+};
+
+// a + b for non-negative double-floats (sums of squares): TwoSum of the high
+// parts, the low parts added to its error, then renormalised.  Relative error
+// about 2^-47; fp32 operations only (GB300's fp64 rate is a small fraction of
+// its fp32 rate).
+__device__ __forceinline__ DFloat df_add(DFloat a, DFloat b) {
+  float s, e;
+  two_sum(a.hi, b.hi, s, e);
+  e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+  const float hi = __fadd_rn(s, e);
+  return DFloat{hi, __fsub_rn(e, __fsub_rn(hi, s))};
+}
+
 // ---------------------------------------------------------------------------
 // Reduce: running compensated sum over the replicas in ascending order.
 // ---------------------------------------------------------------------------
