@@ -443,24 +443,50 @@ def run_ours(args, wl):
     ds = [torch.empty(S, dtype=dev.grads[0].dtype, device=device) for _ in range(n)]
     hout = torch.empty(S, dtype=torch.bfloat16, pin_memory=True)
     Ke = max(1, min(args.e2e_steps, K))
-    barrier()
-    torch.cuda.synchronize(device)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for k in range(Ke):
+
+    def timed_e2e(one_step):
+        barrier()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(Ke):
+            one_step(args.warmup + K + 1 + k)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier()
+        dp.stream_status(stream)
+        return max_over_ranks(e0.elapsed_time(e1), world, device)
+
+    # (1) the step kernel reads the pinned host gradients in place and writes the
+    # bf16 parameters into pinned host memory: each step's inputs cross the
+    # host link (NVLink-C2C on a Grace-Blackwell node) inside the kernel, which
+    # overlaps the inbound gradients, the arithmetic and the outbound parameters
+    def in_place(t):
+        dp.reduce_adam_bucket(hs, 0, dev.master, dev.m, dev.v, hout, step=t, stream=stream,
+                              **hp)
+
+    # (2) copy-engine transfers around a device-resident step, one stream
+    def copies(t):
         for h, d in zip(hs, ds):
             d.copy_(h, non_blocking=True)
-        dp.reduce_adam_bucket(ds, 0, dev.master, dev.m, dev.v, dev.out,
-                              step=args.warmup + K + 1 + k, stream=stream, **hp)
+        dp.reduce_adam_bucket(ds, 0, dev.master, dev.m, dev.v, dev.out, step=t, stream=stream,
+                              **hp)
         hout.copy_(dev.out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize(device)
-    barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
-    e2e = {"value": throughput(world, S, Ke, e2e_ms), "unit": UNIT,
-           "h2d_bytes_per_step": n * S * esize, "d2h_bytes_per_step": S * 2,
-           "path": "pinned host gradients -> cudaMemcpyAsync -> dpopt_reduce_adam_bucket -> "
-                   "bf16 parameters back to pinned host, one stream"}
+
+    with torch.cuda.stream(stream):
+        in_place(args.warmup + K + 1)          # untimed: first touch of the host pages
+        ip_ms = timed_e2e(in_place)
+        ce_ms = timed_e2e(copies)
+    h2d, d2h = n * S * esize, S * 2
+    e2e = {"value": throughput(world, S, Ke, ip_ms), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "host_link_gbs": (h2d + d2h) * Ke / (ip_ms * 1e-3) / 1e9,
+           "path": "pinned host gradients read in place by dpopt_reduce_adam_bucket's kernel, "
+                   "bf16 parameters written into pinned host memory, one launch per step",
+           "copy_engine": {"value": throughput(world, S, Ke, ce_ms), "unit": UNIT,
+                           "path": "pinned host gradients -> cudaMemcpyAsync -> "
+                                   "dpopt_reduce_adam_bucket -> bf16 parameters back to pinned "
+                                   "host, one stream"}}
     dp.stream_status(stream)
     grads = [h.view(torch.int16).numpy().view("uint16") if h.dtype == torch.bfloat16
              else h.numpy() for h in hs]

@@ -36,6 +36,16 @@
  *    are DEVICE pointers of the current CUDA device; the pointer tables
  *    themselves (grads, grad_slices, slice_table) and offsets/lens are HOST
  *    arrays, read during the call only.  The library allocates no memory.
+ *    A "DEVICE pointer" may also point into page-locked host memory that the
+ *    device addresses at the same address (cudaHostAlloc, or cudaHostRegister
+ *    with cudaHostRegisterMapped, on a system with unified addressing): the
+ *    kernels then read the gradients from, or write param_bf16_out to, host
+ *    memory in place -- on a Grace-Blackwell node over NVLink-C2C, which moves
+ *    a step's host gradients in and its bf16 parameters out without separate
+ *    copies.  Such operands run at the host link's bandwidth, not HBM's; the
+ *    results are bitwise those of device-resident operands.  The library does
+ *    not check where a pointer points: pageable host memory the device cannot
+ *    reach is the caller's error, as is any other invalid pointer.
  *  - Layout: flat, contiguous, element-indexed.  bf16 values are IEEE
  *    binary32's upper 16 bits (stored as 2-byte words), fp32 are binary32.
  *  - In place: master, m, v are read and overwritten; param_bf16_out is only

@@ -204,3 +204,19 @@ def test_sqnorm_and_adamw_reject_bad_arguments(dp):
     assert dp.dpopt_reduce_adamw(G[:4], 0, 4, 4096, 0, 1024, MASTER, M, V, OUT, *HP, 1, opt, 0) == 1
     opt = dp.StepOptions(0.01, 1.0, SQ + 3, 0.0)  # misaligned norm pointer
     assert dp.dpopt_reduce_adamw(G[:4], 0, 4, 4096, 0, 1024, MASTER, M, V, OUT, *HP, 1, opt, 0) == 1
+
+
+def test_binding_refuses_pageable_host_operands(dp):
+    """Pinned host memory is a valid operand (the kernels address it in place);
+    pageable host memory is refused by the binding before any call into the
+    library, for gradients, states and the output alike."""
+    import torch
+    S = 64
+    g = [torch.zeros(S, dtype=torch.bfloat16) for _ in range(2)]
+    st = [torch.zeros(S) for _ in range(3)]
+    out = torch.zeros(S, dtype=torch.bfloat16)
+    hp = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, step=1, stream=0)
+    with pytest.raises(ValueError, match="pageable"):
+        dp.reduce_adam_bucket(g, 0, *st, out, **hp)
+    with pytest.raises(ValueError, match="pageable"):
+        dp.reduce_adam(g, 0, S, *st, out, **hp)

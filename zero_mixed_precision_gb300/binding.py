@@ -359,6 +359,17 @@ def _grad_dtype(t) -> int:
     raise TypeError(f"gradients must be bfloat16, float16 or float32, got {t.dtype}")
 
 
+def _operand(t) -> int:
+    """The address of a tensor the kernels may read or write: device memory, or
+    page-locked host memory (which the device reaches at the same address, so
+    the kernels read or write it in place).  Pageable host memory is refused
+    here, before any launch, since a kernel could not reach it."""
+    if t.is_cuda or t.is_pinned():
+        return t.data_ptr()
+    raise ValueError("operand is in pageable host memory: move it to the device or pin it "
+                     "(pin_memory=True) so that the kernels can address it")
+
+
 def _stream_handle(stream) -> int:
     if stream is None:
         import torch
@@ -372,9 +383,9 @@ def reduce_adam(grads, shard_rank: int, bucket_elems: int, master, m, v, param_b
     numel elements each); master/m/v (fp32) and param_bf16_out (bf16) hold
     this rank's S = numel/N shard."""
     dt = _grad_dtype(grads[0])
-    rc = dpopt_reduce_adam_ex([g.data_ptr() for g in grads], dt, len(grads), grads[0].numel(),
-                              shard_rank, bucket_elems, master.data_ptr(), m.data_ptr(),
-                              v.data_ptr(), param_bf16_out.data_ptr(), lr, beta1, beta2, eps, step,
+    rc = dpopt_reduce_adam_ex([_operand(g) for g in grads], dt, len(grads), grads[0].numel(),
+                              shard_rank, bucket_elems, _operand(master), _operand(m),
+                              _operand(v), _operand(param_bf16_out), lr, beta1, beta2, eps, step,
                               _stream_handle(stream))
     _check(rc, "dpopt_reduce_adam_ex")
 
@@ -383,9 +394,9 @@ def reduce_adam_bucket(grad_slices, shard_offset: int, master, m, v, param_bf16_
                        beta1: float, beta2: float, eps: float, step: int, stream=None) -> None:
     """One bucket: grad_slices are N tensors of the bucket's length."""
     dt = _grad_dtype(grad_slices[0])
-    rc = dpopt_reduce_adam_bucket([g.data_ptr() for g in grad_slices], dt, len(grad_slices),
-                                  shard_offset, grad_slices[0].numel(), master.data_ptr(),
-                                  m.data_ptr(), v.data_ptr(), param_bf16_out.data_ptr(), lr, beta1,
+    rc = dpopt_reduce_adam_bucket([_operand(g) for g in grad_slices], dt, len(grad_slices),
+                                  shard_offset, grad_slices[0].numel(), _operand(master),
+                                  _operand(m), _operand(v), _operand(param_bf16_out), lr, beta1,
                                   beta2, eps, step, _stream_handle(stream))
     _check(rc, "dpopt_reduce_adam_bucket")
 
@@ -396,10 +407,10 @@ def reduce_adam_buckets(bucket_slices, offsets, master, m, v, param_bf16_out, *,
     which updates shard elements [offsets[b], offsets[b] + len)."""
     n = len(bucket_slices[0])
     dt = _grad_dtype(bucket_slices[0][0])
-    table = [t.data_ptr() for row in bucket_slices for t in row]
+    table = [_operand(t) for row in bucket_slices for t in row]
     lens = [row[0].numel() for row in bucket_slices]
-    rc = dpopt_reduce_adam_buckets(table, dt, n, list(offsets), lens, master.data_ptr(),
-                                   m.data_ptr(), v.data_ptr(), param_bf16_out.data_ptr(), lr,
+    rc = dpopt_reduce_adam_buckets(table, dt, n, list(offsets), lens, _operand(master),
+                                   _operand(m), _operand(v), _operand(param_bf16_out), lr,
                                    beta1, beta2, eps, step, _stream_handle(stream))
     _check(rc, "dpopt_reduce_adam_buckets")
 
@@ -408,16 +419,16 @@ def step_options(weight_decay: float = 0.0, max_grad_norm: float = 0.0, grad_sqn
                  grad_unscale: float = 0.0) -> StepOptions:
     """Build a dpopt_step_options; grad_sqnorm is a 1-element float64 device tensor."""
     return StepOptions(weight_decay, max_grad_norm,
-                       grad_sqnorm.data_ptr() if grad_sqnorm is not None else None, grad_unscale)
+                       _operand(grad_sqnorm) if grad_sqnorm is not None else None, grad_unscale)
 
 
 def reduce_adamw(grads, shard_rank: int, bucket_elems: int, master, m, v, param_bf16_out, *,
                  lr: float, beta1: float, beta2: float, eps: float, step: int,
                  opts: StepOptions | None, stream=None) -> None:
     dt = _grad_dtype(grads[0])
-    rc = dpopt_reduce_adamw([g.data_ptr() for g in grads], dt, len(grads), grads[0].numel(),
-                            shard_rank, bucket_elems, master.data_ptr(), m.data_ptr(), v.data_ptr(),
-                            param_bf16_out.data_ptr(), lr, beta1, beta2, eps, step, opts,
+    rc = dpopt_reduce_adamw([_operand(g) for g in grads], dt, len(grads), grads[0].numel(),
+                            shard_rank, bucket_elems, _operand(master), _operand(m), _operand(v),
+                            _operand(param_bf16_out), lr, beta1, beta2, eps, step, opts,
                             _stream_handle(stream))
     _check(rc, "dpopt_reduce_adamw")
 
@@ -427,10 +438,10 @@ def reduce_adamw_buckets(bucket_slices, offsets, master, m, v, param_bf16_out, *
                          opts: StepOptions | None, stream=None) -> None:
     n = len(bucket_slices[0])
     dt = _grad_dtype(bucket_slices[0][0])
-    table = [t.data_ptr() for row in bucket_slices for t in row]
+    table = [_operand(t) for row in bucket_slices for t in row]
     lens = [row[0].numel() for row in bucket_slices]
-    rc = dpopt_reduce_adamw_buckets(table, dt, n, list(offsets), lens, master.data_ptr(),
-                                    m.data_ptr(), v.data_ptr(), param_bf16_out.data_ptr(), lr,
+    rc = dpopt_reduce_adamw_buckets(table, dt, n, list(offsets), lens, _operand(master),
+                                    _operand(m), _operand(v), _operand(param_bf16_out), lr,
                                     beta1, beta2, eps, step, opts, _stream_handle(stream))
     _check(rc, "dpopt_reduce_adamw_buckets")
 
@@ -440,8 +451,8 @@ def grad_sqnorm(grads, shard_rank: int, sqnorm_out, scratch, *, grad_unscale: fl
     """sqnorm_out: 1-element float64 device tensor; scratch: device tensor of at least
     dpopt_grad_sqnorm_scratch_bytes(S) bytes."""
     dt = _grad_dtype(grads[0])
-    rc = dpopt_grad_sqnorm([g.data_ptr() for g in grads], dt, len(grads), grads[0].numel(),
-                           shard_rank, grad_unscale, sqnorm_out.data_ptr(), scratch.data_ptr(),
+    rc = dpopt_grad_sqnorm([_operand(g) for g in grads], dt, len(grads), grads[0].numel(),
+                           shard_rank, grad_unscale, _operand(sqnorm_out), _operand(scratch),
                            scratch.numel() * scratch.element_size(), _stream_handle(stream))
     _check(rc, "dpopt_grad_sqnorm")
 
@@ -451,9 +462,9 @@ def grad_average_sqnorm(grads, shard_rank: int, avg_out, sqnorm_out, scratch, *,
     """grad_sqnorm that also writes the shard's fixed-order average gradient to
     avg_out (float32 device tensor of S = numel / N elements)."""
     dt = _grad_dtype(grads[0])
-    rc = dpopt_grad_average_sqnorm([g.data_ptr() for g in grads], dt, len(grads),
-                                   grads[0].numel(), shard_rank, grad_unscale, avg_out.data_ptr(),
-                                   sqnorm_out.data_ptr(), scratch.data_ptr(),
+    rc = dpopt_grad_average_sqnorm([_operand(g) for g in grads], dt, len(grads),
+                                   grads[0].numel(), shard_rank, grad_unscale, _operand(avg_out),
+                                   _operand(sqnorm_out), _operand(scratch),
                                    scratch.numel() * scratch.element_size(),
                                    _stream_handle(stream))
     _check(rc, "dpopt_grad_average_sqnorm")
@@ -462,9 +473,9 @@ def grad_average_sqnorm(grads, shard_rank: int, avg_out, sqnorm_out, scratch, *,
 def amp_average_sqnorm(grads, shard_rank: int, state, avg_out, sqnorm_out, scratch,
                        stream=None) -> None:
     dt = _grad_dtype(grads[0])
-    rc = dpopt_amp_average_sqnorm([g.data_ptr() for g in grads], dt, len(grads),
-                                  grads[0].numel(), shard_rank, state.data_ptr(),
-                                  avg_out.data_ptr(), sqnorm_out.data_ptr(), scratch.data_ptr(),
+    rc = dpopt_amp_average_sqnorm([_operand(g) for g in grads], dt, len(grads),
+                                  grads[0].numel(), shard_rank, _operand(state),
+                                  _operand(avg_out), _operand(sqnorm_out), _operand(scratch),
                                   scratch.numel() * scratch.element_size(), _stream_handle(stream))
     _check(rc, "dpopt_amp_average_sqnorm")
 
@@ -473,10 +484,10 @@ def grad_sqnorm_buckets(bucket_slices, offsets, sqnorm_out, scratch, *, grad_uns
                         stream=None) -> None:
     n = len(bucket_slices[0])
     dt = _grad_dtype(bucket_slices[0][0])
-    table = [t.data_ptr() for row in bucket_slices for t in row]
+    table = [_operand(t) for row in bucket_slices for t in row]
     lens = [row[0].numel() for row in bucket_slices]
     rc = dpopt_grad_sqnorm_buckets(table, dt, n, list(offsets), lens, grad_unscale,
-                                   sqnorm_out.data_ptr(), scratch.data_ptr(),
+                                   _operand(sqnorm_out), _operand(scratch),
                                    scratch.numel() * scratch.element_size(), _stream_handle(stream))
     _check(rc, "dpopt_grad_sqnorm_buckets")
 
@@ -486,7 +497,7 @@ def loss_scale_init(state, init_scale: float = 65536.0, window: int = 1000, hyst
     """state: a device tensor of at least 32 bytes (e.g. torch.zeros(4, dtype=torch.int64)).
     Returns the config to pass to amp_step."""
     cfg = LossScaleConfig(init_scale, window, hysteresis, min_scale)
-    _check(dpopt_loss_scale_init(state.data_ptr(), cfg, _stream_handle(stream)),
+    _check(dpopt_loss_scale_init(_operand(state), cfg, _stream_handle(stream)),
            "dpopt_loss_scale_init")
     return cfg
 
@@ -499,8 +510,8 @@ def read_loss_scale(state) -> LossScaleState:
 
 def amp_sqnorm(grads, shard_rank: int, state, sqnorm_out, scratch, stream=None) -> None:
     dt = _grad_dtype(grads[0])
-    rc = dpopt_amp_sqnorm([g.data_ptr() for g in grads], dt, len(grads), grads[0].numel(),
-                          shard_rank, state.data_ptr(), sqnorm_out.data_ptr(), scratch.data_ptr(),
+    rc = dpopt_amp_sqnorm([_operand(g) for g in grads], dt, len(grads), grads[0].numel(),
+                          shard_rank, _operand(state), _operand(sqnorm_out), _operand(scratch),
                           scratch.numel() * scratch.element_size(), _stream_handle(stream))
     _check(rc, "dpopt_amp_sqnorm")
 
@@ -510,10 +521,10 @@ def amp_step(grads, shard_rank: int, bucket_elems: int, master, m, v, param_bf16
              max_grad_norm: float, global_sqnorm, state, cfg: LossScaleConfig,
              stream=None) -> None:
     dt = _grad_dtype(grads[0])
-    rc = dpopt_amp_step([g.data_ptr() for g in grads], dt, len(grads), grads[0].numel(),
-                        shard_rank, bucket_elems, master.data_ptr(), m.data_ptr(), v.data_ptr(),
-                        param_bf16_out.data_ptr(), lr, beta1, beta2, eps, weight_decay,
-                        max_grad_norm, global_sqnorm.data_ptr(), state.data_ptr(), cfg,
+    rc = dpopt_amp_step([_operand(g) for g in grads], dt, len(grads), grads[0].numel(),
+                        shard_rank, bucket_elems, _operand(master), _operand(m), _operand(v),
+                        _operand(param_bf16_out), lr, beta1, beta2, eps, weight_decay,
+                        max_grad_norm, _operand(global_sqnorm), _operand(state), cfg,
                         _stream_handle(stream))
     _check(rc, "dpopt_amp_step")
 
@@ -524,12 +535,12 @@ def reduce_adam_buckets_when_ready(bucket_slices, offsets, ready_events, master,
     """ready_events: one torch.cuda.Event (already recorded) or None per bucket."""
     n = len(bucket_slices[0])
     dt = _grad_dtype(bucket_slices[0][0])
-    table = [t.data_ptr() for row in bucket_slices for t in row]
+    table = [_operand(t) for row in bucket_slices for t in row]
     lens = [row[0].numel() for row in bucket_slices]
     ready = [e.cuda_event if e is not None else 0 for e in ready_events]
     rc = dpopt_reduce_adam_buckets_when_ready(table, dt, n, list(offsets), lens, ready,
-                                              master.data_ptr(), m.data_ptr(), v.data_ptr(),
-                                              param_bf16_out.data_ptr(), lr, beta1, beta2, eps,
+                                              _operand(master), _operand(m), _operand(v),
+                                              _operand(param_bf16_out), lr, beta1, beta2, eps,
                                               step, _stream_handle(stream))
     _check(rc, "dpopt_reduce_adam_buckets_when_ready")
 
@@ -537,8 +548,8 @@ def reduce_adam_buckets_when_ready(bucket_slices, offsets, ready_events, master,
 def allgather_bf16(shard_bf16, shard_rank: int, param_replicas, stream=None) -> None:
     """Write the bf16 shard tensor into every replica's flat bf16 parameter tensor
     at the shard's position."""
-    rc = dpopt_allgather_bf16(shard_bf16.data_ptr(), shard_bf16.numel(), shard_rank,
-                              [t.data_ptr() for t in param_replicas], len(param_replicas),
+    rc = dpopt_allgather_bf16(_operand(shard_bf16), shard_bf16.numel(), shard_rank,
+                              [_operand(t) for t in param_replicas], len(param_replicas),
                               _stream_handle(stream))
     _check(rc, "dpopt_allgather_bf16")
 
