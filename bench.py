@@ -81,6 +81,11 @@ def parse_args(argv=None):
                          "also stores the averaged gradient (the reduced gradient shard) and the "
                          "step reads it as one fp32 replica; 'fused' -- the step reads the N "
                          "replicas again.  Both give the same bits.")
+    ap.add_argument("--gather-path", choices=("fused", "separate"), default="fused",
+                    help="adam_allgather: 'fused' -- one kernel writes the new bf16 shard into "
+                         "every replica's parameter buffer (dpopt_reduce_adam_allgather); "
+                         "'separate' -- the step, then dpopt_allgather_bf16 reads the bf16 "
+                         "shard back and broadcasts it.  Both give the same bits.")
     return ap.parse_args(argv)
 
 
@@ -332,6 +337,7 @@ def run_ours(args, wl):
         opts = dp.step_options(weight_decay=0.01, max_grad_norm=1.0, grad_sqnorm=sqn)
     if args.optimizer == "adam_allgather":
         param_reps = [torch.empty(S * n, dtype=torch.bfloat16, device=device) for _ in range(n)]
+    gather_fused = args.gather_path == "fused"
     stored = args.clip_path == "stored" and wl.layout == "full"
     if args.optimizer in ("adamw_clip", "amp") and stored:
         avg = torch.empty(S, dtype=torch.float32, device=device)
@@ -342,7 +348,11 @@ def run_ours(args, wl):
         ls_state = torch.zeros(4, dtype=torch.int64, device=device)
         ls_cfg = dp.loss_scale_init(ls_state, init_scale=1024.0, window=1000, stream=stream)
     if wl.layout == "full":
-        if args.optimizer == "adam_allgather":
+        if args.optimizer == "adam_allgather" and gather_fused:
+            def step(t):
+                dp.reduce_adam_allgather(dev.grads, wl.shard_rank, wl.bucket_elems, dev.master,
+                                         dev.m, dev.v, param_reps, step=t, stream=stream, **hp)
+        elif args.optimizer == "adam_allgather":
             def step(t):
                 dp.reduce_adam(dev.grads, wl.shard_rank, wl.bucket_elems, dev.master, dev.m,
                                dev.v, dev.out, step=t, stream=stream, **hp)
@@ -508,6 +518,9 @@ def _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks
         bpp += 8
     elif args.optimizer in ("adamw_clip", "amp"):   # the norm pre-pass reads the N gradients again
         bpp += wl.grad_bytes() * wl.n_replicas
+    elif args.optimizer == "adam_allgather" and args.gather_path == "fused":
+        # the bf16 copy goes to the N replica buffers instead of one output
+        bpp += 2 * wl.n_replicas - 2
     elif args.optimizer == "adam_allgather":   # read the bf16 shard, write N copies
         bpp += 2 + 2 * wl.n_replicas
     ms_per_step = elapsed_ms / K
@@ -523,7 +536,9 @@ def _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks
         "config": {**config_of(wl, args.kernel), "optimizer": args.optimizer,
                    "bytes_per_param": bpp,
                    **({"clip_path": "stored" if stored else "fused"}
-                      if args.optimizer in ("adamw_clip", "amp") else {})},
+                      if args.optimizer in ("adamw_clip", "amp") else {}),
+                   **({"gather_path": args.gather_path}
+                      if args.optimizer == "adam_allgather" else {})},
         "hbm_gbs": S * bpp / (ms_per_step / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth",

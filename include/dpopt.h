@@ -364,6 +364,33 @@ int dpopt_amp_step(const void *const *grads, int grad_dtype, int n_replicas, int
 int dpopt_allgather_bf16(const void *shard_bf16, int64_t shard_elems, int shard_rank,
                          void *const *param_replicas, int n_replicas, dpopt_stream_t stream);
 
+/* The step of dpopt_reduce_adam_ex and the all-gather of its bf16 shard in one
+ * pass over memory (the same section: the optimizer updates the rank's shard,
+ * then every rank's parameters are gathered for the next forward pass).  The
+ * rank's own replica buffer holds the working copy: with S = numel/n_replicas
+ * and base = shard_rank*S,
+ *   param_replicas[r][base + i] = bf16(master_f32[i] after the step),  r < n_replicas,
+ * bit for bit what dpopt_reduce_adam_ex(..., param_replicas[shard_rank] + base, ...)
+ * followed by dpopt_allgather_bf16 of that range writes, and master/m/v as that
+ * step leaves them -- but the bf16 copy is never read back and one kernel runs:
+ * g*N + 24 + 2N bytes per parameter instead of g*N + 28 + 2N.
+ *  grads, grad_dtype, n_replicas, numel, shard_rank, bucket_elems, master_f32,
+ *  m_f32, v_f32, lr, beta1, beta2, eps, step, stream
+ *                  as for dpopt_reduce_adam_ex.
+ *  param_replicas  HOST array of n_replicas DEVICE pointers, each to a flat bf16
+ *                  buffer of at least numel elements; only [base, base + S) of
+ *                  each is written.  The ranges written must not overlap one
+ *                  another, the states or the gradients.  16-byte aligned
+ *                  ranges take 16-byte stores, others go one element at a time.
+ * Errors: as for dpopt_reduce_adam_ex, and DPOPT_ERR_INVALID_ARG for a null
+ * table or replica pointer, a misaligned replica pointer, or overlapping
+ * ranges. */
+int dpopt_reduce_adam_allgather(const void *const *grads, int grad_dtype, int n_replicas,
+                                int64_t numel, int shard_rank, int64_t bucket_elems,
+                                float *master_f32, float *m_f32, float *v_f32,
+                                void *const *param_replicas, float lr, float beta1, float beta2,
+                                float eps, int64_t step, dpopt_stream_t stream);
+
 /* Bucket-as-ready: the batched-bucket step with one launch per bucket, each made
  * to wait on the stream for that bucket's readiness event first.  The producer
  * of the gradients (a backward pass on another stream, last layer first) records

@@ -220,3 +220,37 @@ def test_binding_refuses_pageable_host_operands(dp):
         dp.reduce_adam_bucket(g, 0, *st, out, **hp)
     with pytest.raises(ValueError, match="pageable"):
         dp.reduce_adam(g, 0, S, *st, out, **hp)
+
+
+# replica parameter buffers of the fused step + all-gather (fake addresses)
+R = [0xD0_0000_0000 + r * 0x1_0000_0000 for r in range(64)]
+
+
+def _fused(dp, **over):
+    a = dict(grads=G[:4], n=4, numel=4096, rank=1, bucket=1024, master=MASTER, m=M, v=V,
+             reps=R[:4], lr=HP[0], b1=HP[1], b2=HP[2], eps=HP[3], step=1, dtype=0)
+    a.update(over)
+    return dp.dpopt_reduce_adam_allgather(a["grads"], a["dtype"], a["n"], a["numel"], a["rank"],
+                                          a["bucket"], a["master"], a["m"], a["v"], a["reps"],
+                                          a["lr"], a["b1"], a["b2"], a["eps"], a["step"], 0)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(reps=None), 1), (dict(reps=[R[0], 0, R[2], R[3]]), 1),
+    (dict(reps=[R[0], R[1] + 1, R[2], R[3]]), 1),          # misaligned replica buffer
+    (dict(reps=[R[0], R[1], R[1] + 1000, R[3]]), 1),      # two destinations overlap
+    (dict(reps=[R[0], R[1], MASTER - 1024 * 2 + 16, R[3]]), 1),  # a destination on master
+    (dict(reps=[R[0], R[1], G[0], R[3]]), 1),             # a destination on a gradient shard
+    (dict(master=R[1] + 2048 + 64), 1),                   # master on the working copy
+    (dict(rank=4), 1), (dict(rank=-1), 1), (dict(numel=4095), 1), (dict(step=0), 1),
+    (dict(n=65, grads=G[:64] + [G[0]], reps=R[:64] + [R[0]]), 2), (dict(dtype=5), 1),
+    (dict(b1=1.0), 1), (dict(bucket=0), 1), (dict(grads=None), 1),
+])
+def test_fused_allgather_entry_rejects_bad_arguments(dp, over, code):
+    assert _fused(dp, **over) == code
+    assert dp.dpopt_last_error() != ""
+
+
+def test_fused_allgather_entry_with_nothing_to_update_checks_and_returns(dp):
+    assert _fused(dp, numel=0) == 0
+    assert _fused(dp, numel=0, rank=7) == 1

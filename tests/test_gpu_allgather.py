@@ -13,7 +13,8 @@ pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     import zero_mixed_precision_gb300 as dp
-    from tests.test_gpu_parity import _host_full_buffers, _small_workload, to_dev_grad, u16
+    from tests.test_gpu_parity import _host_full_buffers, _small_workload, f32, to_dev_grad, u16
+    from tests.parity import oracle_trajectory
 else:
     dp = None
 
@@ -85,3 +86,71 @@ def test_allgather_rejects_bad_arguments():
     assert dp.dpopt_allgather_bf16(R[0] + 10, 100, 0, R, 2, 0) == dp.DPOPT_ERR_INVALID_ARG
     assert dp.dpopt_allgather_bf16(P + 1, 100, 0, R, 2, 0) == dp.DPOPT_ERR_INVALID_ARG
     assert dp.dpopt_allgather_bf16(P, 100, 0, R, 65, 0) == dp.DPOPT_ERR_UNSUPPORTED
+
+
+def _states(wl):
+    """The rank's seeded master, m, v on the device."""
+    th, m, v = parity.states_host(wl, np.arange(wl.shard_elems) + wl.shard_base)
+    return [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (th, m, v)]
+
+
+@pytest.mark.parametrize("n,S,kind,rank", [
+    (1, 4_099, 0, 0), (2, 50_001, 0, 1), (3, 30_000, 0, 2), (4, 65_537, 0, 1),
+    (5, 12_345, 0, 3), (8, 20_003, 0, 7), (13, 4_100, 0, 6), (64, 2_056, 0, 17),
+    (4, 40_000, 1, 2), (2, 9_999, 1, 0), (4, 30_011, 2, 3),
+])
+def test_fused_step_allgather_equals_step_then_allgather(n, S, kind, rank):
+    """Two steps of the fused entry against the step followed by the separate
+    all-gather: the same master/m/v and the same bytes in every replica buffer
+    (canary-filled outside the shard), and the oracle's values on a sample."""
+    _need_gpu()
+    wl = _small_workload(n, S, kind=kind, rank=rank, seed=23)
+    numel = n * S
+    res = []
+    for fused in (True, False):
+        st = _states(wl)
+        reps = [torch.full((numel,), 0x7FA1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+                for _ in range(n)]   # a NaN bit pattern no step writes
+        for t in (1, 2):
+            grads = [to_dev_grad(g) for g in _host_full_buffers(wl, t)]
+            if fused:
+                dp.reduce_adam_allgather(grads, rank, S, *st, reps, step=t, **HP)
+            else:
+                own = reps[rank][rank * S:(rank + 1) * S]
+                dp.reduce_adam(grads, rank, S, *st, own, step=t, **HP)
+                dp.allgather_bf16(own, rank, reps)
+        dp.stream_status()
+        res.append([f32(x) for x in st] + [u16(r) for r in reps])
+    for a, b in zip(*res):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+    idx = np.unique(np.concatenate([np.arange(0, S, 97), np.arange(max(0, S - 9), S)]))
+    ref = oracle_trajectory(wl, idx, 1, 2)[-1]
+    th, m, v = (x[idx] for x in res[0][:3])
+    for r in range(n):
+        parity.check(ref, th, m, v, res[0][3 + r][rank * S + idx], where=f"fused gather rep {r}")
+        outside = np.concatenate([res[0][3 + r][:rank * S], res[0][3 + r][(rank + 1) * S:]])
+        assert (outside == 0x7FA1).all()
+
+
+def test_fused_step_allgather_unaligned_replicas():
+    """Replica buffers 2 bytes past a 16-byte boundary: the one-element path,
+    same bits as the separate step and all-gather."""
+    _need_gpu()
+    n, S, rank = 3, 10_007, 1
+    wl = _small_workload(n, S, rank=rank, seed=29)
+    grads = [to_dev_grad(g) for g in _host_full_buffers(wl, 1)]
+    res = []
+    for fused in (True, False):
+        st = _states(wl)
+        base = [torch.zeros(n * S + 8, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+        reps = [b[1:1 + n * S] for b in base]
+        if fused:
+            dp.reduce_adam_allgather(grads, rank, 1000, *st, reps, step=1, **HP)
+        else:
+            own = reps[rank][rank * S:(rank + 1) * S]
+            dp.reduce_adam(grads, rank, 1000, *st, own, step=1, **HP)
+            dp.allgather_bf16(own, rank, reps)
+        dp.stream_status()
+        res.append([f32(x) for x in st] + [u16(b) for b in base])
+    for a, b in zip(*res):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))

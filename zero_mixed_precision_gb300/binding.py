@@ -100,6 +100,8 @@ _SIGS = {
     "dpopt_amp_step": ([_PP, _I, _I, _I64, _I, _I64, _P, _P, _P, _P, _F, _F, _F, _F, _F, _F, _P, _P,
                         _PCFG, _P], _I),
     "dpopt_allgather_bf16": ([_P, _I64, _I, _PP, _I, _P], _I),
+    "dpopt_reduce_adam_allgather": ([_PP, _I, _I, _I64, _I, _I64, _P, _P, _P, _PP, _F, _F, _F, _F,
+                                     _I64, _P], _I),
     "dpopt_reduce_adam_buckets_when_ready": ([_PP, _I, _I, _PI64, _PI64, _I64, _PP, _P, _P, _P,
                                               _P, _F, _F, _F, _F, _I64, _P], _I),
     "dpopt_set_kernel_policy": ([_I], _I),
@@ -299,6 +301,18 @@ def dpopt_allgather_bf16(shard_bf16: int, shard_elems: int, shard_rank: int,
     return _lib.dpopt_allgather_bf16(shard_bf16, shard_elems, shard_rank,
                                      _ptr_array(param_replicas) if param_replicas is not None
                                      else None, n_replicas, stream)
+
+
+def dpopt_reduce_adam_allgather(grads: Sequence[int], grad_dtype: int, n_replicas: int,
+                                numel: int, shard_rank: int, bucket_elems: int, master: int,
+                                m: int, v: int, param_replicas: Sequence[int], lr: float,
+                                beta1: float, beta2: float, eps: float, step: int,
+                                stream: int = 0) -> int:
+    return _lib.dpopt_reduce_adam_allgather(
+        _ptr_array(grads) if grads is not None else None, grad_dtype, n_replicas, numel,
+        shard_rank, bucket_elems, master, m, v,
+        _ptr_array(param_replicas) if param_replicas is not None else None, lr, beta1, beta2,
+        eps, step, stream)
 
 
 def dpopt_stream_status(stream: int = 0) -> int:
@@ -552,6 +566,20 @@ def allgather_bf16(shard_bf16, shard_rank: int, param_replicas, stream=None) -> 
                               [_operand(t) for t in param_replicas], len(param_replicas),
                               _stream_handle(stream))
     _check(rc, "dpopt_allgather_bf16")
+
+
+def reduce_adam_allgather(grads, shard_rank: int, bucket_elems: int, master, m, v,
+                          param_replicas, *, lr: float, beta1: float, beta2: float, eps: float,
+                          step: int, stream=None) -> None:
+    """The full-buffer step with the bf16 shard written into every replica's
+    flat parameter tensor (param_replicas[shard_rank] holds the working copy)."""
+    dt = _grad_dtype(grads[0])
+    rc = dpopt_reduce_adam_allgather([_operand(g) for g in grads], dt, len(grads),
+                                     grads[0].numel(), shard_rank, bucket_elems,
+                                     _operand(master), _operand(m), _operand(v),
+                                     [_operand(t) for t in param_replicas], lr, beta1, beta2,
+                                     eps, step, _stream_handle(stream))
+    _check(rc, "dpopt_reduce_adam_allgather")
 
 
 def stream_status(stream=None) -> None:

@@ -982,6 +982,67 @@ int dpopt_allgather_bf16(const void* shard_bf16, int64_t shard_elems, int shard_
   return DPOPT_OK;
 }
 
+int dpopt_reduce_adam_allgather(const void* const* grads, int grad_dtype, int n_replicas,
+                                int64_t numel, int shard_rank, int64_t bucket_elems,
+                                float* master_f32, float* m_f32, float* v_f32,
+                                void* const* param_replicas, float lr, float beta1, float beta2,
+                                float eps, int64_t step, dpopt_stream_t stream) {
+  int rc = check_replicas(n_replicas, grad_dtype);
+  if (rc) return rc;
+  rc = check_hyper(lr, beta1, beta2, eps, step);
+  if (rc) return rc;
+  const void* ptrs[DPOPT_MAX_REPLICAS];
+  int64_t S = 0;
+  if (numel <= 0 || numel % n_replicas != 0)   // nothing to update: arguments checked only
+    return build_full(grads, grad_dtype, n_replicas, numel, shard_rank, bucket_elems, nullptr, 0,
+                      ptrs, &S);
+  if (shard_rank < 0 || shard_rank >= n_replicas)
+    return fail(DPOPT_ERR_INVALID_ARG, "shard_rank must lie in [0, n_replicas)");
+  if (!param_replicas) return fail(DPOPT_ERR_INVALID_ARG, "param_replicas must be non-null");
+  const int64_t shard = numel / n_replicas;
+  const int64_t base = (int64_t)shard_rank * shard;
+  for (int r = 0; r < n_replicas; ++r) {
+    if (!param_replicas[r]) return fail(DPOPT_ERR_INVALID_ARG, "null replica pointer");
+    if ((uintptr_t)param_replicas[r] & 1u)
+      return fail(DPOPT_ERR_INVALID_ARG, "misaligned replica pointer");
+  }
+  // The rank's own replica buffer is the working copy; the others receive it.
+  uint16_t* own = static_cast<uint16_t*>(param_replicas[shard_rank]) + base;
+  Range avoid[4 + DPOPT_MAX_REPLICAS];
+  rc = check_states(master_f32, m_f32, v_f32, own, 0, shard, avoid);
+  if (rc) return rc;
+  int navoid = 4;
+  GatherDst d{};
+  bool dst16 = true;
+  for (int r = 0; r < n_replicas; ++r) {
+    if (r == shard_rank) continue;
+    uint16_t* q = static_cast<uint16_t*>(param_replicas[r]) + base;
+    const Range dr{(uintptr_t)q, (uintptr_t)(q + shard)};
+    for (int j = 0; j < navoid; ++j)
+      if (overlaps(dr, avoid[j]))
+        return fail(DPOPT_ERR_INVALID_ARG, "a replica's destination overlaps a state array or "
+                                           "another replica's destination");
+    avoid[navoid++] = dr;
+    d.dst[d.n++] = q;
+    dst16 = dst16 && aligned16(q);
+  }
+  rc = build_full(grads, grad_dtype, n_replicas, numel, shard_rank, bucket_elems, avoid, navoid,
+                  ptrs, &S);
+  if (rc) return rc;
+  Hyper h = make_hyper(lr, beta1, beta2, eps, step, n_replicas);
+  SegDesc seg{ptrs, 0, S};
+  SmallParams p{};
+  p.h = h;
+  p.master = master_f32; p.m = m_f32; p.v = v_f32; p.out = own;
+  p.n_rep = n_replicas;
+  if (fill_segments(p, &seg, 0, 1, n_replicas, kGroup, grad_dtype) == 0) return DPOPT_OK;
+  if (!dst16) p.seg[0].vec = 0;  // the 16-byte bf16 stores need every destination aligned
+  cudaStream_t st = (cudaStream_t)stream;
+  if (grad_dtype == DPOPT_GRAD_BF16) return launch_step_gather<0>(p, d, st);
+  if (grad_dtype == DPOPT_GRAD_F16) return launch_step_gather<2>(p, d, st);
+  return launch_step_gather<1>(p, d, st);
+}
+
 int dpopt_stream_status(dpopt_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

@@ -26,6 +26,7 @@ constexpr int kBigPtrs = 2048;
 
 using SmallParams = LaunchParams<kSmallSegs, kSmallPtrs>;
 using BigParams = LaunchParams<kBigSegs, kBigPtrs>;
+static_assert(kMaxGatherDst >= DPOPT_MAX_REPLICAS, "a gather table holds every replica");
 static_assert(sizeof(BigParams) <= 32000, "kernel parameters must fit the 32 KB limit");
 
 // One segment as the host sees it.
@@ -49,6 +50,10 @@ inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 // p must hold at least one non-empty segment.
 template <int GK, int MS, int MP>
 int launch_step(const LaunchParams<MS, MP>& p, bool ext, cudaStream_t stream);
+// The plain step that also writes the bf16 copy into every buffer of d (the
+// fused ZeRO-3 all-gather; one segment).
+template <int GK>
+int launch_step_gather(const SmallParams& p, const GatherDst& d, cudaStream_t stream);
 template <int GK, int MS, int MP>
 int launch_amp_step(const LaunchParams<MS, MP>& p, const LossScaleState* state,
                     const double* sqnorm, cudaStream_t stream);

@@ -278,8 +278,32 @@ struct GroupOutT {
       st_stream16(p + 4, hi.x, hi.y, hi.z, hi.w);
     }
   }
+  // the group's 8 bf16 values, packed two to a word
+  __device__ __forceinline__ void put_bf16(uint32_t a, uint32_t b, uint32_t c, uint32_t d) const {
+    st_stream16u(out, a, b, c, d);
+  }
 };
 using GroupOut = GroupOutT<16>;
+
+// Further destinations of the bf16 copy: the step fused with the ZeRO-3
+// all-gather writes the shard's new bf16 values into the same position of
+// every other replica's parameter buffer.  dst[i] points at the shard's first
+// element in replica buffer i.
+constexpr int kMaxGatherDst = 64;
+struct GatherDst {
+  uint16_t* dst[kMaxGatherDst];
+  int32_t n;
+};
+
+template <int W = 16>
+struct GatherOutT : GroupOutT<W> {
+  const GatherDst* gd;
+  int64_t so;  // the group's first shard element
+  __device__ __forceinline__ void put_bf16(uint32_t a, uint32_t b, uint32_t c, uint32_t d) const {
+    st_stream16u(this->out, a, b, c, d);
+    for (int i = 0; i < gd->n; ++i) st_stream16u(gd->dst[i] + so, a, b, c, d);
+  }
+};
 
 // ---------------------------------------------------------------------------
 // one 8-element group, vector path
@@ -356,8 +380,8 @@ __device__ __forceinline__ void group_vec_x1(const Src& src, int n, const Hyper&
   o.put(o.master, make_float4(th[0], th[1], th[2], th[3]), make_float4(th[4], th[5], th[6], th[7]));
   o.put(o.m, make_float4(mm[0], mm[1], mm[2], mm[3]), make_float4(mm[4], mm[5], mm[6], mm[7]));
   o.put(o.v, make_float4(vv[0], vv[1], vv[2], vv[3]), make_float4(vv[4], vv[5], vv[6], vv[7]));
-  st_stream16u(o.out, to_bf16x2(th[0], th[1]), to_bf16x2(th[2], th[3]),
-               to_bf16x2(th[4], th[5]), to_bf16x2(th[6], th[7]));
+  o.put_bf16(to_bf16x2(th[0], th[1]), to_bf16x2(th[2], th[3]), to_bf16x2(th[4], th[5]),
+             to_bf16x2(th[6], th[7]));
 }
 
 // Packed form: 4 element pairs per thread, every operation on f32x2 lanes.
@@ -449,17 +473,17 @@ __device__ __forceinline__ void group_vec_x2(const Src& src, int n, const Hyper&
         make_float4(mm[2].x, mm[2].y, mm[3].x, mm[3].y));
   o.put(o.v, make_float4(vv[0].x, vv[0].y, vv[1].x, vv[1].y),
         make_float4(vv[2].x, vv[2].y, vv[3].x, vv[3].y));
-  st_stream16u(o.out, to_bf16x2(th[0].x, th[0].y), to_bf16x2(th[1].x, th[1].y),
-               to_bf16x2(th[2].x, th[2].y), to_bf16x2(th[3].x, th[3].y));
+  o.put_bf16(to_bf16x2(th[0].x, th[0].y), to_bf16x2(th[1].x, th[1].y),
+             to_bf16x2(th[2].x, th[2].y), to_bf16x2(th[3].x, th[3].y));
 }
 
 // ---------------------------------------------------------------------------
 // a partial or unaligned group, one element at a time
 // ---------------------------------------------------------------------------
 
-template <int GK, bool EXT, class LP, class SegT>
+template <int GK, bool EXT, bool GATHER, class LP, class SegT>
 __device__ __noinline__ void group_scalar(const LP& p, const Hyper& h, const SegT& sg, int64_t e0,
-                                          int count, float gscale) {
+                                          int count, float gscale, const GatherDst* gd) {
   const void* const* gp = p.gptr + sg.ptr_base;
   const int n = p.n_rep;
   for (int k = 0; k < count; ++k) {
@@ -475,7 +499,10 @@ __device__ __noinline__ void group_scalar(const LP& p, const Hyper& h, const Seg
     p.master[so] = th;
     p.m[so] = mm;
     p.v[so] = vv;
-    p.out[so] = to_bf16(th);
+    const uint16_t b = to_bf16(th);
+    p.out[so] = b;
+    if constexpr (GATHER)
+      for (int i = 0; i < gd->n; ++i) gd->dst[i][so] = b;
   }
 }
 
@@ -512,8 +539,9 @@ constexpr int wide_ctas() { return (NR == 1 && GK != 1) ? 4 : 3; }
 // width of one state access (32: one 256-bit access per array, for segments
 // of vector level 2; 16: two 16-byte accesses, level >= 1); other groups go
 // one element at a time.
-template <int NR, int GK, int PACK, bool EXT, int W, class LP>
-__device__ __forceinline__ void step_loop(const LP& p, const Hyper& h, float gscale) {
+template <int NR, int GK, int PACK, bool EXT, int W, bool GATHER = false, class LP>
+__device__ __forceinline__ void step_loop(const LP& p, const Hyper& h, float gscale,
+                                          const GatherDst* gd = nullptr) {
   constexpr int kLevel = W == 32 ? 2 : 1;
   const uint64_t pol = evict_first_policy();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -528,11 +556,18 @@ __device__ __forceinline__ void step_loop(const LP& p, const Hyper& h, float gsc
     if (sg.vec >= kLevel && rem >= kGroup) {
       const GlobalSource<GK, W> src{p.gptr + sg.ptr_base, e0,
                                     {p.master + so, p.m + so, p.v + so}, pol};
-      const GroupOutT<W> o{p.master + so, p.m + so, p.v + so, p.out + so};
-      if constexpr (PACK) group_vec_x2<NR, GK, EXT>(src, p.n_rep, h, o, gscale);
-      else group_vec_x1<NR, GK, EXT>(src, p.n_rep, h, o, gscale);
+      if constexpr (GATHER) {
+        const GatherOutT<W> o{{p.master + so, p.m + so, p.v + so, p.out + so}, gd, so};
+        if constexpr (PACK) group_vec_x2<NR, GK, EXT>(src, p.n_rep, h, o, gscale);
+        else group_vec_x1<NR, GK, EXT>(src, p.n_rep, h, o, gscale);
+      } else {
+        const GroupOutT<W> o{p.master + so, p.m + so, p.v + so, p.out + so};
+        if constexpr (PACK) group_vec_x2<NR, GK, EXT>(src, p.n_rep, h, o, gscale);
+        else group_vec_x1<NR, GK, EXT>(src, p.n_rep, h, o, gscale);
+      }
     } else {
-      group_scalar<GK, EXT>(p, h, sg, e0, (int)(rem < kGroup ? rem : kGroup), gscale);
+      group_scalar<GK, EXT, GATHER>(p, h, sg, e0, (int)(rem < kGroup ? rem : kGroup), gscale,
+                                    gd);
     }
   }
 }
@@ -545,6 +580,17 @@ __global__ void __launch_bounds__(kThreads, W == 32 ? wide_ctas<NR, GK>() : min_
     reduce_adam_ldg_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p) {
   const float gscale = EXT ? grad_scale_of(p.h) : 1.f;
   step_loop<NR, GK, PACK, EXT, W>(p, p.h, gscale);
+}
+
+// The plain step fused with the ZeRO-3 parameter all-gather: the bf16 copy
+// goes to p.out (the rank's own replica buffer) and to every buffer of d.
+// One pass instead of a step and a broadcast that reads the copy back:
+// 4N + 24 bytes per parameter instead of 4N + 28, one launch instead of two.
+template <int NR, int GK, int PACK, int W, int MAXSEG, int MAXPTR>
+__global__ void __launch_bounds__(kThreads, W == 32 ? wide_ctas<NR, GK>() : min_ctas<NR, PACK>())
+    reduce_adam_gather_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p,
+                              const __grid_constant__ GatherDst d) {
+  step_loop<NR, GK, PACK, false, W, true>(p, p.h, 1.f, &d);
 }
 
 // ---------------------------------------------------------------------------

@@ -119,6 +119,32 @@ int step_n(const LaunchParams<MS, MP>& p, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------
+// the step fused with the ZeRO-3 all-gather (one segment: the full-buffer call)
+// ---------------------------------------------------------------------------
+
+template <int NR, int PACK, int W>
+int gather_kernel(const SmallParams& p, const GatherDst& d, cudaStream_t stream) {
+  auto kern = reduce_adam_gather_kernel<NR, kGK, PACK, W, kSmallSegs, kSmallPtrs>;
+  static std::atomic<int> per_sm{0};
+  unsigned grid = 0;
+  int rc = persistent_grid(kern, per_sm, (p.total_groups + kThreads - 1) / kThreads, &grid);
+  if (rc) return rc;
+  kern<<<grid, kThreads, 0, stream>>>(p, d);
+  return launched();
+}
+
+// The same kernel forms as the plain step (widths by wide_states()).
+template <int NR>
+int gather_nr(const SmallParams& p, const GatherDst& d, cudaStream_t s) {
+  if constexpr (wide_states(NR)) {
+    if (all_wide(p)) return gather_kernel<NR, 0, 32>(p, d, s);
+    return gather_kernel<0, 1, 16>(p, d, s);
+  } else {
+    return gather_kernel<NR, 0, 16>(p, d, s);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // the loss-scaled step
 // ---------------------------------------------------------------------------
 
@@ -205,6 +231,22 @@ int launch_amp_step(const LaunchParams<MS, MP>& p, const LossScaleState* state,
   }
 }
 
+template <int G>
+int launch_step_gather(const SmallParams& p, const GatherDst& d, cudaStream_t stream) {
+  static_assert(G == kGK, "launch_step_gather instantiated for another gradient type");
+  switch (p.n_rep) {
+    case 1: return DPOPT_GK_NS::gather_nr<1>(p, d, stream);
+    case 2: return DPOPT_GK_NS::gather_nr<2>(p, d, stream);
+    case 3: return DPOPT_GK_NS::gather_nr<3>(p, d, stream);
+    case 4: return DPOPT_GK_NS::gather_nr<4>(p, d, stream);
+    case 5: return DPOPT_GK_NS::gather_nr<5>(p, d, stream);
+    case 6: return DPOPT_GK_NS::gather_nr<6>(p, d, stream);
+    case 7: return DPOPT_GK_NS::gather_nr<7>(p, d, stream);
+    case 8: return DPOPT_GK_NS::gather_nr<8>(p, d, stream);
+    default: return DPOPT_GK_NS::gather_kernel<0, 1, 16>(p, d, stream);
+  }
+}
+
 template <int G, int MS, int MP>
 int launch_sqnorm_pass(const LaunchParams<MS, MP>& p, double* partials, int64_t nchunks,
                        bool store_average, cudaStream_t stream) {
@@ -216,6 +258,7 @@ int launch_sqnorm_pass(const LaunchParams<MS, MP>& p, double* partials, int64_t 
 
 template int launch_step<kGK>(const SmallParams&, bool, cudaStream_t);
 template int launch_step<kGK>(const BigParams&, bool, cudaStream_t);
+template int launch_step_gather<kGK>(const SmallParams&, const GatherDst&, cudaStream_t);
 template int launch_amp_step<kGK>(const SmallParams&, const LossScaleState*, const double*,
                                   cudaStream_t);
 template int launch_sqnorm_pass<kGK>(const SmallParams&, double*, int64_t, bool, cudaStream_t);

@@ -220,7 +220,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       for (int j = blockIdx.x; j < p.nseg; j += gridDim.x) {
         const TmaSeg& sg = p.seg[j];
         if (sg.len > sg.body)
-          group_scalar<GK, false>(p, p.h, sg, sg.body, (int)(sg.len - sg.body), 1.f);
+          group_scalar<GK, false, false>(p, p.h, sg, sg.body, (int)(sg.len - sg.body), 1.f,
+                                        nullptr);
       }
     }
   }
