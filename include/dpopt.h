@@ -85,7 +85,10 @@ typedef enum {
     DPOPT_ERR_INVALID_ARG = 1, /* a null/overlapping pointer, a size or hyper-parameter out of range */
     DPOPT_ERR_UNSUPPORTED = 2, /* valid but beyond this build's limits (n_replicas > DPOPT_MAX_REPLICAS) */
     DPOPT_ERR_CUDA = 3,        /* a CUDA call failed; dpopt_last_error() has its message */
-    DPOPT_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up (reported by dpopt_stream_status) */
+    DPOPT_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (reported by dpopt_stream_status) */
+    DPOPT_ERR_BOUNDS = 5       /* bounds-checked build only: a kernel derived an index outside
+                                  its ranges and skipped the access (reported by
+                                  dpopt_stream_status) */
 } dpopt_status;
 
 typedef enum {
@@ -416,8 +419,23 @@ int dpopt_reduce_adam_buckets_when_ready(const void *const *slice_table, int gra
 
 /* Wait for `stream`, then return and clear the current device's status word:
  * DPOPT_OK, or DPOPT_ERR_TIMEOUT if a bounded device-side wait gave up since the
- * last call, or DPOPT_ERR_CUDA if the wait itself failed. */
+ * last call, or DPOPT_ERR_CUDA if the wait itself failed; in the bounds-checked
+ * build also DPOPT_ERR_BOUNDS if a kernel's index check failed since the last
+ * call. */
 int dpopt_stream_status(dpopt_stream_t stream);
+
+/* The bounds-checked build (libdpopt_bounds.so: the same sources compiled with
+ * -DDPOPT_DEBUG_BOUNDS; dpopt_version() ends in "+bounds") is the library's
+ * stand-in for a memory checker.  Before each access whose index a kernel
+ * derives from its launch tables (segment, element offset, state span) it tests
+ * the index against the segment's length and the call's span of shard elements;
+ * a failed test skips the access and sets a device word that
+ * dpopt_stream_status() reports as DPOPT_ERR_BOUNDS.  Results are otherwise
+ * bitwise those of the release build, which compiles the tests away.
+ * dpopt_selftest_bounds enqueues a kernel whose check fails on purpose (it
+ * touches no memory), so that a test can see the report arrive: DPOPT_OK in the
+ * bounds-checked build, DPOPT_ERR_UNSUPPORTED in the release build. */
+int dpopt_selftest_bounds(dpopt_stream_t stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char *dpopt_status_string(int status);

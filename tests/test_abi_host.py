@@ -50,8 +50,24 @@ def test_header_compiles_standalone(lang, tmp_path):
 
 def test_status_strings(dp):
     for code, name in ((0, "DPOPT_OK"), (1, "DPOPT_ERR_INVALID_ARG"), (2, "DPOPT_ERR_UNSUPPORTED"),
-                       (3, "DPOPT_ERR_CUDA"), (4, "DPOPT_ERR_TIMEOUT"), (99, "DPOPT_UNKNOWN_STATUS")):
+                       (3, "DPOPT_ERR_CUDA"), (4, "DPOPT_ERR_TIMEOUT"), (5, "DPOPT_ERR_BOUNDS"),
+                       (99, "DPOPT_UNKNOWN_STATUS")):
         assert dp.dpopt_status_string(code) == name
+
+
+def test_bounds_checked_build_exports_the_same_interface(dp):
+    """The bounds-checked variant is the same interface: every declared symbol,
+    the same status strings, a version marked "+bounds"; the release build
+    refuses the bounds self-test (it has no checks)."""
+    lib = ctypes.CDLL(dp.binding._build.lib_path("bounds"))
+    for n in _declared():
+        assert hasattr(lib, n), n
+    lib.dpopt_version.restype = ctypes.c_char_p
+    lib.dpopt_status_string.restype = ctypes.c_char_p
+    assert lib.dpopt_version().decode().endswith("+bounds")
+    assert lib.dpopt_status_string(5).decode() == "DPOPT_ERR_BOUNDS"
+    assert not dp.dpopt_version().endswith("+bounds")
+    assert dp.dpopt_selftest_bounds(0) == dp.DPOPT_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("row", [r for r in _golden_rows() if r[4] == "total"],

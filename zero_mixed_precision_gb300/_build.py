@@ -17,6 +17,17 @@ LIB_DIR = os.path.join(PKG, "lib")
 OBJ_DIR = os.path.join(LIB_DIR, "obj")
 LIB_PATH = os.path.join(LIB_DIR, "libdpopt.so")
 
+# Library variants: the release build, and the bounds-checked build whose
+# kernels test every derived index before the access (-DDPOPT_DEBUG_BOUNDS).
+VARIANTS = {
+    "release": ("libdpopt.so", "obj", []),
+    "bounds": ("libdpopt_bounds.so", "obj_bounds", ["-DDPOPT_DEBUG_BOUNDS"]),
+}
+
+
+def lib_path(variant: str = "release") -> str:
+    return os.path.join(LIB_DIR, VARIANTS[variant][0])
+
 # (object name, source, extra flags)
 UNITS = [
     ("dpopt", "dpopt.cu", []),
@@ -38,34 +49,36 @@ NVCC_FLAGS = [
 ]
 
 
-def object_path(name: str) -> str:
-    return os.path.join(OBJ_DIR, name + ".o")
+def object_path(name: str, variant: str = "release") -> str:
+    return os.path.join(LIB_DIR, VARIANTS[variant][1], name + ".o")
 
 
-def compile_command(name: str, src: str, extra: list[str]) -> list[str]:
-    return ["nvcc", *NVCC_FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c",
-            os.path.join(CSRC, src), "-o", object_path(name)]
+def compile_command(name: str, src: str, extra: list[str], variant: str = "release") -> list[str]:
+    os.makedirs(os.path.join(LIB_DIR, VARIANTS[variant][1]), exist_ok=True)
+    return ["nvcc", *NVCC_FLAGS, *VARIANTS[variant][2], *extra, "-I", INCLUDE, "-I", CSRC, "-c",
+            os.path.join(CSRC, src), "-o", object_path(name, variant)]
 
 
-def link_command() -> list[str]:
-    return ["nvcc", *ARCH, "-shared", *[object_path(n) for n, _, _ in UNITS], "-o", LIB_PATH]
+def link_command(variant: str = "release") -> list[str]:
+    return ["nvcc", *ARCH, "-shared", *[object_path(n, variant) for n, _, _ in UNITS], "-o",
+            lib_path(variant)]
 
 
-def stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def stale(variant: str = "release") -> bool:
+    path = lib_path(variant)
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return any(os.path.getmtime(f) > t for f in DEPENDS)
 
 
-def build(force: bool = False) -> str:
-    os.makedirs(OBJ_DIR, exist_ok=True)
-    if force or stale():
+def build(force: bool = False, variant: str = "release") -> str:
+    if force or stale(variant):
         with ThreadPoolExecutor(max_workers=len(UNITS)) as ex:
-            procs = list(ex.map(lambda u: subprocess.run(compile_command(*u), capture_output=True,
-                                                         text=True), UNITS))
+            procs = list(ex.map(lambda u: subprocess.run(compile_command(*u, variant=variant),
+                                                         capture_output=True, text=True), UNITS))
         for (name, _, _), pr in zip(UNITS, procs):
             if pr.returncode != 0:
                 raise RuntimeError(f"nvcc failed for {name}:\n{pr.stdout}{pr.stderr}")
-        subprocess.run(link_command(), check=True)
-    return LIB_PATH
+        subprocess.run(link_command(variant), check=True)
+    return lib_path(variant)

@@ -20,6 +20,7 @@ DPOPT_ERR_INVALID_ARG = 1
 DPOPT_ERR_UNSUPPORTED = 2
 DPOPT_ERR_CUDA = 3
 DPOPT_ERR_TIMEOUT = 4
+DPOPT_ERR_BOUNDS = 5
 DPOPT_GRAD_BF16 = 0
 DPOPT_GRAD_F32 = 1
 DPOPT_GRAD_F16 = 2
@@ -28,7 +29,13 @@ DPOPT_KERNEL_AUTO = 0
 DPOPT_KERNEL_DIRECT = 1
 DPOPT_KERNEL_BULK = 2
 
-LIB_PATH = _build.LIB_PATH
+# DPOPT_LIB_VARIANT=bounds loads the bounds-checked build of the same sources
+# (every kernel tests its derived indices; failures are reported as
+# DPOPT_ERR_BOUNDS by dpopt_stream_status); unset or "release": the release build.
+LIB_VARIANT = os.environ.get("DPOPT_LIB_VARIANT", "release")
+if LIB_VARIANT not in _build.VARIANTS:
+    raise ImportError(f"DPOPT_LIB_VARIANT={LIB_VARIANT!r}: expected one of {sorted(_build.VARIANTS)}")
+LIB_PATH = _build.lib_path(LIB_VARIANT)
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -107,6 +114,7 @@ _SIGS = {
     "dpopt_set_kernel_policy": ([_I], _I),
     "dpopt_get_kernel_policy": ([], _I),
     "dpopt_selftest_wait_timeout": ([_I64, _P], _I),
+    "dpopt_selftest_bounds": ([_P], _I),
 }
 
 for _name, (_args, _res) in _SIGS.items():
@@ -317,6 +325,10 @@ def dpopt_reduce_adam_allgather(grads: Sequence[int], grad_dtype: int, n_replica
 
 def dpopt_stream_status(stream: int = 0) -> int:
     return _lib.dpopt_stream_status(stream)
+
+
+def dpopt_selftest_bounds(stream: int = 0) -> int:
+    return _lib.dpopt_selftest_bounds(stream)
 
 
 def dpopt_status_string(status: int) -> str:

@@ -45,6 +45,34 @@ struct DeviceCache {
 };
 DeviceCache g_dev;
 
+#ifdef DPOPT_DEBUG_BOUNDS
+// Bounds-checked build: the word every failed index check sets (bit 0), read
+// and cleared by dpopt_stream_status().  Its device address is looked up once
+// per device; the kernels receive it in their Hyper block.
+__device__ unsigned int g_bounds_status;
+std::once_flag g_bounds_once[kMaxDevices];
+unsigned int* g_bounds_addr[kMaxDevices];
+cudaError_t g_bounds_err[kMaxDevices];
+
+unsigned int* bounds_status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::call_once(g_bounds_once[dev], [dev] {
+    void* ptr = nullptr;
+    g_bounds_err[dev] = cudaGetSymbolAddress(&ptr, g_bounds_status);
+    g_bounds_addr[dev] = static_cast<unsigned int*>(ptr);
+  });
+  return g_bounds_err[dev] == cudaSuccess ? g_bounds_addr[dev] : nullptr;
+}
+
+__global__ void bounds_selftest_kernel(Hyper h, int64_t len) {
+  // an index one past the end: the check fails, sets the word, and nothing
+  // is accessed
+  const int64_t idx = len;
+  (void)dbg_ok(h, idx < len);
+}
+#endif
+
 }  // namespace
 
 int fail(int code, const char* fmt, ...) {
@@ -80,6 +108,17 @@ namespace {
 
 bool is_finite(float x) { return std::isfinite(x); }
 
+// The span of shard elements a call may touch, for the bounds-checked build's
+// kernels (a no-op in a release build).
+void set_span(Hyper& h, int64_t lo, int64_t hi) {
+#ifdef DPOPT_DEBUG_BOUNDS
+  h.dbg_lo = lo;
+  h.dbg_hi = hi;
+#else
+  (void)h; (void)lo; (void)hi;
+#endif
+}
+
 // Scalars of step t, in fp64 on the host, split into fp32 pairs.
 Hyper make_hyper(float lr, float beta1, float beta2, float eps, int64_t step, int n) {
   Hyper h{};
@@ -106,6 +145,11 @@ Hyper make_hyper(float lr, float beta1, float beta2, float eps, int64_t step, in
   h.unscale = 1.f;
   h.lr = lr;
   h.scale_dev = nullptr;
+#ifdef DPOPT_DEBUG_BOUNDS
+  h.dbg_status = bounds_status_word();
+  h.dbg_lo = 0;
+  h.dbg_hi = INT64_MAX;
+#endif
   return h;
 }
 
@@ -455,6 +499,7 @@ int full_impl(const void* const* grads, int grad_dtype, int n_replicas, int64_t 
     // contiguously, so the whole shard is one segment: bucket_elems changes
     // neither the addresses nor the result, only what the iterator reports.
     SegDesc seg{ptrs, 0, S};
+    set_span(h, 0, S);
     return run(&seg, 1, grad_dtype, n_replicas, master, m, v, out, h, ext, stream);
   }
   const void* ptrs[DPOPT_MAX_REPLICAS];
@@ -484,6 +529,7 @@ int buckets_impl(const void* const* slice_table, int grad_dtype, int n_replicas,
   if (rc) return rc;
   rc = check_bucket_grads(segs, n_replicas, grad_dtype, st, 4);
   if (rc) return rc;
+  set_span(h, lo, hi);
   return run(segs.data(), (int)segs.size(), grad_dtype, n_replicas, master, m, v, out, h, ext,
              stream);
 }
@@ -546,6 +592,7 @@ int full_norm_impl(const void* const* grads, int grad_dtype, int n_replicas, int
   Hyper h = make_hyper(1.f, 0.f, 0.f, 0.f, 1, n_replicas);
   h.unscale = grad_unscale == 0.f ? 1.f : grad_unscale;
   if (state) h.scale_dev = &state->scale;
+  set_span(h, 0, S);
   SegDesc seg{ptrs, 0, S};
   return run_sqnorm(&seg, 1, grad_dtype, n_replicas, h, (double*)scratch, sqnorm_out, stream,
                     avg_out);
@@ -783,6 +830,7 @@ int dpopt_grad_sqnorm_buckets(const void* const* slice_table, int grad_dtype, in
   if (segs.empty()) return finish_empty_norm(sqnorm_out, (cudaStream_t)stream);
   Hyper h = make_hyper(1.f, 0.f, 0.f, 0.f, 1, n_replicas);
   h.unscale = grad_unscale == 0.f ? 1.f : grad_unscale;
+  set_span(h, lo, hi);
   return run_sqnorm(segs.data(), (int)segs.size(), grad_dtype, n_replicas, h, (double*)scratch,
                     sqnorm_out, (cudaStream_t)stream);
 }
@@ -869,6 +917,7 @@ int dpopt_amp_step(const void* const* grads, int grad_dtype, int n_replicas, int
     return launch_scale_update((LossScaleState*)state, global_sqnorm, c, (cudaStream_t)stream);
   }
   const int64_t S = numel / n_replicas;
+  set_span(h, 0, S);
   Range st[5];
   rc = check_states(master_f32, m_f32, v_f32, param_bf16_out, 0, S, st);
   if (rc) return rc;
@@ -915,7 +964,8 @@ int dpopt_reduce_adam_buckets_when_ready(const void* const* slice_table, int gra
   if (rc) return rc;
   rc = check_bucket_grads(segs, n_replicas, grad_dtype, st, 4);
   if (rc) return rc;
-  const Hyper h = make_hyper(lr, beta1, beta2, eps, step, n_replicas);
+  Hyper h = make_hyper(lr, beta1, beta2, eps, step, n_replicas);
+  set_span(h, lo, hi);
   // one launch per bucket, each behind its own readiness event, in bucket order
   size_t si = 0;
   for (int64_t b = 0; b < n_buckets; ++b) {
@@ -945,6 +995,9 @@ int dpopt_allgather_bf16(const void* shard_bf16, int64_t shard_elems, int shard_
     return fail(DPOPT_ERR_INVALID_ARG, "shard_bf16 and param_replicas must be non-null");
   if ((uintptr_t)shard_bf16 & 1u) return fail(DPOPT_ERR_INVALID_ARG, "misaligned shard pointer");
   GatherParams p{};
+#ifdef DPOPT_DEBUG_BOUNDS
+  p.dbg_status = bounds_status_word();
+#endif
   p.src = static_cast<const uint16_t*>(shard_bf16);
   p.len = shard_elems;
   const uintptr_t bytes = (uintptr_t)shard_elems * 2u;
@@ -1030,6 +1083,7 @@ int dpopt_reduce_adam_allgather(const void* const* grads, int grad_dtype, int n_
                   ptrs, &S);
   if (rc) return rc;
   Hyper h = make_hyper(lr, beta1, beta2, eps, step, n_replicas);
+  set_span(h, 0, S);
   SegDesc seg{ptrs, 0, S};
   SmallParams p{};
   p.h = h;
@@ -1049,7 +1103,34 @@ int dpopt_stream_status(dpopt_stream_t stream) {
   bool timed_out = false;
   const int rc = take_wait_status(&timed_out);
   if (rc) return rc;
-  return timed_out ? DPOPT_ERR_TIMEOUT : DPOPT_OK;
+  if (timed_out) return DPOPT_ERR_TIMEOUT;
+#ifdef DPOPT_DEBUG_BOUNDS
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_bounds_status, sizeof word);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol");
+  if (word) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_bounds_status, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
+    return fail(DPOPT_ERR_BOUNDS, "a kernel's index check failed (bounds-checked build)");
+  }
+#endif
+  return DPOPT_OK;
+}
+
+int dpopt_selftest_bounds(dpopt_stream_t stream) {
+#ifdef DPOPT_DEBUG_BOUNDS
+  Hyper h = make_hyper(1.f, 0.f, 0.f, 0.f, 1, 1);
+  if (!h.dbg_status) return fail(DPOPT_ERR_CUDA, "no device address for the bounds status word");
+  bounds_selftest_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(h, 1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  ++g_launches;
+  return DPOPT_OK;
+#else
+  (void)stream;
+  return fail(DPOPT_ERR_UNSUPPORTED, "index checks exist in the bounds-checked build only");
+#endif
 }
 
 const char* dpopt_status_string(int status) {
@@ -1059,6 +1140,7 @@ const char* dpopt_status_string(int status) {
     case DPOPT_ERR_UNSUPPORTED: return "DPOPT_ERR_UNSUPPORTED";
     case DPOPT_ERR_CUDA: return "DPOPT_ERR_CUDA";
     case DPOPT_ERR_TIMEOUT: return "DPOPT_ERR_TIMEOUT";
+    case DPOPT_ERR_BOUNDS: return "DPOPT_ERR_BOUNDS";
     default: return "DPOPT_UNKNOWN_STATUS";
   }
 }
@@ -1096,6 +1178,12 @@ int dpopt_selftest_wait_timeout(int64_t limit_cycles, dpopt_stream_t stream) {
   return launch_selftest_wait((long long)limit_cycles, (cudaStream_t)stream);
 }
 
-const char* dpopt_version(void) { return "0.1.0"; }
+const char* dpopt_version(void) {
+#ifdef DPOPT_DEBUG_BOUNDS
+  return "0.1.0+bounds";
+#else
+  return "0.1.0";
+#endif
+}
 
 }  // extern "C"

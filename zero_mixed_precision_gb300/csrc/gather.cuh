@@ -20,6 +20,9 @@ struct GatherParams {
   int64_t len;                           // elements
   int32_t n_dst;
   int32_t vec;                           // every pointer 16-byte aligned
+#ifdef DPOPT_DEBUG_BOUNDS
+  unsigned int* dbg_status;              // set when an index check fails (see dbg_ok)
+#endif
 };
 
 __global__ void __launch_bounds__(kThreads) allgather_bf16_kernel(const __grid_constant__ GatherParams p) {
@@ -28,6 +31,12 @@ __global__ void __launch_bounds__(kThreads) allgather_bf16_kernel(const __grid_c
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < groups; gi += stride) {
     const int64_t e0 = gi * kGroup;
+#ifdef DPOPT_DEBUG_BOUNDS
+    if (e0 < 0 || e0 >= p.len) {
+      if (p.dbg_status) atomicOr(p.dbg_status, 1u);
+      continue;
+    }
+#endif
     if (p.vec && e0 + kGroup <= p.len) {
       const uint4 w = ld_grad16(p.src + e0, pol);
       for (int r = 0; r < p.n_dst; ++r) st_stream16u(p.dst[r] + e0, w.x, w.y, w.z, w.w);

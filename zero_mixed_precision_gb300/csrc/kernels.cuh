@@ -484,6 +484,9 @@ __device__ __forceinline__ void group_vec_x2(const Src& src, int n, const Hyper&
 template <int GK, bool EXT, bool GATHER, class LP, class SegT>
 __device__ __noinline__ void group_scalar(const LP& p, const Hyper& h, const SegT& sg, int64_t e0,
                                           int count, float gscale, const GatherDst* gd) {
+  if (!dbg_ok(h, e0 >= 0 && count >= 0 && e0 + count <= sg.len) ||
+      !dbg_span(h, sg.state_off + e0, sg.state_off + e0 + count))
+    return;
   const void* const* gp = p.gptr + sg.ptr_base;
   const int n = p.n_rep;
   for (int k = 0; k < count; ++k) {
@@ -553,6 +556,9 @@ __device__ __forceinline__ void step_loop(const LP& p, const Hyper& h, float gsc
     const int64_t e0 = (gi - sg.first_group) * kGroup;
     const int64_t rem = sg.len - e0;
     const int64_t so = sg.state_off + e0;
+    if (!dbg_ok(h, si < p.nseg && e0 >= 0 && rem > 0) ||
+        !dbg_span(h, so, so + (rem < kGroup ? rem : kGroup)))
+      continue;
     if (sg.vec >= kLevel && rem >= kGroup) {
       const GlobalSource<GK, W> src{p.gptr + sg.ptr_base, e0,
                                     {p.master + so, p.m + so, p.v + so}, pol};

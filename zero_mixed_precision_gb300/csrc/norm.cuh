@@ -65,6 +65,10 @@ __global__ void __launch_bounds__(kThreads, NR > 0 ? (NR <= 4 ? 5 : 4) : 2)
       const int64_t e0 = c0 + (int64_t)k * kGroup;
       if (e0 >= sg.len) break;
       const int64_t rem = sg.len - e0;
+      if (!dbg_ok(p.h, si < p.nseg && e0 >= 0) ||
+          (STORE && !dbg_span(p.h, sg.state_off + e0,
+                              sg.state_off + e0 + (rem < kGroup ? rem : kGroup))))
+        break;
       float g[kGroup];
       int cnt = kGroup;
       float* const avg = STORE ? p.master + sg.state_off + e0 : nullptr;

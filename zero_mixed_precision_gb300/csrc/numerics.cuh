@@ -49,7 +49,33 @@ struct Hyper {
   float unscale;         // multiplier applied first (1/loss scale; 1 when unused)
   float lr;              // learning rate (for bias corrections formed on the device)
   const float* scale_dev;  // device loss scale: the norm pre-pass unscales by 1/*scale_dev
+#ifdef DPOPT_DEBUG_BOUNDS
+  // bounds-checked builds only: the status word a failed index check sets, and
+  // the span [dbg_lo, dbg_hi) of shard elements the call may touch
+  unsigned int* dbg_status;
+  int64_t dbg_lo, dbg_hi;
+#endif
 };
+
+// Index checks of the bounds-checked build (-DDPOPT_DEBUG_BOUNDS).  A kernel
+// asks dbg_ok(h, cond) before every access whose index it derived from the
+// launch's tables; a false condition sets bit 0 of *h.dbg_status and the
+// caller skips the access, so a wrong index is reported by
+// dpopt_stream_status() as DPOPT_ERR_BOUNDS instead of touching memory.  In a
+// release build dbg_ok is the constant true and compiles away.
+#ifdef DPOPT_DEBUG_BOUNDS
+__device__ __forceinline__ bool dbg_ok(const Hyper& h, bool cond) {
+  if (!cond && h.dbg_status) atomicOr(h.dbg_status, 1u);
+  return cond;
+}
+// [lo, hi) of shard elements lies inside the call's span
+__device__ __forceinline__ bool dbg_span(const Hyper& h, int64_t lo, int64_t hi) {
+  return dbg_ok(h, lo >= h.dbg_lo && lo <= hi && hi <= h.dbg_hi);
+}
+#else
+__device__ __forceinline__ constexpr bool dbg_ok(const Hyper&, bool) { return true; }
+__device__ __forceinline__ constexpr bool dbg_span(const Hyper&, int64_t, int64_t) { return true; }
+#endif
 
 // The extended step's gradient multiplier: c = unscale * min(1, max_norm /
 // (sqrt(sqnorm) + 1e-6)), evaluated in fp64 and rounded once to fp32.

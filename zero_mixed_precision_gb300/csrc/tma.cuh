@@ -170,15 +170,21 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         const uint32_t cnt = (uint32_t)(left < kTmaTile ? left : kTmaTile);
         const uint32_t sb = smem0 + (uint32_t)s * p.stage_bytes;
         const uint32_t fb = smem_u32(&full_bar[s]);
-        mbar_arrive_expect_tx(fb, cnt * ((uint32_t)n * gsize + 12u));
-        const void* const* gp = p.gptr + sg.ptr_base;
-        for (int r = 0; r < n; ++r)
-          bulk_g2s(sb + (uint32_t)r * row_bytes,
-                   static_cast<const unsigned char*>(gp[r]) + e0 * gsize, cnt * gsize, fb, pol);
         const int64_t so = sg.state_off + e0;
-        bulk_g2s(sb + state_base, p.master + so, cnt * 4u, fb, pol);
-        bulk_g2s(sb + state_base + kTmaTile * 4u, p.m + so, cnt * 4u, fb, pol);
-        bulk_g2s(sb + state_base + kTmaTile * 8u, p.v + so, cnt * 4u, fb, pol);
+        // (a tile that fails the bounds-checked build's test is armed without
+        // copies: its phase completes on the arrival alone)
+        const bool good = dbg_ok(p.h, si < p.nseg && e0 >= 0 && left > 0) &&
+                          dbg_span(p.h, so, so + cnt);
+        mbar_arrive_expect_tx(fb, good ? cnt * ((uint32_t)n * gsize + 12u) : 0u);
+        if (good) {
+          const void* const* gp = p.gptr + sg.ptr_base;
+          for (int r = 0; r < n; ++r)
+            bulk_g2s(sb + (uint32_t)r * row_bytes,
+                     static_cast<const unsigned char*>(gp[r]) + e0 * gsize, cnt * gsize, fb, pol);
+          bulk_g2s(sb + state_base, p.master + so, cnt * 4u, fb, pol);
+          bulk_g2s(sb + state_base + kTmaTile * 4u, p.m + so, cnt * 4u, fb, pol);
+          bulk_g2s(sb + state_base + kTmaTile * 8u, p.v + so, cnt * 4u, fb, pol);
+        }
       }
       // drain: the last phase armed on every stage must complete before this
       // thread leaves (the copies write into this CTA's shared memory)
@@ -203,7 +209,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       const int64_t e0 = (t - sg.first_tile) * kTmaTile;
       const int64_t left = sg.body - e0;
       const int cnt = (int)(left < kTmaTile ? left : kTmaTile);
-      if (c * kGroup < cnt) {
+      const bool good = dbg_ok(p.h, si < p.nseg && e0 >= 0 && left > 0) &&
+                        dbg_span(p.h, sg.state_off + e0, sg.state_off + e0 + cnt);
+      if (good && c * kGroup < cnt) {
         const uint32_t sb = smem0 + (uint32_t)s * p.stage_bytes;
         const uint32_t sx = sb + state_base + (uint32_t)c * 32u;
         const SharedSource<GK> src{sb + (uint32_t)c * kGroup * gsize, row_bytes,
