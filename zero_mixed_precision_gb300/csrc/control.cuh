@@ -8,6 +8,7 @@
 namespace dpopt {
 
 __global__ void loss_scale_init_kernel(LossScaleState* st, LossScaleConfig cfg) {
+  pdl_enter();
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   LossScaleState s;
   s.scale = cfg.init_scale;
@@ -24,6 +25,7 @@ __global__ void loss_scale_init_kernel(LossScaleState* st, LossScaleConfig cfg) 
 // steps in a row.
 __global__ void loss_scale_update_kernel(LossScaleState* st, const double* sqnorm,
                                          LossScaleConfig cfg) {
+  pdl_enter();
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   LossScaleState s = *st;
   const bool overflow = !isfinite(*sqnorm);
@@ -56,6 +58,7 @@ constexpr int kFinishThreads = 1024;
 __global__ void __launch_bounds__(kFinishThreads)
     sqnorm_finish_kernel(const DFloat* partials, int64_t nchunks, double* out) {
   __shared__ DFloat warp_sum[kFinishThreads / 32];
+  pdl_enter();
   DFloat acc{0.f, 0.f};
   for (int64_t c = threadIdx.x; c < nchunks; c += kFinishThreads) acc = df_add(acc, partials[c]);
 #pragma unroll

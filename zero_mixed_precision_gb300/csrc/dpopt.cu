@@ -362,9 +362,9 @@ int run_sqnorm(const SegDesc* segs, int nsegs, int grad_dtype, int n, const Hype
     done += chunks;
   }
   // each chunk's partial is a double-float pair in its 8-byte slot
-  sqnorm_finish_kernel<<<1, kFinishThreads, 0, stream>>>(reinterpret_cast<const DFloat*>(partials),
-                                                         done, out);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(sqnorm_finish_kernel, 1, kFinishThreads, 0, stream,
+                             reinterpret_cast<const DFloat*>(partials), done, out);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   ++g_launches;
   return DPOPT_OK;
@@ -630,8 +630,8 @@ int dispatch_amp(const SmallParams& p, int grad_dtype, const LossScaleState* st,
 
 int launch_scale_update(LossScaleState* st, const double* sq, const LossScaleConfig& cfg,
                         cudaStream_t stream) {
-  loss_scale_update_kernel<<<1, 32, 0, stream>>>(st, sq, cfg);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(loss_scale_update_kernel, 1, 32, 0, stream, st, sq, cfg);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   ++g_launches;
   return DPOPT_OK;
@@ -856,8 +856,9 @@ int dpopt_loss_scale_init(dpopt_loss_scale_state* state, const dpopt_loss_scale_
   LossScaleConfig c;
   rc = check_scale_config(cfg, &c);
   if (rc) return rc;
-  loss_scale_init_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((LossScaleState*)state, c);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(loss_scale_init_kernel, 1, 32, 0, (cudaStream_t)stream,
+                             (LossScaleState*)state, c);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   ++g_launches;
   return DPOPT_OK;
@@ -1028,8 +1029,8 @@ int dpopt_allgather_bf16(const void* shard_bf16, int64_t shard_elems, int shard_
   if (rc) return rc;
   const int64_t want = (shard_elems + (int64_t)kThreads * kGroup - 1) / ((int64_t)kThreads * kGroup);
   const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * 8));
-  allgather_bf16_kernel<<<grid, kThreads, 0, (cudaStream_t)stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(allgather_bf16_kernel, grid, kThreads, 0, (cudaStream_t)stream, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   ++g_launches;
   return DPOPT_OK;

@@ -26,6 +26,7 @@ struct GatherParams {
 };
 
 __global__ void __launch_bounds__(kThreads) allgather_bf16_kernel(const __grid_constant__ GatherParams p) {
+  pdl_wait();
   const uint64_t pol = evict_first_policy();
   const int64_t groups = (p.len + kGroup - 1) / kGroup;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;

@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <utility>
 
 #include "dpopt.h"
 #include "kernels.cuh"
@@ -45,6 +46,26 @@ void count_launch();
 int sm_count(int* out);
 
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the preceding kernel on the stream is finishing; every library kernel
+// begins with pdl_enter() (kernels.cuh), which waits for that kernel before
+// any global memory access.  Returns the launch's error code.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Per-gradient-type launchers (launch_gk.cu).  GK: 0 bf16, 1 fp32, 2 fp16.
 // p must hold at least one non-empty segment.

@@ -47,6 +47,23 @@ struct LaunchParams {
 // memory access helpers
 // ---------------------------------------------------------------------------
 
+// Programmatic dependent launch.  The library launches its kernels with
+// programmatic stream serialization, so a kernel's CTAs may be scheduled while
+// the kernel before it on the stream is still finishing.  Every kernel first
+// waits (griddepcontrol.wait: until the preceding grid has completed and its
+// memory is visible) before touching global memory.  The short passes that
+// feed a step -- the norm pre-pass, its ordered finish, the loss-scale
+// kernels -- also let their successor be scheduled at once
+// (griddepcontrol.launch_dependents), so the step's launch and ramp-up hide
+// behind their tail; the step kernels do not, since back-to-back steps
+// measured no faster that way.  Both instructions are no-ops for a kernel
+// launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -584,6 +601,7 @@ __device__ __forceinline__ void step_loop(const LP& p, const Hyper& h, float gsc
 template <int NR, int GK, int PACK, bool EXT, int W, int MAXSEG, int MAXPTR>
 __global__ void __launch_bounds__(kThreads, W == 32 ? wide_ctas<NR, GK>() : min_ctas<NR, PACK>())
     reduce_adam_ldg_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p) {
+  pdl_wait();
   const float gscale = EXT ? grad_scale_of(p.h) : 1.f;
   step_loop<NR, GK, PACK, EXT, W>(p, p.h, gscale);
 }
@@ -596,6 +614,7 @@ template <int NR, int GK, int PACK, int W, int MAXSEG, int MAXPTR>
 __global__ void __launch_bounds__(kThreads, W == 32 ? wide_ctas<NR, GK>() : min_ctas<NR, PACK>())
     reduce_adam_gather_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p,
                               const __grid_constant__ GatherDst d) {
+  pdl_wait();
   step_loop<NR, GK, PACK, false, W, true>(p, p.h, 1.f, &d);
 }
 
@@ -633,6 +652,7 @@ template <int NR, int GK, int PACK, int W, int MAXSEG, int MAXPTR>
 __global__ void __launch_bounds__(kThreads, W == 32 ? 3 : min_ctas<NR, PACK>())
     reduce_adam_amp_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p,
                            const LossScaleState* state, const double* sqnorm) {
+  pdl_wait();
   // Thread 0 forms the step's scalars once; every thread then takes a copy of
   // the grid-constant Hyper with only those overwritten, so the untouched
   // fields stay constant-bank operands instead of occupying registers.

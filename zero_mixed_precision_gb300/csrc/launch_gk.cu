@@ -68,8 +68,8 @@ int persistent_grid(Kern kern, std::atomic<int>& per_sm, int64_t want, unsigned*
   return DPOPT_OK;
 }
 
-int launched() {
-  cudaError_t e = cudaGetLastError();
+int launched(cudaError_t e) {
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   count_launch();
   return DPOPT_OK;
@@ -86,8 +86,7 @@ int step_kernel(const LaunchParams<MS, MP>& p, cudaStream_t stream) {
   unsigned grid = 0;
   int rc = persistent_grid(kern, per_sm, (p.total_groups + kThreads - 1) / kThreads, &grid);
   if (rc) return rc;
-  kern<<<grid, kThreads, 0, stream>>>(p);
-  return launched();
+  return launched(launch_pdl(kern, grid, kThreads, 0, stream, p));
 }
 
 // Unrolled kernel for NR replicas in its measured width; a 32-byte kernel
@@ -129,8 +128,7 @@ int gather_kernel(const SmallParams& p, const GatherDst& d, cudaStream_t stream)
   unsigned grid = 0;
   int rc = persistent_grid(kern, per_sm, (p.total_groups + kThreads - 1) / kThreads, &grid);
   if (rc) return rc;
-  kern<<<grid, kThreads, 0, stream>>>(p, d);
-  return launched();
+  return launched(launch_pdl(kern, grid, kThreads, 0, stream, p, d));
 }
 
 // The same kernel forms as the plain step (widths by wide_states()).
@@ -156,8 +154,7 @@ int amp_kernel(const LaunchParams<MS, MP>& p, const LossScaleState* st, const do
   unsigned grid = 0;
   int rc = persistent_grid(kern, per_sm, (p.total_groups + kThreads - 1) / kThreads, &grid);
   if (rc) return rc;
-  kern<<<grid, kThreads, 0, stream>>>(p, st, sq);
-  return launched();
+  return launched(launch_pdl(kern, grid, kThreads, 0, stream, p, st, sq));
 }
 
 // The loss-scaled kernels take the same widths as the step: their 256-bit
@@ -184,9 +181,8 @@ template <int NR, bool STORE, int MS, int MP>
 int norm_kernel(const LaunchParams<MS, MP>& p, double* partials, int64_t nchunks,
                 cudaStream_t stream) {
   const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nchunks, 1 << 24));
-  grad_sqnorm_kernel<NR, kGK, STORE, MS, MP><<<grid, kThreads, 0, stream>>>(
-      p, reinterpret_cast<DFloat*>(partials), nchunks);
-  return launched();
+  return launched(launch_pdl(grad_sqnorm_kernel<NR, kGK, STORE, MS, MP>, grid, kThreads, 0,
+                             stream, p, reinterpret_cast<DFloat*>(partials), nchunks));
 }
 
 template <bool STORE, int MS, int MP>

@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(kThreads, NR > 0 ? (NR <= 4 ? 5 : 4) : 2)
     grad_sqnorm_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p, DFloat* partials,
                        int64_t nchunks) {
   __shared__ DFloat warp_sum[kThreads / 32];
+  pdl_enter();
   const uint64_t pol = evict_first_policy();
   const float us = p.h.scale_dev ? __fdiv_rn(1.f, *p.h.scale_dev) : p.h.unscale;
   int si = 0;

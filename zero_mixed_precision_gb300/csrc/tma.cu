@@ -41,8 +41,8 @@ int launch_tma(const TmaParams<MS, MP>& p, cudaStream_t stream) {
   if (bps < 1) return fail(DPOPT_ERR_UNSUPPORTED, "bulk-copy kernel does not fit an SM");
   const int64_t want = std::max<int64_t>(p.total_tiles, (int64_t)p.nseg);
   const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * bps));
-  kern<<<grid, kTmaThreads, dyn, stream>>>(p);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, grid, kTmaThreads, dyn, stream, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   count_launch();
   return DPOPT_OK;

@@ -130,6 +130,7 @@ template <int NR, int GK, int W, int MAXSEG, int MAXPTR>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     reduce_adam_tma_kernel(const __grid_constant__ TmaParams<MAXSEG, MAXPTR> p) {
   static_assert(NR >= 1, "one kernel per replica count");
+  pdl_wait();
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full_bar[kTmaMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kTmaMaxStages];
