@@ -48,8 +48,11 @@ KERNEL_SOURCES = ("numerics.cuh", "kernels.cuh")
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about 5 s of the workload's steps at HBM "
+                         "speed, 10 to 20000)")
+    ap.add_argument("--warmup", type=int, default=None,
+                    help="untimed warm-up steps (default: 1 %% of the timed steps, 3 to 200)")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="gpt2s",
                     help="tiny | gpt2s | 1p3b | 70b_shard | sweep_<S>_<N>_<bf16|fp32> "
@@ -609,7 +612,9 @@ def run_overlap(args, wl):
         torch.cuda.synchronize()
         return t0.elapsed_time(t1) / reps
 
-    reps = max(1, args.steps)
+    # each rep also runs the producer (many times the step's time): a default
+    # run takes at most 200 reps
+    reps = max(1, min(args.steps, 200) if getattr(args, "steps_defaulted", False) else args.steps)
     for k in range(args.warmup):
         produce(1, P)
         dp.reduce_adam_buckets(rows, offs, dev.master, dev.m, dev.v, dev.out, step=k + 1,
@@ -732,10 +737,21 @@ def resolve_workload(name: str):
     raise SystemExit(f"unknown workload {name}")
 
 
+def default_steps(wl) -> int:
+    """Timed steps when none are given: about 5 s of steps at 6.5 TB/s."""
+    est_s = wl.shard_elems * (wl.grad_bytes() * wl.n_replicas + 26) / 6.5e12
+    return int(max(10, min(20000, round(5.0 / max(est_s, 1e-9)))))
+
+
 def main(argv=None):
     args = parse_args(argv)
     import synth
     wl = resolve_workload(args.workload)
+    args.steps_defaulted = args.steps is None
+    if args.steps is None:
+        args.steps = default_steps(wl)
+    if args.warmup is None:
+        args.warmup = max(3, min(200, args.steps // 100))
     if args.overlap:
         print(json.dumps(run_overlap(args, wl)), flush=True)
         return
