@@ -401,26 +401,13 @@ __device__ __forceinline__ void group_vec_x1(const Src& src, int n, const Hyper&
              to_bf16x2(th[6], th[7]));
 }
 
-// Packed form: 4 element pairs per thread, every operation on f32x2 lanes.
-// Pays off when the replica sum dominates (large N).
-template <int NR, int GK, bool EXT, class Src, class Out>
-__device__ __forceinline__ void group_vec_x2(const Src& src, int n, const Hyper& h, const Out& o,
-                                             float gscale) {
-  constexpr int P = kGroup / 2;  // element pairs per group
-  float2 th[P], mm[P], vv[P];
-  {
-    float4 a, b;
-    src.state8(0, a, b);
-    th[0] = make_float2(a.x, a.y); th[1] = make_float2(a.z, a.w);
-    th[2] = make_float2(b.x, b.y); th[3] = make_float2(b.z, b.w);
-    src.state8(1, a, b);
-    mm[0] = make_float2(a.x, a.y); mm[1] = make_float2(a.z, a.w);
-    mm[2] = make_float2(b.x, b.y); mm[3] = make_float2(b.z, b.w);
-    src.state8(2, a, b);
-    vv[0] = make_float2(a.x, a.y); vv[1] = make_float2(a.z, a.w);
-    vv[2] = make_float2(b.x, b.y); vv[3] = make_float2(b.z, b.w);
-  }
-  CompSum<float2> acc[P];
+// The fixed-order compensated replica sum of one 8-element group on packed
+// f32x2 lanes (element pairs 2j, 2j+1): the same operations per element as
+// reduce_group_x1, so the same bits.
+template <int NR, int GK, class Src>
+__device__ __forceinline__ void reduce_group_x2(const Src& src, int n,
+                                                CompSum<float2> (&acc)[kGroup / 2]) {
+  constexpr int P = kGroup / 2;
   if constexpr (NR > 0) {
     GradLoad<GK> gl[NR];
 #pragma unroll
@@ -478,6 +465,29 @@ __device__ __forceinline__ void group_vec_x2(const Src& src, int n, const Hyper&
       }
     }
   }
+}
+
+// Packed form: 4 element pairs per thread, every operation on f32x2 lanes.
+// Pays off when the replica sum dominates (large N).
+template <int NR, int GK, bool EXT, class Src, class Out>
+__device__ __forceinline__ void group_vec_x2(const Src& src, int n, const Hyper& h, const Out& o,
+                                             float gscale) {
+  constexpr int P = kGroup / 2;  // element pairs per group
+  float2 th[P], mm[P], vv[P];
+  {
+    float4 a, b;
+    src.state8(0, a, b);
+    th[0] = make_float2(a.x, a.y); th[1] = make_float2(a.z, a.w);
+    th[2] = make_float2(b.x, b.y); th[3] = make_float2(b.z, b.w);
+    src.state8(1, a, b);
+    mm[0] = make_float2(a.x, a.y); mm[1] = make_float2(a.z, a.w);
+    mm[2] = make_float2(b.x, b.y); mm[3] = make_float2(b.z, b.w);
+    src.state8(2, a, b);
+    vv[0] = make_float2(a.x, a.y); vv[1] = make_float2(a.z, a.w);
+    vv[2] = make_float2(b.x, b.y); vv[3] = make_float2(b.z, b.w);
+  }
+  CompSum<float2> acc[P];
+  reduce_group_x2<NR, GK>(src, n, acc);
 #pragma unroll
   for (int j = 0; j < P; ++j) {
     float2 g = acc[j].average(h);

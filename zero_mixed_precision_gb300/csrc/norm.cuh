@@ -32,6 +32,17 @@ __device__ __forceinline__ void norm_group(const void* const* gp, int64_t e0, ui
   for (int j = 0; j < kGroup; ++j) g[j] = cs[j].average(h);
 }
 
+// The same on packed f32x2 lanes: g[j] holds elements 2j and 2j+1.
+template <int NR, int GK, int W>
+__device__ __forceinline__ void norm_group_x2(const void* const* gp, int64_t e0, uint64_t pol,
+                                              int n, const Hyper& h, float2 (&g)[kGroup / 2]) {
+  const GlobalSource<GK, W> src{gp, e0, {nullptr, nullptr, nullptr}, pol};
+  CompSum<float2> cs[kGroup / 2];
+  reduce_group_x2<NR, GK>(src, n, cs);
+#pragma unroll
+  for (int j = 0; j < kGroup / 2; ++j) g[j] = cs[j].average(h);
+}
+
 // One partial per chunk: sum over the chunk's elements of x^2, x = fl32(g *
 // unscale) (exact for a power-of-two unscale) with g the same fixed-order
 // average the step uses.  Each thread accumulates its elements in order as an
@@ -61,7 +72,10 @@ __global__ void __launch_bounds__(kThreads, NR > 0 ? (NR <= 4 ? 5 : 4) : 2)
     const Seg& sg = p.seg[si];
     const int64_t c0 = (c - sg.first_group) * (int64_t)kNormChunk;
     const void* const* gp = p.gptr + sg.ptr_base;
-    float hi = 0.f, lo = 0.f;  // double-float running sum of the squares
+    // double-float running sums of the squares, even and odd elements in the
+    // two lanes
+    float2 hi = make_float2(0.f, 0.f), lo = make_float2(0.f, 0.f);
+    const float2 us2 = make_float2(us, us);
     for (int k = threadIdx.x; k < kNormChunk / kGroup; k += kThreads) {
       const int64_t e0 = c0 + (int64_t)k * kGroup;
       if (e0 >= sg.len) break;
@@ -70,49 +84,55 @@ __global__ void __launch_bounds__(kThreads, NR > 0 ? (NR <= 4 ? 5 : 4) : 2)
           (STORE && !dbg_span(p.h, sg.state_off + e0,
                               sg.state_off + e0 + (rem < kGroup ? rem : kGroup))))
         break;
-      float g[kGroup];
+      float2 g[kGroup / 2];
       int cnt = kGroup;
       float* const avg = STORE ? p.master + sg.state_off + e0 : nullptr;
       if (GK == 1 && sg.vec == 2 && rem >= kGroup) {
-        norm_group<NR, GK, 32>(gp, e0, pol, p.n_rep, p.h, g);
+        norm_group_x2<NR, GK, 32>(gp, e0, pol, p.n_rep, p.h, g);
       } else if (sg.vec && rem >= kGroup) {
-        norm_group<NR, GK, 16>(gp, e0, pol, p.n_rep, p.h, g);
+        norm_group_x2<NR, GK, 16>(gp, e0, pol, p.n_rep, p.h, g);
       } else {
+        // a partial or unaligned group: one element at a time, the missing
+        // elements as zeros (whose squares add nothing)
         cnt = (int)(rem < kGroup ? rem : kGroup);
-        for (int j = 0; j < cnt; ++j) {
-          CompSum<float> cs;
-          cs.init(ld_grad1<GK>(gp[0], e0 + j));
-          for (int r = 1; r < p.n_rep; ++r) cs.add(ld_grad1<GK>(gp[r], e0 + j));
-          g[j] = cs.average(p.h);
+        float t[kGroup];
+        for (int j = 0; j < kGroup; ++j) {
+          t[j] = 0.f;
+          if (j < cnt) {
+            CompSum<float> cs;
+            cs.init(ld_grad1<GK>(gp[0], e0 + j));
+            for (int r = 1; r < p.n_rep; ++r) cs.add(ld_grad1<GK>(gp[r], e0 + j));
+            t[j] = cs.average(p.h);
+          }
         }
+#pragma unroll
+        for (int j = 0; j < kGroup / 2; ++j) g[j] = make_float2(t[2 * j], t[2 * j + 1]);
       }
       if constexpr (STORE) {
-        const float4 lo4 = make_float4(g[0], g[1], g[2], g[3]);
-        const float4 hi4 = make_float4(g[4], g[5], g[6], g[7]);
+        const float4 lo4 = make_float4(g[0].x, g[0].y, g[1].x, g[1].y);
+        const float4 hi4 = make_float4(g[2].x, g[2].y, g[3].x, g[3].y);
         if (sg.vec == 2 && cnt == kGroup) {
           st_global32(avg, lo4, hi4);
         } else if (sg.vec && cnt == kGroup) {
           st_global16(avg, lo4);
           st_global16(avg + 4, hi4);
         } else {
-          for (int j = 0; j < cnt; ++j) avg[j] = g[j];
+          for (int j = 0; j < cnt; ++j) avg[j] = (j & 1) ? g[j >> 1].y : g[j >> 1].x;
         }
       }
 #pragma unroll
-      for (int j = 0; j < kGroup; ++j) {
-        if (j < cnt) {
-          // x^2 exactly as p2 + pe (TwoProd), added with TwoSum
-          const float x = __fmul_rn(g[j], us);
-          const float p2 = __fmul_rn(x, x);
-          const float pe = __fmaf_rn(x, x, -p2);
-          float t, e;
-          two_sum(hi, p2, t, e);
-          hi = t;
-          lo = __fadd_rn(lo, __fadd_rn(e, pe));
-        }
+      for (int j = 0; j < kGroup / 2; ++j) {
+        // x^2 exactly as p2 + pe (TwoProd), added with TwoSum
+        const float2 x = vmul(g[j], us2);
+        const float2 p2 = vmul(x, x);
+        const float2 pe = vfma(x, x, vneg(p2));
+        float2 t, e;
+        two_sum(hi, p2, t, e);
+        hi = t;
+        lo = vadd(lo, vadd(e, pe));
       }
     }
-    DFloat acc{hi, lo};
+    DFloat acc = df_add(DFloat{hi.x, lo.x}, DFloat{hi.y, lo.y});
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const DFloat o{__shfl_down_sync(0xffffffffu, acc.hi, off),

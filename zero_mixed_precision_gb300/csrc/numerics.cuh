@@ -104,6 +104,13 @@ __device__ __forceinline__ float2 vmul(float2 a, float2 b) { return __fmul2_rn(a
 __device__ __forceinline__ float2 vfma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 vneg(float2 a) { return make_float2(-a.x, -a.y); }
 
+// a - b, rounded once.  On f32x2 lanes as fma(b, -1, a): the exact a - b
+// rounded once, the same bits as a subtraction, in one packed instruction.
+__device__ __forceinline__ float vsub(float a, float b) { return __fsub_rn(a, b); }
+__device__ __forceinline__ float2 vsub(float2 a, float2 b) {
+  return __ffma2_rn(b, make_float2(-1.f, -1.f), a);
+}
+
 template <class V> __device__ __forceinline__ V splat(float s);
 template <> __device__ __forceinline__ float splat<float>(float s) { return s; }
 template <> __device__ __forceinline__ float2 splat<float2>(float s) { return make_float2(s, s); }
@@ -137,9 +144,9 @@ __device__ __forceinline__ float rcp_approx(float x) {
 template <class V>
 __device__ __forceinline__ void two_sum(V a, V b, V& s, V& e) {
   s = vadd(a, b);
-  V bp = vadd(s, vneg(a));
-  V ap = vadd(s, vneg(bp));
-  e = vadd(vadd(a, vneg(ap)), vadd(b, vneg(bp)));
+  V bp = vsub(s, a);
+  V ap = vsub(s, bp);
+  e = vadd(vsub(a, ap), vsub(b, bp));
 }
 
 // A double-float: hi + lo with |lo| <= ulp(hi)/2, about 48 significant bits.
