@@ -45,19 +45,23 @@ __device__ __forceinline__ void norm_group_x2(const void* const* gp, int64_t e0,
 
 // One partial per chunk: sum over the chunk's elements of x^2, x = fl32(g *
 // unscale) (exact for a power-of-two unscale) with g the same fixed-order
-// average the step uses.  Each thread accumulates its elements in order as an
-// fp32 pair (TwoProd for each square, TwoSum into the sum), then the threads'
-// pairs are added over a fixed tree of double-float additions -- a shuffle
-// tree inside each warp, then the warps' sums in warp order -- and the chunk's
-// pair is stored (8 bytes per chunk).  No fp64 arithmetic: on GB300 an fp64
-// tree per 4096-element chunk kept the fp64 pipe half busy.  Seg::first_group
-// holds the segment's first chunk here.
+// average the step uses.  Each thread accumulates its elements in order on
+// packed f32x2 lanes -- even elements in one lane, odd in the other, each an
+// fp32 pair (TwoProd for each square, TwoSum into the sum) -- and joins its
+// two pairs; then the threads' pairs are added over a fixed tree of
+// double-float additions -- a shuffle tree inside each warp, then the warps'
+// sums in warp order -- and the chunk's pair is stored (8 bytes per chunk).
+// No fp64 arithmetic: on GB300 an fp64 tree per 4096-element chunk kept the
+// fp64 pipe half busy.  The packed lanes cut the pass from 61 to 42
+// instructions per element at N = 4 (gpt2s: 67.7 -> 62.3 us).
+// Seg::first_group holds the segment's first chunk here.
 //
 // STORE: the pass also writes each element's average g (fp32, before the
 // unscale) to p.master[state_off + e] -- the reduced gradient shard -- so that
 // a following step can read 4 bytes per element instead of N replicas.
-// Five CTAs per SM for N <= 4 (at most 48 registers, no spills; six spilled),
-// four above.
+// Five CTAs per SM for N <= 4 (at most 48 registers; the forms without STORE
+// spill 16-40 bytes there, and measured no slower than at four CTAs without
+// spills), four above.
 template <int NR, int GK, bool STORE, int MAXSEG, int MAXPTR>
 __global__ void __launch_bounds__(kThreads, NR > 0 ? (NR <= 4 ? 5 : 4) : 2)
     grad_sqnorm_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p, DFloat* partials,
