@@ -84,11 +84,13 @@ def parse_args(argv=None):
                          "also stores the averaged gradient (the reduced gradient shard) and the "
                          "step reads it as one fp32 replica; 'fused' -- the step reads the N "
                          "replicas again.  Both give the same bits.")
-    ap.add_argument("--gather-path", choices=("fused", "separate"), default="fused",
-                    help="adam_allgather: 'fused' -- one kernel writes the new bf16 shard into "
-                         "every replica's parameter buffer (dpopt_reduce_adam_allgather); "
-                         "'separate' -- the step, then dpopt_allgather_bf16 reads the bf16 "
-                         "shard back and broadcasts it.  Both give the same bits.")
+    ap.add_argument("--gather-path", choices=("entry", "separate"), default="entry",
+                    help="adam_allgather: 'entry' -- dpopt_reduce_adam_allgather, which runs one "
+                         "kernel writing the new bf16 shard into every replica's parameter "
+                         "buffer, or (3 <= N <= 8, large shards) the step and the broadcast, "
+                         "whichever measured faster; 'separate' -- the step, then "
+                         "dpopt_allgather_bf16 reads the bf16 shard back and broadcasts it, "
+                         "always.  Both give the same bits.")
     return ap.parse_args(argv)
 
 
@@ -340,7 +342,7 @@ def run_ours(args, wl):
         opts = dp.step_options(weight_decay=0.01, max_grad_norm=1.0, grad_sqnorm=sqn)
     if args.optimizer == "adam_allgather":
         param_reps = [torch.empty(S * n, dtype=torch.bfloat16, device=device) for _ in range(n)]
-    gather_fused = args.gather_path == "fused"
+    gather_entry = args.gather_path == "entry"
     stored = args.clip_path == "stored" and wl.layout == "full"
     if args.optimizer in ("adamw_clip", "amp") and stored:
         avg = torch.empty(S, dtype=torch.float32, device=device)
@@ -351,7 +353,7 @@ def run_ours(args, wl):
         ls_state = torch.zeros(4, dtype=torch.int64, device=device)
         ls_cfg = dp.loss_scale_init(ls_state, init_scale=1024.0, window=1000, stream=stream)
     if wl.layout == "full":
-        if args.optimizer == "adam_allgather" and gather_fused:
+        if args.optimizer == "adam_allgather" and gather_entry:
             def step(t):
                 dp.reduce_adam_allgather(dev.grads, wl.shard_rank, wl.bucket_elems, dev.master,
                                          dev.m, dev.v, param_reps, step=t, stream=stream, **hp)
@@ -521,10 +523,16 @@ def _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks
         bpp += 8
     elif args.optimizer in ("adamw_clip", "amp"):   # the norm pre-pass reads the N gradients again
         bpp += wl.grad_bytes() * wl.n_replicas
-    elif args.optimizer == "adam_allgather" and args.gather_path == "fused":
-        # the bf16 copy goes to the N replica buffers instead of one output
-        bpp += 2 * wl.n_replicas - 2
-    elif args.optimizer == "adam_allgather":   # read the bf16 shard, write N copies
+    elif args.optimizer == "adam_allgather" and args.gather_path == "entry":
+        if launches == K:
+            # one fused launch per step: the bf16 copy goes to the N replica
+            # buffers instead of one output (4N + 24)
+            bpp += 2 * wl.n_replicas - 2
+        else:
+            # the step writes the own replica, the broadcast reads it and
+            # writes the other N - 1 (4N + 26)
+            bpp += 2 * wl.n_replicas
+    elif args.optimizer == "adam_allgather":   # read the bf16 shard, write N copies (4N + 28)
         bpp += 2 + 2 * wl.n_replicas
     ms_per_step = elapsed_ms / K
     value = throughput(world, S, K, elapsed_ms)

@@ -154,3 +154,36 @@ def test_fused_step_allgather_unaligned_replicas():
         res.append([f32(x) for x in st] + [u16(b) for b in base])
     for a, b in zip(*res):
         assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+@pytest.mark.parametrize("n,S", [(4, 13_000_003), (8, 9_200_001)])
+def test_large_shard_takes_the_two_pass_form_with_the_same_bits(n, S):
+    """Above 512 MB of working set at 3 <= N <= 8 the entry runs the step into
+    the own replica and then the broadcast; the bits are those of the two
+    public calls."""
+    _need_gpu()
+    rank = n - 1
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(n)
+    grads = [torch.randn(n * S, generator=gen, device="cuda").mul_(1e-3).bfloat16()
+             for _ in range(n)]
+    init = [torch.randn(S, generator=gen, device="cuda").mul_(0.02),
+            torch.randn(S, generator=gen, device="cuda").mul_(1e-4),
+            torch.randn(S, generator=gen, device="cuda").mul_(1e-6).abs()]
+    res = []
+    for fused in (True, False):
+        st = [x.clone() for x in init]
+        reps = [torch.full((n * S,), 0x7FA1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+                for _ in range(n)]
+        if fused:
+            dp.reduce_adam_allgather(grads, rank, S, *st, reps, step=3, **HP)
+        else:
+            own = reps[rank][rank * S:(rank + 1) * S]
+            dp.reduce_adam(grads, rank, S, *st, own, step=3, **HP)
+            dp.allgather_bf16(own, rank, reps)
+        dp.stream_status()
+        res.append([x.view(torch.int32) if x.dtype == torch.float32 else x.view(torch.int16)
+                    for x in st + reps])
+        del reps
+    for a, b in zip(*res):
+        assert torch.equal(a, b)

@@ -671,6 +671,34 @@ int noalloc_partials(double** out) {
   return DPOPT_OK;
 }
 
+// The all-gather kernel over p.len elements into p.n_dst destinations.
+int launch_gather(const GatherParams& p, cudaStream_t stream) {
+  int sms = 0;
+  int rc = sm_count(&sms);
+  if (rc) return rc;
+  const int64_t want = (p.len + (int64_t)kThreads * kGroup - 1) / ((int64_t)kThreads * kGroup);
+  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * 8));
+  cudaError_t e = launch_pdl(allgather_bf16_kernel, grid, kThreads, 0, stream, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  ++g_launches;
+  return DPOPT_OK;
+}
+
+// Whether the step fused with the all-gather (one pass, reads and writes at
+// about 1:1) beats the step into the own replica followed by the broadcast
+// kernel (two passes, each nearer its own best mix), by measurement on GB300
+// (G params/s, fused / separate):
+//   S = 30M:  N = 2 197 / 185, 3 161 / 165, 4 148 / 149, 5 133 / 140,
+//             6 120 / 127, 7 114 / 119, 8 106 / 112, 9 104 / 88;
+//   S = 4M:   fused ahead at every N measured (2, 4, 8, 9, 12, 16, 32, 64).
+// The separate form wins only for 3 <= N <= 8 with a working set well above
+// L2 (S * (4N + 24) bytes > 512 MB).  Both write the same bits.
+bool gather_fused(int n, int64_t shard) {
+  if (n < 3 || n > 8) return true;
+  return (double)shard * (4.0 * n + 24.0) <= 512e6;
+}
+
 }  // namespace
 }  // namespace dpopt
 
@@ -1024,16 +1052,7 @@ int dpopt_allgather_bf16(const void* shard_bf16, int64_t shard_elems, int shard_
   p.n_dst = nd;
   p.vec = vec ? 1 : 0;
   if (nd == 0) return DPOPT_OK;
-  int sms = 0;
-  int rc = sm_count(&sms);
-  if (rc) return rc;
-  const int64_t want = (shard_elems + (int64_t)kThreads * kGroup - 1) / ((int64_t)kThreads * kGroup);
-  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * 8));
-  cudaError_t e = launch_pdl(allgather_bf16_kernel, grid, kThreads, 0, (cudaStream_t)stream, p);
-  if (e == cudaSuccess) e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
-  ++g_launches;
-  return DPOPT_OK;
+  return launch_gather(p, (cudaStream_t)stream);
 }
 
 int dpopt_reduce_adam_allgather(const void* const* grads, int grad_dtype, int n_replicas,
@@ -1090,9 +1109,28 @@ int dpopt_reduce_adam_allgather(const void* const* grads, int grad_dtype, int n_
   p.h = h;
   p.master = master_f32; p.m = m_f32; p.v = v_f32; p.out = own;
   p.n_rep = n_replicas;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (!gather_fused(n_replicas, S)) {
+    // the step into the own replica buffer, then its broadcast
+    rc = run(&seg, 1, grad_dtype, n_replicas, master_f32, m_f32, v_f32, own, h, false, st);
+    if (rc || d.n == 0) return rc;
+    GatherParams g{};
+#ifdef DPOPT_DEBUG_BOUNDS
+    g.dbg_status = bounds_status_word();
+#endif
+    g.src = own;
+    g.len = S;
+    g.n_dst = d.n;
+    bool vec = aligned16(own);
+    for (int i = 0; i < d.n; ++i) {
+      g.dst[i] = d.dst[i];
+      vec = vec && aligned16(d.dst[i]);
+    }
+    g.vec = vec ? 1 : 0;
+    return launch_gather(g, st);
+  }
   if (fill_segments(p, &seg, 0, 1, n_replicas, kGroup, grad_dtype) == 0) return DPOPT_OK;
   if (!dst16) p.seg[0].vec = 0;  // the 16-byte bf16 stores need every destination aligned
-  cudaStream_t st = (cudaStream_t)stream;
   if (grad_dtype == DPOPT_GRAD_BF16) return launch_step_gather<0>(p, d, st);
   if (grad_dtype == DPOPT_GRAD_F16) return launch_step_gather<2>(p, d, st);
   return launch_step_gather<1>(p, d, st);
