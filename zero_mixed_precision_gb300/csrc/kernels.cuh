@@ -401,6 +401,25 @@ __device__ __forceinline__ void group_vec_x1(const Src& src, int n, const Hyper&
              to_bf16x2(th[6], th[7]));
 }
 
+// Replicas r0 .. r0+C-1 of one 8-element group added, in order, to packed
+// running sums (FIRST: replica r0 starts them); all C loads issued before the
+// first addition.
+template <int C, bool FIRST, int GK, class Src>
+__device__ __forceinline__ void add_chunk_x2(const Src& src, int r0,
+                                             CompSum<float2> (&acc)[kGroup / 2]) {
+  GradLoad<GK> gl[C];
+#pragma unroll
+  for (int j = 0; j < C; ++j) src.grad(gl[j], r0 + j);
+#pragma unroll
+  for (int j = 0; j < C; ++j) {
+#pragma unroll
+    for (int k = 0; k < kGroup / 2; ++k) {
+      if (FIRST && j == 0) acc[k].init(gl[j].pair(k));
+      else acc[k].add(gl[j].pair(k));
+    }
+  }
+}
+
 // The fixed-order compensated replica sum of one 8-element group on packed
 // f32x2 lanes (element pairs 2j, 2j+1): the same operations per element as
 // reduce_group_x1, so the same bits.
@@ -420,9 +439,18 @@ __device__ __forceinline__ void reduce_group_x2(const Src& src, int n,
       for (int j = 0; j < P; ++j) acc[j].add(gl[r].pair(j));
     }
   } else {
-    // runtime replica count: chunks of 8 replicas, loads of a chunk in flight together
+    // runtime replica count: chunks of 8 replicas, then the remainder (1..7)
+    // as one more chunk; all loads of a chunk in flight together, every chunk
+    // fully unrolled, replicas in ascending order.  (A predicated 8-wide
+    // remainder left N = 9..15 at 78-85 % of the copy bandwidth, remainders
+    // split 4 + 2 + 1 paid one load latency per piece, and balancing all
+    // chunks slowed the multiples of 8.)
     constexpr int C = 8;
-    {
+    int r0;
+    if (n >= C) {
+      add_chunk_x2<C, true, GK>(src, 0, acc);
+      r0 = C;
+    } else {
       GradLoad<GK> gl[C];
 #pragma unroll
       for (int j = 0; j < C; ++j) {
@@ -438,31 +466,18 @@ __device__ __forceinline__ void reduce_group_x2(const Src& src, int n,
           for (int k = 0; k < P; ++k) acc[k].add(gl[j].pair(k));
         }
       }
+      r0 = n;
     }
-    for (int r0 = C; r0 < n; r0 += C) {
-      GradLoad<GK> gl[C];
-      if (r0 + C <= n) {
-#pragma unroll
-        for (int j = 0; j < C; ++j) src.grad(gl[j], r0 + j);
-#pragma unroll
-        for (int j = 0; j < C; ++j) {
-#pragma unroll
-          for (int k = 0; k < P; ++k) acc[k].add(gl[j].pair(k));
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < C; ++j) {
-          if (r0 + j < n) src.grad(gl[j], r0 + j);
-          else gl[j].zero();
-        }
-#pragma unroll
-        for (int j = 0; j < C; ++j) {
-          if (r0 + j < n) {
-#pragma unroll
-            for (int k = 0; k < P; ++k) acc[k].add(gl[j].pair(k));
-          }
-        }
-      }
+    for (; r0 + C <= n; r0 += C) add_chunk_x2<C, false, GK>(src, r0, acc);
+    switch (n - r0) {
+      case 1: add_chunk_x2<1, false, GK>(src, r0, acc); break;
+      case 2: add_chunk_x2<2, false, GK>(src, r0, acc); break;
+      case 3: add_chunk_x2<3, false, GK>(src, r0, acc); break;
+      case 4: add_chunk_x2<4, false, GK>(src, r0, acc); break;
+      case 5: add_chunk_x2<5, false, GK>(src, r0, acc); break;
+      case 6: add_chunk_x2<6, false, GK>(src, r0, acc); break;
+      case 7: add_chunk_x2<7, false, GK>(src, r0, acc); break;
+      default: break;
     }
   }
 }
