@@ -378,8 +378,9 @@ int dpopt_allgather_bf16(const void *shard_bf16, int64_t shard_elems, int shard_
  * step leaves them.  Where it measured faster the call runs one fused kernel --
  * the bf16 copy is never read back: g*N + 24 + 2N bytes per parameter instead
  * of g*N + 28 + 2N -- and otherwise exactly those two launches: for
- * 3 <= n_replicas <= 8 with S*(4*n_replicas + 24) above 512 MB, where the
- * fused pass's even mix of reads and writes ran 3-6 % slower on GB300.
+ * 3 <= n_replicas <= 8 (16 with bf16 or fp16 gradients) with
+ * S*(4*n_replicas + 24) above 512 MB, where the fused pass's even mix of
+ * reads and writes ran 2-6 % slower on GB300.
  *  grads, grad_dtype, n_replicas, numel, shard_rank, bucket_elems, master_f32,
  *  m_f32, v_f32, lr, beta1, beta2, eps, step, stream
  *                  as for dpopt_reduce_adam_ex.

@@ -156,7 +156,7 @@ def test_fused_step_allgather_unaligned_replicas():
         assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
 
 
-@pytest.mark.parametrize("n,S", [(4, 13_000_003), (8, 9_200_001)])
+@pytest.mark.parametrize("n,S", [(4, 13_000_003), (8, 9_200_001), (12, 7_200_001)])
 def test_large_shard_takes_the_two_pass_form_with_the_same_bits(n, S):
     """Above 512 MB of working set at 3 <= N <= 8 the entry runs the step into
     the own replica and then the broadcast; the bits are those of the two

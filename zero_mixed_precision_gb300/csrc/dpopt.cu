@@ -688,14 +688,18 @@ int launch_gather(const GatherParams& p, cudaStream_t stream) {
 // Whether the step fused with the all-gather (one pass, reads and writes at
 // about 1:1) beats the step into the own replica followed by the broadcast
 // kernel (two passes, each nearer its own best mix), by measurement on GB300
-// (G params/s, fused / separate):
+// (G params/s, fused / separate, bf16):
 //   S = 30M:  N = 2 197 / 185, 3 161 / 165, 4 148 / 149, 5 133 / 140,
-//             6 120 / 127, 7 114 / 119, 8 106 / 112, 9 104 / 88;
+//             6 120 / 127, 7 114 / 119, 8 106-112 / 112, 9 98 / 104,
+//             12 82 / 87, 16 69 / 70 (N = 9..16 with the unrolled step; with
+//             the runtime-count step the separate form lost: N = 9 104 / 88);
 //   S = 4M:   fused ahead at every N measured (2, 4, 8, 9, 12, 16, 32, 64).
-// The separate form wins only for 3 <= N <= 8 with a working set well above
-// L2 (S * (4N + 24) bytes > 512 MB).  Both write the same bits.
-bool gather_fused(int n, int64_t shard) {
-  if (n < 3 || n > 8) return true;
+// The separate form wins where the step has an unrolled kernel (N <= 8, and
+// N <= 16 for 16-bit gradients) past N = 2, with a working set well above L2
+// (S * (4N + 24) bytes > 512 MB).  Both write the same bits.
+bool gather_fused(int n, int64_t shard, int grad_dtype) {
+  const int unrolled = grad_dtype == DPOPT_GRAD_F32 ? 8 : 16;
+  if (n < 3 || n > unrolled) return true;
   return (double)shard * (4.0 * n + 24.0) <= 512e6;
 }
 
@@ -1110,7 +1114,7 @@ int dpopt_reduce_adam_allgather(const void* const* grads, int grad_dtype, int n_
   p.master = master_f32; p.m = m_f32; p.v = v_f32; p.out = own;
   p.n_rep = n_replicas;
   cudaStream_t st = (cudaStream_t)stream;
-  if (!gather_fused(n_replicas, S)) {
+  if (!gather_fused(n_replicas, S, grad_dtype)) {
     // the step into the own replica buffer, then its broadcast
     rc = run(&seg, 1, grad_dtype, n_replicas, master_f32, m_f32, v_f32, own, h, false, st);
     if (rc || d.n == 0) return rc;

@@ -331,7 +331,29 @@ struct GatherOutT : GroupOutT<W> {
 // same bits of g.
 template <int NR, int GK, class Src>
 __device__ __forceinline__ void reduce_group_x1(const Src& src, int n, CompSum<float> (&acc)[kGroup]) {
-  if constexpr (NR > 0) {
+  if constexpr (NR > 8) {
+    // two batches (8, then NR - 8 <= 8) so that at most 8 loads are held at once
+    {
+      GradLoad<GK> gl[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) src.grad(gl[r], r);
+#pragma unroll
+      for (int k = 0; k < kGroup; ++k) acc[k].init(gl[0].get(k));
+#pragma unroll
+      for (int r = 1; r < 8; ++r) {
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) acc[k].add(gl[r].get(k));
+      }
+    }
+    GradLoad<GK> gl[NR - 8];
+#pragma unroll
+    for (int r = 0; r < NR - 8; ++r) src.grad(gl[r], 8 + r);
+#pragma unroll
+    for (int r = 0; r < NR - 8; ++r) {
+#pragma unroll
+      for (int k = 0; k < kGroup; ++k) acc[k].add(gl[r].get(k));
+    }
+  } else if constexpr (NR > 0) {
     GradLoad<GK> gl[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) src.grad(gl[r], r);
