@@ -84,13 +84,16 @@ def parse_args(argv=None):
                          "also stores the averaged gradient (the reduced gradient shard) and the "
                          "step reads it as one fp32 replica; 'fused' -- the step reads the N "
                          "replicas again.  Both give the same bits.")
-    ap.add_argument("--gather-path", choices=("entry", "separate"), default="entry",
+    ap.add_argument("--gather-path", choices=("entry", "fused", "two-pass", "separate"),
+                    default="entry",
                     help="adam_allgather: 'entry' -- dpopt_reduce_adam_allgather, which runs one "
                          "kernel writing the new bf16 shard into every replica's parameter "
-                         "buffer, or (3 <= N <= 8, large shards) the step and the broadcast, "
-                         "whichever measured faster; 'separate' -- the step, then "
-                         "dpopt_allgather_bf16 reads the bf16 shard back and broadcasts it, "
-                         "always.  Both give the same bits.")
+                         "buffer, or (large shards, 3 <= N <= 8 or 16) the step into the own "
+                         "replica and the broadcast, whichever measured faster; 'fused' / "
+                         "'two-pass' -- the entry held to one form (dpopt_set_gather_policy); "
+                         "'separate' -- the step into a separate output, then "
+                         "dpopt_allgather_bf16 reads it back and broadcasts it.  All give the "
+                         "same bits.")
     return ap.parse_args(argv)
 
 
@@ -342,7 +345,11 @@ def run_ours(args, wl):
         opts = dp.step_options(weight_decay=0.01, max_grad_norm=1.0, grad_sqnorm=sqn)
     if args.optimizer == "adam_allgather":
         param_reps = [torch.empty(S * n, dtype=torch.bfloat16, device=device) for _ in range(n)]
-    gather_entry = args.gather_path == "entry"
+    gather_entry = args.gather_path != "separate"
+    if args.optimizer == "adam_allgather" and args.gather_path in ("fused", "two-pass"):
+        pol = dp.DPOPT_GATHER_FUSED if args.gather_path == "fused" else dp.DPOPT_GATHER_SEPARATE
+        if dp.dpopt_set_gather_policy(pol) != dp.DPOPT_OK:
+            raise SystemExit(f"dpopt_set_gather_policy: {dp.dpopt_last_error()}")
     stored = args.clip_path == "stored" and wl.layout == "full"
     if args.optimizer in ("adamw_clip", "amp") and stored:
         avg = torch.empty(S, dtype=torch.float32, device=device)
@@ -523,7 +530,7 @@ def _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks
         bpp += 8
     elif args.optimizer in ("adamw_clip", "amp"):   # the norm pre-pass reads the N gradients again
         bpp += wl.grad_bytes() * wl.n_replicas
-    elif args.optimizer == "adam_allgather" and args.gather_path == "entry":
+    elif args.optimizer == "adam_allgather" and args.gather_path != "separate":
         if launches == K:
             # one fused launch per step: the bf16 copy goes to the N replica
             # buffers instead of one output (4N + 24)

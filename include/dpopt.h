@@ -380,7 +380,8 @@ int dpopt_allgather_bf16(const void *shard_bf16, int64_t shard_elems, int shard_
  * of g*N + 28 + 2N -- and otherwise exactly those two launches: for
  * 3 <= n_replicas <= 8 (16 with bf16 or fp16 gradients) with
  * S*(4*n_replicas + 24) above 512 MB, where the fused pass's even mix of
- * reads and writes ran 2-6 % slower on GB300.
+ * reads and writes ran 2-6 % slower on GB300 (dpopt_set_gather_policy
+ * overrides the choice).
  *  grads, grad_dtype, n_replicas, numel, shard_rank, bucket_elems, master_f32,
  *  m_f32, v_f32, lr, beta1, beta2, eps, step, stream
  *                  as for dpopt_reduce_adam_ex.
@@ -473,6 +474,22 @@ int dpopt_state_bytes(int64_t psi, int variant, int n_dp, int zero_stage, double
 typedef enum { DPOPT_KERNEL_AUTO = 0, DPOPT_KERNEL_DIRECT = 1, DPOPT_KERNEL_BULK = 2 } dpopt_kernel_policy;
 int dpopt_set_kernel_policy(int policy);
 int dpopt_get_kernel_policy(void);
+
+/* Which form dpopt_reduce_adam_allgather takes (process-wide; default
+ * DPOPT_GATHER_AUTO).
+ *  DPOPT_GATHER_AUTO      the faster of the two by measurement (see the entry)
+ *  DPOPT_GATHER_FUSED     always the one fused kernel
+ *  DPOPT_GATHER_SEPARATE  always the step into the own replica, then the
+ *                         broadcast into the others
+ * All give bitwise identical results.  Errors: DPOPT_ERR_INVALID_ARG for an
+ * unknown value. */
+typedef enum {
+    DPOPT_GATHER_AUTO = 0,
+    DPOPT_GATHER_FUSED = 1,
+    DPOPT_GATHER_SEPARATE = 2
+} dpopt_gather_policy;
+int dpopt_set_gather_policy(int policy);
+int dpopt_get_gather_policy(void);
 
 /* Diagnostic: enqueue a kernel whose one bounded wait can never be satisfied, so
  * that it gives up after limit_cycles GPU clock cycles (1 .. 2e9) and sets the

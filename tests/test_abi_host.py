@@ -270,3 +270,11 @@ def test_fused_allgather_entry_rejects_bad_arguments(dp, over, code):
 def test_fused_allgather_entry_with_nothing_to_update_checks_and_returns(dp):
     assert _fused(dp, numel=0) == 0
     assert _fused(dp, numel=0, rank=7) == 1
+
+
+def test_gather_policy_round_trip_and_rejects_unknown(dp):
+    assert dp.dpopt_get_gather_policy() == dp.DPOPT_GATHER_AUTO
+    for pol in (dp.DPOPT_GATHER_FUSED, dp.DPOPT_GATHER_SEPARATE, dp.DPOPT_GATHER_AUTO):
+        assert dp.dpopt_set_gather_policy(pol) == 0 and dp.dpopt_get_gather_policy() == pol
+    assert dp.dpopt_set_gather_policy(3) == dp.DPOPT_ERR_INVALID_ARG
+    assert dp.dpopt_get_gather_policy() == dp.DPOPT_GATHER_AUTO

@@ -187,3 +187,32 @@ def test_large_shard_takes_the_two_pass_form_with_the_same_bits(n, S):
         del reps
     for a, b in zip(*res):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("n,S", [(2, 50_001), (5, 100_003), (13, 20_007)])
+def test_gather_policies_write_the_same_bits(n, S):
+    """The fused kernel and the two-pass form, forced by the gather policy,
+    leave the same states and replica buffers as the automatic choice."""
+    _need_gpu()
+    rank = n // 2
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(100 + n)
+    grads = [torch.randn(n * S, generator=gen, device="cuda").mul_(1e-3).bfloat16()
+             for _ in range(n)]
+    init = [torch.randn(S, generator=gen, device="cuda").mul_(0.02),
+            torch.randn(S, generator=gen, device="cuda").mul_(1e-4),
+            torch.randn(S, generator=gen, device="cuda").mul_(1e-6).abs()]
+    res = []
+    for pol in (dp.DPOPT_GATHER_AUTO, dp.DPOPT_GATHER_FUSED, dp.DPOPT_GATHER_SEPARATE):
+        st = [x.clone() for x in init]
+        reps = [torch.full((n * S,), 0x7FA1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+                for _ in range(n)]
+        with dp.gather_policy(pol):
+            for t in (1, 2):
+                dp.reduce_adam_allgather(grads, rank, S, *st, reps, step=t, **HP)
+        dp.stream_status()
+        res.append([x.view(torch.int32) for x in st] + [r.view(torch.int16) for r in reps])
+    for other in res[1:]:
+        for a, b in zip(res[0], other):
+            assert torch.equal(a, b)
+    assert dp.dpopt_get_gather_policy() == dp.DPOPT_GATHER_AUTO

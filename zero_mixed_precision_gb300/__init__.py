@@ -8,7 +8,8 @@ from .binding import *  # noqa: F401,F403
 from .binding import (  # noqa: F401
     DpoptError, EXPORTED, LIB_PATH, LossScaleConfig, allgather_bf16, LossScaleState, StepOptions, amp_sqnorm,
     amp_average_sqnorm, grad_average_sqnorm,
-    amp_step, grad_sqnorm, grad_sqnorm_buckets, kernel_policy, loss_scale_init, read_loss_scale,
+    amp_step, gather_policy, grad_sqnorm, grad_sqnorm_buckets, kernel_policy, loss_scale_init,
+    read_loss_scale,
     reduce_adam, reduce_adam_allgather, reduce_adam_bucket, reduce_adam_buckets,
     reduce_adam_buckets_when_ready,
     reduce_adamw, reduce_adamw_buckets,

@@ -28,6 +28,9 @@ DPOPT_MAX_REPLICAS = 64
 DPOPT_KERNEL_AUTO = 0
 DPOPT_KERNEL_DIRECT = 1
 DPOPT_KERNEL_BULK = 2
+DPOPT_GATHER_AUTO = 0
+DPOPT_GATHER_FUSED = 1
+DPOPT_GATHER_SEPARATE = 2
 
 # DPOPT_LIB_VARIANT=bounds loads the bounds-checked build of the same sources
 # (every kernel tests its derived indices; failures are reported as
@@ -113,6 +116,8 @@ _SIGS = {
                                               _P, _F, _F, _F, _F, _I64, _P], _I),
     "dpopt_set_kernel_policy": ([_I], _I),
     "dpopt_get_kernel_policy": ([], _I),
+    "dpopt_set_gather_policy": ([_I], _I),
+    "dpopt_get_gather_policy": ([], _I),
     "dpopt_selftest_wait_timeout": ([_I64, _P], _I),
     "dpopt_selftest_bounds": ([_P], _I),
 }
@@ -359,6 +364,14 @@ def dpopt_set_kernel_policy(policy: int) -> int:
 
 def dpopt_get_kernel_policy() -> int:
     return _lib.dpopt_get_kernel_policy()
+
+
+def dpopt_set_gather_policy(policy: int) -> int:
+    return _lib.dpopt_set_gather_policy(policy)
+
+
+def dpopt_get_gather_policy() -> int:
+    return _lib.dpopt_get_gather_policy()
 
 
 def dpopt_selftest_wait_timeout(limit_cycles: int, stream: int = 0) -> int:
@@ -611,4 +624,20 @@ class kernel_policy:
 
     def __exit__(self, *exc):
         dpopt_set_kernel_policy(self.saved)
+        return False
+
+
+class gather_policy:
+    """Context manager: run the enclosed calls with a given all-gather form."""
+
+    def __init__(self, policy: int):
+        self.policy = policy
+
+    def __enter__(self):
+        self.saved = dpopt_get_gather_policy()
+        _check(dpopt_set_gather_policy(self.policy), "dpopt_set_gather_policy")
+        return self
+
+    def __exit__(self, *exc):
+        dpopt_set_gather_policy(self.saved)
         return False

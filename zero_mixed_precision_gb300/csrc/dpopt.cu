@@ -36,6 +36,7 @@ bool auto_bulk(int n, int grad_dtype) {
 }
 
 std::atomic<int> g_policy{DPOPT_KERNEL_AUTO};
+std::atomic<int> g_gather_policy{DPOPT_GATHER_AUTO};
 
 thread_local char g_last_error[512];
 thread_local int64_t g_launches = 0;
@@ -698,6 +699,8 @@ int launch_gather(const GatherParams& p, cudaStream_t stream) {
 // N <= 16 for 16-bit gradients) past N = 2, with a working set well above L2
 // (S * (4N + 24) bytes > 512 MB).  Both write the same bits.
 bool gather_fused(int n, int64_t shard, int grad_dtype) {
+  const int pol = g_gather_policy.load(std::memory_order_relaxed);
+  if (pol != DPOPT_GATHER_AUTO) return pol == DPOPT_GATHER_FUSED;
   const int unrolled = grad_dtype == DPOPT_GRAD_F32 ? 8 : 16;
   if (n < 3 || n > unrolled) return true;
   return (double)shard * (4.0 * n + 24.0) <= 512e6;
@@ -1213,6 +1216,16 @@ int dpopt_set_kernel_policy(int policy) {
 }
 
 int dpopt_get_kernel_policy(void) { return g_policy.load(std::memory_order_relaxed); }
+
+int dpopt_set_gather_policy(int policy) {
+  if (policy != DPOPT_GATHER_AUTO && policy != DPOPT_GATHER_FUSED &&
+      policy != DPOPT_GATHER_SEPARATE)
+    return fail(DPOPT_ERR_INVALID_ARG, "unknown gather policy %d", policy);
+  g_gather_policy.store(policy, std::memory_order_relaxed);
+  return DPOPT_OK;
+}
+
+int dpopt_get_gather_policy(void) { return g_gather_policy.load(std::memory_order_relaxed); }
 
 int dpopt_selftest_wait_timeout(int64_t limit_cycles, dpopt_stream_t stream) {
   if (limit_cycles < 1 || limit_cycles > kWaitLimitCycles)
