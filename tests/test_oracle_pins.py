@@ -524,3 +524,42 @@ def test_amp_step_skips_on_overflow_and_leaves_the_states_alone():
     assert ovf and out is None and sc.step == 0 and sc.skipped == 1 and sc.scale == 32768.0
     np.testing.assert_array_equal(st[0], th0)
     assert np.all(st[1] == 1) and np.all(st[2] == 1)
+
+
+def test_adam_matches_a_50_digit_decimal_evaluation():
+    """The oracle's fp64 Adam against the same steps carried out in 50-digit
+    decimal arithmetic (square root included), the stored states rounded to
+    fp32 after every step as the method stores them: 16 elements x 3 steps,
+    mixed signs and magnitudes, bit for bit."""
+    import decimal
+    from decimal import Decimal as D
+
+    ctx = decimal.Context(prec=50)
+    rng = np.random.default_rng(21)
+    count, steps = 16, 3
+    lr, b1, b2, eps = np.float32(1e-3), np.float32(0.9), np.float32(0.999), np.float32(1e-8)
+    th = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    m = np.zeros(count, np.float32)
+    v = np.zeros(count, np.float32)
+    gs = [(rng.standard_normal(count) * 10.0 ** rng.integers(-6, -1, count)).astype(np.float32)
+          for _ in range(steps)]
+    dth, dm, dv = ([D(float(x)) for x in a] for a in (th, m, v))
+    Dlr, Db1, Db2, Deps = (D(float(x)) for x in (lr, b1, b2, eps))
+    f32 = lambda x: np.float32(float(x))          # noqa: E731 (decimal -> binary64 -> binary32)
+    for t, g in enumerate(gs, start=1):
+        oracle.adam(g, th, m, v, lr=float(lr), beta1=float(b1), beta2=float(b2), eps=float(eps),
+                    step=t)
+        bc1 = ctx.subtract(D(1), ctx.power(Db1, t))
+        bc2 = ctx.subtract(D(1), ctx.power(Db2, t))
+        for j in range(count):
+            gj = D(float(g[j]))
+            mn = ctx.add(ctx.multiply(Db1, dm[j]), ctx.multiply(ctx.subtract(D(1), Db1), gj))
+            vn = ctx.add(ctx.multiply(Db2, dv[j]),
+                         ctx.multiply(ctx.multiply(ctx.subtract(D(1), Db2), gj), gj))
+            m32, v32 = f32(mn), f32(vn)
+            mhat = ctx.divide(D(float(m32)), bc1)
+            vhat = ctx.divide(D(float(v32)), bc2)
+            delta = ctx.divide(ctx.multiply(Dlr, mhat), ctx.add(ctx.sqrt(vhat), Deps))
+            th32 = f32(ctx.subtract(dth[j], delta))
+            dm[j], dv[j], dth[j] = D(float(m32)), D(float(v32)), D(float(th32))
+            assert m[j] == m32 and v[j] == v32 and th[j] == th32, (t, j)
