@@ -62,8 +62,9 @@
  *    the ABI.  On an error no work has been enqueued, except DPOPT_ERR_CUDA
  *    from a launch, after which earlier launches of the same call may have run.
  *  - Threads: all entry points may be called from several host threads; the
- *    only shared state is a per-device status word and cached device
- *    attributes.
+ *    only shared state is a per-device status word, cached device attributes,
+ *    the process-wide kernel and gather policies, and the built-in array of
+ *    the allocation-free norm entry (whose concurrent calls race; see there).
  */
 #ifndef DPOPT_H
 #define DPOPT_H
