@@ -1,7 +1,7 @@
 """Parity harness: seeded inputs for the oracle and the CUDA path, the oracle's
 trajectory on (sampled) elements, and the tolerance check.
 
-Tolerance (spec: fp32 master/m/v within 2.4e-7 relative, ~2 ulp; bf16
+Tolerance (the required bound: fp32 master/m/v within 2.4e-7 relative, ~2 ulp; bf16
 output within 1 bf16 ulp).  "Relative" is taken against the scale of the
 terms each stored value is formed from, so that cancellation does not turn
 one rounding into many ulps:
