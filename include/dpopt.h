@@ -84,7 +84,7 @@ typedef struct CUevent_st *dpopt_event_t;
 typedef enum {
     DPOPT_OK = 0,
     DPOPT_ERR_INVALID_ARG = 1, /* a null/overlapping pointer, a size or hyper-parameter out of range */
-    DPOPT_ERR_UNSUPPORTED = 2, /* valid but beyond this build's limits (n_replicas > DPOPT_MAX_REPLICAS) */
+    DPOPT_ERR_UNSUPPORTED = 2, /* valid but beyond this library's limits (n_replicas > DPOPT_MAX_REPLICAS) */
     DPOPT_ERR_CUDA = 3,        /* a CUDA call failed; dpopt_last_error() has its message */
     DPOPT_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (reported by dpopt_stream_status) */
     DPOPT_ERR_BOUNDS = 5       /* bounds-checked build only: a kernel derived an index outside
