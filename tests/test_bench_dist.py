@@ -69,3 +69,19 @@ def test_reference_arm_under_torchrun_prints_once_from_rank0():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["unit"] == "G params/s"
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_default_timed_steps_are_about_five_seconds_of_the_workload():
+    """Without --steps the timed region is sized to the workload: about 5 s at
+    6.5 TB/s, between 10 and 20000 steps, so that every workload's default run
+    ends within minutes (70b_shard moves 168 GB per step)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    for name in ("tiny", "gpt2s", "1p3b", "70b_shard", "sweep_1000000000_64_fp32"):
+        wl = bench.resolve_workload(name)
+        k = bench.default_steps(wl)
+        assert 10 <= k <= 20000
+        per_step_s = wl.shard_elems * (wl.grad_bytes() * wl.n_replicas + 26) / 6.5e12
+        assert k == 20000 or abs(k * per_step_s - 5.0) < per_step_s + 1e-9
+    assert bench.default_steps(bench.resolve_workload("gpt2s")) == 20000
+    assert bench.default_steps(bench.resolve_workload("70b_shard")) == 193
