@@ -6,10 +6,12 @@ input: the N replica gradients of this rank's shard are averaged in fixed
 order, Adam updates the fp32 master/m/v, and the bf16 working copy is
 written -- one call of the C ABI.
 
-Default workload: the GPT-2-small-sized flat buffer (124M parameters, N = 4
-replicas, rank 0's 31M-parameter shard, 25M-element buckets).  Inputs are
-resident in HBM before the timed region; each step touches 1.05 GB, more
-than the 129 MB L2, so no flush is needed between steps.
+Default workload: one rank's ZeRO-3 shard of a 70B-parameter model at 64-way
+data parallelism (S = 70e9/64 = 1,093,750,000 parameters, N = 64 replica
+gradient slices per 4M-element bucket, 274 buckets, every bucket in one
+launch).  Inputs are resident in HBM before the timed region; each step
+touches 168 GB, far more than the 129 MB L2, so no flush is needed between
+steps.  --workload selects the others (tiny, gpt2s, 1p3b, sweep cells).
 
 Prints ONE JSON line (rank 0).  Under torchrun each rank runs its own
 rank's shard on its own GPU, with no collective on the data path (weak
@@ -54,9 +56,17 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=None,
                     help="untimed warm-up steps (default: 1 %% of the timed steps, 3 to 200)")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="gpt2s",
+    ap.add_argument("--workload", default="70b_shard",
                     help="tiny | gpt2s | 1p3b | 70b_shard | sweep_<S>_<N>_<bf16|fp32> "
-                         "(gpt2s is the default)")
+                         "(70b_shard is the default)")
+    ap.add_argument("--shard-params", type=int, default=0,
+                    help="keep only the first P parameters of the workload's shard (same N, "
+                         "buckets and values): a smaller case of the same kernel, for profiling")
+    ap.add_argument("--bucket-launch", choices=("table", "param"), default="table",
+                    help="bucket-slice workloads: 'table' -- every bucket in one launch, the "
+                         "launch table written to device memory (dpopt_reduce_adam_buckets_table); "
+                         "'param' -- dpopt_reduce_adam_buckets, tables in the kernel's parameter "
+                         "space (2048 slice pointers per launch).  Both give the same bits.")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--overlap", action="store_true",
                     help="measure bucket-as-ready overlap: gradients produced bucket by bucket on "
@@ -143,9 +153,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()
 
 
-def traffic_from_profiles(workload: str):
+def traffic_from_profiles(workload: str, shard_params: int, launches_per_step: float):
     """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the current kernel sources (else None).  A summary taken on a smaller case
+    of the same kernel records bytes per parameter, scaled here to the
+    parameters one launch updates."""
     path = os.path.join(ROOT, "profiles", f"reduce_adam_{workload}_traffic.txt")
     try:
         kv = {}
@@ -156,6 +168,8 @@ def traffic_from_profiles(workload: str):
                     kv[k.strip()] = v.strip()
         if kv.get("source_sha256") != kernel_source_hash():
             return None
+        if "dram_bytes_per_param" in kv:
+            return float(kv["dram_bytes_per_param"]) * shard_params / max(launches_per_step, 1.0)
         return float(kv["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
         return None
@@ -243,6 +257,12 @@ def oracle_rate(wl, host_grads, budget_s: float, threads: int, max_elems: int | 
             return done / el, chunk, calls
 
 
+def sample_elems(wl) -> int:
+    """Shard elements in the oracle's timed sample: 4M, fewer at large N (the
+    sample's N slices are generated on the host first)."""
+    return min(4_000_000, max(250_000, 64_000_000 // wl.n_replicas))
+
+
 def host_grads_for(wl, max_elems: int):
     """The rank's shard slices of step 1's gradients, generated on the host."""
     import synth
@@ -275,7 +295,7 @@ def run_reference(args, wl):
     if rank != 0:
         return None
     threads = len(os.sched_getaffinity(0))
-    grads = host_grads_for(wl, 4_000_000)
+    grads = host_grads_for(wl, sample_elems(wl))
     # size one step's sample so that warmup + steps take about a minute
     rate, _, _ = oracle_rate(wl, grads, 0.5, threads, max_elems=1_000_000)
     per_step = int(max(1, min(len(grads[0]), rate * 60.0 / max(1, args.steps + args.warmup))))
@@ -402,15 +422,21 @@ def run_ours(args, wl):
             raise SystemExit("adam_allgather runs on the full-buffer workloads")
         buckets = dev.bucket_slices()
         rows, offs = [b for _, b in buckets], [o for o, _ in buckets]
+        if args.bucket_launch == "table":
+            # every bucket in one launch: the launch table goes to device memory
+            table = torch.empty(dp.bucket_table_bytes(n, len(rows)), dtype=torch.uint8,
+                                device=device)
+        else:
+            table = None
+        # the call's arguments marshalled once, outside the timed region
+        call = dp.BucketStep(rows, offs, dev.master, dev.m, dev.v, dev.out, table)
         if args.optimizer == "adamw_clip":
             def step(t):
                 dp.grad_sqnorm_buckets(rows, offs, sqn, scratch, stream=stream)
-                dp.reduce_adamw_buckets(rows, offs, dev.master, dev.m, dev.v, dev.out, step=t,
-                                        opts=opts, stream=stream, **hp)
+                call.step(step=t, opts=opts, stream=stream, **hp)
         else:
             def step(t):
-                dp.reduce_adam_buckets(rows, offs, dev.master, dev.m, dev.v, dev.out, step=t,
-                                       stream=stream, **hp)
+                call.step(step=t, stream=stream, **hp)
 
     def barrier():
         if world > 1:
@@ -454,9 +480,17 @@ def run_ours(args, wl):
 
     # end to end through the public API: host gradients in, bf16 parameters out
     esize = dev.grads[0].element_size()
-    if n * S * esize > (8 << 30) or args.optimizer != "adam":
-        # (pinned host copies of the inputs would not fit sensibly; the end-to-end
-        # figure is taken for the default fused step)
+    if args.optimizer != "adam" or args.shard_params:
+        # (the end-to-end figure is taken for the plain fused step on whole workloads)
+        return _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks,
+                       None, None, stored)
+    if wl.layout == "slices" and min(4, -(-S // wl.bucket_elems)) * n * wl.bucket_elems * esize \
+            <= (8 << 30):
+        e2e, grads = e2e_ring(args, wl, dev, stream, hp, world, barrier, K)
+        return _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks,
+                       e2e, grads, stored)
+    if wl.layout == "slices" or n * S * esize > (8 << 30):
+        # (pinned host copies of whole replica shards would not fit sensibly)
         return _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks,
                        None, None, stored)
     hs = [torch.empty(S, dtype=dev.grads[0].dtype, pin_memory=True) for _ in range(n)]
@@ -516,6 +550,68 @@ def run_ours(args, wl):
                    grads, stored)
 
 
+def e2e_ring(args, wl, dev, stream, hp, world, barrier, K):
+    """End to end for bucket-slice workloads: every step, each bucket's N
+    gradient slices come from pinned host memory and the new bf16 shard goes to
+    pinned host memory, all inside the timed region.  The slices sit in a ring
+    of R pinned host bucket slots (bucket b reads slot b mod R, so a producer
+    could refill the other slots meanwhile); the one-launch bucket kernel reads
+    them in place over the host link and writes the bf16 parameters straight
+    to the pinned output.  The slots hold step 1's first R buckets and are not
+    refilled while timed: the bytes still cross the link every step, the
+    values repeat.  Returns (e2e dict, host gradient sample for the oracle)."""
+    import torch
+
+    import zero_mixed_precision_gb300 as dp
+    S, n, be = wl.shard_elems, wl.n_replicas, wl.bucket_elems
+    esize = dev.grads[0].element_size()
+    buckets = dev.bucket_slices()
+    nb = len(buckets)
+    R = min(nb, 4)
+    slots = []
+    for k in range(R):
+        ln = buckets[k][1][0].numel()
+        row = [torch.empty(be, dtype=dev.grads[0].dtype, pin_memory=True) for _ in range(n)]
+        for h, d in zip(row, buckets[k][1]):
+            h[:ln].copy_(d)
+        slots.append(row)
+    hout = torch.empty(S, dtype=torch.bfloat16, pin_memory=True)
+    rows = [[slots[b % R][r][:sl[0].numel()] for r in range(n)]
+            for b, (_, sl) in enumerate(buckets)]
+    offs = [o for o, _ in buckets]
+    table = torch.empty(dp.bucket_table_bytes(n, nb), dtype=torch.uint8, device=dev.device)
+    call = dp.BucketStep(rows, offs, dev.master, dev.m, dev.v, hout, table)
+    h2d, d2h = n * S * esize, S * 2
+    # about 3 s of timed steps at the host link's ~200 GB/s
+    Ke = int(max(2, min(args.e2e_steps, K, round(3.0 / ((h2d + d2h) / 200e9)))))
+    t0 = args.warmup + K + 1
+    with torch.cuda.stream(stream):
+        call.step(step=t0, stream=stream, **hp)   # untimed: first touch of the host pages
+        torch.cuda.synchronize(dev.device)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(Ke):
+            call.step(step=t0 + 1 + k, stream=stream, **hp)
+        e1.record(stream)
+        torch.cuda.synchronize(dev.device)
+        barrier()
+    dp.stream_status(stream)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev.device)
+    e2e = {"value": throughput(world, S, Ke, ms), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "host_link_gbs": (h2d + d2h) * Ke / (ms * 1e-3) / 1e9, "steps": Ke,
+           "path": f"{nb} buckets x {n} gradient slices per step read in place from a ring of "
+                   f"{R} pinned host bucket slots ({R * n * be * esize / 1e9:.2f} GB) by one "
+                   "dpopt_reduce_adam_buckets_table launch, bf16 parameters written into pinned "
+                   "host memory"}
+    # the oracle's sample: bucket 0's slices (the first elements of the shard)
+    cap = min(be, max(250_000, 64_000_000 // n))
+    grads = [h[:cap].view(torch.int16).numpy().view("uint16") if h.dtype == torch.bfloat16
+             else h[:cap].numpy() for h in slots[0]]
+    return e2e, grads
+
+
 def _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks, e2e,
             host_grads, stored=False):
     import torch.distributed as dist
@@ -545,7 +641,8 @@ def _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks
     value = throughput(world, S, K, elapsed_ms)
     peak, peak_kind = load_peaks()
     achieved = S * bpp / (kernel_ms / 1e3) / 1e9
-    traffic = traffic_from_profiles(wl.name)
+    traffic = (traffic_from_profiles(wl.name, S, launches / K)
+               if args.optimizer == "adam" and not args.shard_params else None)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -571,10 +668,11 @@ def _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks
     }
     if world == 1 and not args.no_cpu_baseline:
         threads = len(os.sched_getaffinity(0))
+        cap = sample_elems(wl)
         if host_grads is None:
-            host_grads = host_grads_for(wl, 4_000_000)
+            host_grads = host_grads_for(wl, cap)
         rate, chunk, calls = oracle_rate(wl, host_grads, args.cpu_seconds, threads,
-                                         max_elems=4_000_000)
+                                         max_elems=cap)
         line["cpu_baseline"] = {
             "value": rate / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{chunk:,} of the {S:,} shard params (N={n}), {calls} Adam steps, "
@@ -762,6 +860,11 @@ def main(argv=None):
     args = parse_args(argv)
     import synth
     wl = resolve_workload(args.workload)
+    if args.shard_params:
+        if not 0 < args.shard_params <= wl.shard_elems:
+            raise SystemExit(f"--shard-params must lie in [1, {wl.shard_elems}]")
+        wl = dataclasses.replace(wl, numel=args.shard_params * wl.n_replicas, shard_rank=0,
+                                 name=f"{wl.name}_first{args.shard_params}")
     args.steps_defaulted = args.steps is None
     if args.steps is None:
         args.steps = default_steps(wl)

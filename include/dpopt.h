@@ -215,6 +215,49 @@ int dpopt_reduce_adamw_buckets(const void *const *slice_table, int grad_dtype, i
                                float eps, int64_t step, const dpopt_step_options *opts,
                                dpopt_stream_t stream);
 
+/* Every bucket in ONE launch: the launch table in caller-owned device memory.
+ * dpopt_reduce_adam_buckets passes its pointer tables in the kernel's
+ * parameter space, which holds 2048 slice pointers per launch (32 buckets at
+ * 64 replicas), so one 70B model's ZeRO-3 shard at N = 64 in 4M-element
+ * buckets ("Почему training 70B модели требует optimizer sharding (ZeRO-3)?",
+ * sections 4 and 8: a 1/64 shard, reduce_bucket_size) takes nine launches per
+ * step.  This form writes the checked table into device memory the caller
+ * provides and runs every bucket in one launch of the direct-load kernel; its
+ * results are bitwise those of dpopt_reduce_adam_buckets (opts NULL) and
+ * dpopt_reduce_adamw_buckets (opts given).
+ *
+ * dpopt_bucket_table_bytes: bytes of `table` for n_buckets buckets of
+ *   n_replicas slices: 32 * (n_buckets + 1) + 8 * n_buckets * n_replicas.
+ *   Errors: DPOPT_ERR_INVALID_ARG for a null bytes_out, n_replicas outside
+ *   [1, DPOPT_MAX_REPLICAS] or n_buckets outside [0, 2^30].
+ *
+ * dpopt_reduce_adam_buckets_table:
+ *  slice_table, offsets, lens, n_buckets, states, hyper-parameters
+ *                 as for dpopt_reduce_adam_buckets (host arrays, read during
+ *                 the call only).
+ *  opts           NULL for plain Adam, else as for dpopt_reduce_adamw.
+ *  table          DEVICE pointer, 16-byte aligned, at least
+ *                 dpopt_bucket_table_bytes() bytes, owned by the caller and
+ *                 overlapping no state, output or gradient range.  The call
+ *                 enqueues on `stream` one host-to-device copy of the packed
+ *                 table into it, then the kernel that reads it; its previous
+ *                 contents do not matter.  It is stream ordered like the
+ *                 states: work on another stream must not touch it until this
+ *                 call's kernel has finished.
+ *  table_bytes    size of `table` in bytes.
+ * Errors: as for dpopt_reduce_adamw_buckets, plus DPOPT_ERR_INVALID_ARG for a
+ * null or misaligned table, too small a table_bytes, or a table overlapping a
+ * state, output or gradient range; DPOPT_ERR_CUDA if the copy or the launch
+ * fails. */
+int dpopt_bucket_table_bytes(int n_replicas, int64_t n_buckets, int64_t *bytes_out);
+int dpopt_reduce_adam_buckets_table(const void *const *slice_table, int grad_dtype,
+                                    int n_replicas, const int64_t *offsets, const int64_t *lens,
+                                    int64_t n_buckets, float *master_f32, float *m_f32,
+                                    float *v_f32, void *param_bf16_out, float lr, float beta1,
+                                    float beta2, float eps, int64_t step,
+                                    const dpopt_step_options *opts, void *table,
+                                    int64_t table_bytes, dpopt_stream_t stream);
+
 /* Squared L2 norm of this shard's averaged gradient (the clipping pre-pass):
  *   *sqnorm_out = sum_i (g_i * grad_unscale)^2      (fp64, DEVICE pointer)
  * with g_i the same fixed-order average the step computes.  Partial sums over
@@ -247,8 +290,15 @@ int dpopt_grad_sqnorm_buckets(const void *const *slice_table, int grad_dtype, in
  * shard to 2^31 elements (DPOPT_ERR_UNSUPPORTED beyond that, with a message
  * from dpopt_last_error()).  It allocates nothing and calls no allocating
  * routine.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  Every call on a device shares the one array, and each
+ * (cudaGetSymbolAddress) with that device current and keeps it for the
+ * process; make that first call before any stream capture (a call with
+ * numel = 0 does only that set-up and writes 0 to *sqnorm_out).  The kept
+ * address belongs to the device's primary context: it is not valid in other
+ * contexts made current through the driver API, nor after cudaDeviceReset.
+ * With lazy module loading (CUDA_MODULE_LOADING=LAZY, the default) the 4 MB
+ * are committed when the library's kernels are first used on the device, which
+ * may be this first call; if the device is full by then, it fails with
+ * DPOPT_ERR_CUDA (out of memory).  Every call on a device shares the one array, and each
  * call writes every partial it reads, so no state carries over between calls;
  * but calls that can run at the same time on the GPU (other streams, other host
  * threads) race on it -- serialise them.  Arguments, result and other errors

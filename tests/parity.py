@@ -11,10 +11,17 @@ one rounding into many ulps:
           delta~ = a*M/D is the update with |m_new| replaced by the m scale
           accumulated so far (a = lr/bc1, D = sqrt(v_new/bc2) + eps): the
           part of the master that a difference in m can move.
-Over several steps the allowances add up (a difference left by step t
-carries into step t+1), so step t is checked against 2.4e-7 times the sum
-of the scales of steps 1..t, floored at FLT_MIN.  bf16: ordered-integer
-distance <= 1, and the GPU's bf16 must equal RNE(its own master) exactly.
+Two checks use these scales:
+  per step (the stated bound): the oracle runs step t alone from the GPU's
+      own states after step t-1, and every value of step t must lie within
+      2.4e-7 times that step's scale (check_step);
+  trajectory: the oracle runs every step from the initial states; a
+      difference left by step t carries into step t+1, so step t is checked
+      against 2.4e-7 times the sum of the scales of steps 1..t.
+Both floor the allowance at FLT_MIN.  bf16: ordered-integer distance <= 1,
+and the GPU's bf16 must equal RNE(its own master) exactly.  Every per-step
+check records its largest errors (in ulps of the oracle's value) under its
+configuration's name; the test session prints them at the end.
 """
 from __future__ import annotations
 
@@ -244,3 +251,35 @@ def check(ref: StepRef, master, m, v, out, where: str = "") -> Stats:
     return Stats(int(master.size), ulps[0], ulps[1], ulps[2], worst,
                  float(np.mean(master.view(np.uint32) == ref.master.view(np.uint32))),
                  float(np.mean(out == ref.out)))
+
+
+# ---------------------------------------------------------------------------
+# per-step check: one oracle step from the GPU's own previous states
+# ---------------------------------------------------------------------------
+
+# configuration -> [checks, max ulp master, m, v, max err/tol, min bitwise master]
+ULP_LOG: dict[str, list] = {}
+
+
+def record(config: str, st: Stats) -> None:
+    e = ULP_LOG.setdefault(config, [0, 0.0, 0.0, 0.0, 0.0, 1.0])
+    e[0] += 1
+    e[1] = max(e[1], st.max_ulp_master)
+    e[2] = max(e[2], st.max_ulp_m)
+    e[3] = max(e[3], st.max_ulp_v)
+    e[4] = max(e[4], st.max_err_over_tol)
+    e[5] = min(e[5], st.bitwise_master)
+
+
+def check_step(wl: Workload, local_idx: np.ndarray, t: int, prev, got, config: str,
+               grads_fn=None, hp=None, weight_decay: float = 0.0, gscale_fn=None) -> Stats:
+    """Step t on its own: the oracle starts from prev = (master, m, v), the
+    GPU's states at local_idx after step t-1, and got = (master, m, v, bf16)
+    after step t must match within 2.4e-7 times step t's scales (one step's
+    allowance, nothing carried over) and 1 bf16 ulp."""
+    init = tuple(np.array(x, dtype=np.float32, copy=True) for x in prev)
+    ref = oracle_trajectory(wl, local_idx, t, t, grads_fn=grads_fn, init=init, hp=hp,
+                            weight_decay=weight_decay, gscale_fn=gscale_fn)[0]
+    st = check(ref, *got, where=f"{config} (step {t} alone)")
+    record(config, st)
+    return st

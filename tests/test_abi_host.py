@@ -175,6 +175,36 @@ def test_bucket_entries_reject_bad_arguments(dp):
     assert dp.dpopt_reduce_adam_buckets(G[:64] * 2, 0, 65, [0], [10], *args) == 2
 
 
+def test_bucket_table_bytes(dp):
+    # 274 buckets of 64 slices (a 70B model's 1/64 shard in 4M buckets)
+    assert dp.dpopt_bucket_table_bytes(64, 274) == (0, 32 * 275 + 8 * 274 * 64)
+    assert dp.dpopt_bucket_table_bytes(1, 0) == (0, 32)
+    assert dp.dpopt_bucket_table_bytes(0, 1)[0] == dp.DPOPT_ERR_INVALID_ARG
+    assert dp.dpopt_bucket_table_bytes(65, 1)[0] == dp.DPOPT_ERR_INVALID_ARG
+    assert dp.dpopt_bucket_table_bytes(2, -1)[0] == dp.DPOPT_ERR_INVALID_ARG
+
+
+def test_table_entry_rejects_bad_arguments(dp):
+    TAB = 0xF0_0000_0000
+    need = dp.dpopt_bucket_table_bytes(2, 2)[1]
+
+    def call(table=TAB, nbytes=need, table_slices=G[:4], offs=(0, 10), lens=(10, 10), n=2,
+             master=MASTER, opts=None, step=1):
+        return dp.dpopt_reduce_adam_buckets_table(table_slices, 0, n, list(offs), list(lens),
+                                                  master, M, V, OUT, *HP, step, opts, table,
+                                                  nbytes, 0)
+    assert call(table=0) == 1                    # no table
+    assert call(table=TAB + 8) == 1              # not 16-byte aligned
+    assert call(nbytes=need - 1) == 1            # too small
+    assert call(table=MASTER) == 1               # the table overlaps the master range
+    assert call(table=G[1] - 64) == 1            # a slice overlaps the table
+    assert call(offs=(0, 5)) == 1                # overlapping buckets
+    assert call(step=0) == 1
+    assert call(n=65, table_slices=G[:64] * 3, offs=(0, 10), lens=(10, 10)) == 2
+    assert call(opts=dp.StepOptions(-0.1, 0.0, None, 0.0)) == 1
+    assert dp.dpopt_last_error() != ""
+
+
 def test_sqnorm_scratch_bytes(dp):
     assert dp.dpopt_grad_sqnorm_scratch_bytes(0, 1) == (0, 8)
     assert dp.dpopt_grad_sqnorm_scratch_bytes(65536, 1) == (0, 8 * (65536 // 4096 + 1))

@@ -103,13 +103,22 @@ def _clipped_run(wl, steps, wd, max_norm, unscale=0.0):
     part = torch.zeros(wl.n_replicas, dtype=torch.float64, device="cuda")
     scratch = _scratch(S)
     for t in steps:
-        grads = [to_dev_grad(g) for g in _full_grads(wl, t)]
+        prev = (f32(dm), f32(dmm), f32(dv))
+        host = _full_grads(wl, t)
+        grads = [to_dev_grad(g) for g in host]
         for r in range(wl.n_replicas):
             dp.grad_sqnorm(grads, r, part[r:r + 1], scratch, grad_unscale=unscale)
         torch.sum(part, dim=0, keepdim=True, out=total)
         opts = dp.step_options(weight_decay=wd, max_grad_norm=max_norm, grad_sqnorm=total,
                                grad_unscale=unscale)
         dp.reduce_adamw(grads, wl.shard_rank, S, dm, dmm, dv, dout, step=t, opts=opts, **HP)
+        dp.stream_status()
+        # step t on its own, from the GPU's previous states
+        un = unscale if unscale else 1.0
+        c = oracle.grad_scale(oracle.grad_sqnorm(host, 0, wl.numel, un), max_norm, un)
+        parity.check_step(wl, np.arange(S), t, prev, (f32(dm), f32(dmm), f32(dv), u16(dout)),
+                          f"adamw+clip N={wl.n_replicas} S={S}", weight_decay=wd,
+                          gscale_fn=lambda _t, _g: c)
     dp.stream_status()
     return f32(dm), f32(dmm), f32(dv), u16(dout)
 

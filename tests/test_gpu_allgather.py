@@ -107,14 +107,19 @@ def test_fused_step_allgather_equals_step_then_allgather(n, S, kind, rank):
     wl = _small_workload(n, S, kind=kind, rank=rank, seed=23)
     numel = n * S
     res = []
+    idx = np.unique(np.concatenate([np.arange(0, S, 97), np.arange(max(0, S - 9), S)]))
     for fused in (True, False):
         st = _states(wl)
         reps = [torch.full((numel,), 0x7FA1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
                 for _ in range(n)]   # a NaN bit pattern no step writes
         for t in (1, 2):
+            prev = [f32(x)[idx] for x in st]
             grads = [to_dev_grad(g) for g in _host_full_buffers(wl, t)]
             if fused:
                 dp.reduce_adam_allgather(grads, rank, S, *st, reps, step=t, **HP)
+                dp.stream_status()
+                got = [f32(x)[idx] for x in st] + [u16(reps[(rank + 1) % n])[rank * S + idx]]
+                parity.check_step(wl, idx, t, prev, got, f"fused gather N={n} S={S}")
             else:
                 own = reps[rank][rank * S:(rank + 1) * S]
                 dp.reduce_adam(grads, rank, S, *st, own, step=t, **HP)
@@ -123,7 +128,6 @@ def test_fused_step_allgather_equals_step_then_allgather(n, S, kind, rank):
         res.append([f32(x) for x in st] + [u16(r) for r in reps])
     for a, b in zip(*res):
         assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
-    idx = np.unique(np.concatenate([np.arange(0, S, 97), np.arange(max(0, S - 9), S)]))
     ref = oracle_trajectory(wl, idx, 1, 2)[-1]
     th, m, v = (x[idx] for x in res[0][:3])
     for r in range(n):

@@ -76,7 +76,9 @@ def test_loss_scaled_run_with_overflows_matches_the_oracle(max_norm):
     part = torch.zeros(n, dtype=torch.float64, device="cuda")
     total = torch.zeros(1, dtype=torch.float64, device="cuda")
     for k in range(1, 11):
-        grads = [to_dev_grad(b) for b in full(k)]
+        prev = (f32(dm), f32(dmm), f32(dv))
+        host = full(k)
+        grads = [to_dev_grad(b) for b in host]
         for r in range(n):   # every rank's norm; their sum is the one-scalar all-reduce
             dp.amp_sqnorm(grads, r, state, part[r:r + 1], scratch)
         torch.sum(part, dim=0, keepdim=True, out=total)
@@ -88,7 +90,16 @@ def test_loss_scaled_run_with_overflows_matches_the_oracle(max_norm):
         assert bool(st.last_overflow) == overflow, k
         assert (st.scale, st.step) == (scale, steps), (k, st.scale, st.step, scale, steps)
         if steps > 0:
-            parity.check(ref, f32(dm), f32(dmm), f32(dv), u16(dout), where=f"amp k={k}")
+            got = (f32(dm), f32(dmm), f32(dv), u16(dout))
+            parity.check(ref, *got, where=f"amp k={k}")
+        if not overflow:
+            # this iteration's step on its own, from the GPU's previous states
+            un = 1.0 / refs[k - 2][2] if k > 1 else 1.0 / cfg_args["init_scale"]
+            c = oracle.grad_scale(oracle.grad_sqnorm(host, 0, wl.numel, un), max_norm, un)
+            base = wl.shard_base
+            parity.check_step(wl, np.arange(S), steps, prev, got, f"amp fp16 N={n} S={S}",
+                              grads_fn=lambda r, _t: host[r][base:base + S], weight_decay=0.01,
+                              gscale_fn=lambda _t, _g: c)
     assert st.skipped == 3
 
 

@@ -59,7 +59,11 @@ def test_host_gradients_and_host_output_equal_the_device_call(layout):
     states = {k: _clone_states(dev) for k in ("device", "host")}
     outs = {"device": torch.empty_like(dev.out),
             "host": torch.empty(dev.out.shape, dtype=torch.bfloat16, pin_memory=True)}
+    rng = np.random.default_rng(9)
+    idx = np.unique(np.concatenate([rng.integers(0, wl.shard_elems, 20_000),
+                                    np.arange(wl.shard_elems - 50, wl.shard_elems)]))
     for t in (1, 2):
+        prev = [f32(x)[idx] for x in states["host"]]
         dev.fill_grads(t)
         torch.cuda.synchronize()
         host_grads = [_pinned_like(g) for g in dev.grads]
@@ -72,14 +76,13 @@ def test_host_gradients_and_host_output_equal_the_device_call(layout):
                 dp.reduce_adam_bucket(grads, 0, th, m, v, outs[kind], step=t, **hp)
         torch.cuda.synchronize()
         dp.stream_status()
+        got = [f32(x)[idx] for x in states["host"]] + [u16(outs["host"])[idx]]
+        parity.check_step(wl, idx, t, prev, got, f"host operands ({layout})")
     for kind in ("device", "host"):
         th, m, v = states[kind]
         runs[kind] = [f32(th), f32(m), f32(v), u16(outs[kind])]
     for a, b in zip(runs["device"], runs["host"]):
         assert _same(a, b)
-    rng = np.random.default_rng(9)
-    idx = np.unique(np.concatenate([rng.integers(0, wl.shard_elems, 20_000),
-                                    np.arange(wl.shard_elems - 50, wl.shard_elems)]))
     refs = oracle_trajectory(wl, idx, 1, 2)
     parity.check(refs[-1], *(x[idx] for x in runs["host"]), where=f"host operands ({layout})")
 

@@ -49,11 +49,15 @@ def test_when_ready_equals_the_batched_step_and_the_oracle():
     hp = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps)
     producer, consumer = torch.cuda.Stream(), torch.cuda.Stream()
     results = []
+    rng = np.random.default_rng(5)
+    idx = np.unique(np.concatenate([rng.integers(0, wl.shard_elems, 20_000),
+                                    np.arange(wl.shard_elems - 100, wl.shard_elems)]))
     for mode in ("ready", "batched"):
         dev = DeviceWorkload(wl)
         dev.fill_states()
         torch.cuda.synchronize()
         for t in (1, 2):
+            prev = [f32(x)[idx] for x in (dev.master, dev.m, dev.v)]
             nb = -(-wl.shard_elems // wl.bucket_elems)
             events = [torch.cuda.Event() for _ in range(nb)]
             buckets = _produce(dev, wl, t, producer, events)
@@ -68,12 +72,12 @@ def test_when_ready_equals_the_batched_step_and_the_oracle():
                                        stream=consumer, **hp)
             consumer.synchronize()
             dp.stream_status(consumer)
+            if mode == "ready":
+                got = [f32(x)[idx] for x in (dev.master, dev.m, dev.v)] + [u16(dev.out)[idx]]
+                parity.check_step(wl, idx, t, prev, got, "when_ready")
         results.append([f32(dev.master), f32(dev.m), f32(dev.v), u16(dev.out)])
     for a, b in zip(*results):
         assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
-    rng = np.random.default_rng(5)
-    idx = np.unique(np.concatenate([rng.integers(0, wl.shard_elems, 20_000),
-                                    np.arange(wl.shard_elems - 100, wl.shard_elems)]))
     refs = oracle_trajectory(wl, idx, 1, 2)
     parity.check(refs[-1], *(x[idx] for x in results[0]), where="when_ready")
 

@@ -72,14 +72,17 @@ def _host_full_buffers(wl, t):
     return out
 
 
-def _run_small_full(wl, steps=(1, 2), entry="full", bucket=None, hp=HP):
-    """Host-generated inputs, uploaded; returns final device states as numpy."""
+def _run_small_full(wl, steps=(1, 2), entry="full", bucket=None, hp=HP, per_step=True):
+    """Host-generated inputs, uploaded; returns final device states as numpy.
+    per_step: every step is also checked on its own against one oracle step
+    from the GPU's previous states (the stated per-value bound)."""
     S = wl.shard_elems
     gidx = wl.shard_base + np.arange(S, dtype=np.int64)
     master, m, v = parity.states_host(wl, gidx)
     dm, dmm, dv = (torch.from_numpy(x.copy()).cuda() for x in (master, m, v))
     dout = torch.empty(S, dtype=torch.bfloat16, device="cuda")
     for t in steps:
+        prev = (f32(dm), f32(dmm), f32(dv)) if per_step else None
         grads = [to_dev_grad(g) for g in _host_full_buffers(wl, t)]
         if entry == "full":
             dp.reduce_adam(grads, wl.shard_rank, bucket or wl.bucket_elems, dm, dmm, dv, dout,
@@ -98,8 +101,17 @@ def _run_small_full(wl, steps=(1, 2), entry="full", bucket=None, hp=HP):
                 rows.append([g[wl.shard_base + off:wl.shard_base + off + ln] for g in grads])
                 offs.append(off)
             dp.reduce_adam_buckets(rows, offs, dm, dmm, dv, dout, step=t, **hp)
+        if per_step:
+            dp.stream_status()
+            parity.check_step(wl, np.arange(S), t, prev, (f32(dm), f32(dmm), f32(dv), u16(dout)),
+                              _config_name(wl), hp=hp)
     dp.stream_status()
     return f32(dm), f32(dmm), f32(dv), u16(dout)
+
+
+def _config_name(wl):
+    kind = ("bf16", "fp32", "fp16")[wl.grad_kind]
+    return f"N={wl.n_replicas} S={wl.shard_elems} {kind}"
 
 
 # ---------------------------------------------------------------------------
@@ -132,12 +144,14 @@ def test_tiny_every_element_three_steps():
     dev = DeviceWorkload(wl)
     dev.fill_states()
     for t in range(1, wl.steps + 1):
+        prev = (f32(dev.master), f32(dev.m), f32(dev.v))
         dev.fill_grads(t)
         dp.reduce_adam(dev.grads, wl.shard_rank, wl.bucket_elems, dev.master, dev.m, dev.v,
                        dev.out, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, step=t)
         dp.stream_status()
-        parity.check(refs[t - 1], f32(dev.master), f32(dev.m), f32(dev.v), u16(dev.out),
-                     where=f"tiny t={t}")
+        got = (f32(dev.master), f32(dev.m), f32(dev.v), u16(dev.out))
+        parity.check(refs[t - 1], *got, where=f"tiny t={t}")
+        parity.check_step(wl, np.arange(S), t, prev, got, "tiny")
 
 
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 8, 13, 64])
@@ -396,9 +410,15 @@ def _fits(wl) -> bool:
 
 
 def _run_full_size(wl, entry):
+    """The workload at its full size, sampled elements checked after every
+    measured step: against the oracle's trajectory, and step by step from the
+    GPU's own previous states.  entry: "full" (full replica buffers), "buckets"
+    (the parameter-space bucket table) or "table" (every bucket in one launch)."""
     _need_gpu()
     if not _fits(wl):
-        pytest.skip(f"{wl.name} needs {workload_bytes(wl) / 1e9:.1f} GB of device memory")
+        free, _ = torch.cuda.mem_get_info()
+        pytest.skip(f"{wl.name} needs {workload_bytes(wl) / 1e9:.1f} GB of device memory, "
+                    f"{free / 1e9:.1f} GB free (4 GB kept back)")
     rng = np.random.default_rng(wl.seed)
     idx = _sample(wl.shard_elems, wl.bucket_elems, rng)
     t1 = wl.warmup_steps + wl.steps
@@ -407,19 +427,28 @@ def _run_full_size(wl, entry):
     dev.fill_states()
     tidx = torch.from_numpy(idx).cuda()
     stats = []
+    if entry != "full":
+        bs = dev.bucket_slices()
+        table = (torch.empty(dp.bucket_table_bytes(wl.n_replicas, len(bs)), dtype=torch.uint8,
+                             device="cuda") if entry == "table" else None)
+        call = dp.BucketStep([s for _, s in bs], [o for o, _ in bs], dev.master, dev.m, dev.v,
+                             dev.out, table)
     for t in range(1, t1 + 1):
+        prev = (f32(dev.master[tidx]), f32(dev.m[tidx]), f32(dev.v[tidx]))
         dev.fill_grads(t)
         hp = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, step=t)
+        launches = dp.dpopt_launch_count()
         if entry == "full":
             dp.reduce_adam(dev.grads, wl.shard_rank, wl.bucket_elems, dev.master, dev.m, dev.v,
                            dev.out, **hp)
         else:
-            bs = dev.bucket_slices()
-            dp.reduce_adam_buckets([s for _, s in bs], [o for o, _ in bs], dev.master, dev.m,
-                                   dev.v, dev.out, **hp)
+            call.step(**hp)
+        if entry == "table":
+            assert dp.dpopt_launch_count() - launches == 1
         dp.stream_status()
+        got = (f32(dev.master[tidx]), f32(dev.m[tidx]), f32(dev.v[tidx]), u16(dev.out[tidx]))
+        parity.check_step(wl, idx, t, prev, got, wl.name)
         if t > wl.warmup_steps:
-            got = (f32(dev.master[tidx]), f32(dev.m[tidx]), f32(dev.v[tidx]), u16(dev.out[tidx]))
             stats.append(parity.check(refs[t - 1], *got, where=f"{wl.name} t={t}"))
     del dev
     torch.cuda.empty_cache()
@@ -437,7 +466,9 @@ def test_1p3b_buffer_rank3_sampled_prewarmed():
 
 
 def test_70b_shard_n64_bucket_slices_sampled():
-    st = _run_full_size(synth.WORKLOADS["70b_shard"], "buckets")
+    """The 70B model's 1/64 shard as the benchmark runs it: 274 buckets of 64
+    slices, every bucket in one launch."""
+    st = _run_full_size(synth.WORKLOADS["70b_shard"], "table")
     assert min(s.bitwise_master for s in st) > 0.999
 
 
@@ -449,6 +480,11 @@ def test_sweep_cells_sampled(S, n, kind):
     _run_full_size(wl, "buckets")
 
 
-@pytest.mark.parametrize("n,kind", [(8, 0), (64, 0), (64, 1)])
-def test_sweep_large_cells_sampled(n, kind):
-    _run_full_size(synth.sweep_cell(256_000_000, n, kind), "buckets")
+@pytest.mark.parametrize("S", [256_000_000, 1_000_000_000])
+@pytest.mark.parametrize("n", synth.SWEEP_REPLICAS)
+@pytest.mark.parametrize("kind", [0, 1])
+def test_sweep_large_cells_sampled(S, n, kind):
+    """Every cell of the sweep at 256M and 1B that fits the device: fp32
+    replicas of 1e9 elements are 4 GB each, so byte offsets pass 2^32.  A cell
+    that does not fit (fp32 x 64 x 1B needs 272 GB) is skipped with its size."""
+    _run_full_size(synth.sweep_cell(S, n, kind), "buckets")

@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 
 pytestmark = pytest.mark.gpu
@@ -60,8 +61,17 @@ def test_noalloc_matches_the_scratch_entry_point_twice_in_a_row(n, S, dtype, uns
         assert dp.dpopt_stream_status(stream) == 0
         w, g = float(want.item()), float(got.item())
         assert np.isfinite(g) and w > 0
-        # the tolerance the norm tests use (relative S * 2^-53 per rounded sum)
-        assert g == pytest.approx(w, rel=4 * S * 2.0 ** -53)
+        # the same kernels over the same fixed chunks in the same order: the
+        # same bits, so a stale or misplaced partial cannot hide in a tolerance
+        assert got.view(torch.int64).item() == want.view(torch.int64).item(), (g, w)
+        # and the oracle's value: both sides sum S non-negative terms, the
+        # oracle sequentially in fp64, so they agree within 4 S 2^-53 relative
+        kind = 0 if dtype == torch.bfloat16 else 1
+        host = [synth.host_fill(kind, rank * S, S, 77, synth.stream_id(1, r, step),
+                                synth.Dist(r * 1e-5, 1e-3, outlier_p=0.01, outlier_scale=100.0))
+                for r in range(n)]
+        ref = oracle.grad_sqnorm(host, 0, S, unscale if unscale else 1.0)
+        assert g == pytest.approx(ref, rel=4 * S * 2.0 ** -53)
 
 
 def test_noalloc_rejects_shards_beyond_its_array():
@@ -72,3 +82,16 @@ def test_noalloc_rejects_shards_beyond_its_array():
                                       0xF0_0000_0000, 0)
     assert rc == dp.DPOPT_ERR_UNSUPPORTED
     assert "2147483648" in dp.dpopt_last_error()
+
+
+def test_noalloc_empty_shard_sets_up_and_writes_zero():
+    """A call with an empty shard does only the device's set-up (the array's
+    address) and writes 0, so callers can make it before a stream capture."""
+    dp = _lib()
+    out = torch.full((1,), float("nan"), dtype=torch.float64, device="cuda")
+    g = torch.empty(0, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    assert dp.dpopt_grad_sqnorm_noalloc([g.data_ptr() or 0x10_0000_0000] * 2, dp.DPOPT_GRAD_BF16,
+                                        2, 0, 0, 0.0, out.data_ptr(), stream) == 0
+    assert dp.dpopt_stream_status(stream) == 0
+    assert out.item() == 0.0

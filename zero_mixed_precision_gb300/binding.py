@@ -89,6 +89,9 @@ _SIGS = {
                                   _P], _I),
     "dpopt_reduce_adam_buckets": ([_PP, _I, _I, _PI64, _PI64, _I64, _P, _P, _P, _P, _F, _F, _F, _F,
                                    _I64, _P], _I),
+    "dpopt_bucket_table_bytes": ([_I, _I64, _PI64], _I),
+    "dpopt_reduce_adam_buckets_table": ([_PP, _I, _I, _PI64, _PI64, _I64, _P, _P, _P, _P, _F, _F,
+                                         _F, _F, _I64, _POPT, _P, _I64, _P], _I),
     "dpopt_stream_status": ([_P], _I),
     "dpopt_status_string": ([_I], ctypes.c_char_p),
     "dpopt_last_error": ([], ctypes.c_char_p),
@@ -196,6 +199,25 @@ def dpopt_reduce_adam_buckets(slice_table: Sequence[int], grad_dtype: int, n_rep
     return _lib.dpopt_reduce_adam_buckets(_ptr_array(slice_table), grad_dtype, n_replicas, offs,
                                           lns, nb, master, m, v, param_bf16_out, lr, beta1, beta2,
                                           eps, step, stream)
+
+
+def dpopt_bucket_table_bytes(n_replicas: int, n_buckets: int) -> tuple[int, int]:
+    out = ctypes.c_int64(0)
+    rc = _lib.dpopt_bucket_table_bytes(n_replicas, n_buckets, ctypes.byref(out))
+    return rc, out.value
+
+
+def dpopt_reduce_adam_buckets_table(slice_table: Sequence[int], grad_dtype: int, n_replicas: int,
+                                    offsets: Sequence[int], lens: Sequence[int], master: int,
+                                    m: int, v: int, param_bf16_out: int, lr: float, beta1: float,
+                                    beta2: float, eps: float, step: int, opts, table: int,
+                                    table_bytes: int, stream: int = 0) -> int:
+    nb = len(offsets)
+    offs = (ctypes.c_int64 * nb)(*offsets)
+    lns = (ctypes.c_int64 * nb)(*lens)
+    return _lib.dpopt_reduce_adam_buckets_table(
+        _ptr_array(slice_table), grad_dtype, n_replicas, offs, lns, nb, master, m, v,
+        param_bf16_out, lr, beta1, beta2, eps, step, _opts(opts), table, table_bytes, stream)
 
 
 def _opts(opts):
@@ -452,6 +474,71 @@ def reduce_adam_buckets(bucket_slices, offsets, master, m, v, param_bf16_out, *,
                                    _operand(m), _operand(v), _operand(param_bf16_out), lr,
                                    beta1, beta2, eps, step, _stream_handle(stream))
     _check(rc, "dpopt_reduce_adam_buckets")
+
+
+def bucket_table_bytes(n_replicas: int, n_buckets: int) -> int:
+    """Device bytes the one-launch bucket entry needs for its launch table."""
+    rc, nbytes = dpopt_bucket_table_bytes(n_replicas, n_buckets)
+    _check(rc, "dpopt_bucket_table_bytes")
+    return nbytes
+
+
+def reduce_adam_buckets_table(bucket_slices, offsets, master, m, v, param_bf16_out, table, *,
+                              lr: float, beta1: float, beta2: float, eps: float, step: int,
+                              opts=None, stream=None) -> None:
+    """reduce_adam_buckets in one launch whatever the bucket count: `table` is a
+    device tensor of at least bucket_table_bytes(N, len(bucket_slices)) bytes
+    that receives the launch table (opts: None for Adam, or step_options())."""
+    n = len(bucket_slices[0])
+    dt = _grad_dtype(bucket_slices[0][0])
+    ptrs = [_operand(t) for row in bucket_slices for t in row]
+    lens = [row[0].numel() for row in bucket_slices]
+    nbytes = table.numel() * table.element_size()
+    rc = dpopt_reduce_adam_buckets_table(ptrs, dt, n, list(offsets), lens, _operand(master),
+                                         _operand(m), _operand(v), _operand(param_bf16_out), lr,
+                                         beta1, beta2, eps, step, opts, _operand(table), nbytes,
+                                         _stream_handle(stream))
+    _check(rc, "dpopt_reduce_adam_buckets_table")
+
+
+class BucketStep:
+    """The arguments of one batched-bucket call marshalled once: a 274-bucket,
+    64-replica list is 17,536 pointers, which take milliseconds to convert on
+    every call.  step() then passes the same arrays to
+    dpopt_reduce_adam_buckets_table (with `table`: one launch) or to
+    dpopt_reduce_adam_buckets (without: launches of at most 2048 pointers).
+    The tensors must stay alive and in place while the object is used."""
+
+    def __init__(self, bucket_slices, offsets, master, m, v, param_bf16_out, table=None):
+        self.n = len(bucket_slices[0])
+        self.dtype = _grad_dtype(bucket_slices[0][0])
+        ptrs = [_operand(t) for row in bucket_slices for t in row]
+        self.nb = len(bucket_slices)
+        self.ptrs = _ptr_array(ptrs)
+        self.offs = (ctypes.c_int64 * self.nb)(*offsets)
+        self.lens = (ctypes.c_int64 * self.nb)(*[row[0].numel() for row in bucket_slices])
+        self.states = [_operand(t) for t in (master, m, v, param_bf16_out)]
+        self.table = None if table is None else _operand(table)
+        self.table_bytes = 0 if table is None else table.numel() * table.element_size()
+
+    def step(self, *, lr: float, beta1: float, beta2: float, eps: float, step: int, opts=None,
+             stream=None) -> None:
+        st = _stream_handle(stream)
+        if self.table is not None:
+            rc = _lib.dpopt_reduce_adam_buckets_table(
+                self.ptrs, self.dtype, self.n, self.offs, self.lens, self.nb, *self.states, lr,
+                beta1, beta2, eps, step, _opts(opts), self.table, self.table_bytes, st)
+            _check(rc, "dpopt_reduce_adam_buckets_table")
+        elif opts is not None:
+            rc = _lib.dpopt_reduce_adamw_buckets(self.ptrs, self.dtype, self.n, self.offs,
+                                                 self.lens, self.nb, *self.states, lr, beta1,
+                                                 beta2, eps, step, _opts(opts), st)
+            _check(rc, "dpopt_reduce_adamw_buckets")
+        else:
+            rc = _lib.dpopt_reduce_adam_buckets(self.ptrs, self.dtype, self.n, self.offs,
+                                                self.lens, self.nb, *self.states, lr, beta1,
+                                                beta2, eps, step, st)
+            _check(rc, "dpopt_reduce_adam_buckets")
 
 
 def step_options(weight_decay: float = 0.0, max_grad_norm: float = 0.0, grad_sqnorm=None,

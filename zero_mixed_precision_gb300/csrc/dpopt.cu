@@ -227,10 +227,23 @@ int dispatch(const LaunchParams<MS, MP>& p, int grad_dtype, bool ext, cudaStream
 // thread), 1 when everything is 16-byte aligned, else 0 (one element at a
 // time).  Null state pointers (the norm) count as aligned.  Returns the index
 // total (0 when every segment is empty).
+int vec_level(const float* master, const float* m, const float* v, const uint16_t* out,
+              const SegDesc& d, int n, int grad_dtype) {
+  auto aligned32 = [](const void* q) { return ((uintptr_t)q & 31u) == 0; };
+  bool v16 = aligned16(master + d.state_off) && aligned16(m + d.state_off) &&
+             aligned16(v + d.state_off) && aligned16(out + d.state_off);
+  bool v32 = aligned32(master + d.state_off) && aligned32(m + d.state_off) &&
+             aligned32(v + d.state_off);
+  for (int r = 0; r < n; ++r) {
+    v16 = v16 && aligned16(d.ptrs[r]);
+    if (grad_dtype == DPOPT_GRAD_F32) v32 = v32 && aligned32(d.ptrs[r]);
+  }
+  return v16 ? (v32 ? 2 : 1) : 0;
+}
+
 template <int MS, int MP>
 int64_t fill_segments(LaunchParams<MS, MP>& p, const SegDesc* segs, int s0, int s1, int n,
                       int64_t unit, int grad_dtype) {
-  auto aligned32 = [](const void* q) { return ((uintptr_t)q & 31u) == 0; };
   int64_t units = 0;
   int nseg = 0;
   for (int s = s0; s < s1; ++s) {
@@ -241,16 +254,8 @@ int64_t fill_segments(LaunchParams<MS, MP>& p, const SegDesc* segs, int s0, int 
     sg.state_off = d.state_off;
     sg.len = d.len;
     sg.ptr_base = nseg * n;
-    bool v16 = aligned16(p.master + d.state_off) && aligned16(p.m + d.state_off) &&
-               aligned16(p.v + d.state_off) && aligned16(p.out + d.state_off);
-    bool v32 = aligned32(p.master + d.state_off) && aligned32(p.m + d.state_off) &&
-               aligned32(p.v + d.state_off);
-    for (int r = 0; r < n; ++r) {
-      p.gptr[nseg * n + r] = d.ptrs[r];
-      v16 = v16 && aligned16(d.ptrs[r]);
-      if (grad_dtype == DPOPT_GRAD_F32) v32 = v32 && aligned32(d.ptrs[r]);
-    }
-    sg.vec = v16 ? (v32 ? 2 : 1) : 0;
+    for (int r = 0; r < n; ++r) p.gptr[nseg * n + r] = d.ptrs[r];
+    sg.vec = vec_level(p.master, p.m, p.v, p.out, d, n, grad_dtype);
     units += (d.len + unit - 1) / unit;
     ++nseg;
   }
@@ -535,6 +540,93 @@ int buckets_impl(const void* const* slice_table, int grad_dtype, int n_replicas,
              stream);
 }
 
+// Bytes of a device-resident launch table for nb buckets of n replicas: nb + 1
+// segment records (the last closes the prefix sums), then nb * n pointers.
+int64_t table_bytes_for(int n, int64_t nb) {
+  return (int64_t)sizeof(Seg) * (nb + 1) + (int64_t)sizeof(void*) * nb * n;
+}
+
+// The batched-bucket step with its launch table written into caller-owned
+// device memory: one launch for every bucket, however many.
+int table_impl(const void* const* slice_table, int grad_dtype, int n_replicas,
+               const int64_t* offsets, const int64_t* lens, int64_t n_buckets, float* master,
+               float* m, float* v, void* out, float lr, float beta1, float beta2, float eps,
+               int64_t step, const dpopt_step_options* opts, void* table, int64_t table_bytes,
+               cudaStream_t stream) {
+  int rc = check_replicas(n_replicas, grad_dtype);
+  if (rc) return rc;
+  rc = check_hyper(lr, beta1, beta2, eps, step);
+  if (rc) return rc;
+  Hyper h = make_hyper(lr, beta1, beta2, eps, step, n_replicas);
+  bool ext = false;
+  rc = apply_options(opts, lr, h, &ext);
+  if (rc) return rc;
+  if (n_buckets < 0 || n_buckets > ((int64_t)1 << 30))
+    return fail(DPOPT_ERR_INVALID_ARG, "n_buckets must lie in [0, 2^30]");
+  const int64_t need = table_bytes_for(n_replicas, n_buckets);
+  if (n_buckets > 0 && (!table || ((uintptr_t)table & 15u)))
+    return fail(DPOPT_ERR_INVALID_ARG, "table must be a non-null, 16-byte aligned pointer");
+  if (n_buckets > 0 && table_bytes < need)
+    return fail(DPOPT_ERR_INVALID_ARG, "table holds %lld bytes, %lld needed",
+                (long long)table_bytes, (long long)need);
+  std::vector<SegDesc> segs;
+  int64_t lo = 0, hi = 0;
+  rc = build_buckets(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets, segs, &lo, &hi);
+  if (rc || segs.empty()) return rc;
+  Range avoid[5];
+  rc = check_states(master, m, v, out, lo, hi, avoid);
+  if (rc) return rc;
+  const int nseg = (int)segs.size();
+  const int64_t bytes = table_bytes_for(n_replicas, nseg);
+  avoid[4] = {(uintptr_t)table, (uintptr_t)table + (uintptr_t)bytes};
+  for (int i = 0; i < 4; ++i)
+    if (overlaps(avoid[4], avoid[i]))
+      return fail(DPOPT_ERR_INVALID_ARG, "the table overlaps a state or output range");
+  rc = check_bucket_grads(segs, n_replicas, grad_dtype, avoid, 5);
+  if (rc) return rc;
+  set_span(h, lo, hi);
+
+  // The records and pointers, packed on the host.  A copy from pageable host
+  // memory returns once the bytes have left this buffer, so it is reused by
+  // this thread's next call without waiting for the device.
+  static thread_local std::vector<unsigned char> staging;
+  staging.assign((size_t)bytes, 0);
+  Seg* rec = reinterpret_cast<Seg*>(staging.data());
+  const void** ptrs = reinterpret_cast<const void**>(staging.data() + sizeof(Seg) * (nseg + 1));
+  const uint16_t* out16 = static_cast<const uint16_t*>(out);
+  int64_t units = 0;
+  bool wide = true;
+  for (int s = 0; s < nseg; ++s) {
+    const SegDesc& d = segs[s];
+    rec[s].first_group = units;
+    rec[s].state_off = d.state_off;
+    rec[s].len = d.len;
+    rec[s].ptr_base = s * n_replicas;
+    rec[s].vec = vec_level(master, m, v, out16, d, n_replicas, grad_dtype);
+    wide = wide && rec[s].vec != 1;
+    for (int r = 0; r < n_replicas; ++r) ptrs[(int64_t)s * n_replicas + r] = d.ptrs[r];
+    units += (d.len + kGroup - 1) / kGroup;
+  }
+  rec[nseg].first_group = units;
+  cudaError_t e = cudaMemcpyAsync(table, staging.data(), (size_t)bytes, cudaMemcpyHostToDevice,
+                                  stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (launch table)");
+
+  TableParams p{};
+  p.h = h;
+  p.master = master; p.m = m; p.v = v; p.out = (uint16_t*)out;
+  p.total_groups = units;
+  p.n_rep = n_replicas;
+  p.nseg = nseg;
+  p.seg = static_cast<const Seg*>(table);
+  p.gptr = reinterpret_cast<const void* const*>(static_cast<const unsigned char*>(table) +
+                                                sizeof(Seg) * (nseg + 1));
+  p.wide = wide ? 1 : 0;
+  if (grad_dtype == DPOPT_GRAD_BF16) return launch_step_table<0>(p, ext, stream);
+  if (grad_dtype == DPOPT_GRAD_F16) return launch_step_table<2>(p, ext, stream);
+  return launch_step_table<1>(p, ext, stream);
+}
+
 int check_norm_outputs(double* sqnorm_out, void* scratch, int64_t scratch_bytes, int64_t chunks,
                        Range avoid[2]) {
   if (!sqnorm_out || ((uintptr_t)sqnorm_out & 7u))
@@ -782,6 +874,26 @@ int dpopt_reduce_adamw_buckets(const void* const* slice_table, int grad_dtype, i
                       (cudaStream_t)stream);
 }
 
+int dpopt_bucket_table_bytes(int n_replicas, int64_t n_buckets, int64_t* bytes_out) {
+  if (!bytes_out || n_replicas < 1 || n_replicas > DPOPT_MAX_REPLICAS || n_buckets < 0 ||
+      n_buckets > ((int64_t)1 << 30))
+    return fail(DPOPT_ERR_INVALID_ARG, "bucket_table_bytes: invalid argument");
+  *bytes_out = table_bytes_for(n_replicas, n_buckets);
+  return DPOPT_OK;
+}
+
+int dpopt_reduce_adam_buckets_table(const void* const* slice_table, int grad_dtype,
+                                    int n_replicas, const int64_t* offsets, const int64_t* lens,
+                                    int64_t n_buckets, float* master_f32, float* m_f32,
+                                    float* v_f32, void* param_bf16_out, float lr, float beta1,
+                                    float beta2, float eps, int64_t step,
+                                    const dpopt_step_options* opts, void* table,
+                                    int64_t table_bytes, dpopt_stream_t stream) {
+  return table_impl(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets, master_f32,
+                    m_f32, v_f32, param_bf16_out, lr, beta1, beta2, eps, step, opts, table,
+                    table_bytes, (cudaStream_t)stream);
+}
+
 int dpopt_grad_sqnorm_scratch_bytes(int64_t elems, int64_t n_buckets, int64_t* bytes_out) {
   if (!bytes_out || elems < 0 || n_buckets < 0)
     return fail(DPOPT_ERR_INVALID_ARG, "grad_sqnorm_scratch_bytes: invalid argument");
@@ -834,10 +946,12 @@ int dpopt_grad_sqnorm_noalloc(const void* const* grads, int grad_dtype, int n_re
   int64_t S2 = 0;
   rc = build_full(grads, grad_dtype, n_replicas, numel, shard_rank, 1, avoid, 1, ptrs, &S2);
   if (rc) return rc;
-  if (S == 0) return finish_empty_norm(sqnorm_out, (cudaStream_t)stream);
+  // the array's address is set up even for an empty shard, so that such a
+  // call can serve as the device's set-up before any stream capture
   double* partials = nullptr;
   rc = noalloc_partials(&partials);
   if (rc) return rc;
+  if (S == 0) return finish_empty_norm(sqnorm_out, (cudaStream_t)stream);
   Hyper h = make_hyper(1.f, 0.f, 0.f, 0.f, 1, n_replicas);
   h.unscale = grad_unscale == 0.f ? 1.f : grad_unscale;
   SegDesc seg{ptrs, 0, S};

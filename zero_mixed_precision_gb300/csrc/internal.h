@@ -71,6 +71,10 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // p must hold at least one non-empty segment.
 template <int GK, int MS, int MP>
 int launch_step(const LaunchParams<MS, MP>& p, bool ext, cudaStream_t stream);
+// The step over a device-resident segment table (one launch for any number
+// of buckets; direct loads only).
+template <int GK>
+int launch_step_table(const TableParams& p, bool ext, cudaStream_t stream);
 // The plain step that also writes the bf16 copy into every buffer of d (the
 // fused ZeRO-3 all-gather; one segment).
 template <int GK>

@@ -43,6 +43,24 @@ struct LaunchParams {
   const void* gptr[MAXPTR];
 };
 
+// The same launch with its segment and pointer tables in device memory (a
+// caller-owned buffer the library writes before the launch), so one launch
+// covers any number of buckets: seg holds nseg + 1 entries, gptr nseg * n_rep
+// pointers.  The tables are read-only for the kernel's lifetime.
+struct TableParams {
+  Hyper h;
+  float* master;
+  float* m;
+  float* v;
+  uint16_t* out;
+  int64_t total_groups;
+  int32_t n_rep;
+  int32_t nseg;
+  const Seg* seg;
+  const void* const* gptr;
+  int32_t wide;  // every segment has vector level 2 (read on the host only)
+};
+
 // ---------------------------------------------------------------------------
 // memory access helpers
 // ---------------------------------------------------------------------------
@@ -80,9 +98,12 @@ __device__ __forceinline__ uint4 ld_grad16(const void* p, uint64_t pol) {
 }
 
 // 16 bytes of a state array (read here, written back by the same thread).
+// A coherent load: the non-coherent (.nc) path is for data that stays
+// read-only while the kernel runs, and these addresses are stored to by the
+// same kernel.  L1 is skipped either way (every byte is read once).
 __device__ __forceinline__ float4 ld_state16(const float* p) {
   float4 r;
-  asm("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.global.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
       : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
       : "l"(p));
   return r;
@@ -106,7 +127,7 @@ __device__ __forceinline__ void st_stream16u(void* p, uint32_t a, uint32_t b, ui
 // sectors per instruction, where two 16-byte accesses per thread would each
 // touch every sector of that KB by halves.
 __device__ __forceinline__ void ld_state32(const float* p, float4& lo, float4& hi) {
-  asm("ld.global.nc.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+  asm volatile("ld.global.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
       : "=f"(lo.x), "=f"(lo.y), "=f"(lo.z), "=f"(lo.w), "=f"(hi.x), "=f"(hi.y), "=f"(hi.z),
         "=f"(hi.w)
       : "l"(p));
@@ -648,6 +669,16 @@ __device__ __forceinline__ void step_loop(const LP& p, const Hyper& h, float gsc
 template <int NR, int GK, int PACK, bool EXT, int W, int MAXSEG, int MAXPTR>
 __global__ void __launch_bounds__(kThreads, W == 32 ? wide_ctas<NR, GK>() : min_ctas<NR, PACK>())
     reduce_adam_ldg_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p) {
+  pdl_wait();
+  const float gscale = EXT ? grad_scale_of(p.h) : 1.f;
+  step_loop<NR, GK, PACK, EXT, W>(p, p.h, gscale);
+}
+
+// The step over a device-resident segment table: the same walk, the tables
+// read through L1 instead of the parameter space.
+template <int NR, int GK, int PACK, bool EXT, int W>
+__global__ void __launch_bounds__(kThreads, W == 32 ? wide_ctas<NR, GK>() : min_ctas<NR, PACK>())
+    reduce_adam_table_kernel(const __grid_constant__ TableParams p) {
   pdl_wait();
   const float gscale = EXT ? grad_scale_of(p.h) : 1.f;
   step_loop<NR, GK, PACK, EXT, W>(p, p.h, gscale);

@@ -53,6 +53,8 @@ bool all_wide(const LaunchParams<MS, MP>& p) {
     if (p.seg[s].vec == 1) return false;
   return true;
 }
+// (a device-resident table was checked on the host while it was written)
+bool all_wide(const TableParams& p) { return p.wide != 0; }
 
 // Persistent grid: `want` CTAs of work, capped at the resident CTAs of every
 // SM (occupancy looked up once per kernel).
@@ -83,9 +85,19 @@ int launched(cudaError_t e) {
 // the step
 // ---------------------------------------------------------------------------
 
+// The step kernel for a parameter-space table, or for a device-resident one.
 template <int NR, int PACK, bool EXT, int W, int MS, int MP>
-int step_kernel(const LaunchParams<MS, MP>& p, cudaStream_t stream) {
-  auto kern = reduce_adam_ldg_kernel<NR, kGK, PACK, EXT, W, MS, MP>;
+auto step_kern(const LaunchParams<MS, MP>&) {
+  return reduce_adam_ldg_kernel<NR, kGK, PACK, EXT, W, MS, MP>;
+}
+template <int NR, int PACK, bool EXT, int W>
+auto step_kern(const TableParams&) {
+  return reduce_adam_table_kernel<NR, kGK, PACK, EXT, W>;
+}
+
+template <int NR, int PACK, bool EXT, int W, class LP>
+int step_kernel(const LP& p, cudaStream_t stream) {
+  auto kern = step_kern<NR, PACK, EXT, W>(p);
   static std::atomic<int> per_sm{0};
   unsigned grid = 0;
   int rc = persistent_grid(kern, per_sm, (p.total_groups + kThreads - 1) / kThreads, &grid);
@@ -96,8 +108,8 @@ int step_kernel(const LaunchParams<MS, MP>& p, cudaStream_t stream) {
 // Unrolled kernel for NR replicas in its measured width; a 32-byte kernel
 // whose segments are not all 32-byte aligned hands over to the runtime-count
 // 16-byte kernel.
-template <int NR, bool EXT, int MS, int MP>
-int step_nr(const LaunchParams<MS, MP>& p, cudaStream_t s) {
+template <int NR, bool EXT, class LP>
+int step_nr(const LP& p, cudaStream_t s) {
   if constexpr (wide_states(NR)) {
     if (all_wide(p)) return step_kernel<NR, 0, EXT, 32>(p, s);
     return step_kernel<0, 1, EXT, 16>(p, s);
@@ -106,8 +118,8 @@ int step_nr(const LaunchParams<MS, MP>& p, cudaStream_t s) {
   }
 }
 
-template <bool EXT, int MS, int MP>
-int step_n(const LaunchParams<MS, MP>& p, cudaStream_t s) {
+template <bool EXT, class LP>
+int step_n(const LP& p, cudaStream_t s) {
   switch (p.n_rep) {
     case 1: return step_nr<1, EXT>(p, s);
     case 2: return step_nr<2, EXT>(p, s);
@@ -223,6 +235,12 @@ int launch_step(const LaunchParams<MS, MP>& p, bool ext, cudaStream_t stream) {
   return ext ? DPOPT_GK_NS::step_n<true>(p, stream) : DPOPT_GK_NS::step_n<false>(p, stream);
 }
 
+template <int G>
+int launch_step_table(const TableParams& p, bool ext, cudaStream_t stream) {
+  static_assert(G == kGK, "launch_step_table instantiated for another gradient type");
+  return ext ? DPOPT_GK_NS::step_n<true>(p, stream) : DPOPT_GK_NS::step_n<false>(p, stream);
+}
+
 template <int G, int MS, int MP>
 int launch_amp_step(const LaunchParams<MS, MP>& p, const LossScaleState* state,
                     const double* sqnorm, cudaStream_t stream) {
@@ -285,6 +303,7 @@ int launch_sqnorm_pass(const LaunchParams<MS, MP>& p, double* partials, int64_t 
 
 template int launch_step<kGK>(const SmallParams&, bool, cudaStream_t);
 template int launch_step<kGK>(const BigParams&, bool, cudaStream_t);
+template int launch_step_table<kGK>(const TableParams&, bool, cudaStream_t);
 template int launch_step_gather<kGK>(const SmallParams&, const GatherDst&, cudaStream_t);
 template int launch_amp_step<kGK>(const SmallParams&, const LossScaleState*, const double*,
                                   cudaStream_t);
