@@ -161,7 +161,10 @@ int dpopt_reduce_adam_bucket(const void *const *grad_slices, int grad_dtype, int
                              float *v_f32, void *param_bf16_out, float lr, float beta1,
                              float beta2, float eps, int64_t step, dpopt_stream_t stream);
 
-/* Many buckets per call (as few kernel launches as the pointer tables allow).
+/* Many buckets per call (as few kernel launches as the pointer tables allow;
+ * buckets that continue one another in the shard and in every replica's
+ * gradient memory are joined into one segment first, which gives the same
+ * bits).
  *  slice_table    HOST array of n_buckets * n_replicas DEVICE pointers, bucket
  *                 major: slice_table[b * n_replicas + r] is replica r's slice of
  *                 bucket b (lens[b] elements of grad_dtype).
@@ -220,9 +223,14 @@ int dpopt_reduce_adamw_buckets(const void *const *slice_table, int grad_dtype, i
  * parameter space, which holds 2048 slice pointers per launch (32 buckets at
  * 64 replicas), so one 70B model's ZeRO-3 shard at N = 64 in 4M-element
  * buckets ("Почему training 70B модели требует optimizer sharding (ZeRO-3)?",
- * sections 4 and 8: a 1/64 shard, reduce_bucket_size) takes nine launches per
- * step.  This form writes the checked table into device memory the caller
- * provides and runs every bucket in one launch of the direct-load kernel; its
+ * sections 4 and 8: a 1/64 shard, reduce_bucket_size) could take nine launches
+ * per step.  This form runs every bucket in one launch.  Like
+ * dpopt_reduce_adam_buckets it first joins buckets that continue one another
+ * (bucket b + 1 starting where bucket b ends, in the shard and in every
+ * replica's gradient memory, as in a flat contiguous gradient buffer); if
+ * what remains fits one launch's parameter space it launches from there and
+ * leaves `table` untouched, otherwise it writes the checked launch table into
+ * `table` and the direct-load kernel reads it from device memory.  Its
  * results are bitwise those of dpopt_reduce_adam_buckets (opts NULL) and
  * dpopt_reduce_adamw_buckets (opts given).
  *
@@ -238,12 +246,12 @@ int dpopt_reduce_adamw_buckets(const void *const *slice_table, int grad_dtype, i
  *  opts           NULL for plain Adam, else as for dpopt_reduce_adamw.
  *  table          DEVICE pointer, 16-byte aligned, at least
  *                 dpopt_bucket_table_bytes() bytes, owned by the caller and
- *                 overlapping no state, output or gradient range.  The call
- *                 enqueues on `stream` one host-to-device copy of the packed
- *                 table into it, then the kernel that reads it; its previous
- *                 contents do not matter.  It is stream ordered like the
- *                 states: work on another stream must not touch it until this
- *                 call's kernel has finished.
+ *                 overlapping no state, output or gradient range.  When it is
+ *                 used, the call enqueues on `stream` one host-to-device copy
+ *                 of the packed table into it, then the kernel that reads it;
+ *                 its previous contents do not matter.  It is stream ordered
+ *                 like the states: work on another stream must not touch it
+ *                 until this call's kernel has finished.
  *  table_bytes    size of `table` in bytes.
  * Errors: as for dpopt_reduce_adamw_buckets, plus DPOPT_ERR_INVALID_ARG for a
  * null or misaligned table, too small a table_bytes, or a table overlapping a

@@ -404,9 +404,18 @@ def _sample(S, bucket, rng, k=60_000):
     return np.unique(np.concatenate(pts)).astype(np.int64)
 
 
-def _fits(wl) -> bool:
+def _free_bytes() -> int:
+    """Device memory free for a new workload: what the driver reports plus what
+    torch's caching allocator holds without using it (released first)."""
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
     free, _ = torch.cuda.mem_get_info()
-    return workload_bytes(wl) + (4 << 30) < free
+    return free
+
+
+def _fits(wl) -> bool:
+    return workload_bytes(wl) + (4 << 30) < _free_bytes()
 
 
 def _run_full_size(wl, entry):
@@ -416,9 +425,8 @@ def _run_full_size(wl, entry):
     (the parameter-space bucket table) or "table" (every bucket in one launch)."""
     _need_gpu()
     if not _fits(wl):
-        free, _ = torch.cuda.mem_get_info()
         pytest.skip(f"{wl.name} needs {workload_bytes(wl) / 1e9:.1f} GB of device memory, "
-                    f"{free / 1e9:.1f} GB free (4 GB kept back)")
+                    f"{_free_bytes() / 1e9:.1f} GB free (4 GB kept back)")
     rng = np.random.default_rng(wl.seed)
     idx = _sample(wl.shard_elems, wl.bucket_elems, rng)
     t1 = wl.warmup_steps + wl.steps
@@ -450,8 +458,10 @@ def _run_full_size(wl, entry):
         parity.check_step(wl, idx, t, prev, got, wl.name)
         if t > wl.warmup_steps:
             stats.append(parity.check(refs[t - 1], *got, where=f"{wl.name} t={t}"))
-    del dev
-    torch.cuda.empty_cache()
+    del dev, tidx
+    if entry != "full":
+        del bs, table, call
+    _free_bytes()
     return stats
 
 

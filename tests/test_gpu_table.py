@@ -160,3 +160,34 @@ def test_table_entry_rejects_a_small_table_without_launching():
         dp.reduce_adam_buckets_table(rows, offs, *st, out, table, step=1, **HP)
     assert dp.dpopt_launch_count() == c0
     assert not st[0].any()
+
+
+def test_contiguous_buckets_are_joined_into_one_launch():
+    """Buckets that are consecutive views of flat replica buffers (contiguous
+    gradients) are joined into one segment: one launch from the parameter-space
+    entry, with the bits of the same buckets held in separate allocations."""
+    _need_gpu()
+    wl = _small_workload(64, 300_000, kind=0)
+    S, bucket = wl.shard_elems, 1_000
+    host = [parity.grad_host_range(wl, r, 1, wl.shard_base, S) for r in range(wl.n_replicas)]
+    flat = [to_dev_grad(h) for h in host]
+    rows = [[g[off:off + min(bucket, S - off)] for g in flat] for off in range(0, S, bucket)]
+    offs = list(range(0, S, bucket))
+    master, m, v = parity.states_host(wl, wl.shard_base + np.arange(S))
+    res = []
+    for entry in ("joined", "separate"):
+        st = [torch.from_numpy(x.copy()).cuda() for x in (master, m, v)]
+        out = torch.empty(S, dtype=torch.bfloat16, device="cuda")
+        c0 = dp.dpopt_launch_count()
+        if entry == "joined":
+            dp.reduce_adam_buckets(rows, offs, *st, out, step=1, **HP)
+            assert dp.dpopt_launch_count() - c0 == 1
+        else:
+            sep, _ = _slices(wl, 1, bucket)
+            table = torch.empty(dp.bucket_table_bytes(wl.n_replicas, len(sep)),
+                                dtype=torch.uint8, device="cuda")
+            dp.reduce_adam_buckets_table(sep, offs, *st, out, table, step=1, **HP)
+        dp.stream_status()
+        res.append([f32(x) for x in st] + [u16(out)])
+    for x, y in zip(*res):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))

@@ -91,3 +91,34 @@ def test_planted_mistake_is_caught(name, tmp_path):
     finally:
         oracle._lib = saved
     assert failures >= 1, f"no pin caught the planted mistake: {name}"
+
+
+# The accounting lives in the oracle's Python part: each mutant below replaces
+# state_components with a plausible misreading of the ZeRO stages, and at least
+# one golden accounting row must fail on it.
+def _stage_mutant(shard_p_from, shard_g_from, shard_o_from):
+    real = oracle.state_components
+
+    def mutant(psi, variant, n_dp, zero_stage):
+        c = real(psi, variant, 1, 0)   # the unsharded components
+        return {"params": c["params"] / (n_dp if zero_stage >= shard_p_from else 1),
+                "grads": c["grads"] / (n_dp if zero_stage >= shard_g_from else 1),
+                "optimizer": c["optimizer"] / (n_dp if zero_stage >= shard_o_from else 1)}
+    return mutant
+
+
+@pytest.mark.parametrize("name,stages", [
+    ("gradients sharded from stage 1", (3, 1, 1)),
+    ("optimizer sharded only from stage 2", (3, 2, 2)),
+    ("parameters sharded from stage 2", (2, 2, 1)),
+    ("stages shifted by one", (2, 1, 0)),
+])
+def test_planted_accounting_mistake_is_caught(name, stages, monkeypatch):
+    monkeypatch.setattr(oracle, "state_components", _stage_mutant(*stages))
+    failures = 0
+    for row in pins._golden_rows():
+        try:
+            pins.test_state_accounting_matches_printed_figures(row)
+        except AssertionError:
+            failures += 1
+    assert failures >= 1, f"no golden accounting row caught: {name}"

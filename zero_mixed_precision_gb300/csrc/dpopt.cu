@@ -444,6 +444,31 @@ int build_buckets(const void* const* slice_table, int grad_dtype, int n_replicas
   return DPOPT_OK;
 }
 
+// Joins consecutive buckets whose slices continue one another: bucket b + 1
+// starts where bucket b ends, in the shard and in every replica's gradient
+// memory (the buckets of a flat, contiguous gradient buffer).  The step is
+// elementwise, so the joined segment gives the same bits in fewer segments;
+// 274 resident 4M-element buckets become one segment and one launch.
+void coalesce(std::vector<SegDesc>& segs, int n, int grad_dtype) {
+  const uintptr_t esize = grad_dtype == DPOPT_GRAD_F32 ? 4 : 2;
+  size_t w = 0;
+  for (size_t s = 0; s < segs.size(); ++s) {
+    if (w > 0) {
+      SegDesc& a = segs[w - 1];
+      const SegDesc& b = segs[s];
+      bool joins = b.state_off == a.state_off + a.len;
+      for (int r = 0; joins && r < n; ++r)
+        joins = (uintptr_t)b.ptrs[r] == (uintptr_t)a.ptrs[r] + (uintptr_t)a.len * esize;
+      if (joins) {
+        a.len += b.len;
+        continue;
+      }
+    }
+    segs[w++] = segs[s];
+  }
+  segs.resize(w);
+}
+
 int check_bucket_grads(const std::vector<SegDesc>& segs, int n, int grad_dtype, const Range* avoid,
                        int navoid) {
   const size_t esize = grad_dtype == DPOPT_GRAD_F32 ? 4 : 2;
@@ -536,6 +561,7 @@ int buckets_impl(const void* const* slice_table, int grad_dtype, int n_replicas,
   rc = check_bucket_grads(segs, n_replicas, grad_dtype, st, 4);
   if (rc) return rc;
   set_span(h, lo, hi);
+  coalesce(segs, n_replicas, grad_dtype);
   return run(segs.data(), (int)segs.size(), grad_dtype, n_replicas, master, m, v, out, h, ext,
              stream);
 }
@@ -546,8 +572,10 @@ int64_t table_bytes_for(int n, int64_t nb) {
   return (int64_t)sizeof(Seg) * (nb + 1) + (int64_t)sizeof(void*) * nb * n;
 }
 
-// The batched-bucket step with its launch table written into caller-owned
-// device memory: one launch for every bucket, however many.
+// The batched-bucket step in one launch for every bucket, however many:
+// buckets that continue one another are joined first; if what remains fits
+// one launch's parameter space it runs from there, else its launch table is
+// written into the caller-owned device memory and the kernel reads it there.
 int table_impl(const void* const* slice_table, int grad_dtype, int n_replicas,
                const int64_t* offsets, const int64_t* lens, int64_t n_buckets, float* master,
                float* m, float* v, void* out, float lr, float beta1, float beta2, float eps,
@@ -576,8 +604,7 @@ int table_impl(const void* const* slice_table, int grad_dtype, int n_replicas,
   Range avoid[5];
   rc = check_states(master, m, v, out, lo, hi, avoid);
   if (rc) return rc;
-  const int nseg = (int)segs.size();
-  const int64_t bytes = table_bytes_for(n_replicas, nseg);
+  const int64_t bytes = table_bytes_for(n_replicas, (int64_t)segs.size());
   avoid[4] = {(uintptr_t)table, (uintptr_t)table + (uintptr_t)bytes};
   for (int i = 0; i < 4; ++i)
     if (overlaps(avoid[4], avoid[i]))
@@ -585,12 +612,19 @@ int table_impl(const void* const* slice_table, int grad_dtype, int n_replicas,
   rc = check_bucket_grads(segs, n_replicas, grad_dtype, avoid, 5);
   if (rc) return rc;
   set_span(h, lo, hi);
+  coalesce(segs, n_replicas, grad_dtype);
+  if ((int64_t)segs.size() <= kBigSegs && (int64_t)segs.size() * n_replicas <= kBigPtrs)
+    // the joined buckets fit one launch's parameter space: no table needed
+    return run(segs.data(), (int)segs.size(), grad_dtype, n_replicas, master, m, v, out, h, ext,
+               stream);
 
   // The records and pointers, packed on the host.  A copy from pageable host
   // memory returns once the bytes have left this buffer, so it is reused by
   // this thread's next call without waiting for the device.
+  const int nseg = (int)segs.size();
+  const int64_t used = table_bytes_for(n_replicas, nseg);
   static thread_local std::vector<unsigned char> staging;
-  staging.assign((size_t)bytes, 0);
+  staging.assign((size_t)used, 0);
   Seg* rec = reinterpret_cast<Seg*>(staging.data());
   const void** ptrs = reinterpret_cast<const void**>(staging.data() + sizeof(Seg) * (nseg + 1));
   const uint16_t* out16 = static_cast<const uint16_t*>(out);
@@ -608,7 +642,7 @@ int table_impl(const void* const* slice_table, int grad_dtype, int n_replicas,
     units += (d.len + kGroup - 1) / kGroup;
   }
   rec[nseg].first_group = units;
-  cudaError_t e = cudaMemcpyAsync(table, staging.data(), (size_t)bytes, cudaMemcpyHostToDevice,
+  cudaError_t e = cudaMemcpyAsync(table, staging.data(), (size_t)used, cudaMemcpyHostToDevice,
                                   stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (launch table)");
 
