@@ -463,6 +463,48 @@ __device__ __forceinline__ void add_chunk_x2(const Src& src, int r0,
   }
 }
 
+// Replicas r .. r+K-1 of one 8-element group loaded into g[0 .. K-1].
+template <int K, int GK, class Src>
+__device__ __forceinline__ void load_chunk(const Src& src, int r, GradLoad<GK> (&g)[8]) {
+#pragma unroll
+  for (int j = 0; j < K; ++j) src.grad(g[j], r + j);
+}
+
+// g[0 .. K-1] added, in order, to packed running sums (FIRST: g[0] starts them).
+template <int K, bool FIRST, int GK>
+__device__ __forceinline__ void sum_chunk(const GradLoad<GK> (&g)[8],
+                                          CompSum<float2> (&acc)[kGroup / 2]) {
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+#pragma unroll
+    for (int k = 0; k < kGroup / 2; ++k) {
+      if (FIRST && j == 0) acc[k].init(g[j].pair(k));
+      else acc[k].add(g[j].pair(k));
+    }
+  }
+}
+
+// The end of a pipelined replica walk: `cur` holds the last full chunk of 8
+// (loaded, not yet added); the remaining rem < 8 replicas from r are loaded
+// into `spare` before `cur` is added, so their loads overlap that addition.
+template <int GK, class Src>
+__device__ __forceinline__ void finish_chunks(const Src& src, int r, int rem,
+                                              const GradLoad<GK> (&cur)[8],
+                                              GradLoad<GK> (&spare)[8],
+                                              CompSum<float2> (&acc)[kGroup / 2]) {
+  switch (rem) {
+#define DPOPT_REM(K)                          \
+  case K:                                     \
+    load_chunk<K>(src, r, spare);             \
+    sum_chunk<8, false>(cur, acc);            \
+    sum_chunk<K, false>(spare, acc);          \
+    break;
+    DPOPT_REM(1) DPOPT_REM(2) DPOPT_REM(3) DPOPT_REM(4) DPOPT_REM(5) DPOPT_REM(6) DPOPT_REM(7)
+#undef DPOPT_REM
+    default: sum_chunk<8, false>(cur, acc); break;
+  }
+}
+
 // The fixed-order compensated replica sum of one 8-element group on packed
 // f32x2 lanes (element pairs 2j, 2j+1): the same operations per element as
 // reduce_group_x1, so the same bits.
@@ -470,6 +512,41 @@ template <int NR, int GK, class Src>
 __device__ __forceinline__ void reduce_group_x2(const Src& src, int n,
                                                 CompSum<float2> (&acc)[kGroup / 2]) {
   constexpr int P = kGroup / 2;
+  if constexpr (NR == 0 && GK != 1) {
+    if (n >= 16) {
+      // Runtime replica count of 16 or more, 16-bit gradients, software-
+      // pipelined: the next chunk of 8 replicas is loaded into one register
+      // set while the chunk before it, in the other set, is added -- up to 16
+      // loads of a thread in flight instead of 8, at the same two CTAs per SM
+      // (126 registers).  Same replica order, same bits.  Measured on GB300
+      // (bf16, S = 256M): N = 64 6608 -> 6842 GB/s, 32 6600 -> 6708, 31
+      // 6200 -> 6432, 24 6452 -> 6560, 17 6093 -> 6025; the 70B shard
+      // (N = 64) 43.0 -> 44.5 G params/s.  fp32 gradients keep the chunked
+      // walk below: two 8-replica sets of 32-byte loads would not fit the
+      // registers (fp32 N = 32: 7053 against 6953 GB/s pipelined).
+      GradLoad<GK> ga[8], gb[8];
+      load_chunk<8>(src, 0, ga);
+      load_chunk<8>(src, 8, gb);
+      sum_chunk<8, true>(ga, acc);
+      int r = 16;  // gb holds replicas r-8 .. r-1
+      while (true) {
+        if (r + 8 > n) {
+          finish_chunks(src, r, n - r, gb, ga, acc);
+          return;
+        }
+        load_chunk<8>(src, r, ga);
+        sum_chunk<8, false>(gb, acc);
+        r += 8;      // ga holds replicas r-8 .. r-1
+        if (r + 8 > n) {
+          finish_chunks(src, r, n - r, ga, gb, acc);
+          return;
+        }
+        load_chunk<8>(src, r, gb);
+        sum_chunk<8, false>(ga, acc);
+        r += 8;
+      }
+    }
+  }
   if constexpr (NR > 0) {
     GradLoad<GK> gl[NR];
 #pragma unroll
