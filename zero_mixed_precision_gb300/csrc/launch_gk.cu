@@ -19,6 +19,7 @@
 #include <atomic>
 
 #include "internal.h"
+#include "gather_bulk.cuh"
 #include "norm.cuh"
 
 #ifndef DPOPT_GK
@@ -148,7 +149,7 @@ int step_n(const LP& p, cudaStream_t s) {
 
 template <int NR, int PACK, int W>
 int gather_kernel(const SmallParams& p, const GatherDst& d, cudaStream_t stream) {
-  auto kern = reduce_adam_gather_kernel<NR, kGK, PACK, W, kSmallSegs, kSmallPtrs>;
+  auto kern = reduce_adam_gather_bulk_kernel<NR, kGK, PACK, W, kSmallSegs, kSmallPtrs>;
   static std::atomic<int> per_sm{0};
   unsigned grid = 0;
   int rc = persistent_grid(kern, per_sm, (p.total_groups + kThreads - 1) / kThreads, &grid);
