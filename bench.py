@@ -98,8 +98,8 @@ def parse_args(argv=None):
                     default="entry",
                     help="adam_allgather: 'entry' -- dpopt_reduce_adam_allgather, which runs one "
                          "kernel writing the new bf16 shard into every replica's parameter "
-                         "buffer, or (large shards, 3 <= N <= 8 or 16) the step into the own "
-                         "replica and the broadcast, whichever measured faster; 'fused' / "
+                         "buffer (its automatic choice: faster than the two-pass form at every "
+                         "N measured); 'fused' / "
                          "'two-pass' -- the entry held to one form (dpopt_set_gather_policy); "
                          "'separate' -- the step into a separate output, then "
                          "dpopt_allgather_bf16 reads it back and broadcasts it.  All give the "
@@ -544,8 +544,9 @@ def run_ours(args, wl):
                                    "dpopt_reduce_adam_bucket -> bf16 parameters back to pinned "
                                    "host, one stream"}}
     dp.stream_status(stream)
-    grads = [h.view(torch.int16).numpy().view("uint16") if h.dtype == torch.bfloat16
-             else h.numpy() for h in hs]
+    cap = sample_elems(wl)
+    grads = [(h[:cap].view(torch.int16).numpy().view("uint16") if h.dtype == torch.bfloat16
+              else h[:cap].numpy()).copy() for h in hs]
     return _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks, e2e,
                    grads, stored)
 
@@ -605,10 +606,11 @@ def e2e_ring(args, wl, dev, stream, hp, world, barrier, K):
                    f"{R} pinned host bucket slots ({R * n * be * esize / 1e9:.2f} GB) by one "
                    "dpopt_reduce_adam_buckets_table launch, bf16 parameters written into pinned "
                    "host memory"}
-    # the oracle's sample: bucket 0's slices (the first elements of the shard)
-    cap = min(be, max(250_000, 64_000_000 // n))
-    grads = [h[:cap].view(torch.int16).numpy().view("uint16") if h.dtype == torch.bfloat16
-             else h[:cap].numpy() for h in slots[0]]
+    # the oracle's sample: bucket 0's slices (the first elements of the shard),
+    # copied out of the pinned buffers into ordinary host memory
+    cap = min(be, sample_elems(wl))
+    grads = [(h[:cap].view(torch.int16).numpy().view("uint16") if h.dtype == torch.bfloat16
+              else h[:cap].numpy()).copy() for h in slots[0]]
     return e2e, grads
 
 
@@ -840,13 +842,18 @@ def run_sweep(args):
 
 
 def resolve_workload(name: str):
-    """A named workload, or one sweep cell written sweep_<S>_<N>_<bf16|fp32>."""
+    """A named workload, one sweep cell written sweep_<S>_<N>_<bf16|fp32>, or
+    full_<S>_<N>_<bf16|fp32>: the sweep cell's values as N full replica buffers
+    of S*N elements, rank 0's shard (the layout the all-gather runs on)."""
     import synth
     if name in synth.WORKLOADS:
         return synth.WORKLOADS[name]
     parts = name.split("_")
-    if len(parts) == 4 and parts[0] == "sweep" and parts[3] in ("bf16", "fp32"):
-        return synth.sweep_cell(int(parts[1]), int(parts[2]), 0 if parts[3] == "bf16" else 1)
+    if len(parts) == 4 and parts[0] in ("sweep", "full") and parts[3] in ("bf16", "fp32"):
+        wl = synth.sweep_cell(int(parts[1]), int(parts[2]), 0 if parts[3] == "bf16" else 1)
+        if parts[0] == "full":
+            wl = dataclasses.replace(wl, name="full" + wl.name[len("sweep"):], layout="full")
+        return wl
     raise SystemExit(f"unknown workload {name}")
 
 

@@ -434,13 +434,12 @@ int dpopt_allgather_bf16(const void *shard_bf16, int64_t shard_elems, int shard_
  *   param_replicas[r][base + i] = bf16(master_f32[i] after the step),  r < n_replicas,
  * bit for bit what dpopt_reduce_adam_ex(..., param_replicas[shard_rank] + base, ...)
  * followed by dpopt_allgather_bf16 of that range writes, and master/m/v as that
- * step leaves them.  Where it measured faster the call runs one fused kernel --
- * the bf16 copy is never read back: g*N + 24 + 2N bytes per parameter instead
- * of g*N + 28 + 2N -- and otherwise exactly those two launches: for
- * 3 <= n_replicas <= 8 (16 with bf16 or fp16 gradients) with
- * S*(4*n_replicas + 24) above 512 MB, where the fused pass's even mix of
- * reads and writes ran 2-6 % slower on GB300 (dpopt_set_gather_policy
- * overrides the choice).
+ * step leaves them.  The call runs one fused kernel -- the bf16 copy is never
+ * read back: g*N + 24 + 2N bytes per parameter instead of g*N + 28 + 2N, and
+ * each CTA's 4 KB tile of new bf16 values goes to every replica buffer as bulk
+ * copies from shared memory; it measured faster than the two launches at
+ * every replica count and size on GB300 (dpopt_set_gather_policy can still
+ * select the two launches).
  *  grads, grad_dtype, n_replicas, numel, shard_rank, bucket_elems, master_f32,
  *  m_f32, v_f32, lr, beta1, beta2, eps, step, stream
  *                  as for dpopt_reduce_adam_ex.
@@ -536,7 +535,7 @@ int dpopt_get_kernel_policy(void);
 
 /* Which form dpopt_reduce_adam_allgather takes (process-wide; default
  * DPOPT_GATHER_AUTO).
- *  DPOPT_GATHER_AUTO      the faster of the two by measurement (see the entry)
+ *  DPOPT_GATHER_AUTO      the faster by measurement: the fused kernel (see the entry)
  *  DPOPT_GATHER_FUSED     always the one fused kernel
  *  DPOPT_GATHER_SEPARATE  always the step into the own replica, then the
  *                         broadcast into the others

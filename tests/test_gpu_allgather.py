@@ -161,10 +161,11 @@ def test_fused_step_allgather_unaligned_replicas():
 
 
 @pytest.mark.parametrize("n,S", [(4, 13_000_003), (8, 9_200_001), (12, 7_200_001)])
-def test_large_shard_takes_the_two_pass_form_with_the_same_bits(n, S):
-    """Above 512 MB of working set at 3 <= N <= 8 the entry runs the step into
-    the own replica and then the broadcast; the bits are those of the two
-    public calls."""
+def test_large_shard_entry_writes_the_bits_of_the_two_calls(n, S):
+    """Shards whose working set is far above L2 (0.9-1.2 GB), where whole 4 KB
+    tiles go to the replicas by bulk copies: the entry writes the bits of the
+    step into the own replica followed by the broadcast (the two public
+    calls)."""
     _need_gpu()
     rank = n - 1
     gen = torch.Generator(device="cuda")

@@ -812,24 +812,18 @@ int launch_gather(const GatherParams& p, cudaStream_t stream) {
   return DPOPT_OK;
 }
 
-// Whether the step fused with the all-gather (one pass, reads and writes at
-// about 1:1) beats the step into the own replica followed by the broadcast
-// kernel (two passes, each nearer its own best mix), by measurement on GB300
-// (G params/s, fused / separate, bf16):
-//   S = 30M:  N = 2 197 / 185, 3 161 / 165, 4 148 / 149, 5 133 / 140,
-//             6 120 / 127, 7 114 / 119, 8 106-112 / 112, 9 98 / 104,
-//             12 82 / 87, 16 69 / 70 (N = 9..16 with the unrolled step; with
-//             the runtime-count step the separate form lost: N = 9 104 / 88);
-//   S = 4M:   fused ahead at every N measured (2, 4, 8, 9, 12, 16, 32, 64).
-// The separate form wins where the step has an unrolled kernel (N <= 8, and
-// N <= 16 for 16-bit gradients) past N = 2, with a working set well above L2
-// (S * (4N + 24) bytes > 512 MB).  Both write the same bits.
+// Whether the step fused with the all-gather runs, or the step into the own
+// replica followed by the broadcast kernel.  With its bf16 tiles written by
+// bulk copies the fused kernel measured faster at every N and size on GB300
+// (G params/s, fused / two passes, bf16): S = 30M: N = 2 194.9 / 185.2,
+// 3 177.7 / 165.3, 4 161.0 / 152.1, 5 144.8 / 138.4, 6 130.5 / 126.9,
+// 8 114.3 / 111.3, 9 106.0 / 103.0, 12 88.0 / 86.3, 16 71.4 / 69.9,
+// 24 51.9 / 50.4, 32 41.5 / 40.5; S = 4M: N = 2, 4, 8, 16, 64 likewise;
+// fp32 S = 30M: N = 4 132.6 / 130.6, 8 89.6 / 88.8.  So the automatic policy
+// always fuses; both forms write the same bits.
 bool gather_fused(int n, int64_t shard, int grad_dtype) {
-  const int pol = g_gather_policy.load(std::memory_order_relaxed);
-  if (pol != DPOPT_GATHER_AUTO) return pol == DPOPT_GATHER_FUSED;
-  const int unrolled = grad_dtype == DPOPT_GRAD_F32 ? 8 : 16;
-  if (n < 3 || n > unrolled) return true;
-  return (double)shard * (4.0 * n + 24.0) <= 512e6;
+  (void)n; (void)shard; (void)grad_dtype;
+  return g_gather_policy.load(std::memory_order_relaxed) != DPOPT_GATHER_SEPARATE;
 }
 
 }  // namespace
