@@ -1,8 +1,10 @@
 """A battery of library calls that walks every kernel's index paths: full
 buffers and batched buckets with ragged tails, unaligned slices (the
 one-element path), the bulk-copy kernel, the runtime-replica-count kernel,
-the norm pre-pass with and without the stored average, the loss-scaled step,
-the all-gather and the fused step + all-gather.
+the one-launch bucket entry (launch table in device memory, and contiguous
+buckets joined), the norm pre-pass with and without the stored average, the
+loss-scaled step, the all-gather and the fused step + all-gather (per-thread
+stores, and whole tiles written by bulk copies).
 
 run() returns every output as numpy arrays plus the stream status after each
 call.  tests/test_gpu_bounds.py runs it once on the release library in the
@@ -88,6 +90,24 @@ def run() -> tuple[dict, list]:
                                           step=4, **HP)
         keep(f"when_ready_n{n}", *st2, o2)
 
+    # every bucket in one launch: separate slices through a launch table in
+    # device memory, and contiguous slices joined into one segment
+    n = 8
+    lens = [37, 8, 4096, 1, 2048] * 40 + [5]
+    S = sum(lens)
+    offs = np.concatenate([[0], np.cumsum(lens)[:-1]]).tolist()
+    slices = [[_rand(gen, ln, 1e-3, torch.bfloat16) for _ in range(n)] for ln in lens]
+    table = torch.empty(dp.bucket_table_bytes(n, len(lens)), dtype=torch.uint8, device="cuda")
+    st = _states(gen, S)
+    o = torch.empty(S, dtype=torch.bfloat16, device="cuda")
+    dp.reduce_adam_buckets_table(slices, offs, *st, o, table, step=3, **HP)
+    keep("table_n8", *st, o)
+    flat = [_rand(gen, S, 1e-3, torch.bfloat16) for _ in range(n)]
+    rows = [[f[off:off + ln] for f in flat] for off, ln in zip(offs, lens)]
+    st = _states(gen, S)
+    dp.reduce_adam_buckets(rows, offs, *st, o, step=3, **HP)
+    keep("joined_n8", *st, o)
+
     # unaligned slices: every pointer one element past an aligned address
     n, S = 3, 6_001
     bufs = [_rand(gen, S + 1, 1e-3, torch.bfloat16) for _ in range(n)]
@@ -163,6 +183,14 @@ def run() -> tuple[dict, list]:
         st = _states(gen, S)
         dp.reduce_adam_allgather(grads, rank, 2048, *st, reps, step=2, **HP)
         keep(f"fused_gather_{tag}", *st, *base)
+    # a shard whose replica ranges are 16-byte aligned: whole 2048-element tiles
+    # go out as bulk copies, the last group by per-thread stores
+    n, S, rank = 4, 20_488, 3
+    grads = [_rand(gen, n * S, 1e-3, torch.bfloat16) for _ in range(n)]
+    reps = [torch.zeros(n * S, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    st = _states(gen, S)
+    dp.reduce_adam_allgather(grads, rank, 2048, *st, reps, step=2, **HP)
+    keep("fused_gather_tiles", *st, *reps)
     return out, status
 
 

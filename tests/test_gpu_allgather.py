@@ -160,7 +160,7 @@ def test_fused_step_allgather_unaligned_replicas():
         assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
 
 
-@pytest.mark.parametrize("n,S", [(4, 13_000_003), (8, 9_200_001), (12, 7_200_001)])
+@pytest.mark.parametrize("n,S", [(4, 13_000_000), (8, 9_200_001), (12, 7_200_000)])
 def test_large_shard_entry_writes_the_bits_of_the_two_calls(n, S):
     """Shards whose working set is far above L2 (0.9-1.2 GB), where whole 4 KB
     tiles go to the replicas by bulk copies: the entry writes the bits of the
