@@ -140,7 +140,7 @@ def _oracle_clipped(wl, steps, wd, max_norm, unscale=1.0):
 
 @pytest.mark.parametrize("n,S", [(1, 30_001), (2, 30_001), (3, 20_003), (4, 50_000),
                                  (5, 12_007), (6, 10_001), (7, 9_001), (8, 20_001),
-                                 (16, 9_999)])
+                                 (16, 9_999), (24, 5_003), (64, 2_011)])
 def test_clipped_adamw_matches_the_oracle(n, S):
     _need_gpu()
     wl = _small_workload(n, S, rank=min(1, n - 1))

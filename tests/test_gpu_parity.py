@@ -182,6 +182,24 @@ def test_every_unrolled_replica_count(n, kind):
         assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
 
 
+@pytest.mark.parametrize("kind", [0, 2])
+@pytest.mark.parametrize("n", [17, 23, 24, 40, 56, 57, 63, 64])
+def test_many_replicas_both_walks_every_element(n, kind):
+    """16-bit gradients beyond the unrolled kernels: N = 17..56 take the walk
+    that stages the replica loads in shared memory, larger N the
+    register-pipelined walk; every element agrees with the oracle step by
+    step, and the batched-bucket entry gives the same bits."""
+    _need_gpu()
+    S = 9_001
+    wl = _small_workload(n, S, kind=kind)
+    refs = oracle_trajectory(wl, np.arange(S), 1, 2)
+    got = _run_small_full(wl, steps=(1, 2))
+    parity.check(refs[-1], *got, where=f"N={n} kind={kind}")
+    got_b = _run_small_full(wl, steps=(1, 2), entry="buckets", bucket=2_003)
+    for x, y in zip(got, got_b):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
 @pytest.mark.parametrize("n", [1, 2, 4, 8, 13])
 @pytest.mark.parametrize("S", [9, 40_000])
 def test_fp32_gradients_every_element(n, S):

@@ -19,6 +19,7 @@
 #include <atomic>
 
 #include "internal.h"
+#include "async_walk.cuh"
 #include "gather_bulk.cuh"
 #include "norm.cuh"
 
@@ -106,6 +107,43 @@ int step_kernel(const LP& p, cudaStream_t stream) {
   return launched(launch_pdl(kern, grid, kThreads, 0, stream, p));
 }
 
+// The runtime-count step for 16-bit gradients with the replica loads staged
+// in shared memory by asynchronous copies (async_walk.cuh): kAsyncDepth chunks
+// of 8 replicas in flight per thread, kAsyncMinBlocks CTAs per SM (96 KB of
+// shared memory each).  Measured on GB300 (bf16, S = 256M, GB/s, asynchronous
+// walk against the register-pipelined one): N = 17 6366 / 6356, 18 6428 /
+// 6007, 20 6531 / 6268, 23 6644 / 6531, 24 6670 / 6521, 28 6670 / 6174,
+// 31 6750 / 6217, 32 6835 / 6626, 40 6817 / 6357, 48 6816 / 6627, 56 6773 /
+// 6530, 64 6617 / 6742.  Two chunks at three CTAs per SM (spilling) and four
+// chunks at one CTA measured slower.
+constexpr int kAsyncDepth = 3;
+constexpr int kAsyncMinBlocks = 2;
+// Replica counts up to this take the asynchronous walk, larger ones the
+// register-pipelined walk of kernels.cuh (faster at N = 64).
+constexpr int kAsyncMaxReplicas = 56;
+
+template <bool EXT, class LP>
+int async_step(const LP& p, cudaStream_t stream) {
+  auto kern = reduce_adam_async_kernel<kAsyncDepth, kAsyncMinBlocks, kGK, EXT, LP>;
+  constexpr int smem = (int)async_ring_bytes<kAsyncDepth>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  static std::atomic<int> per_sm{0};
+  int sms = 0;
+  int rc = sm_count(&sms);
+  if (rc) return rc;
+  int bps = per_sm.load(std::memory_order_relaxed);
+  if (bps == 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, kThreads, smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (bps < 1) bps = 1;
+    per_sm.store(bps, std::memory_order_relaxed);
+  }
+  const int64_t want = (p.total_groups + kThreads - 1) / kThreads;
+  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * bps));
+  return launched(launch_pdl(kern, grid, kThreads, (size_t)smem, stream, p));
+}
+
 // Unrolled kernel for NR replicas in its measured width; a 32-byte kernel
 // whose segments are not all 32-byte aligned hands over to the runtime-count
 // 16-byte kernel.
@@ -138,7 +176,10 @@ int step_n(const LP& p, cudaStream_t s) {
     case 14: if constexpr (kGK != 1) return step_nr<14, EXT>(p, s); else break;
     case 15: if constexpr (kGK != 1) return step_nr<15, EXT>(p, s); else break;
     case 16: if constexpr (kGK != 1) return step_nr<16, EXT>(p, s); else break;
-    default: break;
+    default:
+      if constexpr (kGK != 1)
+        if (p.n_rep <= kAsyncMaxReplicas) return async_step<EXT>(p, s);
+      break;
   }
   return step_kernel<0, 1, EXT, 16>(p, s);
 }
