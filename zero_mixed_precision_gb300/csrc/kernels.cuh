@@ -73,8 +73,9 @@ struct TableParams {
 // feed a step -- the norm pre-pass, its ordered finish, the loss-scale
 // kernels -- also let their successor be scheduled at once
 // (griddepcontrol.launch_dependents), so the step's launch and ramp-up hide
-// behind their tail; the step kernels do not, since back-to-back steps
-// measured no faster that way.  Both instructions are no-ops for a kernel
+// behind their tail, and so does the loss-scaled step, whose successor is the
+// one-thread scale update; the other step kernels do not, since back-to-back
+// steps measured no faster that way.  Both instructions are no-ops for a kernel
 // launched without the attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_enter() {
@@ -704,9 +705,8 @@ constexpr int wide_ctas() { return (NR == 1 && GK != 1) ? 4 : 3; }
 // width of one state access (32: one 256-bit access per array, for segments
 // of vector level 2; 16: two 16-byte accesses, level >= 1); other groups go
 // one element at a time.
-template <int NR, int GK, int PACK, bool EXT, int W, bool GATHER = false, class LP>
-__device__ __forceinline__ void step_loop(const LP& p, const Hyper& h, float gscale,
-                                          const GatherDst* gd = nullptr) {
+template <int NR, int GK, int PACK, bool EXT, int W, class LP>
+__device__ __forceinline__ void step_loop(const LP& p, const Hyper& h, float gscale) {
   constexpr int kLevel = W == 32 ? 2 : 1;
   const uint64_t pol = evict_first_policy();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -724,18 +724,12 @@ __device__ __forceinline__ void step_loop(const LP& p, const Hyper& h, float gsc
     if (sg.vec >= kLevel && rem >= kGroup) {
       const GlobalSource<GK, W> src{p.gptr + sg.ptr_base, e0,
                                     {p.master + so, p.m + so, p.v + so}, pol};
-      if constexpr (GATHER) {
-        const GatherOutT<W> o{{p.master + so, p.m + so, p.v + so, p.out + so}, gd, so};
-        if constexpr (PACK) group_vec_x2<NR, GK, EXT>(src, p.n_rep, h, o, gscale);
-        else group_vec_x1<NR, GK, EXT>(src, p.n_rep, h, o, gscale);
-      } else {
-        const GroupOutT<W> o{p.master + so, p.m + so, p.v + so, p.out + so};
-        if constexpr (PACK) group_vec_x2<NR, GK, EXT>(src, p.n_rep, h, o, gscale);
-        else group_vec_x1<NR, GK, EXT>(src, p.n_rep, h, o, gscale);
-      }
+      const GroupOutT<W> o{p.master + so, p.m + so, p.v + so, p.out + so};
+      if constexpr (PACK) group_vec_x2<NR, GK, EXT>(src, p.n_rep, h, o, gscale);
+      else group_vec_x1<NR, GK, EXT>(src, p.n_rep, h, o, gscale);
     } else {
-      group_scalar<GK, EXT, GATHER>(p, h, sg, e0, (int)(rem < kGroup ? rem : kGroup), gscale,
-                                    gd);
+      group_scalar<GK, EXT, false>(p, h, sg, e0, (int)(rem < kGroup ? rem : kGroup), gscale,
+                                   nullptr);
     }
   }
 }
@@ -759,18 +753,6 @@ __global__ void __launch_bounds__(kThreads, W == 32 ? wide_ctas<NR, GK>() : min_
   pdl_wait();
   const float gscale = EXT ? grad_scale_of(p.h) : 1.f;
   step_loop<NR, GK, PACK, EXT, W>(p, p.h, gscale);
-}
-
-// The plain step fused with the ZeRO-3 parameter all-gather: the bf16 copy
-// goes to p.out (the rank's own replica buffer) and to every buffer of d.
-// One pass instead of a step and a broadcast that reads the copy back:
-// 4N + 24 bytes per parameter instead of 4N + 28, one launch instead of two.
-template <int NR, int GK, int PACK, int W, int MAXSEG, int MAXPTR>
-__global__ void __launch_bounds__(kThreads, W == 32 ? wide_ctas<NR, GK>() : min_ctas<NR, PACK>())
-    reduce_adam_gather_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p,
-                              const __grid_constant__ GatherDst d) {
-  pdl_wait();
-  step_loop<NR, GK, PACK, false, W, true>(p, p.h, 1.f, &d);
 }
 
 // ---------------------------------------------------------------------------
@@ -807,7 +789,9 @@ template <int NR, int GK, int PACK, int W, int MAXSEG, int MAXPTR>
 __global__ void __launch_bounds__(kThreads, W == 32 ? 3 : min_ctas<NR, PACK>())
     reduce_adam_amp_kernel(const __grid_constant__ LaunchParams<MAXSEG, MAXPTR> p,
                            const LossScaleState* state, const double* sqnorm) {
-  pdl_wait();
+  // The one-thread loss-scale update that follows is scheduled at once and
+  // waits (griddepcontrol.wait) for this grid to complete.
+  pdl_enter();
   // Thread 0 forms the step's scalars once; every thread then takes a copy of
   // the grid-constant Hyper with only those overwritten, so the untouched
   // fields stay constant-bank operands instead of occupying registers.
