@@ -85,3 +85,45 @@ def test_default_timed_steps_are_about_five_seconds_of_the_workload():
         assert k == 20000 or abs(k * per_step_s - 5.0) < per_step_s + 1e-9
     assert bench.default_steps(bench.resolve_workload("gpt2s")) == 20000
     assert bench.default_steps(bench.resolve_workload("70b_shard")) == 193
+
+
+def test_default_workload_and_named_layouts():
+    """The default line is the 70B model's 1/64 shard; sweep_ names give bucket
+    slices, full_ names the same cell as N full replica buffers; --shard-params
+    keeps the first P parameters of the same workload."""
+    sys.path.insert(0, ROOT)
+    import bench
+    args = bench.parse_args([])
+    assert args.workload == "70b_shard" and args.bucket_launch == "table"
+    wl = bench.resolve_workload("70b_shard")
+    assert (wl.n_replicas, wl.shard_elems, wl.bucket_elems) == (64, 1_093_750_000, 4_000_000)
+    s = bench.resolve_workload("sweep_256000000_24_bf16")
+    f = bench.resolve_workload("full_256000000_24_fp32")
+    assert s.layout == "slices" and f.layout == "full"
+    assert (f.shard_elems, f.n_replicas, f.grad_kind) == (256_000_000, 24, 1)
+    assert f.name.startswith("full_")
+    with pytest.raises(SystemExit):
+        bench.resolve_workload("sweep_1_2_int8")
+    assert bench.sample_elems(wl) == 1_000_000 and bench.sample_elems(s) == 2_666_666
+    assert bench.sample_elems(bench.resolve_workload("gpt2s")) == 4_000_000
+
+
+def test_traffic_is_scaled_per_parameter_and_void_on_other_sources(tmp_path, monkeypatch):
+    """A traffic summary taken on a smaller case records bytes per parameter,
+    scaled to the parameters of one launch; a summary taken on other kernel
+    sources gives no figure."""
+    sys.path.insert(0, ROOT)
+    import bench
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "reduce_adam_w_traffic.txt").write_text(
+        "# comment: ignored\ndram_bytes_per_param: 150.5\nsource_sha256: abc\n")
+    (tmp_path / "profiles" / "reduce_adam_v_traffic.txt").write_text(
+        "dram_bytes_per_launch: 1000\nsource_sha256: abc\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "abc")
+    assert bench.traffic_from_profiles("w", 1_000_000, 1.0) == pytest.approx(150.5e6)
+    assert bench.traffic_from_profiles("w", 1_000_000, 2.0) == pytest.approx(75.25e6)
+    assert bench.traffic_from_profiles("v", 123, 1.0) == 1000.0
+    assert bench.traffic_from_profiles("missing", 1, 1.0) is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "other")
+    assert bench.traffic_from_profiles("w", 1_000_000, 1.0) is None
