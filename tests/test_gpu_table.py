@@ -81,6 +81,8 @@ def _run(wl, bucket, entry, steps=(1, 2), shift=0, opts_fn=None, check=False):
     (64, 40_003, 997, 0),     # 41 buckets x 64 = 2624 pointers: two parameter-space launches
     (64, 70_000, 1_000, 1),   # fp32, 70 buckets
     (13, 300_007, 1_999, 0),  # 151 buckets: beyond 128 segments per launch
+    (24, 60_001, 401, 0),     # 150 buckets: the shared-memory replica walk over the table
+    (40, 20_000, 100, 2),     # fp16, 200 buckets, the same walk
     (4, 100_000, 333, 2),     # fp16, 301 buckets
     (2, 8_192, 4_096, 0),     # two whole buckets, 32-byte state accesses
     (1, 5_000, 7, 0),         # 715 tiny buckets, scalar tails everywhere
