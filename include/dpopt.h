@@ -35,7 +35,9 @@
  *  - Memory: the caller owns all memory.  Gradient, state and output pointers
  *    are DEVICE pointers of the current CUDA device; the pointer tables
  *    themselves (grads, grad_slices, slice_table) and offsets/lens are HOST
- *    arrays, read during the call only.  The library allocates no memory.
+ *    arrays, read during the call only.  The library allocates no device
+ *    memory (no cudaMalloc, no allocating library routine); on the host it
+ *    builds each call's small launch tables in ordinary heap memory.
  *    A "DEVICE pointer" may also point into page-locked host memory that the
  *    device addresses at the same address (cudaHostAlloc, or cudaHostRegister
  *    with cudaHostRegisterMapped, on a system with unified addressing): the
