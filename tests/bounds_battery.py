@@ -1,7 +1,8 @@
 """A battery of library calls that walks every kernel's index paths: full
 buffers and batched buckets with ragged tails, unaligned slices (the
 one-element path), the bulk-copy kernel, the runtime-replica-count kernels
-(the shared-memory walk at N = 24 and 40, the register walk at N = 64),
+(unrolled in three batches at N = 18, the shared-memory walk at N = 24 and
+40, the register walk at N = 64),
 the one-launch bucket entry (launch table in device memory, and contiguous
 buckets joined), the norm pre-pass with and without the stored average, the
 loss-scaled step, the all-gather and the fused step + all-gather (per-thread
@@ -57,7 +58,8 @@ def run() -> tuple[dict, list]:
     for n, S, dt in ((1, 10_007, torch.bfloat16), (2, 9_001, torch.bfloat16),
                      (3, 8_195, torch.bfloat16), (4, 12_289, torch.bfloat16),
                      (8, 4_099, torch.bfloat16), (13, 3_001, torch.bfloat16),
-                     (24, 2_003, torch.bfloat16), (40, 1_001, torch.float16),
+                     (18, 2_011, torch.bfloat16), (24, 2_003, torch.bfloat16),
+                     (40, 1_001, torch.float16),
                      (2, 7_003, torch.float32), (3, 5_005, torch.float32),
                      (5, 6_007, torch.float32), (4, 4_103, torch.float16)):
         rank = n // 2

@@ -183,12 +183,13 @@ def test_every_unrolled_replica_count(n, kind):
 
 
 @pytest.mark.parametrize("kind", [0, 2])
-@pytest.mark.parametrize("n", [17, 23, 24, 40, 56, 57, 63, 64])
+@pytest.mark.parametrize("n", [17, 18, 20, 21, 24, 40, 56, 57, 63, 64])
 def test_many_replicas_both_walks_every_element(n, kind):
-    """16-bit gradients beyond the unrolled kernels: N = 17..56 take the walk
-    that stages the replica loads in shared memory, larger N the
-    register-pipelined walk; every element agrees with the oracle step by
-    step, and the batched-bucket entry gives the same bits."""
+    """16-bit gradients with many replicas: N = 17..20 take unrolled kernels
+    (three batches of loads), N = 21..56 the walk that stages the replica loads
+    in shared memory, larger N the register-pipelined walk; every element
+    agrees with the oracle step by step, and the batched-bucket entry gives
+    the same bits."""
     _need_gpu()
     S = 9_001
     wl = _small_workload(n, S, kind=kind)

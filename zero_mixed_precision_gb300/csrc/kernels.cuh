@@ -351,10 +351,26 @@ struct GatherOutT : GroupOutT<W> {
 // The fixed-order compensated replica sum of one 8-element group (scalar
 // lanes), shared by the step and the squared-norm pre-pass so both see the
 // same bits of g.
+// Replicas R0 .. R0+REM-1 added in order, in batches of at most 8 whose loads
+// are issued together.
+template <int REM, int R0, int GK, class Src>
+__device__ __forceinline__ void add_batches_x1(const Src& src, CompSum<float> (&acc)[kGroup]) {
+  constexpr int B = REM < 8 ? REM : 8;
+  GradLoad<GK> gl[B];
+#pragma unroll
+  for (int r = 0; r < B; ++r) src.grad(gl[r], R0 + r);
+#pragma unroll
+  for (int r = 0; r < B; ++r) {
+#pragma unroll
+    for (int k = 0; k < kGroup; ++k) acc[k].add(gl[r].get(k));
+  }
+  if constexpr (REM > 8) add_batches_x1<REM - 8, R0 + 8, GK>(src, acc);
+}
+
 template <int NR, int GK, class Src>
 __device__ __forceinline__ void reduce_group_x1(const Src& src, int n, CompSum<float> (&acc)[kGroup]) {
   if constexpr (NR > 8) {
-    // two batches (8, then NR - 8 <= 8) so that at most 8 loads are held at once
+    // batches of 8 (the last one NR mod 8) so that at most 8 loads are held at once
     {
       GradLoad<GK> gl[8];
 #pragma unroll
@@ -367,14 +383,7 @@ __device__ __forceinline__ void reduce_group_x1(const Src& src, int n, CompSum<f
         for (int k = 0; k < kGroup; ++k) acc[k].add(gl[r].get(k));
       }
     }
-    GradLoad<GK> gl[NR - 8];
-#pragma unroll
-    for (int r = 0; r < NR - 8; ++r) src.grad(gl[r], 8 + r);
-#pragma unroll
-    for (int r = 0; r < NR - 8; ++r) {
-#pragma unroll
-      for (int k = 0; k < kGroup; ++k) acc[k].add(gl[r].get(k));
-    }
+    add_batches_x1<NR - 8, 8, GK>(src, acc);
   } else if constexpr (NR > 0) {
     GradLoad<GK> gl[NR];
 #pragma unroll

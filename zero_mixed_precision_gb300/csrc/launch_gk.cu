@@ -6,12 +6,15 @@
 // Replica counts 1..8 each get a kernel with the replica loop unrolled: at
 // most 64 registers, so four 256-thread CTAs share an SM and every thread has
 // all N of its gradient loads in flight at once.  bf16 and fp16 gradients with
-// 9..16 replicas get unrolled kernels too, reading the replicas in two batches
-// (8, then the rest) at the same four CTAs per SM: 100-102 % of the copy
+// 9..20 replicas get unrolled kernels too, reading the replicas in batches of
+// 8 (the last one N mod 8) at the same four CTAs per SM: 100-102 % of the copy
 // bandwidth at N = 9..14 against 85-92 % for the runtime-count packed body,
-// which runs above (and for fp32 above 8, where it already reaches the copy
-// rate) at two CTAs per SM.  The accumulation order is the same in
-// every form, so the choice changes speed only, never bits.
+// and at N = 17..20 96.9-97.3 % against 94.1-96.9 % for the shared-memory
+// walk (S = 256M).  Above 20 the 16-bit kernels walk the replicas at runtime
+// count (the shared-memory walk to 56, the register-pipelined walk above);
+// fp32 gradients take the runtime-count packed body above 8, where it already
+// reaches the copy rate.  The accumulation order is the same in every form,
+// so the choice changes speed only, never bits.
 
 //
 // The state access width of each kernel is wide_states() (kernels.cuh).
@@ -118,8 +121,9 @@ int step_kernel(const LP& p, cudaStream_t stream) {
 // chunks at one CTA measured slower.
 constexpr int kAsyncDepth = 3;
 constexpr int kAsyncMinBlocks = 2;
-// Replica counts up to this take the asynchronous walk, larger ones the
-// register-pipelined walk of kernels.cuh (faster at N = 64).
+// Replica counts from 21 up to this take the asynchronous walk (17..20 have
+// unrolled kernels), larger ones the register-pipelined walk of kernels.cuh
+// (faster at N = 64).
 constexpr int kAsyncMaxReplicas = 56;
 
 template <bool EXT, class LP>
@@ -176,10 +180,14 @@ int step_n(const LP& p, cudaStream_t s) {
     case 14: if constexpr (kGK != 1) return step_nr<14, EXT>(p, s); else break;
     case 15: if constexpr (kGK != 1) return step_nr<15, EXT>(p, s); else break;
     case 16: if constexpr (kGK != 1) return step_nr<16, EXT>(p, s); else break;
-    default:
-      if constexpr (kGK != 1)
-        if (p.n_rep <= kAsyncMaxReplicas) return async_step<EXT>(p, s);
-      break;
+    case 17: if constexpr (kGK != 1) return step_nr<17, EXT>(p, s); else break;
+    case 18: if constexpr (kGK != 1) return step_nr<18, EXT>(p, s); else break;
+    case 19: if constexpr (kGK != 1) return step_nr<19, EXT>(p, s); else break;
+    case 20: if constexpr (kGK != 1) return step_nr<20, EXT>(p, s); else break;
+    default: break;
+  }
+  if constexpr (kGK != 1) {
+    if (p.n_rep >= 17 && p.n_rep <= kAsyncMaxReplicas) return async_step<EXT>(p, s);
   }
   return step_kernel<0, 1, EXT, 16>(p, s);
 }
