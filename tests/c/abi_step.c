@@ -2,7 +2,10 @@
  * abi_step.c -- the C ABI used from plain C, with no Python and no PyTorch:
  * cudaMalloc'd buffers, a cudaStream_t, dpopt_reduce_adam for two steps on
  * one rank's shard, dpopt_stream_status, and the results checked against the
- * CPU oracle (oracle/oracle.c, linked as test infrastructure only).
+ * CPU oracle (oracle/oracle.c, linked as test infrastructure only); then a
+ * third step through dpopt_reduce_adam_buckets_table with 159 separately
+ * allocated bucket slices and a cudaMalloc'd launch table, bitwise against
+ * the full-buffer entry.
  * Built and run by tests/test_gpu_c_abi.py; prints "ok" and exits 0 on
  * success.
  */
@@ -127,7 +130,73 @@ int main(void) {
     fprintf(stderr, "%lld of %d elements off (worst relative %.3e)\n", (long long)bad, S, worst);
     return 1;
   }
-  printf("ok: N=%d, %d shard elements, 2 steps, worst relative %.2e, version %s\n", N, S, worst,
-         dpopt_version());
+
+  /* A third step twice, from the same states: once through the full-buffer
+     entry, once through the one-launch bucket entry with every bucket slice in
+     an allocation of its own (159 buckets of 63 elements, the last ragged: more
+     than one launch's parameter space holds, so the launch table goes to the
+     cudaMalloc'd memory). The two must leave the same bits. */
+  enum { BL = 63, NB = (S + BL - 1) / BL };
+  int64_t off[NB], len[NB];
+  for (int b = 0; b < NB; ++b) {
+    off[b] = (int64_t)b * BL;
+    len[b] = S - off[b] < BL ? S - off[b] : BL;
+  }
+  float *st3[2][3];
+  void *out3[2];
+  for (int k = 0; k < 2; ++k) {
+    for (int a = 0; a < 3; ++a) {
+      check(cudaMalloc((void **)&st3[k][a], S * 4), "cudaMalloc");
+      check(cudaMemcpy(st3[k][a], a == 0 ? dth : a == 1 ? dm : dv, S * 4,
+                       cudaMemcpyDeviceToDevice), "cudaMemcpy");
+    }
+    check(cudaMalloc(&out3[k], S * 2), "cudaMalloc");
+  }
+  static const void *slices[NB * N];
+  for (int b = 0; b < NB; ++b)
+    for (int r = 0; r < N; ++r) {
+      void *sl;
+      check(cudaMalloc(&sl, len[b] * 2), "cudaMalloc");
+      check(cudaMemcpy(sl, (const uint16_t *)dg[r] + (int64_t)RANK * S + off[b], len[b] * 2,
+                       cudaMemcpyDeviceToDevice), "cudaMemcpy");
+      slices[b * N + r] = sl;
+    }
+  int64_t tbytes = 0;
+  void *table;
+  if (dpopt_bucket_table_bytes(N, NB, &tbytes) != DPOPT_OK) return 1;
+  check(cudaMalloc(&table, tbytes), "cudaMalloc");
+  if (dpopt_reduce_adam_buckets_table(slices, DPOPT_GRAD_BF16, N, off, len, NB, st3[1][0],
+                                      st3[1][1], st3[1][2], out3[1], lr, b1, b2, eps, 3, NULL,
+                                      table, tbytes - 1, st) != DPOPT_ERR_INVALID_ARG) {
+    fprintf(stderr, "a table one byte short was not rejected\n");
+    return 1;
+  }
+  int rc = dpopt_reduce_adam((const void *const *)dg, N, numel, RANK, 4096, st3[0][0], st3[0][1],
+                             st3[0][2], out3[0], lr, b1, b2, eps, 3, st);
+  if (rc == DPOPT_OK)
+    rc = dpopt_reduce_adam_buckets_table(slices, DPOPT_GRAD_BF16, N, off, len, NB, st3[1][0],
+                                         st3[1][1], st3[1][2], out3[1], lr, b1, b2, eps, 3, NULL,
+                                         table, tbytes, st);
+  if (rc == DPOPT_OK) rc = dpopt_stream_status(st);
+  if (rc != DPOPT_OK) {
+    fprintf(stderr, "step 3: %s (%s)\n", dpopt_status_string(rc), dpopt_last_error());
+    return 1;
+  }
+  for (int a = 0; a < 4; ++a) {
+    const size_t bytes = a < 3 ? S * 4 : S * 2;
+    unsigned char *x = malloc(bytes), *y = malloc(bytes);
+    check(cudaMemcpy(x, a < 3 ? (void *)st3[0][a] : out3[0], bytes, cudaMemcpyDeviceToHost),
+          "cudaMemcpy");
+    check(cudaMemcpy(y, a < 3 ? (void *)st3[1][a] : out3[1], bytes, cudaMemcpyDeviceToHost),
+          "cudaMemcpy");
+    if (memcmp(x, y, bytes) != 0) {
+      fprintf(stderr, "the bucket-table step differs from the full-buffer step (array %d)\n", a);
+      return 1;
+    }
+    free(x);
+    free(y);
+  }
+  printf("ok: N=%d, %d shard elements, 2 steps, worst relative %.2e; step 3 through the "
+         "bucket table bitwise equal; version %s\n", N, S, worst, dpopt_version());
   return 0;
 }

@@ -28,3 +28,4 @@ def test_plain_c_program_steps_through_the_abi(tmp_path):
     pr = subprocess.run([str(exe)], capture_output=True, text=True, timeout=300)
     assert pr.returncode == 0, pr.stdout + pr.stderr
     assert pr.stdout.startswith("ok:"), pr.stdout
+    assert "bucket table bitwise equal" in pr.stdout
