@@ -4,10 +4,10 @@
 // With N = 21..56 replicas the step is bound by how many gradient bytes each
 // SM keeps in flight: the register-pipelined walk holds two chunks of 8
 // 16-byte loads per thread (64 of its 126 registers), two CTAs per SM.  Here
-// every thread copies its own 16-byte pieces of the next kAsyncDepth chunks
+// every thread copies its own 16-byte pieces of the next D chunks (three)
 // straight into a ring of slots in shared memory (cp.async, no registers held
 // while in flight), waits for the oldest chunk, adds it from shared memory in
-// ascending replica order, and refills that slot with the chunk kAsyncDepth
+// ascending replica order, and refills that slot with the chunk D
 // further on.  A thread reads only the slots it filled itself, so no barrier
 // is needed; cp.async.wait_group orders each slot's copy before its read.
 // The arithmetic and the order are those of the other forms: the same bits.

@@ -111,25 +111,27 @@ int step_kernel(const LP& p, cudaStream_t stream) {
 }
 
 // The runtime-count step for 16-bit gradients with the replica loads staged
-// in shared memory by asynchronous copies (async_walk.cuh): kAsyncDepth chunks
-// of 8 replicas in flight per thread, kAsyncMinBlocks CTAs per SM (96 KB of
+// in shared memory by asynchronous copies (async_walk.cuh): `depth` chunks of
+// 8 replicas in flight per thread, `min_blocks` CTAs per SM (96 KB of
 // shared memory each).  Measured on GB300 (bf16, S = 256M, GB/s, asynchronous
 // walk against the register-pipelined one): N = 17 6366 / 6356, 18 6428 /
 // 6007, 20 6531 / 6268, 23 6644 / 6531, 24 6670 / 6521, 28 6670 / 6174,
 // 31 6750 / 6217, 32 6835 / 6626, 40 6817 / 6357, 48 6816 / 6627, 56 6773 /
 // 6530, 64 6617 / 6742.  Two chunks at three CTAs per SM (spilling) and four
 // chunks at one CTA measured slower.
-constexpr int kAsyncDepth = 3;
-constexpr int kAsyncMinBlocks = 2;
-// Replica counts from 21 up to this take the asynchronous walk (17..20 have
-// unrolled kernels), larger ones the register-pipelined walk of kernels.cuh
-// (faster at N = 64).
-constexpr int kAsyncMaxReplicas = 56;
+// max_replicas: replica counts from 21 up to this take the asynchronous walk
+// (17..20 have unrolled kernels), larger ones the register-pipelined walk of
+// kernels.cuh (faster at N = 64).
+struct AsyncWalk {
+  static constexpr int depth = 3;
+  static constexpr int min_blocks = 2;
+  static constexpr int max_replicas = 56;
+};
 
 template <bool EXT, class LP>
 int async_step(const LP& p, cudaStream_t stream) {
-  auto kern = reduce_adam_async_kernel<kAsyncDepth, kAsyncMinBlocks, kGK, EXT, LP>;
-  constexpr int smem = (int)async_ring_bytes<kAsyncDepth>();
+  auto kern = reduce_adam_async_kernel<AsyncWalk::depth, AsyncWalk::min_blocks, kGK, EXT, LP>;
+  constexpr int smem = (int)async_ring_bytes<AsyncWalk::depth>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
   static std::atomic<int> per_sm{0};
@@ -187,7 +189,7 @@ int step_n(const LP& p, cudaStream_t s) {
     default: break;
   }
   if constexpr (kGK != 1) {
-    if (p.n_rep >= 17 && p.n_rep <= kAsyncMaxReplicas) return async_step<EXT>(p, s);
+    if (p.n_rep >= 17 && p.n_rep <= AsyncWalk::max_replicas) return async_step<EXT>(p, s);
   }
   return step_kernel<0, 1, EXT, 16>(p, s);
 }
