@@ -186,8 +186,8 @@ def test_every_unrolled_replica_count(n, kind):
 @pytest.mark.parametrize("n", [17, 18, 20, 21, 24, 40, 56, 57, 63, 64])
 def test_many_replicas_both_walks_every_element(n, kind):
     """16-bit gradients with many replicas: N = 17..20 take unrolled kernels
-    (three batches of loads), N = 21..56 the walk that stages the replica loads
-    in shared memory, larger N the register-pipelined walk; every element
+    (three batches of loads), N = 21..63 the walk that stages the replica loads
+    in shared memory, N = 64 the register-pipelined walk; every element
     agrees with the oracle step by step, and the batched-bucket entry gives
     the same bits."""
     _need_gpu()

@@ -1,7 +1,7 @@
 // async_walk.cuh -- the step for many replicas of 16-bit gradients with the
 // replica loads staged in shared memory by per-thread asynchronous copies.
 //
-// With N = 21..56 replicas the step is bound by how many gradient bytes each
+// With N = 21..63 replicas the step is bound by how many gradient bytes each
 // SM keeps in flight: the register-pipelined walk holds two chunks of 8
 // 16-byte loads per thread (64 of its 126 registers), two CTAs per SM.  Here
 // every thread copies its own 16-byte pieces of the next D chunks (three)

@@ -11,7 +11,7 @@
 // bandwidth at N = 9..14 against 85-92 % for the runtime-count packed body,
 // and at N = 17..20 96.9-97.3 % against 94.1-96.9 % for the shared-memory
 // walk (S = 256M).  Above 20 the 16-bit kernels walk the replicas at runtime
-// count (the shared-memory walk to 56, the register-pipelined walk above);
+// count (the shared-memory walk to 63, the register-pipelined walk at 64);
 // fp32 gradients take the runtime-count packed body above 8, where it already
 // reaches the copy rate.  The accumulation order is the same in every form,
 // so the choice changes speed only, never bits.
@@ -117,15 +117,15 @@ int step_kernel(const LP& p, cudaStream_t stream) {
 // walk against the register-pipelined one): N = 17 6366 / 6356, 18 6428 /
 // 6007, 20 6531 / 6268, 23 6644 / 6531, 24 6670 / 6521, 28 6670 / 6174,
 // 31 6750 / 6217, 32 6835 / 6626, 40 6817 / 6357, 48 6816 / 6627, 56 6773 /
-// 6530, 64 6617 / 6742.  Two chunks at three CTAs per SM (spilling) and four
-// chunks at one CTA measured slower.
+// 6530, 57 6809 / 6361, 63 6743 / 6263, 64 6617 / 6742.  Two chunks at three
+// CTAs per SM (spilling) and four chunks at one CTA measured slower.
 // max_replicas: replica counts from 21 up to this take the asynchronous walk
-// (17..20 have unrolled kernels), larger ones the register-pipelined walk of
-// kernels.cuh (faster at N = 64).
+// (17..20 have unrolled kernels); N = 64 the register-pipelined walk of
+// kernels.cuh, faster there.
 struct AsyncWalk {
   static constexpr int depth = 3;
   static constexpr int min_blocks = 2;
-  static constexpr int max_replicas = 56;
+  static constexpr int max_replicas = 63;
 };
 
 template <bool EXT, class LP>
