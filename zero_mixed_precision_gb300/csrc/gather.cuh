@@ -10,7 +10,7 @@
 // an HBM-bound copy.
 #pragma once
 
-#include "kernels.cuh"
+#include "gather_bulk.cuh"
 
 namespace dpopt {
 
@@ -25,12 +25,37 @@ struct GatherParams {
 #endif
 };
 
+// The CTA walks the shard in tiles of kThreads groups (2048 elements, 4 KB):
+// every thread loads its 16 bytes into the tile in shared memory and one
+// thread writes the whole tile to every replica buffer with bulk copies, so
+// the N writes leave the store pipe (which otherwise sets the pace of this
+// write-heavy copy) for the bulk-copy engine; two tiles alternate.  Tiles that
+// are not whole, or not 16-byte aligned, go element group by group.
 __global__ void __launch_bounds__(kThreads) allgather_bf16_kernel(const __grid_constant__ GatherParams p) {
+  __shared__ __align__(128) uint4 tile[2][kThreads];
   pdl_wait();
   const uint64_t pol = evict_first_policy();
   const int64_t groups = (p.len + kGroup - 1) / kGroup;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < groups; gi += stride) {
+  const int64_t cta_stride = (int64_t)gridDim.x * kThreads;
+  int buf = 0;
+  int64_t base = (int64_t)blockIdx.x * kThreads;
+  for (; base < groups && p.vec && (base + kThreads) * kGroup <= p.len; base += cta_stride) {
+    const int64_t e0 = (base + threadIdx.x) * kGroup;
+    tile[buf][threadIdx.x] = ld_grad16(p.src + e0, pol);
+    fence_proxy_async_shared();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint32_t t = smem_u32_of(&tile[buf][0]);
+      constexpr uint32_t kBytes = kThreads * kGroup * 2;
+      for (int r = 0; r < p.n_dst; ++r) bulk_store(p.dst[r] + base * kGroup, t, kBytes, pol);
+      bulk_commit();
+      bulk_wait_read<1>();  // the other tile is free again
+    }
+    __syncthreads();
+    buf ^= 1;
+  }
+  // the remaining tile (not whole, or unaligned pointers): element groups
+  for (int64_t gi = base + threadIdx.x; gi < groups; gi += cta_stride) {
     const int64_t e0 = gi * kGroup;
 #ifdef DPOPT_DEBUG_BOUNDS
     if (e0 < 0 || e0 >= p.len) {
@@ -49,6 +74,7 @@ __global__ void __launch_bounds__(kThreads) allgather_bf16_kernel(const __grid_c
       }
     }
   }
+  if (threadIdx.x == 0) bulk_wait<0>();  // every bulk copy performed before the CTA exits
 }
 
 }  // namespace dpopt
