@@ -400,13 +400,47 @@ int dpopt_amp_average_sqnorm(const void *const *grads, int grad_dtype, int n_rep
  * averaged gradient times c = (1/scale) * min(1, max_grad_norm / (||g|| + 1e-6))
  * (max_grad_norm 0: no clipping), with the bias corrections of step state->step
  * + 1; then the state is advanced (or the step is counted as skipped).  The
- * step index comes from the state, not from the caller. */
+ * step index comes from the state, not from the caller.
+ * global_sqnorm may be NULL when max_grad_norm is 0: then there is no overflow
+ * test, the step is always taken, and only state->step advances (the scale and
+ * its counters are left as they are; with scale 1 the gradient is used as it
+ * is).  That is the step of a run without loss scaling whose step count lives
+ * on the device -- the form to capture in a CUDA graph (see below).
+ * Errors: as for dpopt_reduce_adam_ex, plus DPOPT_ERR_INVALID_ARG for a
+ * misaligned global_sqnorm, a NULL one with max_grad_norm > 0, or a state
+ * overlapping a state or output array. */
 int dpopt_amp_step(const void *const *grads, int grad_dtype, int n_replicas, int64_t numel,
                    int shard_rank, int64_t bucket_elems, float *master_f32, float *m_f32,
                    float *v_f32, void *param_bf16_out, float lr, float beta1, float beta2,
                    float eps, float weight_decay, float max_grad_norm,
                    const double *global_sqnorm, dpopt_loss_scale_state *state,
                    const dpopt_loss_scale_config *cfg, dpopt_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* CUDA graphs                                                                */
+/* ------------------------------------------------------------------------- */
+
+/* Every entry that takes a stream only enqueues kernels (and, for the table
+ * entry, one copy) on it, allocates nothing and never synchronises, so it may
+ * be called while the stream is being captured into a CUDA graph; the graph
+ * then holds the call's launches with the arguments of the call.  What a
+ * replay does follows from that:
+ *  - the entries that take `step` (and lr) from the caller repeat that step on
+ *    every replay: capture them once per step, or update the kernel nodes'
+ *    parameters between replays;
+ *  - dpopt_amp_sqnorm / dpopt_amp_step read the loss scale and the step count
+ *    from the device state and advance it themselves, so one captured graph of
+ *    an iteration replays iteration after iteration (with global_sqnorm NULL
+ *    for a run without loss scaling);
+ *  - dpopt_reduce_adam_buckets_table refuses with DPOPT_ERR_UNSUPPORTED when
+ *    its launch table must be written (the buckets do not fit the parameter
+ *    space) while `stream` is capturing: the table is copied from host memory
+ *    that the next call reuses, which a replay would read stale;
+ *  - dpopt_stream_status synchronises and must not be called on a capturing
+ *    stream; dpopt_reduce_adam_buckets_when_ready waits on the caller's events,
+ *    which must then belong to the same capture;
+ *  - dpopt_grad_sqnorm_noalloc must have been called once (numel 0 will do)
+ *    before the capture, so that its device array's address is resolved. */
 
 /* ------------------------------------------------------------------------- */
 /* ZeRO-3 parameter all-gather                                                */

@@ -252,6 +252,15 @@ def test_sqnorm_and_adamw_reject_bad_arguments(dp):
     assert dp.dpopt_reduce_adamw(G[:4], 0, 4, 4096, 0, 1024, MASTER, M, V, OUT, *HP, 1, opt, 0) == 1
     opt = dp.StepOptions(0.01, 1.0, SQ + 3, 0.0)  # misaligned norm pointer
     assert dp.dpopt_reduce_adamw(G[:4], 0, 4, 4096, 0, 1024, MASTER, M, V, OUT, *HP, 1, opt, 0) == 1
+    # the loss-scaled step: its norm may be null only without clipping
+    STATE = 0xF0_0000_0000
+    cfg = dp.LossScaleConfig(1024.0, 10, 2, 1.0)
+
+    def amp(sq, max_norm):
+        return dp.dpopt_amp_step(G[:4], 0, 4, 4096, 0, 1024, MASTER, M, V, OUT, *HP, 0.01,
+                                 max_norm, sq, STATE, cfg, 0)
+    assert amp(0, 1.0) == 1
+    assert amp(SQ + 4, 0.0) == 1
 
 
 def test_binding_refuses_pageable_host_operands(dp):

@@ -46,6 +46,9 @@ NVCC_FLAGS = [
     "-O3", "-lineinfo", "-std=c++17",
     "-prec-div=true", "-prec-sqrt=true", "-fmad=true",
     "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
+    # host arithmetic (the step's fp64 scalars) rounds every operation on its
+    # own on x86 and Arm alike: no fused multiply-add contraction
+    "-Xcompiler", "-ffp-contract=off",
 ]
 
 

@@ -650,8 +650,8 @@ def amp_step(grads, shard_rank: int, bucket_elems: int, master, m, v, param_bf16
     rc = dpopt_amp_step([_operand(g) for g in grads], dt, len(grads), grads[0].numel(),
                         shard_rank, bucket_elems, _operand(master), _operand(m), _operand(v),
                         _operand(param_bf16_out), lr, beta1, beta2, eps, weight_decay,
-                        max_grad_norm, _operand(global_sqnorm), _operand(state), cfg,
-                        _stream_handle(stream))
+                        max_grad_norm, 0 if global_sqnorm is None else _operand(global_sqnorm),
+                        _operand(state), cfg, _stream_handle(stream))
     _check(rc, "dpopt_amp_step")
 
 

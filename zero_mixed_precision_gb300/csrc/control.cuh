@@ -22,12 +22,19 @@ __global__ void loss_scale_init_kernel(LossScaleState* st, LossScaleConfig cfg) 
 
 // After a step: skip bookkeeping, halving on every hysteresis-th overflow since
 // the scale last changed (not below min_scale), doubling after `window` clean
-// steps in a row.
+// steps in a row.  Without a squared norm (null: a run without loss scaling)
+// only the step count advances; the scale and its counters stay as they are.
 __global__ void loss_scale_update_kernel(LossScaleState* st, const double* sqnorm,
                                          LossScaleConfig cfg) {
   pdl_enter();
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   LossScaleState s = *st;
+  if (sqnorm == nullptr) {
+    s.last_overflow = 0;
+    s.step += 1;
+    *st = s;
+    return;
+  }
   const bool overflow = !isfinite(*sqnorm);
   s.last_overflow = overflow ? 1 : 0;
   if (overflow) {

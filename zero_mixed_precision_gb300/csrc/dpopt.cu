@@ -620,7 +620,18 @@ int table_impl(const void* const* slice_table, int grad_dtype, int n_replicas,
 
   // The records and pointers, packed on the host.  A copy from pageable host
   // memory returns once the bytes have left this buffer, so it is reused by
-  // this thread's next call without waiting for the device.
+  // this thread's next call without waiting for the device.  A captured graph
+  // would instead read the buffer at every replay, after later calls have
+  // rewritten it: under capture the call is refused before anything is
+  // enqueued.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t ce = cudaStreamIsCapturing(stream, &cap);
+  if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamIsCapturing");
+  if (cap != cudaStreamCaptureStatusNone)
+    return fail(DPOPT_ERR_UNSUPPORTED,
+                "the launch table is copied from reused host memory, which a captured graph "
+                "cannot replay: capture buckets that fit one launch (%d segments, %d slice "
+                "pointers)", kBigSegs, kBigPtrs);
   const int nseg = (int)segs.size();
   const int64_t used = table_bytes_for(n_replicas, nseg);
   static thread_local std::vector<unsigned char> staging;
@@ -1078,8 +1089,9 @@ int dpopt_amp_step(const void* const* grads, int grad_dtype, int n_replicas, int
   LossScaleConfig c;
   rc = check_scale_config(cfg, &c);
   if (rc) return rc;
-  if (!global_sqnorm || ((uintptr_t)global_sqnorm & 7u))
-    return fail(DPOPT_ERR_INVALID_ARG, "global_sqnorm must be a non-null, 8-byte aligned pointer");
+  if (global_sqnorm ? ((uintptr_t)global_sqnorm & 7u) != 0 : max_grad_norm != 0.f)
+    return fail(DPOPT_ERR_INVALID_ARG,
+                "global_sqnorm must be 8-byte aligned, and non-null when clipping");
   Hyper h = make_hyper(lr, beta1, beta2, eps, 1, n_replicas);
   dpopt_step_options o{weight_decay, max_grad_norm, global_sqnorm, 0.f};
   bool ext = false;

@@ -789,7 +789,10 @@ struct LossScaleConfig {
 // of the unscaled gradient is not finite (an overflow somewhere); otherwise
 // the bias corrections of step state->step + 1 and the multiplier 1/scale
 // (times the clip coefficient) are formed here, from device state, so no host
-// synchronisation is needed between steps.
+// synchronisation is needed between steps and the launch replays unchanged
+// from a captured CUDA graph.  A null sqnorm means no overflow test and no
+// clipping (a run without loss scaling that keeps its step count on the
+// device).
 // The 256-bit forms run three CTAs per SM at every N (up to 85 registers): the
 // per-step scalars held in registers make even the one-replica form spill at
 // four (loss-scaled gpt2s step through the stored average: 130.7 against
@@ -809,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, W == 32 ? 3 : min_ctas<NR, PACK>())
   __shared__ int skip;
   if (threadIdx.x == 0) {
     Hyper h = p.h;
-    const double sq = *sqnorm;
+    const double sq = sqnorm ? *sqnorm : 0.0;
     skip = isfinite(sq) ? 0 : 1;
     const LossScaleState st = *state;
     const double t = (double)(st.step + 1);

@@ -1,7 +1,6 @@
 // tma.cu -- launches of the bulk-copy (TMA) staged step kernel, the status
 // word of the bounded device-side waits and their self-test.
 #include <algorithm>
-#include <atomic>
 #include <cstring>
 
 #include "internal.h"
@@ -25,18 +24,17 @@ template <int NR, int GK, int W, int MS, int MP>
 int launch_tma(const TmaParams<MS, MP>& p, cudaStream_t stream) {
   auto kern = reduce_adam_tma_kernel<NR, GK, W, MS, MP>;
   const size_t dyn = (size_t)p.stages * p.stage_bytes;
-  static std::atomic<size_t> configured{0};
-  if (configured.load(std::memory_order_relaxed) < dyn) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kTmaSmemBudget + 1024));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-    configured.store(kTmaSmemBudget + 1024, std::memory_order_relaxed);
-  }
+  // a function attribute belongs to the current device's context: set on
+  // every call (a host-side call, no stream work), so that every device a
+  // process drives gets it
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)(kTmaSmemBudget + 1024));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
   int sms = 0;
   int rc = sm_count(&sms);
   if (rc) return rc;
   int bps = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, kTmaThreads, dyn);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, kTmaThreads, dyn);
   if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
   if (bps < 1) return fail(DPOPT_ERR_UNSUPPORTED, "bulk-copy kernel does not fit an SM");
   const int64_t want = std::max<int64_t>(p.total_tiles, (int64_t)p.nseg);
