@@ -42,9 +42,10 @@ if ROOT not in sys.path:
 METRIC = "G params/s updated and achieved HBM GB/s vs ~8 TB/s roofline, at N replicas"
 UNIT = "G params/s"
 FALLBACK_HBM_GBS = 6800.0
-# the step kernel's device code and its per-N form table (a traffic figure is
-# void once these change; launch plumbing lives elsewhere)
-KERNEL_SOURCES = ("numerics.cuh", "kernels.cuh")
+# the step kernel's device code, the other replica walks and the table that
+# picks the kernel for each N and gradient type: a traffic figure is void once
+# any of these change
+KERNEL_SOURCES = ("numerics.cuh", "kernels.cuh", "async_walk.cuh", "launch_gk.cu")
 
 
 def parse_args(argv=None):
@@ -534,9 +535,12 @@ def run_ours(args, wl):
         ip_ms = timed_e2e(in_place)
         ce_ms = timed_e2e(copies)
     h2d, d2h = n * S * esize, S * 2
+    link = host_link_h2d_gbs(device, stream)
     e2e = {"value": throughput(world, S, Ke, ip_ms), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "host_link_gbs": (h2d + d2h) * Ke / (ip_ms * 1e-3) / 1e9,
+           "host_link_h2d_copy_gbs": link,
+           "h2d_frac_of_copy": h2d * Ke / (ip_ms * 1e-3) / 1e9 / link,
            "path": "pinned host gradients read in place by dpopt_reduce_adam_bucket's kernel, "
                    "bf16 parameters written into pinned host memory, one launch per step",
            "copy_engine": {"value": throughput(world, S, Ke, ce_ms), "unit": UNIT,
@@ -549,6 +553,27 @@ def run_ours(args, wl):
               else h[:cap].numpy()).copy() for h in hs]
     return _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks, e2e,
                    grads, stored)
+
+
+def host_link_h2d_gbs(device, stream, nbytes: int = 1 << 30, reps: int = 3) -> float:
+    """The host link's measured host-to-device rate: one cudaMemcpyAsync of a
+    1 GB pinned buffer into device memory, timed with CUDA events (the rate
+    the end-to-end figures are set against)."""
+    import torch
+    src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    src.fill_(1)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    with torch.cuda.stream(stream):
+        dst.copy_(src, non_blocking=True)              # untimed: first touch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    gbs = nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del src, dst
+    return gbs
 
 
 def e2e_ring(args, wl, dev, stream, hp, world, barrier, K):
@@ -641,9 +666,12 @@ def e2e_ring(args, wl, dev, stream, hp, world, barrier, K):
     barrier()
     dp.stream_status(stream)
     ce_ms = max_over_ranks(c0.elapsed_time(c1), world, dev.device)
+    link = host_link_h2d_gbs(dev.device, stream)
     e2e = {"value": throughput(world, S, Ke, ms), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "host_link_gbs": (h2d + d2h) * Ke / (ms * 1e-3) / 1e9, "steps": Ke,
+           "host_link_h2d_copy_gbs": link,
+           "h2d_frac_of_copy": h2d * Ke / (ms * 1e-3) / 1e9 / link,
            "path": f"{nb} buckets x {n} gradient slices per step read in place from a ring of "
                    f"{R} pinned host bucket slots ({R * n * be * esize / 1e9:.2f} GB) by one "
                    "dpopt_reduce_adam_buckets_table launch, bf16 parameters written into pinned "
