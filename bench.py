@@ -844,8 +844,9 @@ def run_overlap(args, wl):
 def run_sweep(args):
     """One line per sweep cell: N slices of S elements (one bucket), one step
     per rep.  Cells whose working set is under 512 MB would sit in the 129 MB L2
-    between reps, so a 1 GB buffer is written before each rep and only the step
-    is timed (flagged); cells that do not fit the free memory are skipped."""
+    between reps, so a 1 GB buffer is written and a 256 MB one read before each
+    rep and only the step is timed (flagged); cells that do not fit the free
+    memory are skipped."""
     import torch
 
     import synth
@@ -856,7 +857,10 @@ def run_sweep(args):
     peak, peak_kind = load_peaks()
     sizes = ([int(x) for x in args.sweep_sizes.split(",")] if args.sweep_sizes
              else list(synth.SWEEP_SIZES))
+    # the flush writes 1 GB, then reads 256 MB: the step starts with no line of
+    # its own in L2 and no dirty line of the flush left to write back
     flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    clean = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
     for kind in (0, 1):
         for S in sizes:
             for n in synth.SWEEP_REPLICAS:
@@ -886,6 +890,7 @@ def run_sweep(args):
                     tot = 0.0
                     for k in range(reps):
                         flush.fill_(k & 0xFF)
+                        clean.sum()
                         e0 = torch.cuda.Event(enable_timing=True)
                         e1 = torch.cuda.Event(enable_timing=True)
                         e0.record()
@@ -910,8 +915,9 @@ def run_sweep(args):
                 line.update(ms_per_step=ms, g_params_per_s=S / (ms / 1e3) / 1e9, hbm_gbs=gbs,
                             frac_of_measured=gbs / peak, frac_of_8tbs=gbs / 8000.0,
                             peak_source=peak_kind, reps=reps,
-                            l2="flushed before each rep (1 GB write), step timed alone: not a "
-                               "roofline figure" if l2_flush else "working set above L2")
+                            l2="flushed before each rep (1 GB written, 256 MB read), step "
+                               "timed alone: not a roofline figure" if l2_flush
+                               else "working set above L2")
                 print(json.dumps(line), flush=True)
                 del dev, rows, offs
                 torch.cuda.empty_cache()
