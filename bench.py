@@ -91,10 +91,10 @@ def parse_args(argv=None):
                          "dynamic loss scaling -- the unscaled squared-norm pre-pass, then the "
                          "loss-scaled, clipped AdamW step and the device-side scale update")
     ap.add_argument("--clip-path", choices=("stored", "fused"), default="stored",
-                    help="adamw_clip / amp on full-buffer workloads: 'stored' -- the norm pass "
-                         "also stores the averaged gradient (the reduced gradient shard) and the "
-                         "step reads it as one fp32 replica; 'fused' -- the step reads the N "
-                         "replicas again.  Both give the same bits.")
+                    help="adamw_clip (and amp on full-buffer workloads): 'stored' -- the norm "
+                         "pass also stores the averaged gradient (the reduced gradient shard) "
+                         "and the step reads it as one fp32 replica; 'fused' -- the step reads "
+                         "the N replicas again.  Both give the same bits.")
     ap.add_argument("--gather-path", choices=("entry", "fused", "two-pass", "separate"),
                     default="entry",
                     help="adam_allgather: 'entry' -- dpopt_reduce_adam_allgather, which runs one "
@@ -371,7 +371,7 @@ def run_ours(args, wl):
         pol = dp.DPOPT_GATHER_FUSED if args.gather_path == "fused" else dp.DPOPT_GATHER_SEPARATE
         if dp.dpopt_set_gather_policy(pol) != dp.DPOPT_OK:
             raise SystemExit(f"dpopt_set_gather_policy: {dp.dpopt_last_error()}")
-    stored = args.clip_path == "stored" and wl.layout == "full"
+    stored = args.clip_path == "stored" and (wl.layout == "full" or args.optimizer == "adamw_clip")
     if args.optimizer in ("adamw_clip", "amp") and stored:
         avg = torch.empty(S, dtype=torch.float32, device=device)
     if args.optimizer == "amp":
@@ -419,8 +419,8 @@ def run_ours(args, wl):
                 dp.reduce_adam(dev.grads, wl.shard_rank, wl.bucket_elems, dev.master, dev.m,
                                dev.v, dev.out, step=t, stream=stream, **hp)
     else:  # gradients delivered as per-bucket slices of the rank's shard
-        if args.optimizer == "adam_allgather":
-            raise SystemExit("adam_allgather runs on the full-buffer workloads")
+        if args.optimizer in ("adam_allgather", "amp"):
+            raise SystemExit(f"{args.optimizer} runs on the full-buffer workloads")
         buckets = dev.bucket_slices()
         rows, offs = [b for _, b in buckets], [o for o, _ in buckets]
         if args.bucket_launch == "table":
@@ -431,7 +431,14 @@ def run_ours(args, wl):
             table = None
         # the call's arguments marshalled once, outside the timed region
         call = dp.BucketStep(rows, offs, dev.master, dev.m, dev.v, dev.out, table)
-        if args.optimizer == "adamw_clip":
+        if args.optimizer == "adamw_clip" and stored:
+            # the norm pass stores the shard's average (the buckets continue one
+            # another); the step reads it as one fp32 replica
+            def step(t):
+                dp.grad_average_sqnorm_buckets(rows, offs, avg, sqn, scratch, stream=stream)
+                dp.reduce_adamw([avg], 0, S, dev.master, dev.m, dev.v, dev.out, step=t,
+                                opts=opts, stream=stream, **hp)
+        elif args.optimizer == "adamw_clip":
             def step(t):
                 dp.grad_sqnorm_buckets(rows, offs, sqn, scratch, stream=stream)
                 call.step(step=t, opts=opts, stream=stream, **hp)

@@ -283,7 +283,11 @@ int dpopt_grad_sqnorm(const void *const *grads, int grad_dtype, int n_replicas, 
                       int64_t scratch_bytes, dpopt_stream_t stream);
 
 /* The same over a batch of bucket slices (arguments as for
- * dpopt_reduce_adam_buckets). */
+ * dpopt_reduce_adam_buckets).  Buckets that continue one another (in the
+ * shard and in every replica's gradient memory, as in a flat contiguous
+ * gradient buffer) are joined first, so such buckets covering the whole shard
+ * give the bits of dpopt_grad_sqnorm over the full buffers; the scratch size
+ * of dpopt_grad_sqnorm_scratch_bytes(elems, n_buckets) covers every case. */
 int dpopt_grad_sqnorm_buckets(const void *const *slice_table, int grad_dtype, int n_replicas,
                               const int64_t *offsets, const int64_t *lens, int64_t n_buckets,
                               float grad_unscale, double *sqnorm_out, void *scratch,
@@ -336,6 +340,26 @@ int dpopt_grad_average_sqnorm(const void *const *grads, int grad_dtype, int n_re
                               int64_t numel, int shard_rank, float grad_unscale, float *avg_out,
                               double *sqnorm_out, void *scratch, int64_t scratch_bytes,
                               dpopt_stream_t stream);
+
+/* dpopt_grad_average_sqnorm over bucket slices: dpopt_grad_sqnorm_buckets that
+ * also stores each element's average at its shard offset, avg_out[offsets[b]
+ * + j] for element j of bucket b.  The buckets must join into one segment
+ * (contiguous gradients, ZeRO's `contiguous_gradients` layout, as in the
+ * ZeRO-3 answer's config, section 8), else DPOPT_ERR_UNSUPPORTED.  avg_out is
+ * a DEVICE array indexed like the states, 4-byte aligned, whose span the
+ * buckets cover overlapping neither the gradients nor sqnorm_out nor scratch.
+ * The step then reads the average as one fp32 replica --
+ * dpopt_reduce_adamw(&avg_out, DPOPT_GRAD_F32, 1, S, 0, ...) for buckets
+ * covering the shard -- with the bits of the fused bucket step, moving
+ * 2N + 4 bytes per parameter here and 4 + 26 in the step instead of 2N + 26:
+ * at N = 64 about 162 bytes per parameter for the clipped step in place of
+ * 282.  Errors: as for dpopt_grad_sqnorm_buckets, plus DPOPT_ERR_INVALID_ARG
+ * for a null, misaligned or overlapping avg_out. */
+int dpopt_grad_average_sqnorm_buckets(const void *const *slice_table, int grad_dtype,
+                                      int n_replicas, const int64_t *offsets,
+                                      const int64_t *lens, int64_t n_buckets, float grad_unscale,
+                                      float *avg_out, double *sqnorm_out, void *scratch,
+                                      int64_t scratch_bytes, dpopt_stream_t stream);
 
 /* Scratch bytes dpopt_grad_sqnorm{,_buckets} need for `elems` gradient elements
  * per replica cut into n_buckets buckets (use n_buckets = 1 for the full-buffer

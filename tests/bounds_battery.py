@@ -4,7 +4,8 @@ one-element path), the bulk-copy kernel, the runtime-replica-count kernels
 (unrolled in three batches at N = 18, the shared-memory walk at N = 24 and
 40, the register walk at N = 64),
 the one-launch bucket entry (launch table in device memory, and contiguous
-buckets joined), the norm pre-pass with and without the stored average, the
+buckets joined), the norm pre-pass with and without the stored average (over
+full buffers and over joined buckets), the
 loss-scaled step, the all-gather and the fused step + all-gather (per-thread
 stores, and whole tiles written by bulk copies).
 
@@ -140,6 +141,14 @@ def run() -> tuple[dict, list]:
                      dtype=torch.float64, device="cuda")
     dp.grad_sqnorm_buckets(slices, offs, sq3, sc)
     keep("sqnorm_buckets", sq3)
+    # the same lengths as consecutive views of flat buffers: joined into one
+    # segment, the average stored at each element's shard offset
+    flat = [_rand(gen, sum(lens), 1e-3, torch.bfloat16) for _ in range(n)]
+    joined = [[f[o:o + ln] for f in flat] for o, ln in zip(offs, lens)]
+    avg_b = torch.full((sum(lens) + 8,), float("nan"), device="cuda")
+    sq5 = torch.zeros(1, dtype=torch.float64, device="cuda")
+    dp.grad_average_sqnorm_buckets(joined, offs, avg_b[:sum(lens)], sq5, sc)
+    keep("average_sqnorm_buckets", avg_b, sq5)
     sq4 = torch.zeros(1, dtype=torch.float64, device="cuda")
     rc = dp.dpopt_grad_sqnorm_noalloc([g.data_ptr() for g in grads], dp.DPOPT_GRAD_BF16, n,
                                       n * S, 2, 0.0, sq4.data_ptr(), 0)

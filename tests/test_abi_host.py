@@ -177,6 +177,28 @@ def test_bucket_entries_reject_bad_arguments(dp):
     assert dp.dpopt_reduce_adam_buckets(G[:64] * 2, 0, 65, [0], [10], *args) == 2
 
 
+def test_bucket_average_norm_rejects_bad_arguments(dp):
+    SQ, SCR, AVG = 0xD0_0000_0000, 0xE0_0000_0000, 0xC8_0000_0000
+    L = 5000                                       # two buckets: 10000 elements, 3 chunks
+    nbytes = dp.dpopt_grad_sqnorm_scratch_bytes(2 * L, 2)[1]
+    # two buckets continuing one another in the shard and in both replicas
+    joined = [G[0], G[1], G[0] + 2 * L, G[1] + 2 * L]
+
+    def call(table=joined, offs=(0, L), avg=AVG, scr=SCR, nb=nbytes):
+        return dp.dpopt_grad_average_sqnorm_buckets(table, 0, 2, list(offs), [L, L], 0.0,
+                                                    avg, SQ, scr, nb, 0)
+    assert call(avg=0) == dp.DPOPT_ERR_INVALID_ARG
+    assert call(avg=AVG + 2) == dp.DPOPT_ERR_INVALID_ARG
+    assert call(avg=SCR - 4 * 1000) == dp.DPOPT_ERR_INVALID_ARG    # overlaps the partials
+    assert call(avg=G[1] - 4 * 10) == dp.DPOPT_ERR_INVALID_ARG     # overlaps a gradient
+    assert call(nb=16) == dp.DPOPT_ERR_INVALID_ARG                 # 3 partials needed
+    # buckets that do not continue one another (a gap in replica 1's memory)
+    apart = [G[0], G[1], G[0] + 2 * L, G[1] + 2 * L + 64]
+    assert call(table=apart) == dp.DPOPT_ERR_UNSUPPORTED
+    # ... or in the shard
+    assert call(offs=(0, L + 16)) == dp.DPOPT_ERR_UNSUPPORTED
+
+
 def test_bucket_table_bytes(dp):
     # 274 buckets of 64 slices (a 70B model's 1/64 shard in 4M buckets)
     assert dp.dpopt_bucket_table_bytes(64, 274) == (0, 32 * 275 + 8 * 274 * 64)

@@ -197,3 +197,107 @@ def test_stored_average_argument_checks():
                                           scratch.data_ptr(), nb, 0)
         assert rc == dp.DPOPT_ERR_INVALID_ARG, bad
     dp.stream_status()
+
+
+def _contiguous_buckets(grads, base, S, bucket):
+    """Bucket slices as consecutive views of the full replica buffers (a flat,
+    contiguous gradient buffer), and their shard offsets."""
+    rows, offs = [], []
+    for off in range(0, S, bucket):
+        ln = min(bucket, S - off)
+        rows.append([g[base + off:base + off + ln] for g in grads])
+        offs.append(off)
+    return rows, offs
+
+
+def _bucket_scratch(S, nb):
+    rc, nbytes = dp.dpopt_grad_sqnorm_scratch_bytes(S, nb)
+    assert rc == 0
+    return torch.empty(max(1, nbytes // 8), dtype=torch.float64, device="cuda")
+
+
+@pytest.mark.parametrize("n,S,bucket,kind", [(4, 100_003, 9_001, 0), (64, 40_000, 4_000, 0),
+                                             (8, 50_001, 12_345, 2), (3, 30_000, 7_777, 1)])
+def test_bucket_average_equals_the_full_buffer_average(n, S, bucket, kind):
+    """Contiguous buckets join into one segment: the bucket norm, and the
+    bucket average with its norm, are bit for bit those of the full-buffer
+    entries over the same shard."""
+    _need_gpu()
+    wl = _small_workload(n, S, kind=kind, rank=min(2, n - 1))
+    grads = [to_dev_grad(g) for g in _full_grads(wl, 1)]
+    rows, offs = _contiguous_buckets(grads, wl.shard_base, S, bucket)
+    sq_full, sq_b, sq_ab = (torch.zeros(1, dtype=torch.float64, device="cuda") for _ in range(3))
+    avg_full = torch.full((S,), float("nan"), device="cuda")
+    avg_b = torch.full((S,), float("nan"), device="cuda")
+    dp.grad_average_sqnorm(grads, wl.shard_rank, avg_full, sq_full, _scratch(S))
+    c0 = dp.dpopt_launch_count()
+    dp.grad_sqnorm_buckets(rows, offs, sq_b, _bucket_scratch(S, len(rows)))
+    assert dp.dpopt_launch_count() - c0 == 2          # one norm pass, one ordered finish
+    dp.grad_average_sqnorm_buckets(rows, offs, avg_b, sq_ab, _bucket_scratch(S, len(rows)))
+    dp.stream_status()
+    assert torch.equal(sq_b, sq_full) and torch.equal(sq_ab, sq_full)
+    assert np.array_equal(f32(avg_b).view(np.uint32), f32(avg_full).view(np.uint32))
+
+
+def test_two_pass_clipped_step_over_buckets_equals_the_fused_bucket_step():
+    """N = 64 in 4000-element contiguous buckets: the norm pass stores the
+    average, the step reads it as one fp32 replica -- the bits of the fused
+    bucket step that reads the 64 slices, step after step."""
+    _need_gpu()
+    n, S, bucket = 64, 40_000, 4_000
+    wl = _small_workload(n, S, kind=0, rank=5)
+    master, m, v = parity.states_host(wl, wl.shard_base + np.arange(S))
+    res = []
+    for stored in (True, False):
+        st = [torch.from_numpy(x.copy()).cuda() for x in (master, m, v)]
+        out = torch.zeros(S, dtype=torch.bfloat16, device="cuda")
+        sq = torch.zeros(1, dtype=torch.float64, device="cuda")
+        avg = torch.empty(S, device="cuda")
+        for t in (1, 2, 3):
+            grads = [to_dev_grad(g) for g in _full_grads(wl, t)]
+            rows, offs = _contiguous_buckets(grads, wl.shard_base, S, bucket)
+            scratch = _bucket_scratch(S, len(rows))
+            if stored:
+                dp.grad_average_sqnorm_buckets(rows, offs, avg, sq, scratch)
+            else:
+                dp.grad_sqnorm_buckets(rows, offs, sq, scratch)
+            # this shard's norm stands for the global one here (one rank)
+            opts = dp.step_options(weight_decay=0.01, max_grad_norm=1e-4 * np.sqrt(S),
+                                   grad_sqnorm=sq)
+            prev = tuple(f32(x) for x in st)
+            if stored:
+                dp.reduce_adamw([avg], 0, S, *st, out, step=t, opts=opts, **HP)
+            else:
+                dp.reduce_adamw_buckets(rows, offs, *st, out, step=t, opts=opts, **HP)
+            dp.stream_status()
+            if stored:
+                host = _full_grads(wl, t)
+                base = wl.shard_base
+                sh = [h[base:base + S] for h in host]
+                c = oracle.grad_scale(oracle.grad_sqnorm(sh, 0, S, 1.0), 1e-4 * np.sqrt(S),
+                                      1.0)
+                parity.check_step(wl, np.arange(S), t, prev, [f32(x) for x in st] + [u16(out)],
+                                  "clipped AdamW, bucket average N=64",
+                                  grads_fn=lambda r, _t: sh[r], weight_decay=0.01,
+                                  gscale_fn=lambda _t, _g: c)
+        res.append([f32(x) for x in st] + [u16(out)])
+    for x, y in zip(*res):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+def test_bucket_average_needs_joined_buckets():
+    _need_gpu()
+    wl = _small_workload(4, 20_000, kind=0)
+    grads = [to_dev_grad(g) for g in _full_grads(wl, 1)]
+    rows, offs = _contiguous_buckets(grads, wl.shard_base, 20_000, 5_000)
+    rows[2] = [x.clone() for x in rows[2]]          # bucket 2 in memory of its own
+    sq = torch.zeros(1, dtype=torch.float64, device="cuda")
+    avg = torch.empty(20_000, device="cuda")
+    c0 = dp.dpopt_launch_count()
+    with pytest.raises(dp.DpoptError, match="join into one segment"):
+        dp.grad_average_sqnorm_buckets(rows, offs, avg, sq, _bucket_scratch(20_000, 4))
+    assert dp.dpopt_launch_count() == c0
+    # the norm alone still runs over the separate pieces
+    dp.grad_sqnorm_buckets(rows, offs, sq, _bucket_scratch(20_000, 4))
+    dp.stream_status()
+    assert float(sq.item()) > 0.0

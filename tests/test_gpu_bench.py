@@ -50,3 +50,20 @@ def test_bench_line_has_the_contract_keys(args):
     else:
         e = d["e2e"]
         assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+
+
+def test_bench_clipped_line_over_bucket_slices():
+    """adamw_clip on bucket slices through the stored average: norm pass, ordered
+    finish, step on the average -- three launches, 2N + 34 bytes per parameter."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    d = _line("--workload", "70b_shard", "--shard-params", "8000000", "--optimizer",
+              "adamw_clip", "--steps", "5", "--warmup", "3", "--no-cpu-baseline")
+    assert d["config"]["clip_path"] == "stored"
+    assert d["config"]["bytes_per_param"] == 2 * 64 + 34
+    assert d["roofline"]["launches_per_step"] == 3 and d["value"] > 0
+    f = _line("--workload", "70b_shard", "--shard-params", "8000000", "--optimizer",
+              "adamw_clip", "--clip-path", "fused", "--steps", "5", "--warmup", "3",
+              "--no-cpu-baseline")
+    assert f["config"]["clip_path"] == "fused"
+    assert f["config"]["bytes_per_param"] == 4 * 64 + 26

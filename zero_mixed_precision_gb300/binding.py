@@ -104,6 +104,8 @@ _SIGS = {
                                     _F, _I64, _POPT, _P], _I),
     "dpopt_grad_sqnorm": ([_PP, _I, _I, _I64, _I, _F, _P, _P, _I64, _P], _I),
     "dpopt_grad_sqnorm_buckets": ([_PP, _I, _I, _PI64, _PI64, _I64, _F, _P, _P, _I64, _P], _I),
+    "dpopt_grad_average_sqnorm_buckets": ([_PP, _I, _I, _PI64, _PI64, _I64, _F, _P, _P, _P, _I64,
+                                           _P], _I),
     "dpopt_grad_sqnorm_scratch_bytes": ([_I64, _I64, _PI64], _I),
     "dpopt_grad_sqnorm_noalloc": ([_PP, _I, _I, _I64, _I, _F, _P, _P], _I),
     "dpopt_grad_average_sqnorm": ([_PP, _I, _I, _I64, _I, _F, _P, _P, _P, _I64, _P], _I),
@@ -262,6 +264,18 @@ def dpopt_grad_sqnorm_buckets(slice_table: Sequence[int], grad_dtype: int, n_rep
     return _lib.dpopt_grad_sqnorm_buckets(
         _ptr_array(slice_table), grad_dtype, n_replicas, (ctypes.c_int64 * nb)(*offsets),
         (ctypes.c_int64 * nb)(*lens), nb, grad_unscale, sqnorm_out, scratch, scratch_bytes, stream)
+
+
+def dpopt_grad_average_sqnorm_buckets(slice_table: Sequence[int], grad_dtype: int,
+                                      n_replicas: int, offsets: Sequence[int],
+                                      lens: Sequence[int], grad_unscale: float, avg_out: int,
+                                      sqnorm_out: int, scratch: int, scratch_bytes: int,
+                                      stream: int = 0) -> int:
+    nb = len(offsets)
+    return _lib.dpopt_grad_average_sqnorm_buckets(
+        _ptr_array(slice_table), grad_dtype, n_replicas, (ctypes.c_int64 * nb)(*offsets),
+        (ctypes.c_int64 * nb)(*lens), nb, grad_unscale, avg_out, sqnorm_out, scratch,
+        scratch_bytes, stream)
 
 
 def dpopt_grad_sqnorm_noalloc(grads: Sequence[int], grad_dtype: int, n_replicas: int,
@@ -616,6 +630,23 @@ def grad_sqnorm_buckets(bucket_slices, offsets, sqnorm_out, scratch, *, grad_uns
                                    _operand(sqnorm_out), _operand(scratch),
                                    scratch.numel() * scratch.element_size(), _stream_handle(stream))
     _check(rc, "dpopt_grad_sqnorm_buckets")
+
+
+def grad_average_sqnorm_buckets(bucket_slices, offsets, avg_out, sqnorm_out, scratch, *,
+                                grad_unscale: float = 0.0, stream=None) -> None:
+    """grad_sqnorm_buckets that also writes each element's fixed-order average
+    to avg_out at its shard offset (float32 device tensor indexed like the
+    states); the buckets must continue one another (contiguous gradients)."""
+    n = len(bucket_slices[0])
+    dt = _grad_dtype(bucket_slices[0][0])
+    table = [_operand(t) for row in bucket_slices for t in row]
+    lens = [row[0].numel() for row in bucket_slices]
+    rc = dpopt_grad_average_sqnorm_buckets(table, dt, n, list(offsets), lens, grad_unscale,
+                                           _operand(avg_out), _operand(sqnorm_out),
+                                           _operand(scratch),
+                                           scratch.numel() * scratch.element_size(),
+                                           _stream_handle(stream))
+    _check(rc, "dpopt_grad_average_sqnorm_buckets")
 
 
 def loss_scale_init(state, init_scale: float = 65536.0, window: int = 1000, hysteresis: int = 2,

@@ -998,10 +998,15 @@ int dpopt_grad_sqnorm_noalloc(const void* const* grads, int grad_dtype, int n_re
                     (cudaStream_t)stream);
 }
 
-int dpopt_grad_sqnorm_buckets(const void* const* slice_table, int grad_dtype, int n_replicas,
-                              const int64_t* offsets, const int64_t* lens, int64_t n_buckets,
-                              float grad_unscale, double* sqnorm_out, void* scratch,
-                              int64_t scratch_bytes, dpopt_stream_t stream) {
+// The squared norm over bucket slices, buckets that continue one another
+// joined first (so contiguous buckets take the chunk partition, and the bits,
+// of one full-buffer call over the same elements); with avg_out each
+// element's average is stored at its shard offset, which needs the buckets to
+// join into one segment.
+int buckets_norm_impl(const void* const* slice_table, int grad_dtype, int n_replicas,
+                      const int64_t* offsets, const int64_t* lens, int64_t n_buckets,
+                      float grad_unscale, float* avg_out, double* sqnorm_out, void* scratch,
+                      int64_t scratch_bytes, cudaStream_t stream) {
   if (!std::isfinite(grad_unscale) || grad_unscale < 0.f)
     return fail(DPOPT_ERR_INVALID_ARG, "grad_unscale must be finite and >= 0");
   std::vector<SegDesc> segs;
@@ -1009,18 +1014,53 @@ int dpopt_grad_sqnorm_buckets(const void* const* slice_table, int grad_dtype, in
   int rc = build_buckets(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets, segs, &lo,
                          &hi);
   if (rc) return rc;
+  coalesce(segs, n_replicas, grad_dtype);
+  if (avg_out && segs.size() > 1)
+    return fail(DPOPT_ERR_UNSUPPORTED,
+                "the average is stored for buckets that join into one segment (each bucket "
+                "continuing the previous one in the shard and in every replica's gradients); "
+                "these form %zu", segs.size());
   const int64_t chunks = norm_chunks(segs.data(), (int)segs.size());
-  Range avoid[2];
+  Range avoid[3];
   rc = check_norm_outputs(sqnorm_out, scratch, scratch_bytes, chunks, avoid);
   if (rc) return rc;
-  rc = check_bucket_grads(segs, n_replicas, grad_dtype, avoid, chunks ? 2 : 1);
+  int navoid = chunks ? 2 : 1;
+  if (avg_out && hi > lo) {
+    if ((uintptr_t)avg_out & 3u) return fail(DPOPT_ERR_INVALID_ARG, "avg_out must be 4-byte aligned");
+    const Range a{(uintptr_t)(avg_out + lo), (uintptr_t)(avg_out + hi)};
+    for (int i = 0; i < navoid; ++i)
+      if (overlaps(a, avoid[i]))
+        return fail(DPOPT_ERR_INVALID_ARG, "avg_out overlaps sqnorm_out or the scratch partials");
+    avoid[navoid++] = a;
+  }
+  rc = check_bucket_grads(segs, n_replicas, grad_dtype, avoid, navoid);
   if (rc) return rc;
-  if (segs.empty()) return finish_empty_norm(sqnorm_out, (cudaStream_t)stream);
+  if (segs.empty()) return finish_empty_norm(sqnorm_out, stream);
   Hyper h = make_hyper(1.f, 0.f, 0.f, 0.f, 1, n_replicas);
   h.unscale = grad_unscale == 0.f ? 1.f : grad_unscale;
   set_span(h, lo, hi);
   return run_sqnorm(segs.data(), (int)segs.size(), grad_dtype, n_replicas, h, (double*)scratch,
-                    sqnorm_out, (cudaStream_t)stream);
+                    sqnorm_out, stream, avg_out);
+}
+
+int dpopt_grad_sqnorm_buckets(const void* const* slice_table, int grad_dtype, int n_replicas,
+                              const int64_t* offsets, const int64_t* lens, int64_t n_buckets,
+                              float grad_unscale, double* sqnorm_out, void* scratch,
+                              int64_t scratch_bytes, dpopt_stream_t stream) {
+  return buckets_norm_impl(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets,
+                           grad_unscale, nullptr, sqnorm_out, scratch, scratch_bytes,
+                           (cudaStream_t)stream);
+}
+
+int dpopt_grad_average_sqnorm_buckets(const void* const* slice_table, int grad_dtype,
+                                      int n_replicas, const int64_t* offsets,
+                                      const int64_t* lens, int64_t n_buckets, float grad_unscale,
+                                      float* avg_out, double* sqnorm_out, void* scratch,
+                                      int64_t scratch_bytes, dpopt_stream_t stream) {
+  if (!avg_out) return fail(DPOPT_ERR_INVALID_ARG, "avg_out must be non-null");
+  return buckets_norm_impl(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets,
+                           grad_unscale, avg_out, sqnorm_out, scratch, scratch_bytes,
+                           (cudaStream_t)stream);
 }
 
 int dpopt_reduce_adam_bucket(const void* const* grad_slices, int grad_dtype, int n_replicas,
