@@ -91,10 +91,10 @@ def parse_args(argv=None):
                          "dynamic loss scaling -- the unscaled squared-norm pre-pass, then the "
                          "loss-scaled, clipped AdamW step and the device-side scale update")
     ap.add_argument("--clip-path", choices=("stored", "fused"), default="stored",
-                    help="adamw_clip (and amp on full-buffer workloads): 'stored' -- the norm "
-                         "pass also stores the averaged gradient (the reduced gradient shard) "
-                         "and the step reads it as one fp32 replica; 'fused' -- the step reads "
-                         "the N replicas again.  Both give the same bits.")
+                    help="adamw_clip / amp: 'stored' -- the norm pass also stores the "
+                         "averaged gradient (the reduced gradient shard) and the step reads it "
+                         "as one fp32 replica; 'fused' -- the step reads the N replicas again "
+                         "(amp: full-buffer workloads only).  Both give the same bits.")
     ap.add_argument("--gather-path", choices=("entry", "fused", "two-pass", "separate"),
                     default="entry",
                     help="adam_allgather: 'entry' -- dpopt_reduce_adam_allgather, which runs one "
@@ -342,8 +342,9 @@ def run_ours(args, wl):
         dist.init_process_group("nccl", device_id=device)
     wl = rank_workload(wl, rank)
     if args.optimizer == "amp":
-        if wl.layout != "full":
-            raise SystemExit("amp runs on the full-buffer workloads")
+        if wl.layout != "full" and args.clip_path != "stored":
+            raise SystemExit("amp on bucket slices runs through the stored average "
+                             "(--clip-path stored)")
         wl = dataclasses.replace(wl, grad_kind=2)   # fp16 gradients, the loss-scaled recipe
     dp.dpopt_set_kernel_policy({"auto": dp.DPOPT_KERNEL_AUTO, "direct": dp.DPOPT_KERNEL_DIRECT,
                                 "bulk": dp.DPOPT_KERNEL_BULK}[args.kernel])
@@ -356,7 +357,7 @@ def run_ours(args, wl):
     stream = torch.cuda.current_stream(device)
     hp = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps)
 
-    if args.optimizer == "adamw_clip":
+    if args.optimizer in ("adamw_clip", "amp"):
         # one rank's view: this shard's squared norm stands in for the global one
         # (a multi-rank run adds the ranks' scalars with one all-reduce)
         sqn = torch.zeros(1, dtype=torch.float64, device=device)
@@ -371,13 +372,10 @@ def run_ours(args, wl):
         pol = dp.DPOPT_GATHER_FUSED if args.gather_path == "fused" else dp.DPOPT_GATHER_SEPARATE
         if dp.dpopt_set_gather_policy(pol) != dp.DPOPT_OK:
             raise SystemExit(f"dpopt_set_gather_policy: {dp.dpopt_last_error()}")
-    stored = args.clip_path == "stored" and (wl.layout == "full" or args.optimizer == "adamw_clip")
+    stored = args.clip_path == "stored"
     if args.optimizer in ("adamw_clip", "amp") and stored:
         avg = torch.empty(S, dtype=torch.float32, device=device)
     if args.optimizer == "amp":
-        sqn = torch.zeros(1, dtype=torch.float64, device=device)
-        scratch = torch.empty(dp.dpopt_grad_sqnorm_scratch_bytes(S, 1)[1] // 8 + 1,
-                              dtype=torch.float64, device=device)
         ls_state = torch.zeros(4, dtype=torch.int64, device=device)
         ls_cfg = dp.loss_scale_init(ls_state, init_scale=1024.0, window=1000, stream=stream)
     if wl.layout == "full":
@@ -419,8 +417,8 @@ def run_ours(args, wl):
                 dp.reduce_adam(dev.grads, wl.shard_rank, wl.bucket_elems, dev.master, dev.m,
                                dev.v, dev.out, step=t, stream=stream, **hp)
     else:  # gradients delivered as per-bucket slices of the rank's shard
-        if args.optimizer in ("adam_allgather", "amp"):
-            raise SystemExit(f"{args.optimizer} runs on the full-buffer workloads")
+        if args.optimizer == "adam_allgather":
+            raise SystemExit("adam_allgather runs on the full-buffer workloads")
         buckets = dev.bucket_slices()
         rows, offs = [b for _, b in buckets], [o for o, _ in buckets]
         if args.bucket_launch == "table":
@@ -431,7 +429,15 @@ def run_ours(args, wl):
             table = None
         # the call's arguments marshalled once, outside the timed region
         call = dp.BucketStep(rows, offs, dev.master, dev.m, dev.v, dev.out, table)
-        if args.optimizer == "adamw_clip" and stored:
+        if args.optimizer == "amp":
+            # the norm pass stores the average, unscaled by the device scale
+            def step(t):   # t is implied: the device state counts the steps taken
+                dp.amp_average_sqnorm_buckets(rows, offs, ls_state, avg, sqn, scratch,
+                                              stream=stream)
+                dp.amp_step([avg], 0, S, dev.master, dev.m, dev.v, dev.out, weight_decay=0.01,
+                            max_grad_norm=1.0, global_sqnorm=sqn, state=ls_state, cfg=ls_cfg,
+                            stream=stream, **hp)
+        elif args.optimizer == "adamw_clip" and stored:
             # the norm pass stores the shard's average (the buckets continue one
             # another); the step reads it as one fp32 replica
             def step(t):

@@ -419,6 +419,17 @@ int dpopt_amp_average_sqnorm(const void *const *grads, int grad_dtype, int n_rep
                              float *avg_out, double *sqnorm_out, void *scratch,
                              int64_t scratch_bytes, dpopt_stream_t stream);
 
+/* dpopt_amp_average_sqnorm over bucket slices that join into one segment (as
+ * dpopt_grad_average_sqnorm_buckets, with the unscale 1 / state->scale read on
+ * the device): the loss-scaled step of a bucketed, contiguous gradient buffer
+ * is this pass, the scalar all-reduce, then dpopt_amp_step on (&avg_out,
+ * DPOPT_GRAD_F32, 1, S, 0, ...). */
+int dpopt_amp_average_sqnorm_buckets(const void *const *slice_table, int grad_dtype,
+                                     int n_replicas, const int64_t *offsets, const int64_t *lens,
+                                     int64_t n_buckets, const dpopt_loss_scale_state *state,
+                                     float *avg_out, double *sqnorm_out, void *scratch,
+                                     int64_t scratch_bytes, dpopt_stream_t stream);
+
 /* One loss-scaled step of this rank's shard (full-buffer layout, arguments as for
  * dpopt_reduce_adam_ex): if *global_sqnorm is finite, AdamW (weight_decay) on the
  * averaged gradient times c = (1/scale) * min(1, max_grad_norm / (||g|| + 1e-6))

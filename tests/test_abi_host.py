@@ -197,6 +197,16 @@ def test_bucket_average_norm_rejects_bad_arguments(dp):
     assert call(table=apart) == dp.DPOPT_ERR_UNSUPPORTED
     # ... or in the shard
     assert call(offs=(0, L + 16)) == dp.DPOPT_ERR_UNSUPPORTED
+    # the loss-scaled form: its state pointer is checked first
+    STATE = 0xF8_0000_0000
+
+    def amp(state, avg=AVG):
+        return dp.dpopt_amp_average_sqnorm_buckets(joined, 2, 2, [0, L], [L, L], state, avg, SQ,
+                                                   SCR, nbytes, 0)
+    assert amp(0) == dp.DPOPT_ERR_INVALID_ARG
+    assert amp(STATE + 4) == dp.DPOPT_ERR_INVALID_ARG
+    assert amp(STATE, avg=0) == dp.DPOPT_ERR_INVALID_ARG
+    assert amp(STATE, avg=AVG + 1) == dp.DPOPT_ERR_INVALID_ARG
 
 
 def test_bucket_table_bytes(dp):

@@ -301,3 +301,54 @@ def test_bucket_average_needs_joined_buckets():
     dp.grad_sqnorm_buckets(rows, offs, sq, _bucket_scratch(20_000, 4))
     dp.stream_status()
     assert float(sq.item()) > 0.0
+
+
+def test_loss_scaled_run_over_buckets_equals_the_full_buffer_run():
+    """The loss-scaled iterations of the two-pass test with every rank's norm
+    pass over contiguous bucket slices (dpopt_amp_average_sqnorm_buckets): the
+    same skips, scales and bits as the full-buffer stored-average run."""
+    _need_gpu()
+    n, S, bucket = 4, 20_000, 3_001
+    wl = _amp_workload(n, S)
+    inject = {2: (1, 3 * S + 7, 0x7C00), 5: (3, 11, 0xFC00)}
+
+    def full(k):
+        bufs = [grad_host_range(wl, r, k, 0, wl.numel) for r in range(n)]
+        if k in inject:
+            r, i, bits = inject[k]
+            bufs[r][i] = bits
+        return bufs
+
+    def run(buckets):
+        master, m, v = parity.states_host(wl, wl.shard_base + np.arange(S))
+        dm, dmm, dv = (torch.from_numpy(x.copy()).cuda() for x in (master, m, v))
+        dout = torch.zeros(S, dtype=torch.bfloat16, device="cuda")
+        state = torch.zeros(4, dtype=torch.int64, device="cuda")
+        cfg = dp.loss_scale_init(state, init_scale=1024.0, window=2, hysteresis=2, min_scale=1.0)
+        scratch = _bucket_scratch(S, -(-S // bucket))
+        part = torch.zeros(n, dtype=torch.float64, device="cuda")
+        total = torch.zeros(1, dtype=torch.float64, device="cuda")
+        avgs = [torch.empty(S, device="cuda") for _ in range(n)]
+        trail = []
+        for k in range(1, 8):
+            grads = [to_dev_grad(b) for b in full(k)]
+            for r in range(n):
+                if buckets:
+                    rows, offs = _contiguous_buckets(grads, r * S, S, bucket)
+                    dp.amp_average_sqnorm_buckets(rows, offs, state, avgs[r], part[r:r + 1],
+                                                  scratch)
+                else:
+                    dp.amp_average_sqnorm(grads, r, state, avgs[r], part[r:r + 1], scratch)
+            torch.sum(part, dim=0, keepdim=True, out=total)
+            dp.amp_step([avgs[wl.shard_rank]], 0, S, dm, dmm, dv, dout, weight_decay=0.01,
+                        max_grad_norm=1.0, global_sqnorm=total, state=state, cfg=cfg, **HP)
+            st = dp.read_loss_scale(state)
+            trail.append((st.scale, st.step, st.skipped, st.last_overflow))
+        dp.stream_status()
+        return trail, (f32(dm), f32(dmm), f32(dv), u16(dout))
+
+    ta, a = run(True)
+    tb, b = run(False)
+    assert ta == tb and ta[-1][2] == 2
+    for x, y in zip(a, b):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))

@@ -67,3 +67,15 @@ def test_bench_clipped_line_over_bucket_slices():
               "--no-cpu-baseline")
     assert f["config"]["clip_path"] == "fused"
     assert f["config"]["bytes_per_param"] == 4 * 64 + 26
+
+
+def test_bench_loss_scaled_line_over_bucket_slices():
+    """amp on bucket slices: fp16 gradients, the norm pass storing the average,
+    the loss-scaled step on it and the scale update -- four launches."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    d = _line("--workload", "70b_shard", "--shard-params", "8000000", "--optimizer", "amp",
+              "--steps", "5", "--warmup", "3", "--no-cpu-baseline")
+    assert d["config"]["clip_path"] == "stored" and "fp16" in d["config"]["workload"]
+    assert d["config"]["bytes_per_param"] == 2 * 64 + 34
+    assert d["roofline"]["launches_per_step"] == 4 and d["value"] > 0

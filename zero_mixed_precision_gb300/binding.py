@@ -112,6 +112,8 @@ _SIGS = {
     "dpopt_loss_scale_init": ([_P, _PCFG, _P], _I),
     "dpopt_amp_sqnorm": ([_PP, _I, _I, _I64, _I, _P, _P, _P, _I64, _P], _I),
     "dpopt_amp_average_sqnorm": ([_PP, _I, _I, _I64, _I, _P, _P, _P, _P, _I64, _P], _I),
+    "dpopt_amp_average_sqnorm_buckets": ([_PP, _I, _I, _PI64, _PI64, _I64, _P, _P, _P, _P, _I64,
+                                          _P], _I),
     "dpopt_amp_step": ([_PP, _I, _I, _I64, _I, _I64, _P, _P, _P, _P, _F, _F, _F, _F, _F, _F, _P, _P,
                         _PCFG, _P], _I),
     "dpopt_allgather_bf16": ([_P, _I64, _I, _PP, _I, _P], _I),
@@ -276,6 +278,17 @@ def dpopt_grad_average_sqnorm_buckets(slice_table: Sequence[int], grad_dtype: in
         _ptr_array(slice_table), grad_dtype, n_replicas, (ctypes.c_int64 * nb)(*offsets),
         (ctypes.c_int64 * nb)(*lens), nb, grad_unscale, avg_out, sqnorm_out, scratch,
         scratch_bytes, stream)
+
+
+def dpopt_amp_average_sqnorm_buckets(slice_table: Sequence[int], grad_dtype: int,
+                                     n_replicas: int, offsets: Sequence[int], lens: Sequence[int],
+                                     state: int, avg_out: int, sqnorm_out: int, scratch: int,
+                                     scratch_bytes: int, stream: int = 0) -> int:
+    nb = len(offsets)
+    return _lib.dpopt_amp_average_sqnorm_buckets(
+        _ptr_array(slice_table), grad_dtype, n_replicas, (ctypes.c_int64 * nb)(*offsets),
+        (ctypes.c_int64 * nb)(*lens), nb, state, avg_out, sqnorm_out, scratch, scratch_bytes,
+        stream)
 
 
 def dpopt_grad_sqnorm_noalloc(grads: Sequence[int], grad_dtype: int, n_replicas: int,
@@ -647,6 +660,22 @@ def grad_average_sqnorm_buckets(bucket_slices, offsets, avg_out, sqnorm_out, scr
                                            scratch.numel() * scratch.element_size(),
                                            _stream_handle(stream))
     _check(rc, "dpopt_grad_average_sqnorm_buckets")
+
+
+def amp_average_sqnorm_buckets(bucket_slices, offsets, state, avg_out, sqnorm_out, scratch, *,
+                               stream=None) -> None:
+    """amp_sqnorm over bucket slices that continue one another, storing each
+    element's average at its shard offset (the step then reads avg_out)."""
+    n = len(bucket_slices[0])
+    dt = _grad_dtype(bucket_slices[0][0])
+    table = [_operand(t) for row in bucket_slices for t in row]
+    lens = [row[0].numel() for row in bucket_slices]
+    rc = dpopt_amp_average_sqnorm_buckets(table, dt, n, list(offsets), lens, _operand(state),
+                                          _operand(avg_out), _operand(sqnorm_out),
+                                          _operand(scratch),
+                                          scratch.numel() * scratch.element_size(),
+                                          _stream_handle(stream))
+    _check(rc, "dpopt_amp_average_sqnorm_buckets")
 
 
 def loss_scale_init(state, init_scale: float = 65536.0, window: int = 1000, hysteresis: int = 2,

@@ -1005,8 +1005,9 @@ int dpopt_grad_sqnorm_noalloc(const void* const* grads, int grad_dtype, int n_re
 // join into one segment.
 int buckets_norm_impl(const void* const* slice_table, int grad_dtype, int n_replicas,
                       const int64_t* offsets, const int64_t* lens, int64_t n_buckets,
-                      float grad_unscale, float* avg_out, double* sqnorm_out, void* scratch,
-                      int64_t scratch_bytes, cudaStream_t stream) {
+                      float grad_unscale, const LossScaleState* state, float* avg_out,
+                      double* sqnorm_out, void* scratch, int64_t scratch_bytes,
+                      cudaStream_t stream) {
   if (!std::isfinite(grad_unscale) || grad_unscale < 0.f)
     return fail(DPOPT_ERR_INVALID_ARG, "grad_unscale must be finite and >= 0");
   std::vector<SegDesc> segs;
@@ -1038,6 +1039,7 @@ int buckets_norm_impl(const void* const* slice_table, int grad_dtype, int n_repl
   if (segs.empty()) return finish_empty_norm(sqnorm_out, stream);
   Hyper h = make_hyper(1.f, 0.f, 0.f, 0.f, 1, n_replicas);
   h.unscale = grad_unscale == 0.f ? 1.f : grad_unscale;
+  if (state) h.scale_dev = &state->scale;
   set_span(h, lo, hi);
   return run_sqnorm(segs.data(), (int)segs.size(), grad_dtype, n_replicas, h, (double*)scratch,
                     sqnorm_out, stream, avg_out);
@@ -1048,7 +1050,7 @@ int dpopt_grad_sqnorm_buckets(const void* const* slice_table, int grad_dtype, in
                               float grad_unscale, double* sqnorm_out, void* scratch,
                               int64_t scratch_bytes, dpopt_stream_t stream) {
   return buckets_norm_impl(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets,
-                           grad_unscale, nullptr, sqnorm_out, scratch, scratch_bytes,
+                           grad_unscale, nullptr, nullptr, sqnorm_out, scratch, scratch_bytes,
                            (cudaStream_t)stream);
 }
 
@@ -1059,7 +1061,7 @@ int dpopt_grad_average_sqnorm_buckets(const void* const* slice_table, int grad_d
                                       int64_t scratch_bytes, dpopt_stream_t stream) {
   if (!avg_out) return fail(DPOPT_ERR_INVALID_ARG, "avg_out must be non-null");
   return buckets_norm_impl(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets,
-                           grad_unscale, avg_out, sqnorm_out, scratch, scratch_bytes,
+                           grad_unscale, nullptr, avg_out, sqnorm_out, scratch, scratch_bytes,
                            (cudaStream_t)stream);
 }
 
@@ -1112,6 +1114,19 @@ int dpopt_amp_average_sqnorm(const void* const* grads, int grad_dtype, int n_rep
   return full_norm_impl(grads, grad_dtype, n_replicas, numel, shard_rank, 0.f,
                         (const LossScaleState*)state, avg_out, sqnorm_out, scratch, scratch_bytes,
                         (cudaStream_t)stream);
+}
+
+int dpopt_amp_average_sqnorm_buckets(const void* const* slice_table, int grad_dtype,
+                                     int n_replicas, const int64_t* offsets, const int64_t* lens,
+                                     int64_t n_buckets, const dpopt_loss_scale_state* state,
+                                     float* avg_out, double* sqnorm_out, void* scratch,
+                                     int64_t scratch_bytes, dpopt_stream_t stream) {
+  int rc = check_state_ptr(state);
+  if (rc) return rc;
+  if (!avg_out) return fail(DPOPT_ERR_INVALID_ARG, "avg_out must be non-null");
+  return buckets_norm_impl(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets, 0.f,
+                           (const LossScaleState*)state, avg_out, sqnorm_out, scratch,
+                           scratch_bytes, (cudaStream_t)stream);
 }
 
 int dpopt_amp_step(const void* const* grads, int grad_dtype, int n_replicas, int64_t numel,
