@@ -441,6 +441,12 @@ int dpopt_amp_average_sqnorm_buckets(const void *const *slice_table, int grad_dt
  * its counters are left as they are; with scale 1 the gradient is used as it
  * is).  That is the step of a run without loss scaling whose step count lives
  * on the device -- the form to capture in a CUDA graph (see below).
+ * lr_dev: NULL, or a DEVICE pointer (4-byte aligned) to the learning rate as
+ * one float, read by the step when it runs (the `lr` argument is then not
+ * used): a learning-rate schedule writes it between replays of a captured
+ * graph.  The step forms lr / (1 - beta1^t) and 1 - lr * weight_decay from it
+ * in fp64 exactly as the host forms them from `lr`, so the same rate gives the
+ * same bits either way; a non-finite rate gives non-finite states.
  * Errors: as for dpopt_reduce_adam_ex, plus DPOPT_ERR_INVALID_ARG for a
  * misaligned global_sqnorm, a NULL one with max_grad_norm > 0, or a state
  * overlapping a state or output array. */
@@ -449,7 +455,8 @@ int dpopt_amp_step(const void *const *grads, int grad_dtype, int n_replicas, int
                    float *v_f32, void *param_bf16_out, float lr, float beta1, float beta2,
                    float eps, float weight_decay, float max_grad_norm,
                    const double *global_sqnorm, dpopt_loss_scale_state *state,
-                   const dpopt_loss_scale_config *cfg, dpopt_stream_t stream);
+                   const dpopt_loss_scale_config *cfg, const float *lr_dev,
+                   dpopt_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
 /* CUDA graphs                                                                */
@@ -464,9 +471,10 @@ int dpopt_amp_step(const void *const *grads, int grad_dtype, int n_replicas, int
  *    every replay: capture them once per step, or update the kernel nodes'
  *    parameters between replays;
  *  - dpopt_amp_sqnorm / dpopt_amp_step read the loss scale and the step count
- *    from the device state and advance it themselves, so one captured graph of
- *    an iteration replays iteration after iteration (with global_sqnorm NULL
- *    for a run without loss scaling);
+ *    from the device state and advance it themselves, and dpopt_amp_step can
+ *    read the learning rate from device memory (lr_dev), so one captured graph
+ *    of an iteration replays iteration after iteration, learning-rate schedule
+ *    included (with global_sqnorm NULL for a run without loss scaling);
  *  - dpopt_reduce_adam_buckets_table refuses with DPOPT_ERR_UNSUPPORTED when
  *    its launch table must be written (the buckets do not fit the parameter
  *    space) while `stream` is capturing: the table is copied from host memory

@@ -288,11 +288,12 @@ def test_sqnorm_and_adamw_reject_bad_arguments(dp):
     STATE = 0xF0_0000_0000
     cfg = dp.LossScaleConfig(1024.0, 10, 2, 1.0)
 
-    def amp(sq, max_norm):
+    def amp(sq, max_norm, lr_dev=0):
         return dp.dpopt_amp_step(G[:4], 0, 4, 4096, 0, 1024, MASTER, M, V, OUT, *HP, 0.01,
-                                 max_norm, sq, STATE, cfg, 0)
+                                 max_norm, sq, STATE, cfg, lr_dev, 0)
     assert amp(0, 1.0) == 1
     assert amp(SQ + 4, 0.0) == 1
+    assert amp(0, 0.0, lr_dev=0xF4_0000_0002) == 1      # a misaligned learning-rate pointer
 
 
 def test_binding_refuses_pageable_host_operands(dp):

@@ -163,6 +163,50 @@ def test_device_step_count_without_loss_scaling_replays():
                           grads_fn=lambda r, _t: host[r][base:base + S], weight_decay=0.01)
 
 
+def test_learning_rate_schedule_from_device_memory_replays():
+    """The step reads its learning rate from device memory: one captured step,
+    the rate rewritten before every replay (a warm-up then decay schedule),
+    each replayed step against the oracle at that step's rate, and bit for bit
+    the direct calls that pass the same rates from the host."""
+    _need_gpu()
+    n, S = 4, 30_007
+    wl = _small_workload(n, S, kind=0, rank=1)
+    master, m, v = parity.states_host(wl, wl.shard_base + np.arange(S))
+    cfg = dict(init_scale=1.0, window=1, hysteresis=1, min_scale=1.0)
+    rates = [float(np.float32(x)) for x in (2e-4, 6e-4, 1e-3, 7e-4, 3e-4)]
+    lr_dev = torch.zeros(1, device="cuda")
+    hp = dict(beta1=HP["beta1"], beta2=HP["beta2"], eps=HP["eps"])
+
+    def step(x, **kw):
+        dp.amp_step(x.grads, wl.shard_rank, S, *x.st, x.out, weight_decay=0.05,
+                    max_grad_norm=0.0, global_sqnorm=None, state=x.state, cfg=x.cfg, **hp, **kw)
+
+    warm = _Iteration(wl, master, m, v, cfg, 0.0)
+    step(warm, lr=0.0, lr_dev=lr_dev)
+    dp.stream_status()
+    it = _Iteration(wl, master, m, v, cfg, 0.0)
+    direct = _Iteration(wl, master, m, v, cfg, 0.0)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(it, lr=float("nan"), lr_dev=lr_dev)    # the host rate is not used
+    base = wl.shard_base
+    for t, lr in enumerate(rates, start=1):
+        host = [grad_host_range(wl, r, t, 0, wl.numel) for r in range(n)]
+        prev = tuple(f32(x) for x in it.st)
+        it.fill(host)
+        direct.fill(host)
+        lr_dev.fill_(lr)
+        graph.replay()
+        step(direct, lr=lr)
+        dp.stream_status()
+        got = it.snapshot()
+        for x, y in zip(got, direct.snapshot()):
+            assert np.array_equal(x.view(np.uint8), y.view(np.uint8)), t
+        parity.check_step(wl, np.arange(S), t, prev, got, "graph, device learning rate",
+                          grads_fn=lambda r, _t: host[r][base:base + S],
+                          hp=dict(lr=lr, **hp), weight_decay=0.05)
+
+
 def test_clipping_without_a_norm_is_refused():
     _need_gpu()
     wl = _small_workload(2, 1_000, kind=0)

@@ -115,7 +115,7 @@ _SIGS = {
     "dpopt_amp_average_sqnorm_buckets": ([_PP, _I, _I, _PI64, _PI64, _I64, _P, _P, _P, _P, _I64,
                                           _P], _I),
     "dpopt_amp_step": ([_PP, _I, _I, _I64, _I, _I64, _P, _P, _P, _P, _F, _F, _F, _F, _F, _F, _P, _P,
-                        _PCFG, _P], _I),
+                        _PCFG, _P, _P], _I),
     "dpopt_allgather_bf16": ([_P, _I64, _I, _PP, _I, _P], _I),
     "dpopt_reduce_adam_allgather": ([_PP, _I, _I, _I64, _I, _I64, _P, _P, _P, _PP, _F, _F, _F, _F,
                                      _I64, _P], _I),
@@ -338,11 +338,11 @@ def dpopt_amp_step(grads: Sequence[int], grad_dtype: int, n_replicas: int, numel
                    shard_rank: int, bucket_elems: int, master: int, m: int, v: int,
                    param_bf16_out: int, lr: float, beta1: float, beta2: float, eps: float,
                    weight_decay: float, max_grad_norm: float, global_sqnorm: int, state: int,
-                   cfg: LossScaleConfig | None, stream: int = 0) -> int:
+                   cfg: LossScaleConfig | None, lr_dev: int = 0, stream: int = 0) -> int:
     return _lib.dpopt_amp_step(_ptr_array(grads), grad_dtype, n_replicas, numel, shard_rank,
                                bucket_elems, master, m, v, param_bf16_out, lr, beta1, beta2, eps,
                                weight_decay, max_grad_norm, global_sqnorm, state,
-                               ctypes.byref(cfg) if cfg is not None else None, stream)
+                               ctypes.byref(cfg) if cfg is not None else None, lr_dev, stream)
 
 
 def dpopt_reduce_adam_buckets_when_ready(slice_table: Sequence[int], grad_dtype: int,
@@ -705,13 +705,16 @@ def amp_sqnorm(grads, shard_rank: int, state, sqnorm_out, scratch, stream=None) 
 def amp_step(grads, shard_rank: int, bucket_elems: int, master, m, v, param_bf16_out, *,
              lr: float, beta1: float, beta2: float, eps: float, weight_decay: float,
              max_grad_norm: float, global_sqnorm, state, cfg: LossScaleConfig,
-             stream=None) -> None:
+             lr_dev=None, stream=None) -> None:
+    """lr_dev: None, or a float32 device tensor holding the learning rate, read
+    when the step runs (lr is then not used)."""
     dt = _grad_dtype(grads[0])
     rc = dpopt_amp_step([_operand(g) for g in grads], dt, len(grads), grads[0].numel(),
                         shard_rank, bucket_elems, _operand(master), _operand(m), _operand(v),
                         _operand(param_bf16_out), lr, beta1, beta2, eps, weight_decay,
                         max_grad_norm, 0 if global_sqnorm is None else _operand(global_sqnorm),
-                        _operand(state), cfg, _stream_handle(stream))
+                        _operand(state), cfg, 0 if lr_dev is None else _operand(lr_dev),
+                        stream=_stream_handle(stream))
     _check(rc, "dpopt_amp_step")
 
 

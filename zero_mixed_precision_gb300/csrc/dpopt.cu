@@ -146,6 +146,8 @@ Hyper make_hyper(float lr, float beta1, float beta2, float eps, int64_t step, in
   h.unscale = 1.f;
   h.lr = lr;
   h.scale_dev = nullptr;
+  h.lr_dev = nullptr;
+  h.wd = 0.f;
 #ifdef DPOPT_DEBUG_BOUNDS
   h.dbg_status = bounds_status_word();
   h.dbg_lo = 0;
@@ -1134,9 +1136,12 @@ int dpopt_amp_step(const void* const* grads, int grad_dtype, int n_replicas, int
                    float* v_f32, void* param_bf16_out, float lr, float beta1, float beta2,
                    float eps, float weight_decay, float max_grad_norm,
                    const double* global_sqnorm, dpopt_loss_scale_state* state,
-                   const dpopt_loss_scale_config* cfg, dpopt_stream_t stream) {
+                   const dpopt_loss_scale_config* cfg, const float* lr_dev,
+                   dpopt_stream_t stream) {
   int rc = check_replicas(n_replicas, grad_dtype);
   if (rc) return rc;
+  if ((uintptr_t)lr_dev & 3u) return fail(DPOPT_ERR_INVALID_ARG, "lr_dev must be 4-byte aligned");
+  if (lr_dev) lr = 0.f;  // not used: the kernel reads the rate from lr_dev
   rc = check_hyper(lr, beta1, beta2, eps, 1);
   if (rc) return rc;
   rc = check_state_ptr(state);
@@ -1153,6 +1158,8 @@ int dpopt_amp_step(const void* const* grads, int grad_dtype, int n_replicas, int
   rc = apply_options(&o, lr, h, &ext);
   if (rc) return rc;
   h.max_norm = (double)max_grad_norm;
+  h.lr_dev = lr_dev;
+  h.wd = weight_decay;
   if (numel < 0 || numel % n_replicas != 0 || numel == 0) {
     const void* ptrs[DPOPT_MAX_REPLICAS];
     int64_t S = 0;

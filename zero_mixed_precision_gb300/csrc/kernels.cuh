@@ -807,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, W == 32 ? 3 : min_ctas<NR, PACK>())
   // Thread 0 forms the step's scalars once; every thread then takes a copy of
   // the grid-constant Hyper with only those overwritten, so the untouched
   // fields stay constant-bank operands instead of occupying registers.
-  __shared__ float s_ab[4];
+  __shared__ float s_ab[6];
   __shared__ float s_gscale;
   __shared__ int skip;
   if (threadIdx.x == 0) {
@@ -818,12 +818,21 @@ __global__ void __launch_bounds__(kThreads, W == 32 ? 3 : min_ctas<NR, PACK>())
     const double t = (double)(st.step + 1);
     const double bc1 = 1.0 - pow((double)h.beta1, t);
     const double bc2 = 1.0 - pow((double)h.beta2, t);
-    const double a = (double)h.lr / bc1;
+    // the learning rate of this step: from device memory when given (a
+    // schedule a captured graph replays), and then the AdamW factor
+    // 1 - lr*wd too, rounded as the host forms it
+    const float lr = h.lr_dev ? *h.lr_dev : h.lr;
+    const double a = (double)lr / bc1;
     const double b = 1.0 / sqrt(bc2);
     s_ab[0] = __double2float_rn(a);
     s_ab[1] = __double2float_rn(a - (double)s_ab[0]);
     s_ab[2] = __double2float_rn(b);
     s_ab[3] = __double2float_rn(b - (double)s_ab[2]);
+    if (h.lr_dev) {
+      const double k = __dsub_rn(1.0, __dmul_rn((double)lr, (double)h.wd));
+      s_ab[4] = __double2float_rn(k);
+      s_ab[5] = __double2float_rn(__dsub_rn(k, (double)s_ab[4]));
+    }
     h.unscale = __fdiv_rn(1.f, st.scale);
     h.sqnorm = sqnorm;
     s_gscale = grad_scale_of(h);
@@ -835,6 +844,10 @@ __global__ void __launch_bounds__(kThreads, W == 32 ? 3 : min_ctas<NR, PACK>())
   h.a_lo = s_ab[1];
   h.b_hi = s_ab[2];
   h.b_lo = s_ab[3];
+  if (p.h.lr_dev) {
+    h.k_hi = s_ab[4];
+    h.k_lo = s_ab[5];
+  }
   step_loop<NR, GK, PACK, true, W>(p, h, s_gscale);
 }
 

@@ -49,6 +49,8 @@ struct Hyper {
   float unscale;         // multiplier applied first (1/loss scale; 1 when unused)
   float lr;              // learning rate (for bias corrections formed on the device)
   const float* scale_dev;  // device loss scale: the norm pre-pass unscales by 1/*scale_dev
+  const float* lr_dev;     // device learning rate of the loss-scaled step (null: lr above),
+  float wd;                // with the weight decay its 1 - lr*wd is formed from
 #ifdef DPOPT_DEBUG_BOUNDS
   // bounds-checked builds only: the status word a failed index check sets, and
   // the span [dbg_lo, dbg_hi) of shard elements the call may touch
