@@ -122,7 +122,7 @@ def test_loss_scaled_iteration_replays_from_one_graph(max_norm):
         sa, sb = dp.read_loss_scale(direct.state), dp.read_loss_scale(replay.state)
         assert (sa.scale, sa.step, sa.skipped, sa.last_overflow) == \
                (sb.scale, sb.step, sb.skipped, sb.last_overflow), k
-        ref, overflow, scale, steps = refs[k - 1]
+        _, overflow, scale, steps = refs[k - 1]
         assert (bool(sb.last_overflow), sb.scale, sb.step) == (overflow, scale, steps), k
     parity.check(refs[-1][0], *replay.snapshot(), where=f"graph amp max_norm={max_norm}")
     assert sb.skipped == 3
