@@ -254,8 +254,11 @@ def test_two_pass_clipped_step_over_buckets_equals_the_fused_bucket_step():
         sq = torch.zeros(1, dtype=torch.float64, device="cuda")
         avg = torch.empty(S, device="cuda")
         for t in (1, 2, 3):
-            grads = [to_dev_grad(g) for g in _full_grads(wl, t)]
-            rows, offs = _contiguous_buckets(grads, wl.shard_base, S, bucket)
+            # each replica's slice of this rank's shard (what a reduce-scatter
+            # hands over), one flat buffer cut into contiguous buckets
+            sh = [grad_host_range(wl, r, t, wl.shard_base, S) for r in range(n)]
+            grads = [to_dev_grad(g) for g in sh]
+            rows, offs = _contiguous_buckets(grads, 0, S, bucket)
             scratch = _bucket_scratch(S, len(rows))
             if stored:
                 dp.grad_average_sqnorm_buckets(rows, offs, avg, sq, scratch)
@@ -271,9 +274,6 @@ def test_two_pass_clipped_step_over_buckets_equals_the_fused_bucket_step():
                 dp.reduce_adamw_buckets(rows, offs, *st, out, step=t, opts=opts, **HP)
             dp.stream_status()
             if stored:
-                host = _full_grads(wl, t)
-                base = wl.shard_base
-                sh = [h[base:base + S] for h in host]
                 c = oracle.grad_scale(oracle.grad_sqnorm(sh, 0, S, 1.0), 1e-4 * np.sqrt(S),
                                       1.0)
                 parity.check_step(wl, np.arange(S), t, prev, [f32(x) for x in st] + [u16(out)],
