@@ -164,7 +164,8 @@ int dpopt_reduce_adam_bucket(const void *const *grad_slices, int grad_dtype, int
                              float beta2, float eps, int64_t step, dpopt_stream_t stream);
 
 /* Many buckets per call (as few kernel launches as the pointer tables allow;
- * buckets that continue one another in the shard and in every replica's
+ * the buckets are put in shard order, whatever order they are listed in, and
+ * those that continue one another in the shard and in every replica's
  * gradient memory are joined into one segment first, which gives the same
  * bits).
  *  slice_table    HOST array of n_buckets * n_replicas DEVICE pointers, bucket
@@ -228,8 +229,9 @@ int dpopt_reduce_adamw_buckets(const void *const *slice_table, int grad_dtype, i
  * sections 4 and 8: a 1/64 shard, reduce_bucket_size) could take nine launches
  * per step.  This form runs every bucket in one launch.  Like
  * dpopt_reduce_adam_buckets it first joins buckets that continue one another
- * (bucket b + 1 starting where bucket b ends, in the shard and in every
- * replica's gradient memory, as in a flat contiguous gradient buffer); if
+ * (taken in shard order, one bucket starting where the previous one ends, in
+ * the shard and in every replica's gradient memory, as in a flat contiguous
+ * gradient buffer); if
  * what remains fits one launch's parameter space it launches from there and
  * leaves `table` untouched, otherwise it writes the checked launch table into
  * `table` and the direct-load kernel reads it from device memory.  Its
@@ -283,11 +285,13 @@ int dpopt_grad_sqnorm(const void *const *grads, int grad_dtype, int n_replicas, 
                       int64_t scratch_bytes, dpopt_stream_t stream);
 
 /* The same over a batch of bucket slices (arguments as for
- * dpopt_reduce_adam_buckets).  Buckets that continue one another (in the
+ * dpopt_reduce_adam_buckets).  The buckets are taken in shard order, in
+ * whatever order they are listed, and those that continue one another (in the
  * shard and in every replica's gradient memory, as in a flat contiguous
- * gradient buffer) are joined first, so such buckets covering the whole shard
- * give the bits of dpopt_grad_sqnorm over the full buffers; the scratch size
- * of dpopt_grad_sqnorm_scratch_bytes(elems, n_buckets) covers every case. */
+ * gradient buffer) are joined first: the result does not depend on the
+ * listing order, and such buckets covering the whole shard give the bits of
+ * dpopt_grad_sqnorm over the full buffers.  The scratch size of
+ * dpopt_grad_sqnorm_scratch_bytes(elems, n_buckets) covers every case. */
 int dpopt_grad_sqnorm_buckets(const void *const *slice_table, int grad_dtype, int n_replicas,
                               const int64_t *offsets, const int64_t *lens, int64_t n_buckets,
                               float grad_unscale, double *sqnorm_out, void *scratch,

@@ -352,3 +352,34 @@ def test_loss_scaled_run_over_buckets_equals_the_full_buffer_run():
     assert ta == tb and ta[-1][2] == 2
     for x, y in zip(a, b):
         assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+def test_bucket_norm_does_not_depend_on_the_listing_order():
+    """Buckets listed last first (the order a backward pass produces them) are
+    put in shard order and joined: the norm and the stored average are bit for
+    bit those of the ascending listing, and the step gives the same bits."""
+    _need_gpu()
+    n, S, bucket = 8, 60_001, 7_000
+    wl = _small_workload(n, S, kind=0, rank=2)
+    sh = [grad_host_range(wl, r, 1, wl.shard_base, S) for r in range(n)]
+    grads = [to_dev_grad(g) for g in sh]
+    rows, offs = _contiguous_buckets(grads, 0, S, bucket)
+    res = []
+    for order in (1, -1):
+        r, o = rows[::order], offs[::order]
+        sq = torch.zeros(1, dtype=torch.float64, device="cuda")
+        sq2 = torch.zeros(1, dtype=torch.float64, device="cuda")
+        avg = torch.full((S,), float("nan"), device="cuda")
+        dp.grad_sqnorm_buckets(r, o, sq, _bucket_scratch(S, len(r)))
+        dp.grad_average_sqnorm_buckets(r, o, avg, sq2, _bucket_scratch(S, len(r)))
+        master, m, v = parity.states_host(wl, wl.shard_base + np.arange(S))
+        st = [torch.from_numpy(x.copy()).cuda() for x in (master, m, v)]
+        out = torch.zeros(S, dtype=torch.bfloat16, device="cuda")
+        c0 = dp.dpopt_launch_count()
+        dp.reduce_adam_buckets(r, o, *st, out, step=1, **HP)
+        assert dp.dpopt_launch_count() - c0 == 1          # joined into one segment
+        dp.stream_status()
+        assert torch.equal(sq, sq2)
+        res.append([f32(sq), f32(avg)] + [f32(x) for x in st] + [u16(out)])
+    for x, y in zip(*res):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))

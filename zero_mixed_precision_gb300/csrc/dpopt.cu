@@ -446,12 +446,18 @@ int build_buckets(const void* const* slice_table, int grad_dtype, int n_replicas
   return DPOPT_OK;
 }
 
-// Joins consecutive buckets whose slices continue one another: bucket b + 1
-// starts where bucket b ends, in the shard and in every replica's gradient
-// memory (the buckets of a flat, contiguous gradient buffer).  The step is
-// elementwise, so the joined segment gives the same bits in fewer segments;
-// 274 resident 4M-element buckets become one segment and one launch.
+// Puts the buckets in shard order and joins those whose slices continue one
+// another: bucket b + 1 starts where bucket b ends, in the shard and in every
+// replica's gradient memory (the buckets of a flat, contiguous gradient
+// buffer), whatever order the caller listed them in.  The step is
+// elementwise, so the joined segments give the same bits in fewer segments
+// (274 resident 4M-element buckets become one segment and one launch), and
+// the norm's chunk partials then follow the shard order, so its bits do not
+// depend on the listing order either.  Offsets are distinct (overlapping
+// buckets were refused).
 void coalesce(std::vector<SegDesc>& segs, int n, int grad_dtype) {
+  std::sort(segs.begin(), segs.end(),
+            [](const SegDesc& a, const SegDesc& b) { return a.state_off < b.state_off; });
   const uintptr_t esize = grad_dtype == DPOPT_GRAD_F32 ? 4 : 2;
   size_t w = 0;
   for (size_t s = 0; s < segs.size(); ++s) {
