@@ -816,21 +816,39 @@ def run_overlap(args, wl):
         torch.cuda.synchronize()
         return t0.elapsed_time(t1) / reps
 
+    clip = args.optimizer == "adamw_clip"
+    if args.optimizer not in ("adam", "adamw_clip"):
+        raise SystemExit("--overlap measures adam and adamw_clip")
+    S = wl.shard_elems
+    if clip:
+        # the clipped step: the norm pass storing the average, then the step on it
+        avg = torch.empty(S, dtype=torch.float32, device="cuda")
+        sqn = torch.zeros(1, dtype=torch.float64, device="cuda")
+        scratch = torch.empty(dp.dpopt_grad_sqnorm_scratch_bytes(S, len(buckets))[1] // 8 + 1,
+                              dtype=torch.float64, device="cuda")
+        opts = dp.step_options(weight_decay=0.01, max_grad_norm=1.0, grad_sqnorm=sqn)
+
+    def step_batched(k, stream):
+        if clip:
+            dp.grad_average_sqnorm_buckets(rows, offs, avg, sqn, scratch, stream=stream)
+            dp.reduce_adamw([avg], 0, S, dev.master, dev.m, dev.v, dev.out, step=k + 1,
+                            opts=opts, stream=stream, **hp)
+        else:
+            dp.reduce_adam_buckets(rows, offs, dev.master, dev.m, dev.v, dev.out, step=k + 1,
+                                   stream=stream, **hp)
+
     # each rep also runs the producer (many times the step's time): a default
     # run takes at most 200 reps
     reps = max(1, min(args.steps, 200) if getattr(args, "steps_defaulted", False) else args.steps)
     for k in range(args.warmup):
         produce(1, P)
-        dp.reduce_adam_buckets(rows, offs, dev.master, dev.m, dev.v, dev.out, step=k + 1,
-                               stream=P, **hp)
+        step_batched(k, P)
     t_prod = timed(lambda k: produce(k + 2, P), reps)
-    t_step = timed(lambda k: dp.reduce_adam_buckets(rows, offs, dev.master, dev.m, dev.v, dev.out,
-                                                    step=k + 1, stream=C, **hp), reps)
+    t_step = timed(lambda k: step_batched(k, C), reps)
 
     def serial(k):
         produce(k + 2, P)
-        dp.reduce_adam_buckets(rows, offs, dev.master, dev.m, dev.v, dev.out, step=k + 1,
-                               stream=P, **hp)
+        step_batched(k, P)
     t_serial = timed(serial, reps)
     evs = [torch.cuda.Event() for _ in buckets]
 
@@ -839,13 +857,20 @@ def run_overlap(args, wl):
 
     def overlapped(k):
         produce(k + 2, P, evs)
-        dp.reduce_adam_buckets_when_ready(rrows, roffs, revs, dev.master, dev.m, dev.v, dev.out,
-                                          step=k + 1, stream=C, **hp)
+        if clip:   # the norm pass bucket by bucket; the short step on the average after
+            dp.grad_sqnorm_buckets_when_ready(rrows, roffs, revs, sqn, scratch, avg_out=avg,
+                                              stream=C)
+            dp.reduce_adamw([avg], 0, S, dev.master, dev.m, dev.v, dev.out, step=k + 1,
+                            opts=opts, stream=C, **hp)
+        else:
+            dp.reduce_adam_buckets_when_ready(rrows, roffs, revs, dev.master, dev.m, dev.v,
+                                              dev.out, step=k + 1, stream=C, **hp)
         P.wait_stream(C)   # the next step's backward starts after this step's update
     t_over = timed(overlapped, reps)
     dp.stream_status(C)
     hidden = (t_serial - t_over) / t_step if t_step > 0 else 0.0
     return {"metric": "bucket-as-ready overlap of the step with gradient production",
+            "optimizer": args.optimizer,
             "workload": wl.name, "n_replicas": wl.n_replicas, "shard_params": wl.shard_elems,
             "buckets": len(buckets), "bucket_elems": wl.bucket_elems, "steps": reps,
             "ms_produce": t_prod, "ms_step": t_step, "ms_produce_then_step": t_serial,

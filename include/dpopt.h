@@ -345,6 +345,28 @@ int dpopt_grad_average_sqnorm(const void *const *grads, int grad_dtype, int n_re
                               double *sqnorm_out, void *scratch, int64_t scratch_bytes,
                               dpopt_stream_t stream);
 
+/* The norm pass bucket by bucket as the gradients become ready (row f4's
+ * overlap for the clipped and loss-scaled steps: the pass over each bucket runs
+ * while the backward pass is still producing the others; only the short step
+ * on the stored average waits for the last bucket).  For each bucket with
+ * lens[b] > 0, in the listed order: if ready[b] is non-null, `stream` waits
+ * for that event, then the bucket's pass is launched; after the last bucket
+ * the ordered finish writes *sqnorm_out.  The buckets are not joined: each
+ * bucket's partials sit at its rank in shard order, so the result is bitwise
+ * that of dpopt_grad_sqnorm_buckets over the same buckets held in separate
+ * memory, whatever the listing order.  avg_out: NULL (norm only), or a DEVICE
+ * array indexed like the states (as for dpopt_grad_average_sqnorm_buckets,
+ * here for any buckets) that receives each element's average.
+ *  ready          HOST array of n_buckets events (dpopt_event_t = cudaEvent_t).
+ * Other arguments and errors as for dpopt_grad_average_sqnorm_buckets, plus
+ * DPOPT_ERR_INVALID_ARG for a null `ready` with n_buckets > 0. */
+int dpopt_grad_sqnorm_buckets_when_ready(const void *const *slice_table, int grad_dtype,
+                                         int n_replicas, const int64_t *offsets,
+                                         const int64_t *lens, int64_t n_buckets,
+                                         const dpopt_event_t *ready, float grad_unscale,
+                                         float *avg_out, double *sqnorm_out, void *scratch,
+                                         int64_t scratch_bytes, dpopt_stream_t stream);
+
 /* dpopt_grad_average_sqnorm over bucket slices: dpopt_grad_sqnorm_buckets that
  * also stores each element's average at its shard offset, avg_out[offsets[b]
  * + j] for element j of bucket b.  The buckets must join into one segment

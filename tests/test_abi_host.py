@@ -207,6 +207,14 @@ def test_bucket_average_norm_rejects_bad_arguments(dp):
     assert amp(STATE + 4) == dp.DPOPT_ERR_INVALID_ARG
     assert amp(STATE, avg=0) == dp.DPOPT_ERR_INVALID_ARG
     assert amp(STATE, avg=AVG + 1) == dp.DPOPT_ERR_INVALID_ARG
+    # the readiness-driven form: events are required, buckets need not join
+    def ready(events, table=joined):
+        return dp.dpopt_grad_sqnorm_buckets_when_ready(table, 0, 2, [0, L], [L, L], events, 0.0,
+                                                       AVG, SQ, SCR, nbytes, 0)
+    assert ready(None) == dp.DPOPT_ERR_INVALID_ARG
+    assert dp.dpopt_grad_sqnorm_buckets_when_ready(joined, 0, 2, [0, L], [L, L], [0, 0], 0.0,
+                                                   AVG + 2, SQ, SCR, nbytes, 0) == \
+        dp.DPOPT_ERR_INVALID_ARG
 
 
 def test_bucket_table_bytes(dp):

@@ -98,3 +98,73 @@ def test_null_events_mean_ready_now():
     refs = oracle_trajectory(wl, np.arange(0, wl.shard_elems, 997), 1, 1)
     parity.check(refs[0], f32(dev.master)[::997], f32(dev.m)[::997], f32(dev.v)[::997],
                  u16(dev.out)[::997], where="null events")
+
+
+def test_norm_pass_when_ready_then_the_step_on_the_average():
+    """The clipping pre-pass bucket by bucket behind the producer's events,
+    storing the average; then the clipped step reads the average.  The norm is
+    bitwise that of the batched norm over the same buckets held apart, the
+    average that of the joined buckets, the states those of the fused bucket
+    step, and the norm within the oracle's bound."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import oracle
+    from tests.parity import grad_host_range
+    wl = _wl()
+    S, n = wl.shard_elems, wl.n_replicas
+    hp = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps)
+    producer, consumer = torch.cuda.Stream(), torch.cuda.Stream()
+    dev = DeviceWorkload(wl)
+    dev.fill_states()
+    nb = -(-S // wl.bucket_elems)
+
+    def scratch():
+        return torch.empty(dp.dpopt_grad_sqnorm_scratch_bytes(S, nb)[1] // 8 + 1,
+                           dtype=torch.float64, device="cuda")
+    events = [torch.cuda.Event() for _ in range(nb)]
+    torch.cuda.synchronize()
+    buckets = _produce(dev, wl, 1, producer, events)
+    rows, offs = [s for _, s in buckets], [o for o, _ in buckets]
+    sq = torch.zeros(1, dtype=torch.float64, device="cuda")
+    avg = torch.full((S,), float("nan"), device="cuda")
+    c0 = dp.dpopt_launch_count()
+    dp.grad_sqnorm_buckets_when_ready(rows[::-1], offs[::-1], events[::-1], sq, scratch(),
+                                      avg_out=avg, stream=consumer)
+    assert dp.dpopt_launch_count() - c0 == nb + 1      # one pass per bucket, one finish
+    consumer.synchronize()
+    dp.stream_status(consumer)
+    # the same buckets held apart (no joining), batched; and joined, storing the average
+    apart = [[x.clone() for x in row] for row in rows]
+    sq_apart = torch.zeros(1, dtype=torch.float64, device="cuda")
+    dp.grad_sqnorm_buckets(apart, offs, sq_apart, scratch())
+    sq_joined = torch.zeros(1, dtype=torch.float64, device="cuda")
+    avg_joined = torch.full((S,), float("nan"), device="cuda")
+    dp.grad_average_sqnorm_buckets(rows, offs, avg_joined, sq_joined, scratch())
+    dp.stream_status()
+    assert torch.equal(sq, sq_apart)
+    assert np.array_equal(f32(avg).view(np.uint32), f32(avg_joined).view(np.uint32))
+    gh = [grad_host_range(wl, r, 1, wl.shard_base, S) for r in range(n)]
+    want = oracle.grad_sqnorm(gh, 0, S, 1.0)
+    assert float(sq.item()) == pytest.approx(want, rel=4 * S * 2.0 ** -53)
+    # the clipped step on the average, against the fused bucket step with the same norm
+    max_norm = 0.3 * float(np.sqrt(want))
+    res = []
+    for form in ("average", "fused"):
+        st = [x.clone() for x in (dev.master, dev.m, dev.v)]
+        out = torch.zeros(S, dtype=torch.bfloat16, device="cuda")
+        opts = dp.step_options(weight_decay=0.01, max_grad_norm=max_norm, grad_sqnorm=sq)
+        if form == "average":
+            dp.reduce_adamw([avg], 0, S, *st, out, step=1, opts=opts, **hp)
+        else:
+            dp.reduce_adamw_buckets(rows, offs, *st, out, step=1, opts=opts, **hp)
+        dp.stream_status()
+        res.append([f32(x) for x in st] + [u16(out)])
+    for a, b in zip(*res):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+    idx = np.arange(0, S, 101)
+    c = oracle.grad_scale(want, max_norm, 1.0)
+    base = wl.shard_base
+    parity.check_step(wl, idx, 1, [f32(x)[idx] for x in (dev.master, dev.m, dev.v)],
+                      [x[idx] for x in res[0]], "norm when ready, step on the average",
+                      grads_fn=lambda r, _t: gh[r][idx], weight_decay=0.01,
+                      gscale_fn=lambda _t, _g: c)

@@ -106,6 +106,8 @@ _SIGS = {
     "dpopt_grad_sqnorm_buckets": ([_PP, _I, _I, _PI64, _PI64, _I64, _F, _P, _P, _I64, _P], _I),
     "dpopt_grad_average_sqnorm_buckets": ([_PP, _I, _I, _PI64, _PI64, _I64, _F, _P, _P, _P, _I64,
                                            _P], _I),
+    "dpopt_grad_sqnorm_buckets_when_ready": ([_PP, _I, _I, _PI64, _PI64, _I64, _PP, _F, _P, _P, _P,
+                                              _I64, _P], _I),
     "dpopt_grad_sqnorm_scratch_bytes": ([_I64, _I64, _PI64], _I),
     "dpopt_grad_sqnorm_noalloc": ([_PP, _I, _I, _I64, _I, _F, _P, _P], _I),
     "dpopt_grad_average_sqnorm": ([_PP, _I, _I, _I64, _I, _F, _P, _P, _P, _I64, _P], _I),
@@ -278,6 +280,19 @@ def dpopt_grad_average_sqnorm_buckets(slice_table: Sequence[int], grad_dtype: in
         _ptr_array(slice_table), grad_dtype, n_replicas, (ctypes.c_int64 * nb)(*offsets),
         (ctypes.c_int64 * nb)(*lens), nb, grad_unscale, avg_out, sqnorm_out, scratch,
         scratch_bytes, stream)
+
+
+def dpopt_grad_sqnorm_buckets_when_ready(slice_table: Sequence[int], grad_dtype: int,
+                                         n_replicas: int, offsets: Sequence[int],
+                                         lens: Sequence[int], ready: Sequence[int],
+                                         grad_unscale: float, avg_out: int, sqnorm_out: int,
+                                         scratch: int, scratch_bytes: int,
+                                         stream: int = 0) -> int:
+    nb = len(offsets)
+    return _lib.dpopt_grad_sqnorm_buckets_when_ready(
+        _ptr_array(slice_table), grad_dtype, n_replicas, (ctypes.c_int64 * nb)(*offsets),
+        (ctypes.c_int64 * nb)(*lens), nb, _ptr_array(ready) if ready is not None else None,
+        grad_unscale, avg_out, sqnorm_out, scratch, scratch_bytes, stream)
 
 
 def dpopt_amp_average_sqnorm_buckets(slice_table: Sequence[int], grad_dtype: int,
@@ -732,6 +747,26 @@ def reduce_adam_buckets_when_ready(bucket_slices, offsets, ready_events, master,
                                               _operand(param_bf16_out), lr, beta1, beta2, eps,
                                               step, _stream_handle(stream))
     _check(rc, "dpopt_reduce_adam_buckets_when_ready")
+
+
+def grad_sqnorm_buckets_when_ready(bucket_slices, offsets, ready_events, sqnorm_out, scratch, *,
+                                   avg_out=None, grad_unscale: float = 0.0,
+                                   stream=None) -> None:
+    """The norm pass bucket by bucket behind each bucket's event (one
+    torch.cuda.Event or None per bucket); avg_out (float32 device tensor indexed
+    like the states) also receives each element's average."""
+    n = len(bucket_slices[0])
+    dt = _grad_dtype(bucket_slices[0][0])
+    table = [_operand(t) for row in bucket_slices for t in row]
+    lens = [row[0].numel() for row in bucket_slices]
+    ready = [e.cuda_event if e is not None else 0 for e in ready_events]
+    rc = dpopt_grad_sqnorm_buckets_when_ready(table, dt, n, list(offsets), lens, ready,
+                                              grad_unscale,
+                                              0 if avg_out is None else _operand(avg_out),
+                                              _operand(sqnorm_out), _operand(scratch),
+                                              scratch.numel() * scratch.element_size(),
+                                              _stream_handle(stream))
+    _check(rc, "dpopt_grad_sqnorm_buckets_when_ready")
 
 
 def allgather_bf16(shard_bf16, shard_rank: int, param_replicas, stream=None) -> None:

@@ -338,44 +338,55 @@ int launch_sqnorm(LaunchParams<MS, MP>& p, int64_t nchunks, double* partials, in
 
 // Squared norm of segments [0, nsegs) into *out (device), partials in scratch.
 // avg_out (one segment only): also store each element's average there.
-int run_sqnorm(const SegDesc* segs, int nsegs, int grad_dtype, int n, const Hyper& h,
-               double* partials, double* out, cudaStream_t stream, float* avg_out = nullptr) {
-  if (avg_out && nsegs != 1)
-    return fail(DPOPT_ERR_UNSUPPORTED, "the averaged gradient is stored for one segment only");
-  const int per_launch = nsegs == 1 ? 1 : std::min(kBigSegs, kBigPtrs / n);
-  int64_t done = 0;
-  for (int s0 = 0; s0 < nsegs; s0 += per_launch) {
-    const int s1 = std::min(nsegs, s0 + per_launch);
-    int64_t chunks;
-    int rc;
-    if (nsegs == 1) {
-      SmallParams p{};
-      p.h = h;
-      p.n_rep = n;
-      p.master = avg_out;  // the average's destination (null: norm only)
-      chunks = fill_segments(p, segs, s0, s1, n, kNormChunk, grad_dtype);
-      rc = chunks ? launch_sqnorm(p, chunks, partials + done, grad_dtype, avg_out != nullptr,
-                                  stream)
-                  : DPOPT_OK;
-    } else {
-      static thread_local BigParams p;
-      std::memset(&p, 0, sizeof p);
-      p.h = h;
-      p.n_rep = n;
-      chunks = fill_segments(p, segs, s0, s1, n, kNormChunk, grad_dtype);
-      rc = chunks ? launch_sqnorm(p, chunks, partials + done, grad_dtype, false, stream)
-                  : DPOPT_OK;
-    }
-    if (rc) return rc;
-    done += chunks;
-  }
-  // each chunk's partial is a double-float pair in its 8-byte slot
+// The norm pass over one segment: its chunk partials from `partials` on, each
+// element's average stored at its shard offset in avg_out when given.
+int norm_segment(const SegDesc& seg, int grad_dtype, int n, const Hyper& h, double* partials,
+                 float* avg_out, cudaStream_t stream, int64_t* chunks_out) {
+  SmallParams p{};
+  p.h = h;
+  p.n_rep = n;
+  p.master = avg_out;  // the average's destination (null: norm only)
+  const int64_t chunks = fill_segments(p, &seg, 0, 1, n, kNormChunk, grad_dtype);
+  *chunks_out = chunks;
+  return chunks ? launch_sqnorm(p, chunks, partials, grad_dtype, avg_out != nullptr, stream)
+                : DPOPT_OK;
+}
+
+// The ordered sum of `count` chunk partials (double-float pairs, one per 8-byte
+// slot) into *out.
+int norm_finish(const double* partials, int64_t count, double* out, cudaStream_t stream) {
   cudaError_t e = launch_pdl(sqnorm_finish_kernel, 1, kFinishThreads, 0, stream,
-                             reinterpret_cast<const DFloat*>(partials), done, out);
+                             reinterpret_cast<const DFloat*>(partials), count, out);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   ++g_launches;
   return DPOPT_OK;
+}
+
+int run_sqnorm(const SegDesc* segs, int nsegs, int grad_dtype, int n, const Hyper& h,
+               double* partials, double* out, cudaStream_t stream, float* avg_out = nullptr) {
+  if (avg_out && nsegs != 1)
+    return fail(DPOPT_ERR_UNSUPPORTED, "the averaged gradient is stored for one segment only");
+  int64_t done = 0;
+  if (nsegs == 1) {
+    int rc = norm_segment(segs[0], grad_dtype, n, h, partials, avg_out, stream, &done);
+    if (rc) return rc;
+  } else {
+    const int per_launch = std::min(kBigSegs, kBigPtrs / n);
+    for (int s0 = 0; s0 < nsegs; s0 += per_launch) {
+      const int s1 = std::min(nsegs, s0 + per_launch);
+      static thread_local BigParams p;
+      std::memset(&p, 0, sizeof p);
+      p.h = h;
+      p.n_rep = n;
+      const int64_t chunks = fill_segments(p, segs, s0, s1, n, kNormChunk, grad_dtype);
+      int rc = chunks ? launch_sqnorm(p, chunks, partials + done, grad_dtype, false, stream)
+                      : DPOPT_OK;
+      if (rc) return rc;
+      done += chunks;
+    }
+  }
+  return norm_finish(partials, done, out, stream);
 }
 
 
@@ -1010,12 +1021,16 @@ int dpopt_grad_sqnorm_noalloc(const void* const* grads, int grad_dtype, int n_re
 // joined first (so contiguous buckets take the chunk partition, and the bits,
 // of one full-buffer call over the same elements); with avg_out each
 // element's average is stored at its shard offset, which needs the buckets to
-// join into one segment.
+// join into one segment.  With `ready` (one event per bucket) the buckets are
+// neither joined nor reordered: each one's pass is launched behind its own
+// event, in the listed order, its partials placed at its rank in shard order,
+// so the ordered finish gives the bits of the call without events over the
+// same buckets kept apart; the average may then span any number of buckets.
 int buckets_norm_impl(const void* const* slice_table, int grad_dtype, int n_replicas,
                       const int64_t* offsets, const int64_t* lens, int64_t n_buckets,
                       float grad_unscale, const LossScaleState* state, float* avg_out,
                       double* sqnorm_out, void* scratch, int64_t scratch_bytes,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, const dpopt_event_t* ready = nullptr) {
   if (!std::isfinite(grad_unscale) || grad_unscale < 0.f)
     return fail(DPOPT_ERR_INVALID_ARG, "grad_unscale must be finite and >= 0");
   std::vector<SegDesc> segs;
@@ -1023,8 +1038,8 @@ int buckets_norm_impl(const void* const* slice_table, int grad_dtype, int n_repl
   int rc = build_buckets(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets, segs, &lo,
                          &hi);
   if (rc) return rc;
-  coalesce(segs, n_replicas, grad_dtype);
-  if (avg_out && segs.size() > 1)
+  if (!ready) coalesce(segs, n_replicas, grad_dtype);
+  if (!ready && avg_out && segs.size() > 1)
     return fail(DPOPT_ERR_UNSUPPORTED,
                 "the average is stored for buckets that join into one segment (each bucket "
                 "continuing the previous one in the shard and in every replica's gradients); "
@@ -1049,8 +1064,34 @@ int buckets_norm_impl(const void* const* slice_table, int grad_dtype, int n_repl
   h.unscale = grad_unscale == 0.f ? 1.f : grad_unscale;
   if (state) h.scale_dev = &state->scale;
   set_span(h, lo, hi);
-  return run_sqnorm(segs.data(), (int)segs.size(), grad_dtype, n_replicas, h, (double*)scratch,
-                    sqnorm_out, stream, avg_out);
+  if (!ready)
+    return run_sqnorm(segs.data(), (int)segs.size(), grad_dtype, n_replicas, h,
+                      (double*)scratch, sqnorm_out, stream, avg_out);
+  // each bucket's first partial: the chunks of the buckets before it in shard order
+  std::vector<size_t> order(segs.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = i;
+  std::sort(order.begin(), order.end(),
+            [&](size_t a, size_t b) { return segs[a].state_off < segs[b].state_off; });
+  std::vector<int64_t> base(segs.size());
+  int64_t done = 0;
+  for (size_t i : order) {
+    base[i] = done;
+    done += (segs[i].len + kNormChunk - 1) / kNormChunk;
+  }
+  size_t si = 0;
+  for (int64_t b = 0; b < n_buckets; ++b) {
+    if (lens[b] == 0) continue;
+    if (ready[b]) {
+      cudaError_t e = cudaStreamWaitEvent(stream, (cudaEvent_t)ready[b], 0);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+    }
+    int64_t chunks = 0;
+    rc = norm_segment(segs[si], grad_dtype, n_replicas, h, (double*)scratch + base[si], avg_out,
+                      stream, &chunks);
+    if (rc) return rc;
+    ++si;
+  }
+  return norm_finish((const double*)scratch, done, sqnorm_out, stream);
 }
 
 int dpopt_grad_sqnorm_buckets(const void* const* slice_table, int grad_dtype, int n_replicas,
@@ -1060,6 +1101,19 @@ int dpopt_grad_sqnorm_buckets(const void* const* slice_table, int grad_dtype, in
   return buckets_norm_impl(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets,
                            grad_unscale, nullptr, nullptr, sqnorm_out, scratch, scratch_bytes,
                            (cudaStream_t)stream);
+}
+
+int dpopt_grad_sqnorm_buckets_when_ready(const void* const* slice_table, int grad_dtype,
+                                         int n_replicas, const int64_t* offsets,
+                                         const int64_t* lens, int64_t n_buckets,
+                                         const dpopt_event_t* ready, float grad_unscale,
+                                         float* avg_out, double* sqnorm_out, void* scratch,
+                                         int64_t scratch_bytes, dpopt_stream_t stream) {
+  if (n_buckets > 0 && !ready) return fail(DPOPT_ERR_INVALID_ARG, "ready must be non-null");
+  static const dpopt_event_t kNoEvents[1] = {nullptr};
+  return buckets_norm_impl(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets,
+                           grad_unscale, nullptr, avg_out, sqnorm_out, scratch, scratch_bytes,
+                           (cudaStream_t)stream, n_buckets > 0 ? ready : kNoEvents);
 }
 
 int dpopt_grad_average_sqnorm_buckets(const void* const* slice_table, int grad_dtype,
