@@ -1085,9 +1085,9 @@ int buckets_norm_impl(const void* const* slice_table, int grad_dtype, int n_repl
       cudaError_t e = cudaStreamWaitEvent(stream, (cudaEvent_t)ready[b], 0);
       if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
     }
-    int64_t chunks = 0;
+    int64_t launched_chunks = 0;
     rc = norm_segment(segs[si], grad_dtype, n_replicas, h, (double*)scratch + base[si], avg_out,
-                      stream, &chunks);
+                      stream, &launched_chunks);
     if (rc) return rc;
     ++si;
   }
