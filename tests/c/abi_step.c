@@ -5,7 +5,9 @@
  * CPU oracle (oracle/oracle.c, linked as test infrastructure only); then a
  * third step through dpopt_reduce_adam_buckets_table with 159 separately
  * allocated bucket slices and a cudaMalloc'd launch table, bitwise against
- * the full-buffer entry.
+ * the full-buffer entry; then three loss-scaled steps captured once into a
+ * CUDA graph (cudaStreamBeginCapture) and replayed, bitwise against direct
+ * calls.
  * Built and run by tests/test_gpu_c_abi.py; prints "ok" and exits 0 on
  * success.
  */
@@ -196,7 +198,88 @@ int main(void) {
     free(x);
     free(y);
   }
+  /* Steps 4-6 captured once into a CUDA graph with the runtime API and replayed:
+     the loss-scaled entry without a squared norm keeps the step count in the
+     device state and reads the learning rate from device memory, so each replay
+     is the next step at the rate written before it -- bitwise the direct calls
+     that pass the same rates from the host. */
+  const dpopt_loss_scale_config cfg = {1.0f, 1, 1, 1.0f};
+  const float rates[3] = {1e-3f, 6e-4f, 2e-4f};
+  float *st4[2][3];
+  void *out4[2], *state4[2];
+  for (int k = 0; k < 2; ++k) {
+    for (int a = 0; a < 3; ++a) {
+      check(cudaMalloc((void **)&st4[k][a], S * 4), "cudaMalloc");
+      check(cudaMemcpy(st4[k][a], st3[0][a], S * 4, cudaMemcpyDeviceToDevice), "cudaMemcpy");
+    }
+    check(cudaMalloc(&out4[k], S * 2), "cudaMalloc");
+    check(cudaMalloc(&state4[k], sizeof(dpopt_loss_scale_state)), "cudaMalloc");
+    if (dpopt_loss_scale_init((dpopt_loss_scale_state *)state4[k], &cfg, st) != DPOPT_OK) return 1;
+  }
+  float *lr_dev;
+  check(cudaMalloc((void **)&lr_dev, 4), "cudaMalloc");
+  /* one direct call on spare arrays first: the kernels are loaded before the capture */
+  void *state_w;
+  check(cudaMalloc(&state_w, sizeof(dpopt_loss_scale_state)), "cudaMalloc");
+  rc = dpopt_loss_scale_init((dpopt_loss_scale_state *)state_w, &cfg, st);
+  if (rc == DPOPT_OK)
+    rc = dpopt_amp_step((const void *const *)dg, DPOPT_GRAD_BF16, N, numel, RANK, 4096,
+                        st3[1][0], st3[1][1], st3[1][2], out3[1], 1e-3f, b1, b2, eps, 0.01f, 0.f,
+                        NULL, (dpopt_loss_scale_state *)state_w, &cfg, NULL, st);
+  if (rc == DPOPT_OK) rc = dpopt_stream_status(st);
+  if (rc != DPOPT_OK) {
+    fprintf(stderr, "warm-up: %s (%s)\n", dpopt_status_string(rc), dpopt_last_error());
+    return 1;
+  }
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+  check(cudaStreamBeginCapture(st, cudaStreamCaptureModeGlobal), "cudaStreamBeginCapture");
+  rc = dpopt_amp_step((const void *const *)dg, DPOPT_GRAD_BF16, N, numel, RANK, 4096, st4[1][0],
+                      st4[1][1], st4[1][2], out4[1], 0.f, b1, b2, eps, 0.01f, 0.f, NULL,
+                      (dpopt_loss_scale_state *)state4[1], &cfg, lr_dev, st);
+  check(cudaStreamEndCapture(st, &graph), "cudaStreamEndCapture");
+  if (rc != DPOPT_OK) {
+    fprintf(stderr, "capture: %s (%s)\n", dpopt_status_string(rc), dpopt_last_error());
+    return 1;
+  }
+  check(cudaGraphInstantiate(&exec, graph, 0), "cudaGraphInstantiate");
+  for (int k = 0; k < 3; ++k) {
+    check(cudaMemcpy(lr_dev, &rates[k], 4, cudaMemcpyHostToDevice), "cudaMemcpy");
+    check(cudaGraphLaunch(exec, st), "cudaGraphLaunch");
+    rc = dpopt_amp_step((const void *const *)dg, DPOPT_GRAD_BF16, N, numel, RANK, 4096,
+                        st4[0][0], st4[0][1], st4[0][2], out4[0], rates[k], b1, b2, eps, 0.01f,
+                        0.f, NULL, (dpopt_loss_scale_state *)state4[0], &cfg, NULL, st);
+    if (rc == DPOPT_OK) rc = dpopt_stream_status(st);
+    if (rc != DPOPT_OK) {
+      fprintf(stderr, "graph step %d: %s (%s)\n", k, dpopt_status_string(rc),
+              dpopt_last_error());
+      return 1;
+    }
+  }
+  for (int a = 0; a < 5; ++a) {
+    const size_t bytes = a < 3 ? S * 4 : a == 3 ? S * 2 : sizeof(dpopt_loss_scale_state);
+    const void *src0 = a < 3 ? (void *)st4[0][a] : a == 3 ? out4[0] : state4[0];
+    const void *src1 = a < 3 ? (void *)st4[1][a] : a == 3 ? out4[1] : state4[1];
+    unsigned char *x = malloc(bytes), *y = malloc(bytes);
+    check(cudaMemcpy(x, src0, bytes, cudaMemcpyDeviceToHost), "cudaMemcpy");
+    check(cudaMemcpy(y, src1, bytes, cudaMemcpyDeviceToHost), "cudaMemcpy");
+    if (memcmp(x, y, bytes) != 0) {
+      fprintf(stderr, "the graph replays differ from the direct calls (array %d)\n", a);
+      return 1;
+    }
+    if (a == 4 && ((const dpopt_loss_scale_state *)x)->step != 3) {
+      fprintf(stderr, "the device step count is %lld after 3 steps\n",
+              (long long)((const dpopt_loss_scale_state *)x)->step);
+      return 1;
+    }
+    free(x);
+    free(y);
+  }
+  check(cudaGraphExecDestroy(exec), "cudaGraphExecDestroy");
+  check(cudaGraphDestroy(graph), "cudaGraphDestroy");
+
   printf("ok: N=%d, %d shard elements, 2 steps, worst relative %.2e; step 3 through the "
-         "bucket table bitwise equal; version %s\n", N, S, worst, dpopt_version());
+         "bucket table bitwise equal; steps 4-6 as graph replays bitwise equal; version %s\n",
+         N, S, worst, dpopt_version());
   return 0;
 }

@@ -29,3 +29,4 @@ def test_plain_c_program_steps_through_the_abi(tmp_path):
     assert pr.returncode == 0, pr.stdout + pr.stderr
     assert pr.stdout.startswith("ok:"), pr.stdout
     assert "bucket table bitwise equal" in pr.stdout
+    assert "graph replays bitwise equal" in pr.stdout
