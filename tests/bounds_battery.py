@@ -5,7 +5,7 @@ one-element path), the bulk-copy kernel, the runtime-replica-count kernels
 40, the register walk at N = 64),
 the one-launch bucket entry (launch table in device memory, and contiguous
 buckets joined), the norm pre-pass with and without the stored average (over
-full buffers and over joined buckets), the
+full buffers, over joined buckets, and bucket by bucket as each is ready), the
 loss-scaled step, the all-gather and the fused step + all-gather (per-thread
 stores, and whole tiles written by bulk copies).
 
@@ -149,6 +149,13 @@ def run() -> tuple[dict, list]:
     sq5 = torch.zeros(1, dtype=torch.float64, device="cuda")
     dp.grad_average_sqnorm_buckets(joined, offs, avg_b[:sum(lens)], sq5, sc)
     keep("average_sqnorm_buckets", avg_b, sq5)
+    # bucket by bucket as each is ready (here: listed last first, null events),
+    # the separate slices, the average stored for each
+    avg_r = torch.full((sum(lens) + 8,), float("nan"), device="cuda")
+    sq6 = torch.zeros(1, dtype=torch.float64, device="cuda")
+    dp.grad_sqnorm_buckets_when_ready(slices[::-1], offs[::-1], [None] * len(lens), sq6, sc,
+                                      avg_out=avg_r[:sum(lens)])
+    keep("sqnorm_buckets_when_ready", avg_r, sq6)
     sq4 = torch.zeros(1, dtype=torch.float64, device="cuda")
     rc = dp.dpopt_grad_sqnorm_noalloc([g.data_ptr() for g in grads], dp.DPOPT_GRAD_BF16, n,
                                       n * S, 2, 0.0, sq4.data_ptr(), 0)
