@@ -786,6 +786,8 @@ def run_overlap(args, wl):
     if args.bucket_elems:
         wl = replace(wl, bucket_elems=args.bucket_elems)
     wl = replace(wl, layout="slices")
+    if args.optimizer == "amp":
+        wl = replace(wl, grad_kind=2)   # fp16 gradients, the loss-scaled recipe
     dev = DeviceWorkload(wl)
     dev.fill_states()
     buckets = dev.bucket_slices()
@@ -816,23 +818,39 @@ def run_overlap(args, wl):
         torch.cuda.synchronize()
         return t0.elapsed_time(t1) / reps
 
-    clip = args.optimizer == "adamw_clip"
-    if args.optimizer not in ("adam", "adamw_clip"):
-        raise SystemExit("--overlap measures adam and adamw_clip")
+    clip = args.optimizer in ("adamw_clip", "amp")
+    if args.optimizer not in ("adam", "adamw_clip", "amp"):
+        raise SystemExit("--overlap measures adam, adamw_clip and amp")
     S = wl.shard_elems
     if clip:
-        # the clipped step: the norm pass storing the average, then the step on it
+        # the clipped (or loss-scaled) step: the norm pass storing the average,
+        # then the step on it
         avg = torch.empty(S, dtype=torch.float32, device="cuda")
         sqn = torch.zeros(1, dtype=torch.float64, device="cuda")
         scratch = torch.empty(dp.dpopt_grad_sqnorm_scratch_bytes(S, len(buckets))[1] // 8 + 1,
                               dtype=torch.float64, device="cuda")
         opts = dp.step_options(weight_decay=0.01, max_grad_norm=1.0, grad_sqnorm=sqn)
+    if args.optimizer == "amp":
+        ls_state = torch.zeros(4, dtype=torch.int64, device="cuda")
+        ls_cfg = dp.loss_scale_init(ls_state, init_scale=1024.0, window=1000)
 
-    def step_batched(k, stream):
-        if clip:
-            dp.grad_average_sqnorm_buckets(rows, offs, avg, sqn, scratch, stream=stream)
+    def step_on_average(k, stream):
+        if args.optimizer == "amp":
+            dp.amp_step([avg], 0, S, dev.master, dev.m, dev.v, dev.out, weight_decay=0.01,
+                        max_grad_norm=1.0, global_sqnorm=sqn, state=ls_state, cfg=ls_cfg,
+                        stream=stream, **hp)
+        else:
             dp.reduce_adamw([avg], 0, S, dev.master, dev.m, dev.v, dev.out, step=k + 1,
                             opts=opts, stream=stream, **hp)
+
+    def step_batched(k, stream):
+        if args.optimizer == "amp":
+            dp.amp_average_sqnorm_buckets(rows, offs, ls_state, avg, sqn, scratch,
+                                          stream=stream)
+            step_on_average(k, stream)
+        elif clip:
+            dp.grad_average_sqnorm_buckets(rows, offs, avg, sqn, scratch, stream=stream)
+            step_on_average(k, stream)
         else:
             dp.reduce_adam_buckets(rows, offs, dev.master, dev.m, dev.v, dev.out, step=k + 1,
                                    stream=stream, **hp)
@@ -857,11 +875,14 @@ def run_overlap(args, wl):
 
     def overlapped(k):
         produce(k + 2, P, evs)
-        if clip:   # the norm pass bucket by bucket; the short step on the average after
+        if args.optimizer == "amp":
+            dp.amp_sqnorm_buckets_when_ready(rrows, roffs, revs, ls_state, sqn, scratch,
+                                             avg_out=avg, stream=C)
+            step_on_average(k, C)
+        elif clip:   # the norm pass bucket by bucket; the short step on the average after
             dp.grad_sqnorm_buckets_when_ready(rrows, roffs, revs, sqn, scratch, avg_out=avg,
                                               stream=C)
-            dp.reduce_adamw([avg], 0, S, dev.master, dev.m, dev.v, dev.out, step=k + 1,
-                            opts=opts, stream=C, **hp)
+            step_on_average(k, C)
         else:
             dp.reduce_adam_buckets_when_ready(rrows, roffs, revs, dev.master, dev.m, dev.v,
                                               dev.out, step=k + 1, stream=C, **hp)

@@ -456,6 +456,19 @@ int dpopt_amp_average_sqnorm_buckets(const void *const *slice_table, int grad_dt
                                      float *avg_out, double *sqnorm_out, void *scratch,
                                      int64_t scratch_bytes, dpopt_stream_t stream);
 
+/* dpopt_grad_sqnorm_buckets_when_ready for the loss-scaled step: the unscale
+ * 1 / state->scale read on the device.  With the ZeRO-3 answer's config
+ * (section 8: fp16 with a dynamic loss scale, overlap_comm) each bucket's pass
+ * runs as soon as the bucket's gradients exist; the scalar all-reduce and
+ * dpopt_amp_step on avg_out follow the last bucket. */
+int dpopt_amp_sqnorm_buckets_when_ready(const void *const *slice_table, int grad_dtype,
+                                        int n_replicas, const int64_t *offsets,
+                                        const int64_t *lens, int64_t n_buckets,
+                                        const dpopt_event_t *ready,
+                                        const dpopt_loss_scale_state *state, float *avg_out,
+                                        double *sqnorm_out, void *scratch, int64_t scratch_bytes,
+                                        dpopt_stream_t stream);
+
 /* One loss-scaled step of this rank's shard (full-buffer layout, arguments as for
  * dpopt_reduce_adam_ex): if *global_sqnorm is finite, AdamW (weight_decay) on the
  * averaged gradient times c = (1/scale) * min(1, max_grad_norm / (||g|| + 1e-6))

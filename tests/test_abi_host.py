@@ -212,6 +212,11 @@ def test_bucket_average_norm_rejects_bad_arguments(dp):
         return dp.dpopt_grad_sqnorm_buckets_when_ready(table, 0, 2, [0, L], [L, L], events, 0.0,
                                                        AVG, SQ, SCR, nbytes, 0)
     assert ready(None) == dp.DPOPT_ERR_INVALID_ARG
+    assert dp.dpopt_amp_sqnorm_buckets_when_ready(joined, 2, 2, [0, L], [L, L], [0, 0], 0, AVG,
+                                                  SQ, SCR, nbytes, 0) == dp.DPOPT_ERR_INVALID_ARG
+    assert dp.dpopt_amp_sqnorm_buckets_when_ready(joined, 2, 2, [0, L], [L, L], None, STATE,
+                                                  AVG, SQ, SCR, nbytes, 0) == \
+        dp.DPOPT_ERR_INVALID_ARG
     assert dp.dpopt_grad_sqnorm_buckets_when_ready(joined, 0, 2, [0, L], [L, L], [0, 0], 0.0,
                                                    AVG + 2, SQ, SCR, nbytes, 0) == \
         dp.DPOPT_ERR_INVALID_ARG

@@ -168,3 +168,60 @@ def test_norm_pass_when_ready_then_the_step_on_the_average():
                       [x[idx] for x in res[0]], "norm when ready, step on the average",
                       grads_fn=lambda r, _t: gh[r][idx], weight_decay=0.01,
                       gscale_fn=lambda _t, _g: c)
+
+
+def test_loss_scaled_norm_when_ready_equals_the_batched_run():
+    """Five loss-scaled iterations, fp16 gradients produced bucket by bucket
+    (an Inf planted at iteration 3): the norm pass behind each bucket's event
+    then the step on the stored average skips, rescales and steps exactly as
+    the batched run over joined buckets (no clipping: only the overflow test
+    reads the norm, so the two partitions give the same decisions and bits)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dataclasses import replace
+    wl = replace(_wl(), grad_kind=2, numel=4 * 1_000_003, bucket_elems=150_000)
+    S = wl.shard_elems
+    hp = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps)
+    producer, consumer = torch.cuda.Stream(), torch.cuda.Stream()
+    nb = -(-S // wl.bucket_elems)
+    res = []
+    for mode in ("ready", "batched"):
+        dev = DeviceWorkload(wl)
+        dev.fill_states()
+        state = torch.zeros(4, dtype=torch.int64, device="cuda")
+        cfg = dp.loss_scale_init(state, init_scale=1024.0, window=2, hysteresis=1,
+                                 min_scale=1.0)
+        avg = torch.empty(S, device="cuda")
+        sq = torch.zeros(1, dtype=torch.float64, device="cuda")
+        scratch = torch.empty(dp.dpopt_grad_sqnorm_scratch_bytes(S, nb)[1] // 8 + 1,
+                              dtype=torch.float64, device="cuda")
+        trail = []
+        torch.cuda.synchronize()
+        for t in range(1, 6):
+            events = [torch.cuda.Event() for _ in range(nb)]
+            buckets = _produce(dev, wl, t, producer, events)
+            rows, offs = [s for _, s in buckets], [o for o, _ in buckets]
+            if t == 3:   # an overflow in one replica of the middle bucket
+                with torch.cuda.stream(producer):
+                    rows[nb // 2][1][7] = float("inf")
+                events[nb // 2].record(producer)
+            if mode == "ready":
+                dp.amp_sqnorm_buckets_when_ready(rows[::-1], offs[::-1], events[::-1], state, sq,
+                                                 scratch, avg_out=avg, stream=consumer)
+            else:
+                consumer.wait_stream(producer)
+                dp.amp_average_sqnorm_buckets(rows, offs, state, avg, sq, scratch,
+                                              stream=consumer)
+            dp.amp_step([avg], 0, S, dev.master, dev.m, dev.v, dev.out, weight_decay=0.01,
+                        max_grad_norm=0.0, global_sqnorm=sq, state=state, cfg=cfg,
+                        stream=consumer, **hp)
+            producer.wait_stream(consumer)
+            consumer.synchronize()
+            dp.stream_status(consumer)
+            st = dp.read_loss_scale(state)
+            trail.append((st.scale, st.step, st.skipped, st.last_overflow))
+        res.append((trail, [f32(dev.master), f32(dev.m), f32(dev.v), u16(dev.out)]))
+    assert res[0][0] == res[1][0]
+    assert res[0][0][2][3] == 1 and res[0][0][-1][2] == 1      # iteration 3 skipped
+    for a, b in zip(res[0][1], res[1][1]):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))

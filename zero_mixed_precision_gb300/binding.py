@@ -108,6 +108,8 @@ _SIGS = {
                                            _P], _I),
     "dpopt_grad_sqnorm_buckets_when_ready": ([_PP, _I, _I, _PI64, _PI64, _I64, _PP, _F, _P, _P, _P,
                                               _I64, _P], _I),
+    "dpopt_amp_sqnorm_buckets_when_ready": ([_PP, _I, _I, _PI64, _PI64, _I64, _PP, _P, _P, _P, _P,
+                                             _I64, _P], _I),
     "dpopt_grad_sqnorm_scratch_bytes": ([_I64, _I64, _PI64], _I),
     "dpopt_grad_sqnorm_noalloc": ([_PP, _I, _I, _I64, _I, _F, _P, _P], _I),
     "dpopt_grad_average_sqnorm": ([_PP, _I, _I, _I64, _I, _F, _P, _P, _P, _I64, _P], _I),
@@ -293,6 +295,18 @@ def dpopt_grad_sqnorm_buckets_when_ready(slice_table: Sequence[int], grad_dtype:
         _ptr_array(slice_table), grad_dtype, n_replicas, (ctypes.c_int64 * nb)(*offsets),
         (ctypes.c_int64 * nb)(*lens), nb, _ptr_array(ready) if ready is not None else None,
         grad_unscale, avg_out, sqnorm_out, scratch, scratch_bytes, stream)
+
+
+def dpopt_amp_sqnorm_buckets_when_ready(slice_table: Sequence[int], grad_dtype: int,
+                                        n_replicas: int, offsets: Sequence[int],
+                                        lens: Sequence[int], ready: Sequence[int], state: int,
+                                        avg_out: int, sqnorm_out: int, scratch: int,
+                                        scratch_bytes: int, stream: int = 0) -> int:
+    nb = len(offsets)
+    return _lib.dpopt_amp_sqnorm_buckets_when_ready(
+        _ptr_array(slice_table), grad_dtype, n_replicas, (ctypes.c_int64 * nb)(*offsets),
+        (ctypes.c_int64 * nb)(*lens), nb, _ptr_array(ready) if ready is not None else None,
+        state, avg_out, sqnorm_out, scratch, scratch_bytes, stream)
 
 
 def dpopt_amp_average_sqnorm_buckets(slice_table: Sequence[int], grad_dtype: int,
@@ -767,6 +781,24 @@ def grad_sqnorm_buckets_when_ready(bucket_slices, offsets, ready_events, sqnorm_
                                               scratch.numel() * scratch.element_size(),
                                               _stream_handle(stream))
     _check(rc, "dpopt_grad_sqnorm_buckets_when_ready")
+
+
+def amp_sqnorm_buckets_when_ready(bucket_slices, offsets, ready_events, state, sqnorm_out,
+                                  scratch, *, avg_out=None, stream=None) -> None:
+    """grad_sqnorm_buckets_when_ready with the unscale 1/scale read from the
+    device loss-scale state."""
+    n = len(bucket_slices[0])
+    dt = _grad_dtype(bucket_slices[0][0])
+    table = [_operand(t) for row in bucket_slices for t in row]
+    lens = [row[0].numel() for row in bucket_slices]
+    ready = [e.cuda_event if e is not None else 0 for e in ready_events]
+    rc = dpopt_amp_sqnorm_buckets_when_ready(table, dt, n, list(offsets), lens, ready,
+                                             _operand(state),
+                                             0 if avg_out is None else _operand(avg_out),
+                                             _operand(sqnorm_out), _operand(scratch),
+                                             scratch.numel() * scratch.element_size(),
+                                             _stream_handle(stream))
+    _check(rc, "dpopt_amp_sqnorm_buckets_when_ready")
 
 
 def allgather_bf16(shard_bf16, shard_rank: int, param_replicas, stream=None) -> None:

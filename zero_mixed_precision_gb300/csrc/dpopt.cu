@@ -1191,6 +1191,23 @@ int dpopt_amp_average_sqnorm_buckets(const void* const* slice_table, int grad_dt
                            scratch_bytes, (cudaStream_t)stream);
 }
 
+int dpopt_amp_sqnorm_buckets_when_ready(const void* const* slice_table, int grad_dtype,
+                                        int n_replicas, const int64_t* offsets,
+                                        const int64_t* lens, int64_t n_buckets,
+                                        const dpopt_event_t* ready,
+                                        const dpopt_loss_scale_state* state, float* avg_out,
+                                        double* sqnorm_out, void* scratch, int64_t scratch_bytes,
+                                        dpopt_stream_t stream) {
+  int rc = check_state_ptr(state);
+  if (rc) return rc;
+  if (n_buckets > 0 && !ready) return fail(DPOPT_ERR_INVALID_ARG, "ready must be non-null");
+  static const dpopt_event_t kNoEvents[1] = {nullptr};
+  return buckets_norm_impl(slice_table, grad_dtype, n_replicas, offsets, lens, n_buckets, 0.f,
+                           (const LossScaleState*)state, avg_out, sqnorm_out, scratch,
+                           scratch_bytes, (cudaStream_t)stream,
+                           n_buckets > 0 ? ready : kNoEvents);
+}
+
 int dpopt_amp_step(const void* const* grads, int grad_dtype, int n_replicas, int64_t numel,
                    int shard_rank, int64_t bucket_elems, float* master_f32, float* m_f32,
                    float* v_f32, void* param_bf16_out, float lr, float beta1, float beta2,
