@@ -774,7 +774,9 @@ def _finish(args, wl, rank, world, S, K, elapsed_ms, kernel_ms, launches, clocks
 
 
 def run_overlap(args, wl):
-    """Bucket-as-ready against produce-then-step, on one GPU, one line of JSON."""
+    """Bucket-as-ready against produce-then-step, on one GPU, one line of JSON:
+    the plain step per bucket, or (adamw_clip, amp) the norm pass per bucket
+    storing the average, then the step on the average."""
     import torch
     from dataclasses import replace
 
