@@ -79,3 +79,17 @@ def test_bench_loss_scaled_line_over_bucket_slices():
     assert d["config"]["clip_path"] == "stored" and "fp16" in d["config"]["workload"]
     assert d["config"]["bytes_per_param"] == 2 * 64 + 34
     assert d["roofline"]["launches_per_step"] == 4 and d["value"] > 0
+
+
+@pytest.mark.parametrize("opt", ["adam", "adamw_clip", "amp"])
+def test_bench_overlap_line(opt):
+    """--overlap prints one line with the produce / step / serial / when-ready
+    times for each optimizer form."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    d = _line("--overlap", "--workload", "gpt2s", "--optimizer", opt, "--bucket-elems",
+              "8000000", "--steps", "3", "--warmup", "1")
+    assert d["optimizer"] == opt and d["buckets"] == 4
+    for k in ("ms_produce", "ms_step", "ms_produce_then_step", "ms_when_ready"):
+        assert d[k] > 0, k
+    assert d["ms_when_ready"] <= d["ms_produce_then_step"] * 1.05
